@@ -1,0 +1,312 @@
+"""Pins of the float64 oracle against things other than itself.
+
+Each test ties one oracle part to a closed form, an invariant, a library
+routine, a hand-built fixture, or the independent scalar statement in
+tests/bruteforce.py, chosen so that a dropped term, a wrong sign or index or a
+transposed operand fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import model as om
+from oracle.quant import dequant, float32_is_exact
+from quantized_moe_decode_gb300 import synth
+
+from bruteforce import BruteModel, decode_rows, rot
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+FMT = {"q8_0": 1, "q4_0": 2, "i8asym": 3}
+
+
+# ------------------------------------------------------------------ dequantisation
+def _golden_blocks():
+    out = []
+    with open(os.path.join(GOLDEN, "quant_blocks.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            left, right = line.split("|")
+            name, hexs = left.split()
+            out.append((name, bytes.fromhex(hexs), [float(v) for v in right.split()]))
+    return out
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_hand_built_blocks_dequantise_exactly(case):
+    name, raw, expected = _golden_blocks()[case]
+    got = dequant(np.frombuffer(raw, np.uint8), FMT[name], 1, 32)[0]
+    assert got.tolist() == expected
+
+
+@pytest.mark.parametrize("fmt", [synth.F16, synth.Q8_0, synth.Q4_0, synth.I8ASYM])
+def test_dequant_matches_scalar_parser(fmt):
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((5, 96), dtype=np.float32) * 0.02
+    t = synth.Tensor(0, 0, 0, fmt, 5, 96, synth.encode(x, fmt))
+    got = dequant(t.blob, fmt, 5, 96)
+    ref = np.array(decode_rows(t))
+    assert np.array_equal(got, ref)
+    # and the encoding is a faithful quantisation of the draw (catches a wrong scale / sign)
+    assert np.max(np.abs(got - x)) < (0.02 * 4 / 7 if fmt == synth.Q4_0 else 0.02 * 4 / 100)
+
+
+def test_q8_q4_values_are_exact_in_float32():
+    rng = np.random.default_rng(8)
+    for fmt in (synth.Q8_0, synth.Q4_0, synth.I8ASYM):
+        x = rng.standard_normal((7, 64), dtype=np.float32)
+        w = dequant(synth.encode(x, fmt), fmt, 7, 64)
+        assert float32_is_exact(w)
+
+
+# ------------------------------------------------------------------ elementwise parts
+def test_rmsnorm_unit_rms_and_scale_invariance():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(1280) * 3.7
+    y = om.rmsnorm(x, np.ones(1280), 0.0)
+    assert abs(math.sqrt(np.mean(y * y)) - 1.0) < 1e-12
+    assert np.allclose(om.rmsnorm(5.0 * x, np.ones(1280), 0.0), y, rtol=1e-12, atol=0)
+    w = rng.standard_normal(1280)
+    assert np.allclose(om.rmsnorm(x, w, 0.0), y * w, rtol=1e-12, atol=0)
+    # eps enters inside the root: a zero vector stays zero, a tiny one is damped
+    assert np.all(om.rmsnorm(np.zeros(8), np.ones(8), 1e-6) == 0)
+    t = np.full(4, 1e-3)
+    assert np.allclose(om.rmsnorm(t, np.ones(4), 1e-6), t / math.sqrt(1e-6 + 1e-6))
+
+
+def test_silu_closed_forms():
+    assert om.silu(np.float64(0.0)) == 0.0
+    z = np.linspace(-6, 6, 25)
+    assert np.allclose(om.silu(z) - om.silu(-z), z, atol=1e-14)
+    assert np.allclose(om.silu(z), z / (1 + np.exp(-z)))
+    assert abs(om.silu(np.float64(40.0)) - 40.0) < 1e-12
+
+
+def test_rope_identity_norm_and_relative_position():
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal(128)
+    k = rng.standard_normal(128)
+    assert np.array_equal(om.rope(q, 0, 1e4), q)
+    for p in (1, 17, 300, 3000):
+        assert abs(np.linalg.norm(om.rope(q, p, 1e4)) - np.linalg.norm(q)) < 1e-12
+    # <R_p q, R_p' k> depends only on p - p'
+    a = om.rope(q, 310, 1e4) @ om.rope(k, 300, 1e4)
+    b = om.rope(q, 10, 1e4) @ om.rope(k, 0, 1e4)
+    assert abs(a - b) < 1e-10
+
+
+def test_rope_pairs_first_and_second_half_like_complex_rotation():
+    # D = 2: a plain rotation by angle p
+    v = np.array([0.3, -1.2])
+    p = 5
+    c, s = math.cos(p), math.sin(p)
+    assert np.allclose(om.rope(v, p, 1e4), [0.3 * c + 1.2 * s, -1.2 * c + 0.3 * s])
+    # D = 16: pair (i, i + 8) rotates as the complex number v[i] + 1j*v[i+8]
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal(16)
+    assert np.allclose(om.rope(v, 37, 1e4), rot(list(v), 37, 1e4), atol=1e-13)
+
+
+def test_ring_slot_closed_cases():
+    assert [om.ring_slot(p, 289, 128) for p in (0, 288, 289, 416, 417, 418, 588)] == \
+        [0, 288, 289, 416, 289, 290, 289 + (588 - 289) % 128]
+
+
+# ------------------------------------------------------------------ attention
+def test_attention_single_key_and_equal_logits():
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal(64)
+    K = rng.standard_normal((1, 64))
+    V = rng.standard_normal((1, 64))
+    assert np.allclose(om.attend(q, K, V), V[0])
+    K = np.zeros((5, 64))
+    V = rng.standard_normal((5, 64))
+    assert np.allclose(om.attend(q, K, V), V.mean(axis=0))
+
+
+def test_attention_two_keys_closed_form_and_scale():
+    q = np.zeros(4)
+    q[0] = 2.0
+    K = np.array([[1.0, 0, 0, 0], [0.0, 0, 0, 0]])
+    V = np.array([[1.0, 0, 0, 0], [0.0, 1, 0, 0]])
+    # logits 2*1/sqrt(4) = 1 and 0 -> weights sigmoid(1), sigmoid(-1)
+    s1 = 1 / (1 + math.exp(-1.0))
+    assert np.allclose(om.attend(q, K, V), [s1, 1 - s1, 0, 0])
+
+
+def test_attention_split_merge_equals_one_pass():
+    rng = np.random.default_rng(5)
+    q, K, V = rng.standard_normal(128), rng.standard_normal((300, 128)), rng.standard_normal((300, 128))
+    o, lse = om.attend_lse(q, K, V)
+    parts = [om.attend_lse(q, K[a:b], V[a:b]) for a, b in ((0, 77), (77, 200), (200, 300))]
+    M = max(l for _, l in parts)
+    w = np.array([math.exp(l - M) for _, l in parts])
+    merged = sum(wi * oi for wi, (oi, _) in zip(w, parts)) / w.sum()
+    assert np.allclose(merged, o, atol=1e-12)
+    assert abs(M + math.log(w.sum()) - lse) < 1e-12
+
+
+def test_sink_key_equals_sigmoid_rescale():
+    """Falcon-OCR card: output * sigmoid(lse - sink) == softmax with one more zero-value key."""
+    rng = np.random.default_rng(6)
+    for s in (-3.0, 0.0, 0.7, 5.0):
+        q, K, V = rng.standard_normal(64), rng.standard_normal((40, 64)), rng.standard_normal((40, 64))
+        o, lse = om.attend_lse(q, K, V)
+        assert np.allclose(om.attend(q, K, V, sink=s), o / (1 + math.exp(-(lse - s))), atol=1e-13)
+    assert np.allclose(om.attend(q, K, V, sink=-1e4), o, atol=1e-13)
+
+
+# ------------------------------------------------------------------ routing
+def test_route_selection_weights_and_ties():
+    lg = np.array([0.1, 2.0, -1.0, 2.0, 0.5, 2.0])
+    idx, w = om.route(lg, 2)
+    assert idx.tolist() == [1, 3]             # lowest indices among the tied maxima
+    assert np.allclose(w, [0.5, 0.5])
+    idx, w = om.route(lg, 1)
+    assert idx.tolist() == [int(np.argmax(lg))] and w.tolist() == [1.0]
+    rng = np.random.default_rng(9)
+    lg = rng.standard_normal(64)
+    idx, w = om.route(lg, 6)
+    assert abs(w.sum() - 1) < 1e-14
+    assert set(idx.tolist()) == set(np.argsort(lg)[-6:].tolist())
+    # ratio of two weights is exp of the logit difference
+    assert abs(w[0] / w[1] - math.exp(lg[idx[0]] - lg[idx[1]])) < 1e-12
+    # k = E: the renormalised weights are the full softmax
+    idx, w = om.route(lg, 64)
+    sm = np.exp(lg - lg.max()) / np.exp(lg - lg.max()).sum()
+    assert np.allclose(w, sm[idx], atol=1e-15)
+
+
+def test_grouping_is_a_stable_sort_by_expert():
+    rng = np.random.default_rng(10)
+    for rows, k, E in ((1, 6, 64), (8, 6, 64), (64, 6, 64), (5, 2, 4)):
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(rows)])
+        count, offset, perm = om.group_by_expert(idx, E)
+        assert np.array_equal(count, np.bincount(idx.reshape(-1), minlength=E))
+        assert np.array_equal(offset, np.concatenate([[0], np.cumsum(count)]))
+        assert np.array_equal(perm, np.argsort(idx.reshape(-1), kind="stable"))
+
+
+def _tiny_cfg(**kw):
+    base = dict(hidden=32, n_heads=2, head_dim=16, n_layers=3, n_dense_layers=1, dense_inter=64,
+                n_experts=4, top_k=2, n_shared=2, expert_inter=32, vocab=10, fmt_attn=synth.Q8_0,
+                fmt_dense=synth.Q8_0, fmt_shared=synth.Q8_0, fmt_routed=synth.Q4_0,
+                prefix_len=3, ring_len=4, max_rows=2)
+    base.update(kw)
+    return synth.ModelConfig(**base)
+
+
+def test_top_all_experts_equals_dense_softmax_mixture():
+    cfg = _tiny_cfg(n_layers=1, n_dense_layers=0, top_k=4, n_shared=0, vocab=0)
+    wl = synth.make_workload("t", cfg, 2, 1, 11)
+    m = oracle.OracleModel(cfg, wl.tensors, 2, kv_prefix=wl.kv_prefix)
+    res = m.step(wl.positions(0), x=wl.step_x[0])
+    Hh = res.h_attn[0]
+    Hn = om.rmsnorm(Hh, m.w(om.T_MLP_NORM, 0), cfg.rms_eps)
+    for r in range(2):
+        lg = m.w(om.T_ROUTER, 0) @ Hn[r]
+        p = np.exp(lg - lg.max())
+        p /= p.sum()
+        mix = sum(p[e] * om.swiglu(Hn[r], m.w(om.T_EXPERT_GATE, 0, e), m.w(om.T_EXPERT_UP, 0, e),
+                                   m.w(om.T_EXPERT_DOWN, 0, e)) for e in range(4))
+        assert np.allclose(res.hidden[1][r], Hh[r] + mix, atol=1e-12)
+
+
+def test_two_shared_experts_equal_one_concatenated_expert():
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal(32)
+    g = [rng.standard_normal((16, 32)) for _ in range(2)]
+    u = [rng.standard_normal((16, 32)) for _ in range(2)]
+    d = [rng.standard_normal((32, 16)) for _ in range(2)]
+    two = om.swiglu(x, g[0], u[0], d[0]) + om.swiglu(x, g[1], u[1], d[1])
+    one = om.swiglu(x, np.vstack(g), np.vstack(u), np.hstack(d))
+    assert np.allclose(two, one, atol=1e-12)
+
+
+def test_argmax_first_maximum():
+    assert om.argmax_first(np.array([1.0, 3.0, 3.0, -1.0])) == 1
+    assert om.argmax_first(np.array([-2.0])) == 0
+
+
+# ------------------------------------------------------------------ whole step vs brute force
+def _compare_with_brute(cfg, rows, steps, seed, prefix="cached", n_embeds=0, ids=False):
+    wl = synth.make_workload("t", cfg, rows, steps, seed, prefix=prefix,
+                             n_prefill_embeds=n_embeds, step_input="ids" if ids else "x")
+    orc = oracle.OracleModel(cfg, wl.tensors, rows, kv_prefix=wl.kv_prefix, sinks=wl.sinks)
+    bru = BruteModel(cfg, wl.tensors, rows, kv_prefix=wl.kv_prefix, sinks=wl.sinks)
+    plan = []
+    if prefix == "prefill":
+        for p in range(cfg.prefix_len):
+            pos = np.full(rows, p, np.int32)
+            if p < n_embeds:
+                plan.append((pos, None, wl.prefill_embeds[:, p]))
+            else:
+                plan.append((pos, wl.prefill_ids[:, p - n_embeds], None))
+    for s in range(steps):
+        pos = wl.positions(s)
+        if ids:
+            plan.append((pos, "greedy", None))
+        else:
+            plan.append((pos, None, wl.step_x[s]))
+    last = None
+    for pos, idv, x in plan:
+        if isinstance(idv, str):
+            idv = last.next_ids if last is not None and last.next_ids is not None else wl.first_ids
+        a = orc.step(pos, ids=idv, x=x)
+        b = bru.step(pos, ids=idv, x=x)
+        for r in range(rows):
+            layers, logits = b[r]
+            for l in range(cfg.n_layers):
+                assert np.allclose(a.hidden[l + 1][r], layers[l], rtol=1e-10, atol=1e-10), (pos, l, r)
+            if logits is not None:
+                assert np.allclose(a.logits[r], logits, rtol=1e-10, atol=1e-10)
+        last = a
+    return orc
+
+
+def test_tiny_moe_model_matches_brute_force_through_ring_wrap():
+    # prefix of 3 built by decode (2 embeddings + 1 token), then 7 greedy steps, ring of 4
+    _compare_with_brute(_tiny_cfg(), rows=2, steps=7, seed=13, prefix="prefill", n_embeds=2, ids=True)
+
+
+def test_tiny_dense_sink_model_matches_brute_force():
+    cfg = _tiny_cfg(n_layers=2, n_dense_layers=2, n_experts=0, top_k=0, n_shared=0, vocab=0,
+                    fmt_attn=synth.I8ASYM, fmt_dense=synth.I8ASYM, use_sink=1, prefix_len=5)
+    _compare_with_brute(cfg, rows=2, steps=6, seed=14)
+
+
+def test_tiny_q4_attention_cached_prefix_matches_brute_force():
+    cfg = _tiny_cfg(n_layers=2, n_dense_layers=1, fmt_attn=synth.Q4_0, fmt_shared=synth.Q4_0, vocab=0,
+                    prefix_len=6, ring_len=3)
+    _compare_with_brute(cfg, rows=1, steps=5, seed=15)
+
+
+def test_ring_equals_full_attention_while_generated_fits():
+    """With g <= R the ring holds every generated token: same as an unbounded cache."""
+    cfg = _tiny_cfg(n_layers=2, n_dense_layers=1, vocab=0, ring_len=6)
+    big = cfg.replace(ring_len=1000)
+    wl = synth.make_workload("t", cfg, 2, 6, 16)
+    a = oracle.OracleModel(cfg, wl.tensors, 2, kv_prefix=wl.kv_prefix)
+    b = oracle.OracleModel(big, wl.tensors, 2, kv_prefix=wl.kv_prefix)
+    for s in range(6):
+        ra = a.step(wl.positions(s), x=wl.step_x[s])
+        rb = b.step(wl.positions(s), x=wl.step_x[s])
+        assert np.array_equal(ra.hidden, rb.hidden)
+    # one step more and the oldest generated token has left the ring
+    x = wl.step_x[0]
+    ra = a.step(wl.positions(6), x=x)
+    rb = b.step(wl.positions(6), x=x)
+    assert not np.allclose(ra.hidden[-1], rb.hidden[-1])
+
+
+def test_float32_cache_gives_identical_results():
+    cfg = _tiny_cfg(vocab=10)
+    wl = synth.make_workload("t", cfg, 2, 2, 17, step_input="ids")
+    a = oracle.OracleModel(cfg, wl.tensors, 2, kv_prefix=wl.kv_prefix, cache="float64")
+    b = oracle.OracleModel(cfg, wl.tensors, 2, kv_prefix=wl.kv_prefix, cache="float32")
+    ra = a.step(wl.positions(0), ids=wl.first_ids)
+    rb = b.step(wl.positions(0), ids=wl.first_ids)
+    assert np.array_equal(ra.logits, rb.logits)
