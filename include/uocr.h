@@ -1,0 +1,260 @@
+/*
+ * uocr.h — C ABI of the GB300 quantized MoE decode step.
+ *
+ * One decode step of a DeepSeek-V2-style OCR text decoder whose weights are
+ * block-quantized (Q8_0, Q4_0, per-group int8-asymmetric) and dequantized
+ * inside the matmul kernels, with fp16 activations, a KV cache made of a fixed
+ * prefix followed by a ring of generated tokens, optional attention sinks,
+ * batched rows that share one weight read, and a greedy argmax over the LM
+ * head.
+ *
+ * Sources (page title, section):
+ *  - "Unlimited-OCR on Apple Silicon with C and Metal":
+ *      "Il decoder e il Mixture of Experts" (layer stack, 64 routed experts,
+ *      top-6, 2 shared, grouping tokens by expert, KV append, 128-token ring,
+ *      argmax over the language head);
+ *      "Quantizzazione: Q8 prima, Q4 dove conviene" (Q8_0 / Q4_0 profiles,
+ *      fused dequantisation, attention kept Q8, norms and activations fp16);
+ *      "Memoria: il vincolo principale" (per-category working set checked
+ *      against a budget before running, refused with a detailed error);
+ *      "Dall'ABI C all'API Python" (a deliberately small C ABI, one lock per
+ *      engine, one instance per execution lane).
+ *  - "Falcon-OCR INT8 OpenVINO IR" model card: intro (the sink as one more
+ *      key with value zero; the KV cache is an input written in place, never
+ *      rebuilt); "How it is meant to be run" (dynamic batch: rows share one
+ *      weight read; lengths are explicit, never inferred from shapes).
+ *
+ * Conventions
+ *  - Every call returns a uocr_status; uocr_last_error() gives the text of
+ *    the last failure on that context.  Calls on one context are serialised
+ *    by a per-context mutex; use one context per execution lane.
+ *  - The library owns all device memory it allocates (one arena sized at
+ *    uocr_create).  Pointers documented as "device" must point to device
+ *    memory of the context's GPU; "host" pointers are ordinary memory.
+ *  - Device work is enqueued on an internal stream ordered after the caller's
+ *    stream (uocr_config.stream, 0 = legacy default stream) and the caller's
+ *    stream is made to wait for it, so the calls are asynchronous with respect
+ *    to the host unless stated otherwise.
+ *  - Kernels never trap.  Invalid device-side inputs (a token id outside
+ *    [0, vocab), a negative position) set bits of a device status word that
+ *    uocr_sync() reports as UOCR_E_TOKEN / UOCR_E_POSITION; the offending
+ *    row uses id 0 / position 0 for that step.
+ */
+#ifndef UOCR_H
+#define UOCR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define UOCR_API __attribute__((visibility("default")))
+#else
+#define UOCR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  UOCR_OK = 0,
+  UOCR_E_INVALID_ARG = 1, /* a NULL pointer, a size or a config value out of range */
+  UOCR_E_OOM = 2,         /* device allocation failed */
+  UOCR_E_BUDGET = 3,      /* the working set exceeds uocr_config.mem_budget */
+  UOCR_E_FORMAT = 4,      /* weight tensor with wrong kind/format/shape/byte size */
+  UOCR_E_STATE = 5,       /* call not valid in the context's current state */
+  UOCR_E_CUDA = 6,        /* a CUDA runtime error (text in uocr_last_error) */
+  UOCR_E_POSITION = 7,    /* a device-side position was invalid */
+  UOCR_E_TOKEN = 8        /* a device-side token id was outside [0, vocab) */
+} uocr_status;
+
+/* Canonical weight formats.  Blocks hold 32 consecutive values of one row;
+ * blocks run along the row (K), rows follow each other.  fp16 little endian.
+ *   UOCR_F16     plain fp16 [rows][cols]
+ *   UOCR_Q8_0    {fp16 d; int8 q[32]}           34 B   value = d*q
+ *   UOCR_Q4_0    {fp16 d; uint8 qs[16]}         18 B   value = d*(q-8), q of
+ *                element j<16 = low nibble of qs[j], j>=16 = high nibble of qs[j-16]
+ *   UOCR_I8ASYM  {fp16 s; fp16 z; uint8 q[32]}  36 B   value = s*(q-z)      */
+typedef enum { UOCR_F16 = 0, UOCR_Q8_0 = 1, UOCR_Q4_0 = 2, UOCR_I8ASYM = 3 } uocr_format;
+
+/* Weight tensor kinds.  Shapes use H = hidden, S = n_heads*head_dim,
+ * I = dense_inter, Ie = expert_inter, E = n_experts, V = vocab.
+ * Matrices are [out_features][in_features] (y = W x).                       */
+typedef enum {
+  UOCR_T_EMBED = 0,         /* [V][H]   F16 only                     layer 0 */
+  UOCR_T_FINAL_NORM = 1,    /* [1][H]   F16                          layer 0 */
+  UOCR_T_LM_HEAD = 2,       /* [V][H]   F16 only                     layer 0 */
+  UOCR_T_ATTN_NORM = 3,     /* [1][H]   F16                                  */
+  UOCR_T_WQ = 4,            /* [S][H]   fmt_attn                             */
+  UOCR_T_WK = 5,            /* [S][H]   fmt_attn                             */
+  UOCR_T_WV = 6,            /* [S][H]   fmt_attn                             */
+  UOCR_T_WO = 7,            /* [H][S]   fmt_attn                             */
+  UOCR_T_MLP_NORM = 8,      /* [1][H]   F16                                  */
+  UOCR_T_GATE = 9,          /* [I][H]   fmt_dense      dense layers only     */
+  UOCR_T_UP = 10,           /* [I][H]   fmt_dense                            */
+  UOCR_T_DOWN = 11,         /* [H][I]   fmt_dense                            */
+  UOCR_T_ROUTER = 12,       /* [E][H]   F16 only       MoE layers only       */
+  UOCR_T_SHARED_GATE = 13,  /* [Ie][H]  fmt_shared     expert = shared index */
+  UOCR_T_SHARED_UP = 14,    /* [Ie][H]  fmt_shared                           */
+  UOCR_T_SHARED_DOWN = 15,  /* [H][Ie]  fmt_shared                           */
+  UOCR_T_EXPERT_GATE = 16,  /* [Ie][H]  fmt_routed     expert = routed index */
+  UOCR_T_EXPERT_UP = 17,    /* [Ie][H]  fmt_routed                           */
+  UOCR_T_EXPERT_DOWN = 18   /* [H][Ie]  fmt_routed                           */
+} uocr_tensor_kind;
+
+typedef struct {
+  /* model */
+  int32_t hidden;          /* H, multiple of 64                                  */
+  int32_t n_heads;
+  int32_t head_dim;        /* D, multiple of 16, <= 256                          */
+  int32_t n_layers;
+  int32_t n_dense_layers;  /* layers [0, n_dense_layers) use the dense MLP       */
+  int32_t dense_inter;     /* multiple of 64 (0 if no dense layer)               */
+  int32_t n_experts;       /* routed experts E (0 = every layer dense), <= 256   */
+  int32_t top_k;           /* 1..8                                               */
+  int32_t n_shared;        /* shared experts (weight 1 each), 0..4               */
+  int32_t expert_inter;    /* multiple of 64                                     */
+  int32_t vocab;           /* 0 = no embedding / LM head                         */
+  int32_t fmt_attn, fmt_dense, fmt_shared, fmt_routed; /* uocr_format           */
+  /* cache */
+  int32_t prefix_len;      /* P: slots [0, P) hold positions [0, P)              */
+  int32_t ring_len;        /* R: positions p >= P live in slot P + (p-P) mod R   */
+  int32_t max_rows;        /* rows of one step, 1..64                            */
+  int32_t use_sink;        /* 1: per-layer, per-head sink logit (uocr_set_sinks) */
+  float rms_eps;           /* RMSNorm epsilon                                    */
+  float rope_theta;        /* rotary base                                        */
+  /* runtime */
+  uint64_t mem_budget;     /* bytes; 0 = no limit                                */
+  void* stream;            /* cudaStream_t the calls are ordered with (0 = legacy) */
+  int32_t device;          /* CUDA device ordinal                                */
+  int32_t use_graphs;      /* 1: capture each step shape in a CUDA graph         */
+} uocr_config;
+
+typedef struct {
+  int32_t kind;     /* uocr_tensor_kind                                   */
+  int32_t layer;    /* 0..n_layers-1 (0 for global tensors)               */
+  int32_t expert;   /* routed or shared expert index, else 0              */
+  int32_t format;   /* uocr_format                                        */
+  int32_t rows;     /* out features                                       */
+  int32_t cols;     /* in features                                        */
+  const void* data; /* host pointer to the canonical bytes                */
+  uint64_t bytes;   /* byte size of data                                  */
+} uocr_tensor;
+
+/* Bytes per category (the Metal page's memory categories). */
+typedef struct {
+  uint64_t weights;      /* packed weights, norms, router, embedding, LM head  */
+  uint64_t kv_cache;     /* [layer][row][K|V][head][P+R][D] fp16               */
+  uint64_t activations;  /* residual stream, q, attention partials, MLP/expert scratch */
+  uint64_t routing;      /* router logits, top-k, counts, offsets, permutation */
+  uint64_t logits;       /* [max_rows][vocab] fp32 readback buffer             */
+  uint64_t total;        /* the arena allocated at uocr_create                 */
+} uocr_mem_report;
+
+typedef struct uocr_ctx uocr_ctx;
+
+/* Validate cfg, size the arena per category, compare it with cfg->mem_budget
+ * (UOCR_E_BUDGET with a per-category message when it does not fit), allocate
+ * it, zero the KV cache.  Launches no compute kernel.  *out receives the
+ * context (NULL on failure).  cfg is copied.                                 */
+UOCR_API uocr_status uocr_create(const uocr_config* cfg, uocr_ctx** out);
+
+/* Release everything; NULL-safe; the context must not be used afterwards.   */
+UOCR_API void uocr_destroy(uocr_ctx* ctx);
+
+/* Copy and pack weight tensors (host pointers, caller keeps ownership and may
+ * free them on return).  Tensors may come in any order and over several
+ * calls; a group (Q/K/V of a layer, gate/up of an MLP or expert, the shared
+ * experts of a layer) is packed once all its members have arrived.  Wrong
+ * kind, index, format, shape or byte size -> UOCR_E_FORMAT (nothing of that
+ * tensor is kept).  Synchronous.                                             */
+UOCR_API uocr_status uocr_load_weights(uocr_ctx* ctx, const uocr_tensor* t, size_t n);
+
+/* Write n cached prefix positions [start, start+n) of one row and layer.
+ * k, v: host fp16 [n_heads][n][head_dim].  Requires start+n <= prefix_len.
+ * Synchronous.                                                               */
+UOCR_API uocr_status uocr_kv_write_prefix(uocr_ctx* ctx, int32_t row, int32_t layer,
+                                 const uint16_t* k, const uint16_t* v,
+                                 int32_t start, int32_t n);
+
+/* Read back cache slots [slot0, slot0+n) of one row and layer into host fp16
+ * [n_heads][n][head_dim] buffers.  Synchronous.                               */
+UOCR_API uocr_status uocr_kv_read(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0,
+                         int32_t n, uint16_t* k, uint16_t* v);
+
+/* Per-layer, per-head sink logits, host fp32 [n_layers][n_heads]; they enter
+ * the softmax unscaled as one more key with value zero.  Synchronous.        */
+UOCR_API uocr_status uocr_set_sinks(uocr_ctx* ctx, const float* sinks);
+
+/* One decode step for rows 0..rows-1 (row i uses KV row i).
+ *   token_ids  device int32 [rows]  (embedding lookup; requires vocab > 0)
+ *   positions  device int32 [rows]  absolute positions; slot(p) is written
+ *              with the new key/value, then attention reads every slot whose
+ *              position q has q <= p and (q < P or q > p - R)
+ *   next_ids   device int32 [rows]  greedy argmax (lowest index on ties)
+ *   logits     device fp32 [rows][vocab] or NULL
+ * Asynchronous (see conventions).                                            */
+UOCR_API uocr_status uocr_decode_step(uocr_ctx* ctx, int32_t rows, const int32_t* token_ids,
+                             const int32_t* positions, int32_t* next_ids, float* logits);
+
+/* The same step fed with hidden vectors instead of token ids.
+ *   x         device fp16 [rows][hidden]
+ *   y         device fp32 [rows][hidden] or NULL: residual stream after the
+ *             last layer (before the final norm)
+ *   next_ids  device int32 [rows] or NULL (requires vocab > 0 when given)
+ *   logits    device fp32 [rows][vocab] or NULL                              */
+UOCR_API uocr_status uocr_decode_step_embeds(uocr_ctx* ctx, int32_t rows, const uint16_t* x,
+                                    const int32_t* positions, float* y,
+                                    int32_t* next_ids, float* logits);
+
+/* uocr_decode_step with HOST buffers: copies token_ids/positions to the
+ * device, runs the step, copies next_ids back, and returns when they are on
+ * the host.                                                                  */
+UOCR_API uocr_status uocr_decode_step_host(uocr_ctx* ctx, int32_t rows, const int32_t* token_ids,
+                                  const int32_t* positions, int32_t* next_ids);
+
+/* n_steps greedy steps chained on the device: step s uses positions+s and
+ * the ids produced by step s-1 (token_ids for s = 0).  out_ids: device int32
+ * [n_steps][rows].  Asynchronous.                                            */
+UOCR_API uocr_status uocr_generate(uocr_ctx* ctx, int32_t rows, const int32_t* token_ids,
+                          const int32_t* positions, int32_t n_steps, int32_t* out_ids);
+
+/* Zero the ring slots (and the prefix when keep_prefix == 0) of one row
+ * (row = -1: all rows).  Attention never reads a slot not written for the
+ * current sequence, so this is hygiene, not a correctness requirement.      */
+UOCR_API uocr_status uocr_kv_reset(uocr_ctx* ctx, int32_t row, int32_t keep_prefix);
+
+/* Wait for the context's work; report a device-side status raised since the
+ * last uocr_sync (UOCR_E_TOKEN, UOCR_E_POSITION) and clear it.               */
+UOCR_API uocr_status uocr_sync(uocr_ctx* ctx);
+
+/* Text of the last failure on ctx ("" if none); valid until the next call.
+ * uocr_last_error(NULL) gives the text of the last failed uocr_create on the
+ * calling thread.                                                            */
+UOCR_API const char* uocr_last_error(uocr_ctx* ctx);
+
+UOCR_API uocr_status uocr_memory_report(uocr_ctx* ctx, uocr_mem_report* out);
+
+/* Debug taps of the last completed step (synchronous, host outputs).
+ *   uocr_debug_hidden: fp32 [rows][hidden] residual stream at tap `layer`:
+ *     2*l   = after attention of layer l, 2*l+1 = output of layer l,
+ *     -1    = input of layer 0.
+ *   uocr_debug_router: MoE layer l: idx int32 [rows][k], w fp32 [rows][k],
+ *     count int32 [E], offset int32 [E+1], perm int32 [rows*k]; any output
+ *     may be NULL.                                                           */
+UOCR_API uocr_status uocr_debug_hidden(uocr_ctx* ctx, int32_t tap, int32_t rows, float* out);
+UOCR_API uocr_status uocr_debug_router(uocr_ctx* ctx, int32_t layer, int32_t rows, int32_t* idx,
+                              float* w, int32_t* count, int32_t* offset, int32_t* perm);
+
+/* Per-kernel-class device time (ms) of one un-graphed step with the given
+ * rows and input kind (0 = token ids, 1 = hidden vectors), measured with CUDA
+ * events; names[i] points into static storage.  n_inout: in = capacity,
+ * out = number of classes.  The step mutates the KV cache like a real step. */
+UOCR_API uocr_status uocr_profile(uocr_ctx* ctx, int32_t rows, int32_t input_kind,
+                         const int32_t* token_ids, const uint16_t* x, const int32_t* positions,
+                         const char** names, float* ms, int32_t* n_inout);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* UOCR_H */

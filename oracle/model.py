@@ -67,6 +67,11 @@ def swiglu(x, wg, wu, wd):
     return wd @ (silu(wg @ x) * (wu @ x))
 
 
+def swiglu_rows(X, wg, wu, wd):
+    """swiglu applied to every row of X (one matmul per projection)."""
+    return (silu(X @ wg.T) * (X @ wu.T)) @ wd.T
+
+
 def rope(v, pos, theta):
     """Rotate-half rotary embedding of v[..., D] at absolute position pos.
 
@@ -297,8 +302,7 @@ class OracleModel:
             res.h_attn[l] = Hh
             Hn = rmsnorm(Hh, self.w(T_MLP_NORM, l), cfg.rms_eps)
             if l < cfg.n_dense_layers or cfg.n_experts == 0:
-                Y = Hh + np.stack([swiglu(Hn[r], self.w(T_GATE, l), self.w(T_UP, l),
-                                          self.w(T_DOWN, l)) for r in range(rows)])
+                Y = Hh + swiglu_rows(Hn, self.w(T_GATE, l), self.w(T_UP, l), self.w(T_DOWN, l))
             else:
                 Y, info = self._moe(l, Hh, Hn)
                 res.router[l] = info
@@ -314,26 +318,33 @@ class OracleModel:
         return res
 
     def _moe(self, l, Hh, Hn):
+        """Router, top-k, weighted routed experts plus shared experts, residual.
+
+        Each expert is applied to all the rows that selected it with one
+        matmul; row r's result is still exactly sum_j w_rj * E_j(x_r).
+        """
         cfg = self.cfg
         rows, k, E = self.rows, cfg.top_k, cfg.n_experts
         Wr = self.w(T_ROUTER, l)
         logits = Hn @ Wr.T
         idx = np.zeros((rows, k), dtype=np.int64)
         wts = np.zeros((rows, k))
-        Y = np.zeros_like(Hh)
         for r in range(rows):
             idx[r], wts[r] = route(logits[r], k)
-            y = Hh[r].copy()
-            for j in range(k):
-                e = int(idx[r, j])
-                y += wts[r, j] * swiglu(Hn[r], self.w(T_EXPERT_GATE, l, e),
-                                        self.w(T_EXPERT_UP, l, e), self.w(T_EXPERT_DOWN, l, e))
-            for s in range(cfg.n_shared):
-                y += swiglu(Hn[r], self.w(T_SHARED_GATE, l, s), self.w(T_SHARED_UP, l, s),
-                            self.w(T_SHARED_DOWN, l, s))
-            Y[r] = y
+        Y = Hh.copy()
+        for e in range(E):
+            sel_r, sel_j = np.nonzero(idx == e)
+            if sel_r.size == 0:
+                continue
+            out = swiglu_rows(Hn[sel_r], self.w(T_EXPERT_GATE, l, e), self.w(T_EXPERT_UP, l, e),
+                              self.w(T_EXPERT_DOWN, l, e))
+            for i in range(sel_r.size):
+                Y[sel_r[i]] += wts[sel_r[i], sel_j[i]] * out[i]
+        for s in range(cfg.n_shared):
+            Y += swiglu_rows(Hn, self.w(T_SHARED_GATE, l, s), self.w(T_SHARED_UP, l, s),
+                             self.w(T_SHARED_DOWN, l, s))
         count, offset, perm = group_by_expert(idx, E)
-        # the 6th-vs-7th logit gap decides whether the selected set is well defined
+        # the k-th vs (k+1)-th logit gap decides whether the selected set is well defined
         srt = np.sort(logits, axis=-1)[:, ::-1]
         gap = srt[:, k - 1] - srt[:, k] if k < E else np.full(rows, np.inf)
         return Y, dict(logits=logits, idx=idx, w=wts, count=count, offset=offset,

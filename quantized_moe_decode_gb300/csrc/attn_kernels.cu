@@ -1,0 +1,393 @@
+// Split-K flash-decoding attention over the prefix + ring KV cache, and the
+// small kernels around the step (embedding gather, weight packer, ring reset).
+//
+// Attention ("Unlimited-OCR on Apple Silicon with C and Metal", "Il decoder e
+// il Mixture of Experts": KV append and a 128-token ring for generated
+// tokens; "Falcon-OCR INT8 OpenVINO IR", intro: the sink is one more key
+// whose logit is the sink and whose value is zero, and the cache is read in
+// place).  For a row at position p the valid slots are a contiguous range:
+// [0, p] while p < P, else [0, P + min(p - P + 1, R)) (every ring slot
+// written for this sequence; softmax does not care about their order).  CTA
+// (split, head, row) takes one chunk of that range; each warp streams 4*G
+// slots per iteration with 16-byte loads (D/8 lanes per slot) and keeps an
+// online softmax; the last CTA of a (row, head) merges the splits with their
+// log-sum-exp weights and the sink, and writes the fp16 output.
+#include <math.h>
+
+#include "launch.h"
+
+namespace uocr {
+
+template <int D>
+__global__ void __launch_bounds__(128) k_attn(const AttnArgs a) {
+  constexpr int LPS = D / 8;    // lanes per slot
+  constexpr int G = 32 / LPS;   // slots per load instruction
+  constexpr int SPI = 4 * G;    // slots per warp iteration
+  constexpr int NW = 4;
+  __shared__ float sm_m[NW], sm_l[NW];
+  __shared__ float sm_acc[NW][D];
+  __shared__ int s_last;
+
+  const int split = blockIdx.x, head = blockIdx.y, row = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane / LPS, li = lane % LPS;
+  int p = a.pos[row];
+  if (p < 0) p = 0;
+  const int n_valid = (p < a.P) ? p + 1 : a.P + min(p - a.P + 1, a.R);
+  const int s_begin = split * a.chunk;
+  const int s_end = min(n_valid, s_begin + a.chunk);
+
+  float qv[8];
+  {
+    const float* qp = a.q + ((size_t)row * a.nh + head) * D + 8 * li;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qv[i] = qp[i] * a.scale;
+  }
+  const __half* Kb = a.kv + (((size_t)row * 2 + 0) * a.nh + head) * (size_t)a.SL * D + 8 * li;
+  const __half* Vb = a.kv + (((size_t)row * 2 + 1) * a.nh + head) * (size_t)a.SL * D + 8 * li;
+
+  float m = -INFINITY, l = 0.f;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+
+  for (int base = s_begin + warp * SPI; base < s_end; base += NW * SPI) {
+    uint4 kr[4], vr[4];
+    bool ok[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int slot = base + j * G + grp;
+      ok[j] = slot < s_end;
+      if (ok[j]) {
+        kr[j] = ldg_stream(Kb + (size_t)slot * D);
+        vr[j] = ldg_stream(Vb + (size_t)slot * D);
+      } else {
+        kr[j] = make_uint4(0u, 0u, 0u, 0u);
+        vr[j] = kr[j];
+      }
+    }
+    float sc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2* kh = reinterpret_cast<const __half2*>(&kr[j]);
+      float d = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(kh[i]);
+        d = fmaf(qv[2 * i], f.x, d);
+        d = fmaf(qv[2 * i + 1], f.y, d);
+      }
+#pragma unroll
+      for (int o = LPS / 2; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      sc[j] = ok[j] ? d : -INFINITY;
+    }
+    float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+#pragma unroll
+    for (int o = LPS; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float m_new = fmaxf(m, mx);  // finite: slot `base` is valid
+    const float corr = __expf(m - m_new);
+    float ps = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] *= corr;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float pj = ok[j] ? __expf(sc[j] - m_new) : 0.f;
+      ps += pj;
+      const __half2* vh = reinterpret_cast<const __half2*>(&vr[j]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(vh[i]);
+        acc[2 * i] = fmaf(pj, f.x, acc[2 * i]);
+        acc[2 * i + 1] = fmaf(pj, f.y, acc[2 * i + 1]);
+      }
+    }
+#pragma unroll
+    for (int o = LPS; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+    l = l * corr + ps;
+    m = m_new;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+#pragma unroll
+    for (int o = LPS; o < 32; o <<= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+  }
+  if (lane == 0) {
+    sm_m[warp] = m;
+    sm_l[warp] = l;
+  }
+  if (grp == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sm_acc[warp][8 * li + i] = acc[i];
+  }
+  __syncthreads();
+
+  // CTA merge -> split partial {m, l, acc[D]}
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w]);
+  float* part = a.part + (((size_t)row * a.nh + head) * a.nsplit + split) * (D + 2);
+  float wsc[NW];
+#pragma unroll
+  for (int w = 0; w < NW; ++w) wsc[w] = (M == -INFINITY) ? 0.f : __expf(sm_m[w] - M);
+  if (threadIdx.x == 0) {
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) L += sm_l[w] * wsc[w];
+    part[0] = M;
+    part[1] = L;
+  }
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) v += sm_acc[w][d] * wsc[w];
+    part[2 + d] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    int* ctr = a.counter + row * a.nh + head;
+    const int done = atomicAdd(ctr, 1);
+    s_last = (done == a.nsplit - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const float* pbase = a.part + ((size_t)row * a.nh + head) * a.nsplit * (D + 2);
+  float Mt = a.sink ? a.sink[head] : -INFINITY;
+  for (int sp = 0; sp < a.nsplit; ++sp) Mt = fmaxf(Mt, __ldcg(pbase + (size_t)sp * (D + 2)));
+  float Lt = a.sink ? __expf(a.sink[head] - Mt) : 0.f;
+  for (int sp = 0; sp < a.nsplit; ++sp) {
+    const float ms = __ldcg(pbase + (size_t)sp * (D + 2));
+    if (ms != -INFINITY) Lt += __ldcg(pbase + (size_t)sp * (D + 2) + 1) * __expf(ms - Mt);
+  }
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float v = 0.f;
+    for (int sp = 0; sp < a.nsplit; ++sp) {
+      const float ms = __ldcg(pbase + (size_t)sp * (D + 2));
+      if (ms != -INFINITY) v += __ldcg(pbase + (size_t)sp * (D + 2) + 2 + d) * __expf(ms - Mt);
+    }
+    a.out[(size_t)row * a.nh * D + head * D + d] = __float2half_rn(v / Lt);
+  }
+  if (threadIdx.x == 0) atomicExch(a.counter + row * a.nh + head, 0);
+}
+
+cudaError_t launch_attn(const AttnArgs& a, int rows, cudaStream_t st) {
+  const dim3 grid(a.nsplit, a.nh, rows);
+  switch (a.D) {
+    case 16: k_attn<16><<<grid, 128, 0, st>>>(a); break;
+    case 32: k_attn<32><<<grid, 128, 0, st>>>(a); break;
+    case 64: k_attn<64><<<grid, 128, 0, st>>>(a); break;
+    case 128: k_attn<128><<<grid, 128, 0, st>>>(a); break;
+    case 256: k_attn<256><<<grid, 128, 0, st>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ embedding
+// Token ids -> fp16 embedding row, or the given fp16 hidden vectors, widened
+// into the fp32 residual stream; validates ids and positions.
+__global__ void k_embed(const EmbedArgs a) {
+  const int row = blockIdx.x;
+  const __half* src;
+  if (a.ids) {
+    int id = a.ids[row];
+    if (id < 0 || id >= a.V) {
+      if (threadIdx.x == 0) atomicOr(a.status, kStatusToken);
+      id = 0;
+    }
+    src = a.emb + (size_t)id * a.H;
+  } else {
+    src = a.x + (size_t)row * a.H;
+  }
+  if (threadIdx.x == 0 && a.pos[row] < 0) atomicOr(a.status, kStatusPosition);
+  for (int k = threadIdx.x * 2; k < a.H; k += blockDim.x * 2) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(src + k));
+    a.out[(size_t)row * a.H + k] = f.x;
+    a.out[(size_t)row * a.H + k + 1] = f.y;
+  }
+}
+
+cudaError_t launch_embed(const EmbedArgs& a, int rows, cudaStream_t st) {
+  k_embed<<<rows, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ packer
+// Canonical blocks -> fragment-ordered device layout (see device_common.cuh).
+// One thread per (slab, unit, lane); packed row pr maps to (source, row) by
+// the matrix's row map: identity, Q/K/V sections with the rotary pairs (i,
+// i + D/2) placed in rows g and g + 8 of one slab, interleaved gate/up rows
+// (gate in rows 0..7 of a slab, up in 8..15) over one or more experts, or
+// column concatenation of several experts (shared down projections).
+struct PackSrcRef {
+  int src;  // -1: zero padding
+  int row;
+};
+
+__device__ __forceinline__ PackSrcRef pack_row(const PackArgs& a, int pr) {
+  PackSrcRef r{-1, 0};
+  switch (a.map) {
+    case MAP_IDENT:
+    case MAP_KCAT:
+      if (pr < a.src_rows) r = {0, pr};
+      break;
+    case MAP_QKV: {
+      const int sec = pr / a.S, w = pr - sec * a.S;
+      const int head = w / a.D, wi = w - head * a.D;
+      const int js = wi >> 4, j = wi & 15;
+      const int dim = j < 8 ? 8 * js + j : (a.D >> 1) + 8 * js + (j - 8);
+      if (sec < a.nsrc) r = {sec, head * a.D + dim};
+      break;
+    }
+    case MAP_SWIGLU: {
+      const int s = pr >> 4, j = pr & 15;
+      const int gr = 8 * s + (j & 7);
+      const int ex = gr / a.I;
+      const int src = 2 * ex + (j < 8 ? 0 : 1);
+      if (src < a.nsrc) r = {src, gr - ex * a.I};
+      break;
+    }
+  }
+  return r;
+}
+
+// code and scale fetch from canonical blocks; k is the packed column
+struct Code {
+  const uint8_t* blk;
+  int j;
+};
+
+__device__ __forceinline__ Code locate(const PackArgs& a, PackSrcRef r, int k) {
+  int src = r.src, kk = k;
+  if (a.map == MAP_KCAT) {
+    src = k / a.I;
+    kk = k - src * a.I;
+  }
+  const int bb = a.fmt == Q8_0 ? 34 : (a.fmt == Q4_0 ? 18 : 36);
+  const uint8_t* blk = a.src[src] + ((size_t)r.row * (a.src_cols / 32) + kk / 32) * bb;
+  return Code{blk, kk & 31};
+}
+
+__device__ __forceinline__ uint32_t get_code(const PackArgs& a, PackSrcRef r, int k) {
+  if (r.src < 0) return a.fmt == Q4_0 ? 8u : 0u;
+  const Code c = locate(a, r, k);
+  if (a.fmt == Q8_0) return c.blk[2 + c.j];
+  if (a.fmt == Q4_0) return c.j < 16 ? (c.blk[2 + c.j] & 0xF) : (c.blk[2 + c.j - 16] >> 4);
+  return c.blk[4 + c.j];  // I8ASYM
+}
+
+__device__ __forceinline__ uint16_t get_half(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+__device__ __forceinline__ uint16_t get_f16(const PackArgs& a, PackSrcRef r, int k) {
+  if (r.src < 0) return 0;
+  int src = r.src, kk = k;
+  if (a.map == MAP_KCAT) {
+    src = k / a.I;
+    kk = k - src * a.I;
+  }
+  return get_half(a.src[src] + ((size_t)r.row * a.src_cols + kk) * 2);
+}
+
+__device__ __forceinline__ uint16_t get_scale(const PackArgs& a, PackSrcRef r, int k, int which) {
+  if (r.src < 0) return 0;
+  const Code c = locate(a, r, k);
+  return get_half(c.blk + 2 * which);
+}
+
+__global__ void k_pack(const PackArgs a) {
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long total = (long long)a.n_slabs * a.U * 32;
+  if (gid >= total) return;
+  const int lane = (int)(gid & 31);
+  const long long su = gid >> 5;
+  const int u = (int)(su % a.U);
+  const int slab = (int)(su / a.U);
+  const int g = lane >> 2, t = lane & 3;
+  const PackSrcRef r0 = pack_row(a, 16 * slab + g);
+  const PackSrcRef r1 = pack_row(a, 16 * slab + g + 8);
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  if (a.fmt == F16) {
+    const int kk = u * 16 + 2 * t;
+    w[0] = get_f16(a, r0, kk) | ((uint32_t)get_f16(a, r0, kk + 1) << 16);
+    w[1] = get_f16(a, r1, kk) | ((uint32_t)get_f16(a, r1, kk + 1) << 16);
+    w[2] = get_f16(a, r0, kk + 8) | ((uint32_t)get_f16(a, r0, kk + 9) << 16);
+    w[3] = get_f16(a, r1, kk + 8) | ((uint32_t)get_f16(a, r1, kk + 9) << 16);
+  } else if (a.fmt == Q4_0) {
+    for (int ks = 0; ks < 4; ++ks) {
+      const int kk = u * 64 + 16 * ks + 2 * t;
+      const uint32_t c0 = get_code(a, r0, kk), c1 = get_code(a, r0, kk + 1);
+      const uint32_t c2 = get_code(a, r1, kk), c3 = get_code(a, r1, kk + 1);
+      const uint32_t c4 = get_code(a, r0, kk + 8), c5 = get_code(a, r0, kk + 9);
+      const uint32_t c6 = get_code(a, r1, kk + 8), c7 = get_code(a, r1, kk + 9);
+      w[ks] = c0 | (c2 << 4) | (c4 << 8) | (c6 << 12) | (c1 << 16) | (c3 << 20) | (c5 << 24) | (c7 << 28);
+    }
+  } else {  // Q8_0, I8ASYM: byte order a0..a7 per k-step
+    for (int ks = 0; ks < 2; ++ks) {
+      const int kk = u * 32 + 16 * ks + 2 * t;
+      const uint32_t c0 = get_code(a, r0, kk), c1 = get_code(a, r0, kk + 1);
+      const uint32_t c2 = get_code(a, r1, kk), c3 = get_code(a, r1, kk + 1);
+      const uint32_t c4 = get_code(a, r0, kk + 8), c5 = get_code(a, r0, kk + 9);
+      const uint32_t c6 = get_code(a, r1, kk + 8), c7 = get_code(a, r1, kk + 9);
+      w[2 * ks] = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+      w[2 * ks + 1] = c4 | (c5 << 8) | (c6 << 16) | (c7 << 24);
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(a.q + ((size_t)slab * a.U + u) * kUnitBytes + lane * 16);
+  *dst = make_uint4(w[0], w[1], w[2], w[3]);
+  if (t == 0 && a.fmt != F16) {
+    const size_t unit = (size_t)slab * a.U + u;
+    if (a.fmt == Q8_0) {
+      uint16_t* sp = reinterpret_cast<uint16_t*>(a.s + unit * 32 + g * 4);
+      sp[0] = get_scale(a, r0, u * 32, 0);
+      sp[1] = get_scale(a, r1, u * 32, 0);
+    } else if (a.fmt == Q4_0) {
+      uint16_t* sp = reinterpret_cast<uint16_t*>(a.s + unit * 64 + g * 8);
+      sp[0] = get_scale(a, r0, u * 64, 0);
+      sp[1] = get_scale(a, r1, u * 64, 0);
+      sp[2] = get_scale(a, r0, u * 64 + 32, 0);
+      sp[3] = get_scale(a, r1, u * 64 + 32, 0);
+    } else {
+      uint16_t* sp = reinterpret_cast<uint16_t*>(a.s + unit * 64 + g * 8);
+      sp[0] = get_scale(a, r0, u * 32, 0);
+      sp[1] = get_scale(a, r1, u * 32, 0);
+      sp[2] = get_scale(a, r0, u * 32, 1);
+      sp[3] = get_scale(a, r1, u * 32, 1);
+    }
+  }
+}
+
+cudaError_t launch_pack(const PackArgs& a, cudaStream_t st) {
+  const long long total = (long long)a.n_slabs * a.U * 32;
+  const int blocks = (int)((total + 255) / 256);
+  k_pack<<<blocks, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ reset
+__global__ void k_zero_slots(__half* base, long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    base[i] = __float2half_rn(0.f);
+}
+
+// Zero slots [from_slot, SL) of every head of both K and V of one (layer, row).
+cudaError_t launch_fill_zero_ring(__half* kv_layer_row, int nh, int SL, int D, int from_slot, cudaStream_t st) {
+  for (int kvh = 0; kvh < 2 * nh; ++kvh) {
+    __half* b = kv_layer_row + ((size_t)kvh * SL + from_slot) * D;
+    const long long n = (long long)(SL - from_slot) * D;
+    if (n <= 0) continue;
+    k_zero_slots<<<(int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024), 256, 0, st>>>(b, n);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t init_gemv_attributes();
+cudaError_t init_moe_attributes();
+
+cudaError_t init_kernel_attributes() {
+  cudaError_t e = init_gemv_attributes();
+  if (e == cudaSuccess) e = init_moe_attributes();
+  return e;
+}
+
+}  // namespace uocr

@@ -1,0 +1,1170 @@
+// Host side of the library: configuration checks, the per-category memory
+// plan and its single device arena, weight loading and packing, the launch
+// sequence of one decode step (captured once per step shape into a CUDA
+// graph), and the C ABI declared in include/uocr.h.
+//
+// Memory categories and the budget check follow "Unlimited-OCR on Apple
+// Silicon with C and Metal", "Memoria: il vincolo principale" (every buffer
+// belongs to a category; the working set is estimated per category and
+// compared with the configured budget before running; a request that does
+// not fit is refused with a detailed error).  The per-context lock follows
+// "Dall'ABI C all'API Python" (one lock per engine, one instance per lane).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "launch.h"
+#include "uocr.h"
+
+using namespace uocr;
+
+namespace {
+
+struct DMat {
+  uint8_t* q = nullptr;
+  uint8_t* s = nullptr;
+  int fmt = 0, n_slabs = 0, U = 0, K = 0;
+  size_t qbytes = 0, sbytes = 0;  // of one matrix (one expert for expert arrays)
+  PMat view(int n_experts_stride = 0) const {
+    PMat p;
+    p.q = q;
+    p.s = s;
+    p.n_slabs = n_slabs;
+    p.U = U;
+    p.K = K;
+    p.q_stride = n_experts_stride ? (long long)qbytes : 0;
+    p.s_stride = n_experts_stride ? (long long)sbytes : 0;
+    return p;
+  }
+};
+
+size_t packed_q_bytes(int n_rows_packed, int K, int fmt) {
+  const size_t slabs = (size_t)(n_rows_packed + 15) / 16;
+  return slabs * (K / unit_k(fmt)) * kUnitBytes;
+}
+size_t packed_s_bytes(int n_rows_packed, int K, int fmt) {
+  const size_t slabs = (size_t)(n_rows_packed + 15) / 16;
+  return slabs * (K / unit_k(fmt)) * unit_scale_bytes(fmt);
+}
+size_t blob_bytes(int fmt, int rows, int cols) {
+  if (fmt == F16) return (size_t)rows * cols * 2;
+  const int bb = fmt == Q8_0 ? 34 : (fmt == Q4_0 ? 18 : 36);
+  return (size_t)rows * (cols / 32) * bb;
+}
+
+struct LayerW {
+  DMat qkv, o, gateup, down, router, sh_gateup, sh_down, ex_gateup, ex_down;
+  __half* attn_norm = nullptr;
+  __half* mlp_norm = nullptr;
+  float* sink = nullptr;
+  bool dense = true;
+};
+
+// bump allocator over the arena, with a measuring pass
+struct Carver {
+  char* base = nullptr;
+  size_t off = 0;
+  template <class T>
+  T* take(size_t count, uint64_t& cat) {
+    const size_t bytes = ((count * sizeof(T)) + 255) / 256 * 256;
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += bytes;
+    cat += bytes;
+    return p;
+  }
+};
+
+constexpr int kMaxSplits = 32;
+thread_local std::string g_create_err;  // text of the last failed uocr_create on this thread
+constexpr int kHistCap = 1024;
+
+enum Group : int { G_SINGLE = 0, G_QKV, G_DENSE_GU, G_SHARED_GU, G_SHARED_DOWN, G_EXPERT_GU };
+
+struct Pending {
+  std::vector<void*> dev;  // staged canonical blobs (device), by member index
+  int have = 0;
+};
+
+}  // namespace
+
+struct uocr_ctx {
+  uocr_config cfg{};
+  std::mutex mu;
+  std::string err;
+  int n_sm = 148;
+  cudaStream_t st = nullptr;
+  cudaStream_t ust = nullptr;
+  cudaEvent_t ev_in = nullptr, ev_out = nullptr;
+  char* arena = nullptr;
+  uocr_mem_report rep{};
+  std::vector<LayerW> L;
+  __half* emb = nullptr;
+  __half* final_norm = nullptr;
+  DMat lm;
+  double* inv_freq = nullptr;
+  __half* kv = nullptr;
+  size_t kv_layer = 0;  // elements per layer
+  int S = 0, SL = 0;
+  float* hid = nullptr;  // [2L+1][MR][H]
+  __half* x_in = nullptr;
+  float* q = nullptr;
+  __half* attn_out = nullptr;
+  float* attn_part = nullptr;
+  int* attn_counter = nullptr;
+  __half* act_dense = nullptr;
+  __half* xhat = nullptr;
+  __half* act_r = nullptr;
+  __half* act_s = nullptr;
+  float* part_r = nullptr;
+  float* part_s = nullptr;
+  int* slab_counter = nullptr;
+  float* r_logits = nullptr;
+  int *r_idx = nullptr, *r_count = nullptr, *r_offset = nullptr, *r_perm = nullptr, *r_inv = nullptr;
+  int *r_active = nullptr, *r_nactive = nullptr, *r_counter = nullptr;
+  float* r_w = nullptr;
+  float* sinks = nullptr;
+  float* logits = nullptr;
+  unsigned long long* keys = nullptr;
+  int *lm_counter = nullptr, *next_ids = nullptr, *ids_buf = nullptr, *pos_buf = nullptr;
+  int *hist = nullptr, *hist_ctr = nullptr, *status = nullptr;
+  // loading
+  std::map<std::vector<int>, bool> loaded;  // (kind, layer, expert) -> present
+  std::map<std::vector<int>, Pending> pending;
+  bool sinks_set = false;
+  // graphs
+  std::map<uint64_t, cudaGraphExec_t> graphs;
+
+  int H() const { return cfg.hidden; }
+  int MR() const { return cfg.max_rows; }
+  bool layer_dense(int l) const { return l < cfg.n_dense_layers || cfg.n_experts == 0; }
+  bool any_moe() const {
+    for (int l = 0; l < cfg.n_layers; ++l)
+      if (!layer_dense(l)) return true;
+    return false;
+  }
+  int shared_fmt() const { return cfg.n_shared > 0 ? cfg.fmt_shared : cfg.fmt_routed; }
+
+  uocr_status fail(uocr_status s, const char* fmt, ...) {
+    char buf[1024];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    err = buf;
+    return s;
+  }
+  uocr_status cuda(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return UOCR_OK;
+    return fail(UOCR_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  }
+};
+
+#define CK(expr, what)                                        \
+  do {                                                        \
+    uocr_status _s = ctx->cuda((expr), what);                 \
+    if (_s != UOCR_OK) return _s;                             \
+  } while (0)
+
+// ------------------------------------------------------------------ config
+static bool fmt_ok(int f) { return f >= UOCR_F16 && f <= UOCR_I8ASYM; }
+static bool quant_fmt(int f) { return f == UOCR_Q8_0 || f == UOCR_Q4_0 || f == UOCR_I8ASYM; }
+static bool expert_pair_ok(int fr, int fs) {
+  return (fr == Q8_0 && fs == Q8_0) || (fr == Q4_0 && fs == Q8_0) || (fr == Q4_0 && fs == Q4_0) ||
+         (fr == Q8_0 && fs == Q4_0) || (fr == I8ASYM && fs == I8ASYM);
+}
+
+static uocr_status check_config(uocr_ctx* ctx, const uocr_config& c) {
+  auto bad = [&](const char* m) { return ctx->fail(UOCR_E_INVALID_ARG, "invalid config: %s", m); };
+  if (c.hidden <= 0 || c.hidden % 64) return bad("hidden must be a positive multiple of 64");
+  if (c.n_heads <= 0) return bad("n_heads must be positive");
+  if (!(c.head_dim == 16 || c.head_dim == 32 || c.head_dim == 64 || c.head_dim == 128 || c.head_dim == 256))
+    return bad("head_dim must be 16, 32, 64, 128 or 256");
+  if ((c.n_heads * c.head_dim) % 64) return bad("n_heads*head_dim must be a multiple of 64");
+  if (c.n_layers <= 0 || c.n_dense_layers < 0 || c.n_dense_layers > c.n_layers) return bad("layer counts");
+  if (c.n_experts < 0 || c.n_experts > 256) return bad("n_experts must be in [0, 256]");
+  const bool has_dense = c.n_dense_layers > 0 || c.n_experts == 0;
+  const bool has_moe = c.n_experts > 0 && c.n_layers > c.n_dense_layers;
+  if (has_dense && (c.dense_inter <= 0 || c.dense_inter % 64)) return bad("dense_inter must be a positive multiple of 64");
+  if (!fmt_ok(c.fmt_attn) || !fmt_ok(c.fmt_dense) || !fmt_ok(c.fmt_shared) || !fmt_ok(c.fmt_routed))
+    return bad("unknown weight format");
+  if (has_moe) {
+    if (c.top_k < 1 || c.top_k > 8 || c.top_k > c.n_experts) return bad("top_k must be in [1, min(8, n_experts)]");
+    if (c.expert_inter <= 0 || c.expert_inter % 64) return bad("expert_inter must be a positive multiple of 64");
+    if (c.n_shared < 0 || c.n_shared > 4) return bad("n_shared must be in [0, 4]");
+    const int fs = c.n_shared > 0 ? c.fmt_shared : c.fmt_routed;
+    if (!quant_fmt(c.fmt_routed) || !expert_pair_ok(c.fmt_routed, fs))
+      return bad("unsupported (routed, shared) expert format pair");
+    const StagePlan sp = plan_stage(2, c.hidden, I8ASYM);
+    if (sp.kc < c.hidden) return bad("hidden too large for the expert kernels");
+    if (plan_stage(2, c.n_shared * c.expert_inter, I8ASYM).kc < c.n_shared * c.expert_inter ||
+        plan_stage(2, c.expert_inter, I8ASYM).kc < c.expert_inter)
+      return bad("expert_inter too large for the expert kernels");
+  }
+  if (c.vocab < 0) return bad("vocab must be >= 0");
+  if (c.prefix_len < 0 || c.ring_len < 1) return bad("prefix_len >= 0 and ring_len >= 1 required");
+  if ((long long)c.prefix_len + c.ring_len > (1 << 24)) return bad("cache too long");
+  if (c.max_rows < 1 || c.max_rows > 64) return bad("max_rows must be in [1, 64]");
+  if (c.use_sink != 0 && c.use_sink != 1) return bad("use_sink must be 0 or 1");
+  if (!(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f)) return bad("rms_eps >= 0 and rope_theta > 0 required");
+  return UOCR_OK;
+}
+
+// ------------------------------------------------------------------ memory plan
+static void carve(uocr_ctx* ctx, Carver& cv) {
+  const uocr_config& c = ctx->cfg;
+  uocr_mem_report& r = ctx->rep;
+  r = uocr_mem_report{};
+  const int H = c.hidden, S = c.n_heads * c.head_dim, MR = c.max_rows, Lc = c.n_layers, V = c.vocab;
+  const int E = c.n_experts, k = c.top_k, Ie = c.expert_inter, Ish = c.n_shared * c.expert_inter;
+  auto mat = [&](DMat& m, int rows_packed, int K, int fmt, int count = 1) {
+    m.fmt = fmt;
+    m.K = K;
+    m.U = K / unit_k(fmt);
+    m.n_slabs = (rows_packed + 15) / 16;
+    m.qbytes = packed_q_bytes(rows_packed, K, fmt);
+    m.sbytes = packed_s_bytes(rows_packed, K, fmt);
+    m.q = cv.take<uint8_t>(m.qbytes * count, r.weights);
+    m.s = m.sbytes ? cv.take<uint8_t>(m.sbytes * count, r.weights) : nullptr;
+  };
+  ctx->L.assign(Lc, LayerW{});
+  for (int l = 0; l < Lc; ++l) {
+    LayerW& w = ctx->L[l];
+    w.dense = ctx->layer_dense(l);
+    mat(w.qkv, 3 * S, H, c.fmt_attn);
+    mat(w.o, H, S, c.fmt_attn);
+    w.attn_norm = cv.take<__half>(H, r.weights);
+    w.mlp_norm = cv.take<__half>(H, r.weights);
+    if (w.dense) {
+      mat(w.gateup, 2 * c.dense_inter, H, c.fmt_dense);
+      mat(w.down, H, c.dense_inter, c.fmt_dense);
+    } else {
+      mat(w.router, E, H, F16);
+      if (c.n_shared > 0) {
+        mat(w.sh_gateup, 2 * Ish, H, c.fmt_shared);
+        mat(w.sh_down, H, Ish, c.fmt_shared);
+      }
+      mat(w.ex_gateup, 2 * Ie, H, c.fmt_routed, E);
+      mat(w.ex_down, H, Ie, c.fmt_routed, E);
+    }
+  }
+  if (V > 0) {
+    ctx->emb = cv.take<__half>((size_t)V * H, r.weights);
+    ctx->final_norm = cv.take<__half>(H, r.weights);
+    mat(ctx->lm, V, H, F16);
+  }
+  ctx->inv_freq = cv.take<double>(c.head_dim / 2, r.weights);
+  ctx->sinks = cv.take<float>((size_t)Lc * c.n_heads, r.weights);
+  // KV cache [L][MR][2][nh][SL][D]
+  ctx->S = S;
+  ctx->SL = c.prefix_len + c.ring_len;
+  ctx->kv_layer = (size_t)MR * 2 * c.n_heads * ctx->SL * c.head_dim;
+  ctx->kv = cv.take<__half>(ctx->kv_layer * Lc, r.kv_cache);
+  // activations
+  ctx->hid = cv.take<float>((size_t)(2 * Lc + 1) * MR * H, r.activations);
+  ctx->x_in = cv.take<__half>((size_t)MR * H, r.activations);
+  ctx->q = cv.take<float>((size_t)MR * S, r.activations);
+  ctx->attn_out = cv.take<__half>((size_t)MR * S, r.activations);
+  ctx->attn_part = cv.take<float>((size_t)MR * c.n_heads * kMaxSplits * (c.head_dim + 2), r.activations);
+  ctx->attn_counter = cv.take<int>((size_t)MR * c.n_heads, r.activations);
+  if (c.n_dense_layers > 0 || E == 0) ctx->act_dense = cv.take<__half>((size_t)MR * c.dense_inter, r.activations);
+  if (ctx->any_moe()) {
+    ctx->xhat = cv.take<__half>((size_t)MR * H, r.activations);
+    ctx->act_r = cv.take<__half>((size_t)MR * k * Ie, r.activations);
+    ctx->act_s = cv.take<__half>((size_t)MR * (Ish > 0 ? Ish : 1), r.activations);
+    ctx->part_r = cv.take<float>((size_t)MR * k * H, r.activations);
+    ctx->part_s = cv.take<float>((size_t)MR * H, r.activations);
+    ctx->slab_counter = cv.take<int>(H / 16, r.activations);
+    ctx->r_logits = cv.take<float>((size_t)Lc * MR * E, r.routing);
+    ctx->r_idx = cv.take<int>((size_t)Lc * MR * k, r.routing);
+    ctx->r_w = cv.take<float>((size_t)Lc * MR * k, r.routing);
+    ctx->r_count = cv.take<int>((size_t)Lc * E, r.routing);
+    ctx->r_offset = cv.take<int>((size_t)Lc * (E + 1), r.routing);
+    ctx->r_perm = cv.take<int>((size_t)Lc * MR * k, r.routing);
+    ctx->r_inv = cv.take<int>((size_t)Lc * MR * k, r.routing);
+    ctx->r_active = cv.take<int>((size_t)Lc * E, r.routing);
+    ctx->r_nactive = cv.take<int>((size_t)Lc, r.routing);
+    ctx->r_counter = cv.take<int>(1, r.routing);
+  }
+  if (V > 0) {
+    ctx->logits = cv.take<float>((size_t)MR * V, r.logits);
+    ctx->keys = cv.take<unsigned long long>(MR, r.logits);
+    ctx->lm_counter = cv.take<int>(1, r.logits);
+  }
+  ctx->next_ids = cv.take<int>(MR, r.activations);
+  ctx->ids_buf = cv.take<int>(MR, r.activations);
+  ctx->pos_buf = cv.take<int>(MR, r.activations);
+  ctx->hist = cv.take<int>((size_t)kHistCap * MR, r.activations);
+  ctx->hist_ctr = cv.take<int>(1, r.activations);
+  ctx->status = cv.take<int>(1, r.activations);
+  r.total = cv.off;
+}
+
+// ------------------------------------------------------------------ step
+namespace {
+
+struct Prof {
+  std::vector<std::pair<const char*, std::pair<cudaEvent_t, cudaEvent_t>>> ev;
+};
+
+struct StepShape {
+  int rows;
+  bool ids;     // input: token ids (else hidden vectors)
+  bool lm;      // run the LM head + argmax
+  bool logits;  // store logits
+  bool chain;   // feed the argmax into the next step (uocr_generate)
+};
+
+}  // namespace
+
+static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) {
+  const uocr_config& c = ctx->cfg;
+  cudaStream_t st = ctx->st;
+  const int H = c.hidden, S = ctx->S, MR = ctx->MR(), rows = sh.rows;
+  const int nt = rows <= 8 ? 1 : 2;
+  const int tg = (rows + nt * 8 - 1) / (nt * 8);
+  const int G = 4 * ctx->n_sm;
+  auto gx_for = [&](int slabs) {
+    int g = G / tg;
+    if (g < 1) g = 1;
+    return slabs < g ? slabs : g;
+  };
+  auto mark = [&](const char* name, bool begin) {
+    if (!prof) return;
+    if (begin) {
+      cudaEvent_t a, b;
+      cudaEventCreate(&a);
+      cudaEventCreate(&b);
+      cudaEventRecord(a, st);
+      prof->ev.push_back({name, {a, b}});
+    } else {
+      cudaEventRecord(prof->ev.back().second.second, st);
+    }
+  };
+  auto hid = [&](int idx) { return ctx->hid + (size_t)idx * MR * H; };
+
+  EmbedArgs ea{};
+  ea.ids = sh.ids ? ctx->ids_buf : nullptr;
+  ea.x = ctx->x_in;
+  ea.emb = ctx->emb;
+  ea.pos = ctx->pos_buf;
+  ea.out = hid(0);
+  ea.H = H;
+  ea.V = c.vocab;
+  ea.status = ctx->status;
+  mark("embed", true);
+  CK(launch_embed(ea, rows, st), "embed launch");
+  mark("embed", false);
+
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerW& w = ctx->L[l];
+    __half* kvl = ctx->kv + ctx->kv_layer * l;
+    // QKV + RoPE + in-place KV append
+    GemvArgs qa{};
+    qa.w = w.qkv.view();
+    qa.sp = plan_stage(nt, H, c.fmt_attn);
+    qa.ntok = rows;
+    qa.xf = hid(2 * l);
+    qa.ld_src = H;
+    qa.norm_w = w.attn_norm;
+    qa.eps = c.rms_eps;
+    qa.pos = ctx->pos_buf;
+    qa.q_out = ctx->q;
+    qa.kv = kvl;
+    qa.inv_freq = ctx->inv_freq;
+    qa.nh = c.n_heads;
+    qa.D = c.head_dim;
+    qa.S = S;
+    qa.P = c.prefix_len;
+    qa.R = c.ring_len;
+    qa.SL = ctx->SL;
+    qa.status = ctx->status;
+    mark("qkv", true);
+    CK(launch_gemv(c.fmt_attn, SRC_NORM, EPI_QKV, qa, gx_for(w.qkv.n_slabs), tg, st), "qkv launch");
+    mark("qkv", false);
+    // attention
+    AttnArgs aa{};
+    aa.q = ctx->q;
+    aa.kv = kvl;
+    aa.pos = ctx->pos_buf;
+    aa.part = ctx->attn_part;
+    aa.counter = ctx->attn_counter;
+    aa.out = ctx->attn_out;
+    aa.sink = c.use_sink ? ctx->sinks + (size_t)l * c.n_heads : nullptr;
+    aa.nh = c.n_heads;
+    aa.D = c.head_dim;
+    aa.P = c.prefix_len;
+    aa.R = c.ring_len;
+    aa.SL = ctx->SL;
+    {
+      int ns = (2 * ctx->n_sm + rows * c.n_heads - 1) / (rows * c.n_heads);
+      const int cap = (ctx->SL + 63) / 64;
+      if (ns > cap) ns = cap;
+      if (ns > kMaxSplits) ns = kMaxSplits;
+      if (ns < 1) ns = 1;
+      aa.nsplit = ns;
+      aa.chunk = (ctx->SL + ns - 1) / ns;
+    }
+    aa.scale = 1.0f / sqrtf((float)c.head_dim);
+    mark("attention", true);
+    CK(launch_attn(aa, rows, st), "attention launch");
+    mark("attention", false);
+    // O projection + residual
+    GemvArgs oa{};
+    oa.w = w.o.view();
+    oa.sp = plan_stage(nt, S, c.fmt_attn);
+    oa.ntok = rows;
+    oa.xh = ctx->attn_out;
+    oa.ld_src = S;
+    oa.res_in = hid(2 * l);
+    oa.out_f = hid(2 * l + 1);
+    oa.ld_out = H;
+    mark("o_proj", true);
+    CK(launch_gemv(c.fmt_attn, SRC_F16, EPI_RESID, oa, gx_for(w.o.n_slabs), tg, st), "o_proj launch");
+    mark("o_proj", false);
+    if (w.dense) {
+      GemvArgs ga{};
+      ga.w = w.gateup.view();
+      ga.sp = plan_stage(nt, H, c.fmt_dense);
+      ga.ntok = rows;
+      ga.xf = hid(2 * l + 1);
+      ga.ld_src = H;
+      ga.norm_w = w.mlp_norm;
+      ga.eps = c.rms_eps;
+      ga.out_h = ctx->act_dense;
+      ga.ld_out = c.dense_inter;
+      mark("mlp_gate_up", true);
+      CK(launch_gemv(c.fmt_dense, SRC_NORM, EPI_SWIGLU, ga, gx_for(w.gateup.n_slabs), tg, st), "gate/up launch");
+      mark("mlp_gate_up", false);
+      GemvArgs da{};
+      da.w = w.down.view();
+      da.sp = plan_stage(nt, c.dense_inter, c.fmt_dense);
+      da.ntok = rows;
+      da.xh = ctx->act_dense;
+      da.ld_src = c.dense_inter;
+      da.res_in = hid(2 * l + 1);
+      da.out_f = hid(2 * l + 2);
+      da.ld_out = H;
+      mark("mlp_down", true);
+      CK(launch_gemv(c.fmt_dense, SRC_F16, EPI_RESID, da, gx_for(w.down.n_slabs), tg, st), "down launch");
+      mark("mlp_down", false);
+    } else {
+      const int E = c.n_experts, k = c.top_k;
+      RouterArgs ra{};
+      ra.w = reinterpret_cast<const __half*>(w.router.q);
+      ra.n_slabs = w.router.n_slabs;
+      ra.U = w.router.U;
+      ra.sp = plan_stage(nt, H, F16);
+      ra.ntok = rows;
+      ra.H = H;
+      ra.E = E;
+      ra.k = k;
+      ra.h = hid(2 * l + 1);
+      ra.norm_w = w.mlp_norm;
+      ra.eps = c.rms_eps;
+      ra.xhat = ctx->xhat;
+      ra.logits = ctx->r_logits + (size_t)l * MR * E;
+      ra.idx = ctx->r_idx + (size_t)l * MR * k;
+      ra.wts = ctx->r_w + (size_t)l * MR * k;
+      ra.count = ctx->r_count + (size_t)l * E;
+      ra.offset = ctx->r_offset + (size_t)l * (E + 1);
+      ra.perm = ctx->r_perm + (size_t)l * MR * k;
+      ra.inv = ctx->r_inv + (size_t)l * MR * k;
+      ra.active = ctx->r_active + (size_t)l * E;
+      ra.n_active = ctx->r_nactive + l;
+      ra.counter = ctx->r_counter;
+      mark("router", true);
+      CK(launch_router(ra, tg, st), "router launch");
+      mark("router", false);
+
+      const int fs = ctx->shared_fmt();
+      ExpertArgs xa{};
+      xa.ntok = rows;
+      xa.k = k;
+      xa.H = H;
+      xa.Ie = c.expert_inter;
+      xa.Ish = c.n_shared * c.expert_inter;
+      xa.xhat = ctx->xhat;
+      xa.count = ra.count;
+      xa.offset = ra.offset;
+      xa.perm = ra.perm;
+      xa.active = ra.active;
+      xa.n_active = ra.n_active;
+      xa.act_r = ctx->act_r;
+      xa.act_s = ctx->act_s;
+      xa.part_r = ctx->part_r;
+      xa.part_s = ctx->part_s;
+      xa.h = hid(2 * l + 1);
+      xa.wts = ra.wts;
+      xa.inv = ra.inv;
+      xa.out = hid(2 * l + 2);
+      xa.slab_counter = ctx->slab_counter;
+      const int max_act = E < rows * k ? E : rows * k;
+      // gate/up
+      xa.wr = w.ex_gateup.view(1);
+      xa.ws = c.n_shared > 0 ? w.sh_gateup.view() : PMat{};
+      xa.sp = plan_stage(nt, H, I8ASYM);
+      {
+        const int items = max_act * w.ex_gateup.n_slabs + xa.ws.n_slabs;
+        const int grid = items < G ? items : G;
+        mark("expert_gate_up", true);
+        CK(launch_expert_gateup(c.fmt_routed, fs, xa, grid, st), "expert gate/up launch");
+        mark("expert_gate_up", false);
+      }
+      // down + combine
+      xa.wr = w.ex_down.view(1);
+      xa.ws = c.n_shared > 0 ? w.sh_down.view() : PMat{};
+      {
+        const int kmax = xa.Ish > xa.Ie ? xa.Ish : xa.Ie;
+        xa.sp = plan_stage(nt, kmax, I8ASYM);
+        const int nS = H / 16;
+        const int items = max_act * nS + (c.n_shared > 0 ? nS : 0);
+        const int grid = items < G ? items : G;
+        mark("expert_down_combine", true);
+        CK(launch_expert_down(c.fmt_routed, fs, xa, grid, st), "expert down launch");
+        mark("expert_down_combine", false);
+      }
+    }
+  }
+
+  if (sh.lm) {
+    GemvArgs la{};
+    la.w = ctx->lm.view();
+    la.sp = plan_stage(nt, H, F16);
+    la.ntok = rows;
+    la.xf = hid(2 * c.n_layers);
+    la.ld_src = H;
+    la.norm_w = ctx->final_norm;
+    la.eps = c.rms_eps;
+    la.out_f = sh.logits ? ctx->logits : nullptr;
+    la.n_valid = c.vocab;
+    la.keys = ctx->keys;
+    la.counter = ctx->lm_counter;
+    la.next_ids = ctx->next_ids;
+    if (sh.chain) {
+      la.feed_ids = ctx->ids_buf;
+      la.feed_pos = ctx->pos_buf;
+      la.hist = ctx->hist;
+      la.hist_ctr = ctx->hist_ctr;
+    }
+    mark("lm_head_argmax", true);
+    CK(launch_gemv(F16, SRC_NORM, EPI_LOGITS, la, gx_for(ctx->lm.n_slabs), tg, st), "lm head launch");
+    mark("lm_head_argmax", false);
+  }
+  return UOCR_OK;
+}
+
+static uocr_status run_step(uocr_ctx* ctx, const StepShape& sh) {
+  if (!ctx->cfg.use_graphs) return enqueue_step(ctx, sh, nullptr);
+  const uint64_t key = (uint64_t)sh.rows | ((uint64_t)sh.ids << 8) | ((uint64_t)sh.lm << 9) |
+                       ((uint64_t)sh.logits << 10) | ((uint64_t)sh.chain << 11);
+  auto it = ctx->graphs.find(key);
+  if (it == ctx->graphs.end()) {
+    cudaGraph_t g = nullptr;
+    CK(cudaStreamBeginCapture(ctx->st, cudaStreamCaptureModeThreadLocal), "begin capture");
+    uocr_status s = enqueue_step(ctx, sh, nullptr);
+    cudaError_t e = cudaStreamEndCapture(ctx->st, &g);
+    if (s != UOCR_OK) {
+      if (g) cudaGraphDestroy(g);
+      return s;
+    }
+    CK(e, "end capture");
+    cudaGraphExec_t ge = nullptr;
+    e = cudaGraphInstantiate(&ge, g, 0);
+    cudaGraphDestroy(g);
+    CK(e, "graph instantiate");
+    it = ctx->graphs.emplace(key, ge).first;
+  }
+  CK(cudaGraphLaunch(it->second, ctx->st), "graph launch");
+  return UOCR_OK;
+}
+
+// ------------------------------------------------------------------ weights
+namespace {
+
+struct Expect {
+  int fmt;  // -1: any quantised? no: exact format required
+  int rows, cols;
+  Group group;
+  int n_members;  // members of the group
+  int member;     // index of this tensor in the group
+};
+
+}  // namespace
+
+static bool expect_for(uocr_ctx* ctx, const uocr_tensor& t, Expect& ex, std::string& why) {
+  const uocr_config& c = ctx->cfg;
+  const int H = c.hidden, S = ctx->S, V = c.vocab, E = c.n_experts;
+  const bool glob = t.kind == UOCR_T_EMBED || t.kind == UOCR_T_FINAL_NORM || t.kind == UOCR_T_LM_HEAD;
+  if (glob) {
+    if (V <= 0) return why = "the config has no vocabulary", false;
+    if (t.layer != 0 || t.expert != 0) return why = "global tensors use layer 0, expert 0", false;
+  } else if (t.layer < 0 || t.layer >= c.n_layers) {
+    return why = "layer out of range", false;
+  }
+  const bool dense = glob ? true : ctx->layer_dense(t.layer);
+  ex.group = G_SINGLE;
+  ex.n_members = 1;
+  ex.member = 0;
+  auto need_expert0 = [&]() { return t.expert == 0 ? true : (why = "expert must be 0", false); };
+  switch (t.kind) {
+    case UOCR_T_EMBED: ex = {UOCR_F16, V, H, G_SINGLE, 1, 0}; return true;
+    case UOCR_T_FINAL_NORM: ex = {UOCR_F16, 1, H, G_SINGLE, 1, 0}; return true;
+    case UOCR_T_LM_HEAD: ex = {UOCR_F16, V, H, G_SINGLE, 1, 0}; return true;
+    case UOCR_T_ATTN_NORM:
+    case UOCR_T_MLP_NORM: ex = {UOCR_F16, 1, H, G_SINGLE, 1, 0}; return need_expert0();
+    case UOCR_T_WQ:
+    case UOCR_T_WK:
+    case UOCR_T_WV:
+      ex = {c.fmt_attn, S, H, G_QKV, 3, t.kind - UOCR_T_WQ};
+      return need_expert0();
+    case UOCR_T_WO: ex = {c.fmt_attn, H, S, G_SINGLE, 1, 0}; return need_expert0();
+    case UOCR_T_GATE:
+    case UOCR_T_UP:
+      if (!dense) return why = "dense MLP tensor on a MoE layer", false;
+      ex = {c.fmt_dense, c.dense_inter, H, G_DENSE_GU, 2, t.kind - UOCR_T_GATE};
+      return need_expert0();
+    case UOCR_T_DOWN:
+      if (!dense) return why = "dense MLP tensor on a MoE layer", false;
+      ex = {c.fmt_dense, H, c.dense_inter, G_SINGLE, 1, 0};
+      return need_expert0();
+    case UOCR_T_ROUTER:
+      if (dense) return why = "router on a dense layer", false;
+      ex = {UOCR_F16, E, H, G_SINGLE, 1, 0};
+      return need_expert0();
+    case UOCR_T_SHARED_GATE:
+    case UOCR_T_SHARED_UP:
+    case UOCR_T_SHARED_DOWN:
+      if (dense) return why = "expert tensor on a dense layer", false;
+      if (t.expert < 0 || t.expert >= c.n_shared) return why = "shared expert index out of range", false;
+      if (t.kind == UOCR_T_SHARED_DOWN)
+        ex = {c.fmt_shared, H, c.expert_inter, G_SHARED_DOWN, c.n_shared, t.expert};
+      else
+        ex = {c.fmt_shared, c.expert_inter, H, G_SHARED_GU, 2 * c.n_shared,
+              2 * t.expert + (t.kind == UOCR_T_SHARED_UP ? 1 : 0)};
+      return true;
+    case UOCR_T_EXPERT_GATE:
+    case UOCR_T_EXPERT_UP:
+    case UOCR_T_EXPERT_DOWN:
+      if (dense) return why = "expert tensor on a dense layer", false;
+      if (t.expert < 0 || t.expert >= E) return why = "routed expert index out of range", false;
+      if (t.kind == UOCR_T_EXPERT_DOWN)
+        ex = {c.fmt_routed, H, c.expert_inter, G_SINGLE, 1, 0};
+      else
+        ex = {c.fmt_routed, c.expert_inter, H, G_EXPERT_GU, 2, t.kind == UOCR_T_EXPERT_UP ? 1 : 0};
+      return true;
+  }
+  why = "unknown tensor kind";
+  return false;
+}
+
+static uocr_status pack_into(uocr_ctx* ctx, const DMat& dst, size_t expert_off_q, size_t expert_off_s, int map,
+                             const std::vector<void*>& srcs, int src_rows, int src_cols, int I) {
+  PackArgs pa{};
+  pa.q = dst.q + expert_off_q;
+  pa.s = dst.s ? dst.s + expert_off_s : nullptr;
+  pa.fmt = dst.fmt;
+  pa.n_slabs = dst.n_slabs;
+  pa.U = dst.U;
+  pa.K = dst.K;
+  pa.map = map;
+  pa.nsrc = (int)srcs.size();
+  for (size_t i = 0; i < srcs.size() && i < 8; ++i) pa.src[i] = reinterpret_cast<const uint8_t*>(srcs[i]);
+  pa.src_rows = src_rows;
+  pa.src_cols = src_cols;
+  pa.S = ctx->S;
+  pa.D = ctx->cfg.head_dim;
+  pa.I = I;
+  CK(launch_pack(pa, ctx->st), "pack launch");
+  CK(cudaStreamSynchronize(ctx->st), "pack");
+  return UOCR_OK;
+}
+
+static uocr_status finish_group(uocr_ctx* ctx, int kind, int layer, int expert, Group grp, std::vector<void*>& srcs) {
+  const uocr_config& c = ctx->cfg;
+  const int H = c.hidden;
+  LayerW* w = (kind == UOCR_T_EMBED || kind == UOCR_T_FINAL_NORM || kind == UOCR_T_LM_HEAD) ? nullptr : &ctx->L[layer];
+  switch (grp) {
+    case G_QKV: return pack_into(ctx, w->qkv, 0, 0, MAP_QKV, srcs, ctx->S, H, 0);
+    case G_DENSE_GU: return pack_into(ctx, w->gateup, 0, 0, MAP_SWIGLU, srcs, c.dense_inter, H, c.dense_inter);
+    case G_SHARED_GU: return pack_into(ctx, w->sh_gateup, 0, 0, MAP_SWIGLU, srcs, c.expert_inter, H, c.expert_inter);
+    case G_SHARED_DOWN: return pack_into(ctx, w->sh_down, 0, 0, MAP_KCAT, srcs, H, c.expert_inter, c.expert_inter);
+    case G_EXPERT_GU:
+      return pack_into(ctx, w->ex_gateup, w->ex_gateup.qbytes * expert, w->ex_gateup.sbytes * expert, MAP_SWIGLU,
+                       srcs, c.expert_inter, H, c.expert_inter);
+    case G_SINGLE: break;
+  }
+  switch (kind) {
+    case UOCR_T_WO: return pack_into(ctx, w->o, 0, 0, MAP_IDENT, srcs, H, ctx->S, 0);
+    case UOCR_T_DOWN: return pack_into(ctx, w->down, 0, 0, MAP_IDENT, srcs, H, c.dense_inter, 0);
+    case UOCR_T_ROUTER: return pack_into(ctx, w->router, 0, 0, MAP_IDENT, srcs, c.n_experts, H, 0);
+    case UOCR_T_EXPERT_DOWN:
+      return pack_into(ctx, w->ex_down, w->ex_down.qbytes * expert, w->ex_down.sbytes * expert, MAP_IDENT, srcs, H,
+                       c.expert_inter, 0);
+    case UOCR_T_LM_HEAD: return pack_into(ctx, ctx->lm, 0, 0, MAP_IDENT, srcs, c.vocab, H, 0);
+  }
+  return ctx->fail(UOCR_E_FORMAT, "internal: no packer for kind %d", kind);
+}
+
+static uocr_status load_one(uocr_ctx* ctx, const uocr_tensor& t) {
+  Expect ex{};
+  std::string why;
+  if (!expect_for(ctx, t, ex, why))
+    return ctx->fail(UOCR_E_FORMAT, "tensor kind %d layer %d expert %d: %s", t.kind, t.layer, t.expert, why.c_str());
+  if (t.format != ex.fmt)
+    return ctx->fail(UOCR_E_FORMAT, "tensor kind %d layer %d expert %d: format %d, expected %d", t.kind, t.layer,
+                     t.expert, t.format, ex.fmt);
+  if (t.rows != ex.rows || t.cols != ex.cols)
+    return ctx->fail(UOCR_E_FORMAT, "tensor kind %d layer %d expert %d: shape [%d][%d], expected [%d][%d]", t.kind,
+                     t.layer, t.expert, t.rows, t.cols, ex.rows, ex.cols);
+  const size_t want = blob_bytes(t.format, t.rows, t.cols);
+  if (t.bytes != want || t.data == nullptr)
+    return ctx->fail(UOCR_E_FORMAT, "tensor kind %d layer %d expert %d: %llu bytes, expected %zu", t.kind, t.layer,
+                     t.expert, (unsigned long long)t.bytes, want);
+  // plain copies
+  const uocr_config& c = ctx->cfg;
+  if (t.kind == UOCR_T_EMBED || t.kind == UOCR_T_FINAL_NORM || t.kind == UOCR_T_ATTN_NORM ||
+      t.kind == UOCR_T_MLP_NORM) {
+    void* dst = t.kind == UOCR_T_EMBED        ? (void*)ctx->emb
+                : t.kind == UOCR_T_FINAL_NORM ? (void*)ctx->final_norm
+                : t.kind == UOCR_T_ATTN_NORM  ? (void*)ctx->L[t.layer].attn_norm
+                                              : (void*)ctx->L[t.layer].mlp_norm;
+    CK(cudaMemcpy(dst, t.data, t.bytes, cudaMemcpyHostToDevice), "weight copy");
+    ctx->loaded[{t.kind, t.layer, t.expert}] = true;
+    return UOCR_OK;
+  }
+  void* dev = nullptr;
+  CK(cudaMalloc(&dev, t.bytes), "staging allocation");
+  cudaError_t e = cudaMemcpy(dev, t.data, t.bytes, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(dev);
+    return ctx->cuda(e, "staging copy");
+  }
+  // group key: (group, layer, expert for per-expert groups)
+  const int gexp = ex.group == G_EXPERT_GU ? t.expert : 0;
+  std::vector<int> gk = {(int)ex.group, t.layer, ex.group == G_SINGLE ? t.kind : gexp,
+                         ex.group == G_SINGLE ? t.expert : 0};
+  Pending& p = ctx->pending[gk];
+  if (p.dev.empty()) p.dev.assign(ex.n_members, nullptr);
+  if (p.dev[ex.member]) {
+    cudaFree(p.dev[ex.member]);
+    --p.have;
+  }
+  p.dev[ex.member] = dev;
+  ++p.have;
+  uocr_status s = UOCR_OK;
+  if (p.have == ex.n_members) {
+    s = finish_group(ctx, t.kind, t.layer, t.expert, ex.group, p.dev);
+    for (void* d : p.dev) cudaFree(d);
+    ctx->pending.erase(gk);
+  }
+  (void)c;
+  if (s == UOCR_OK) ctx->loaded[{t.kind, t.layer, t.expert}] = true;
+  return s;
+}
+
+static uocr_status check_complete(uocr_ctx* ctx) {
+  const uocr_config& c = ctx->cfg;
+  auto has = [&](int k, int l, int e) { return ctx->loaded.count({k, l, e}) > 0; };
+  auto miss = [&](int k, int l, int e) {
+    return ctx->fail(UOCR_E_STATE, "weight tensor kind %d layer %d expert %d has not been loaded", k, l, e);
+  };
+  if (c.vocab > 0)
+    for (int k : {UOCR_T_EMBED, UOCR_T_FINAL_NORM, UOCR_T_LM_HEAD})
+      if (!has(k, 0, 0)) return miss(k, 0, 0);
+  for (int l = 0; l < c.n_layers; ++l) {
+    for (int k : {UOCR_T_ATTN_NORM, UOCR_T_WQ, UOCR_T_WK, UOCR_T_WV, UOCR_T_WO, UOCR_T_MLP_NORM})
+      if (!has(k, l, 0)) return miss(k, l, 0);
+    if (ctx->layer_dense(l)) {
+      for (int k : {UOCR_T_GATE, UOCR_T_UP, UOCR_T_DOWN})
+        if (!has(k, l, 0)) return miss(k, l, 0);
+    } else {
+      if (!has(UOCR_T_ROUTER, l, 0)) return miss(UOCR_T_ROUTER, l, 0);
+      for (int s = 0; s < c.n_shared; ++s)
+        for (int k : {UOCR_T_SHARED_GATE, UOCR_T_SHARED_UP, UOCR_T_SHARED_DOWN})
+          if (!has(k, l, s)) return miss(k, l, s);
+      for (int e = 0; e < c.n_experts; ++e)
+        for (int k : {UOCR_T_EXPERT_GATE, UOCR_T_EXPERT_UP, UOCR_T_EXPERT_DOWN})
+          if (!has(k, l, e)) return miss(k, l, e);
+    }
+  }
+  if (c.use_sink && !ctx->sinks_set) return ctx->fail(UOCR_E_STATE, "use_sink = 1 but uocr_set_sinks was not called");
+  return UOCR_OK;
+}
+
+// ------------------------------------------------------------------ C ABI
+extern "C" {
+
+uocr_status uocr_create(const uocr_config* cfg, uocr_ctx** out) {
+  if (!out) return UOCR_E_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg) return UOCR_E_INVALID_ARG;
+  uocr_ctx* ctx = new uocr_ctx();
+  ctx->cfg = *cfg;
+  uocr_status s = check_config(ctx, ctx->cfg);
+  if (s != UOCR_OK) {
+    g_create_err = ctx->err;
+    delete ctx;
+    return s;
+  }
+  // measuring pass for the budget check
+  Carver m;
+  carve(ctx, m);
+  if (cfg->mem_budget && ctx->rep.total > cfg->mem_budget) {
+    const uocr_mem_report& r = ctx->rep;
+    g_create_err = ctx->fail(UOCR_E_BUDGET,
+              "working set %llu B exceeds the budget %llu B (weights %llu, kv_cache %llu, activations %llu, "
+              "routing %llu, logits %llu)",
+              (unsigned long long)r.total, (unsigned long long)cfg->mem_budget, (unsigned long long)r.weights,
+              (unsigned long long)r.kv_cache, (unsigned long long)r.activations, (unsigned long long)r.routing,
+              (unsigned long long)r.logits) == UOCR_E_BUDGET ? ctx->err : std::string();
+    delete ctx;
+    return UOCR_E_BUDGET;
+  }
+  cudaError_t e = cudaSetDevice(cfg->device);
+  if (e != cudaSuccess) {
+    g_create_err = std::string("cudaSetDevice: ") + cudaGetErrorString(e);
+    delete ctx;
+    return UOCR_E_CUDA;
+  }
+  cudaDeviceGetAttribute(&ctx->n_sm, cudaDevAttrMultiProcessorCount, cfg->device);
+  e = init_kernel_attributes();
+  if (e == cudaSuccess) e = cudaMalloc(&ctx->arena, m.off);
+  if (e != cudaSuccess) {
+    const bool oom = e == cudaErrorMemoryAllocation;
+    g_create_err = std::string("arena allocation / kernel set-up: ") + cudaGetErrorString(e);
+    cudaGetLastError();
+    delete ctx;
+    return oom ? UOCR_E_OOM : UOCR_E_CUDA;
+  }
+  Carver a;
+  a.base = ctx->arena;
+  carve(ctx, a);
+  e = cudaStreamCreateWithFlags(&ctx->st, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_in, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_out, cudaEventDisableTiming);
+  ctx->ust = reinterpret_cast<cudaStream_t>(cfg->stream);
+  // zero everything (KV cache, counters, argmax keys, status)
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->arena, 0, m.off, ctx->st);
+  if (e == cudaSuccess) {
+    std::vector<double> inv(cfg->head_dim / 2);
+    for (int i = 0; i < cfg->head_dim / 2; ++i)
+      inv[i] = std::pow((double)cfg->rope_theta, -2.0 * i / cfg->head_dim);
+    e = cudaMemcpyAsync(ctx->inv_freq, inv.data(), inv.size() * sizeof(double), cudaMemcpyHostToDevice, ctx->st);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->st);
+  if (e != cudaSuccess) {
+    g_create_err = std::string("context set-up: ") + cudaGetErrorString(e);
+    uocr_destroy(ctx);
+    return UOCR_E_CUDA;
+  }
+  g_create_err.clear();
+  *out = ctx;
+  return UOCR_OK;
+}
+
+void uocr_destroy(uocr_ctx* ctx) {
+  if (!ctx) return;
+  {
+    std::lock_guard<std::mutex> lk(ctx->mu);
+    if (ctx->st) cudaStreamSynchronize(ctx->st);
+    for (auto& kv : ctx->graphs) cudaGraphExecDestroy(kv.second);
+    for (auto& kv : ctx->pending)
+      for (void* d : kv.second.dev)
+        if (d) cudaFree(d);
+    if (ctx->arena) cudaFree(ctx->arena);
+    if (ctx->ev_in) cudaEventDestroy(ctx->ev_in);
+    if (ctx->ev_out) cudaEventDestroy(ctx->ev_out);
+    if (ctx->st) cudaStreamDestroy(ctx->st);
+  }
+  delete ctx;
+}
+
+uocr_status uocr_load_weights(uocr_ctx* ctx, const uocr_tensor* t, size_t n) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  if (!t && n) return ctx->fail(UOCR_E_INVALID_ARG, "tensor list is NULL");
+  for (size_t i = 0; i < n; ++i) {
+    uocr_status s = load_one(ctx, t[i]);
+    if (s != UOCR_OK) return s;
+  }
+  return UOCR_OK;
+}
+
+uocr_status uocr_kv_write_prefix(uocr_ctx* ctx, int32_t row, int32_t layer, const uint16_t* k, const uint16_t* v,
+                                 int32_t start, int32_t n) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  const uocr_config& c = ctx->cfg;
+  if (!k || !v || row < 0 || row >= c.max_rows || layer < 0 || layer >= c.n_layers || start < 0 || n < 0 ||
+      start + n > c.prefix_len)
+    return ctx->fail(UOCR_E_INVALID_ARG, "kv_write_prefix: bad row/layer/range");
+  const size_t D = c.head_dim;
+  for (int kv = 0; kv < 2; ++kv) {
+    const uint16_t* src = kv ? v : k;
+    for (int h = 0; h < c.n_heads; ++h) {
+      __half* dst = ctx->kv + ctx->kv_layer * layer + ((((size_t)row * 2 + kv) * c.n_heads + h) * ctx->SL + start) * D;
+      CK(cudaMemcpyAsync(dst, src + (size_t)h * n * D, (size_t)n * D * 2, cudaMemcpyHostToDevice, ctx->st),
+         "kv prefix copy");
+    }
+  }
+  CK(cudaStreamSynchronize(ctx->st), "kv prefix copy");
+  return UOCR_OK;
+}
+
+uocr_status uocr_kv_read(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0, int32_t n, uint16_t* k,
+                         uint16_t* v) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  const uocr_config& c = ctx->cfg;
+  if (!k || !v || row < 0 || row >= c.max_rows || layer < 0 || layer >= c.n_layers || slot0 < 0 || n < 0 ||
+      slot0 + n > ctx->SL)
+    return ctx->fail(UOCR_E_INVALID_ARG, "kv_read: bad row/layer/range");
+  CK(cudaStreamSynchronize(ctx->st), "kv read");
+  const size_t D = c.head_dim;
+  for (int kv = 0; kv < 2; ++kv) {
+    uint16_t* dst = kv ? v : k;
+    for (int h = 0; h < c.n_heads; ++h) {
+      const __half* src =
+          ctx->kv + ctx->kv_layer * layer + ((((size_t)row * 2 + kv) * c.n_heads + h) * ctx->SL + slot0) * D;
+      CK(cudaMemcpy(dst + (size_t)h * n * D, src, (size_t)n * D * 2, cudaMemcpyDeviceToHost), "kv read");
+    }
+  }
+  return UOCR_OK;
+}
+
+uocr_status uocr_set_sinks(uocr_ctx* ctx, const float* sinks) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  if (!sinks) return ctx->fail(UOCR_E_INVALID_ARG, "sinks is NULL");
+  if (!ctx->cfg.use_sink) return ctx->fail(UOCR_E_STATE, "the config has use_sink = 0");
+  CK(cudaMemcpy(ctx->sinks, sinks, sizeof(float) * ctx->cfg.n_layers * ctx->cfg.n_heads, cudaMemcpyHostToDevice),
+     "sink copy");
+  ctx->sinks_set = true;
+  return UOCR_OK;
+}
+
+static uocr_status step_prologue(uocr_ctx* ctx, int rows) {
+  if (rows < 1 || rows > ctx->cfg.max_rows)
+    return ctx->fail(UOCR_E_INVALID_ARG, "rows %d outside [1, max_rows = %d]", rows, ctx->cfg.max_rows);
+  uocr_status s = check_complete(ctx);
+  if (s != UOCR_OK) return s;
+  CK(cudaEventRecord(ctx->ev_in, ctx->ust), "event record");
+  CK(cudaStreamWaitEvent(ctx->st, ctx->ev_in, 0), "stream wait");
+  return UOCR_OK;
+}
+
+static uocr_status step_epilogue(uocr_ctx* ctx) {
+  CK(cudaEventRecord(ctx->ev_out, ctx->st), "event record");
+  CK(cudaStreamWaitEvent(ctx->ust, ctx->ev_out, 0), "stream wait");
+  return UOCR_OK;
+}
+
+uocr_status uocr_decode_step(uocr_ctx* ctx, int32_t rows, const int32_t* token_ids, const int32_t* positions,
+                             int32_t* next_ids, float* logits) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  if (ctx->cfg.vocab <= 0) return ctx->fail(UOCR_E_STATE, "decode_step needs a vocabulary (use decode_step_embeds)");
+  if (!token_ids || !positions || !next_ids) return ctx->fail(UOCR_E_INVALID_ARG, "NULL device pointer");
+  uocr_status s = step_prologue(ctx, rows);
+  if (s != UOCR_OK) return s;
+  CK(cudaMemcpyAsync(ctx->ids_buf, token_ids, rows * 4, cudaMemcpyDeviceToDevice, ctx->st), "ids copy");
+  CK(cudaMemcpyAsync(ctx->pos_buf, positions, rows * 4, cudaMemcpyDeviceToDevice, ctx->st), "positions copy");
+  s = run_step(ctx, StepShape{rows, true, true, logits != nullptr, false});
+  if (s != UOCR_OK) return s;
+  CK(cudaMemcpyAsync(next_ids, ctx->next_ids, rows * 4, cudaMemcpyDeviceToDevice, ctx->st), "ids copy");
+  if (logits)
+    CK(cudaMemcpyAsync(logits, ctx->logits, (size_t)rows * ctx->cfg.vocab * 4, cudaMemcpyDeviceToDevice, ctx->st),
+       "logits copy");
+  return step_epilogue(ctx);
+}
+
+uocr_status uocr_decode_step_embeds(uocr_ctx* ctx, int32_t rows, const uint16_t* x, const int32_t* positions,
+                                    float* y, int32_t* next_ids, float* logits) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  if (!x || !positions) return ctx->fail(UOCR_E_INVALID_ARG, "NULL device pointer");
+  const bool lm = next_ids != nullptr || logits != nullptr;
+  if (lm && ctx->cfg.vocab <= 0) return ctx->fail(UOCR_E_STATE, "next_ids/logits need a vocabulary");
+  uocr_status s = step_prologue(ctx, rows);
+  if (s != UOCR_OK) return s;
+  const int H = ctx->cfg.hidden;
+  CK(cudaMemcpyAsync(ctx->x_in, x, (size_t)rows * H * 2, cudaMemcpyDeviceToDevice, ctx->st), "x copy");
+  CK(cudaMemcpyAsync(ctx->pos_buf, positions, rows * 4, cudaMemcpyDeviceToDevice, ctx->st), "positions copy");
+  s = run_step(ctx, StepShape{rows, false, lm, logits != nullptr, false});
+  if (s != UOCR_OK) return s;
+  if (y)
+    CK(cudaMemcpyAsync(y, ctx->hid + (size_t)2 * ctx->cfg.n_layers * ctx->MR() * H, (size_t)rows * H * 4,
+                       cudaMemcpyDeviceToDevice, ctx->st),
+       "y copy");
+  if (next_ids) CK(cudaMemcpyAsync(next_ids, ctx->next_ids, rows * 4, cudaMemcpyDeviceToDevice, ctx->st), "ids copy");
+  if (logits)
+    CK(cudaMemcpyAsync(logits, ctx->logits, (size_t)rows * ctx->cfg.vocab * 4, cudaMemcpyDeviceToDevice, ctx->st),
+       "logits copy");
+  return step_epilogue(ctx);
+}
+
+uocr_status uocr_decode_step_host(uocr_ctx* ctx, int32_t rows, const int32_t* token_ids, const int32_t* positions,
+                                  int32_t* next_ids) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  if (ctx->cfg.vocab <= 0) return ctx->fail(UOCR_E_STATE, "decode_step_host needs a vocabulary");
+  if (!token_ids || !positions || !next_ids) return ctx->fail(UOCR_E_INVALID_ARG, "NULL host pointer");
+  if (rows < 1 || rows > ctx->cfg.max_rows) return ctx->fail(UOCR_E_INVALID_ARG, "rows out of range");
+  uocr_status s = check_complete(ctx);
+  if (s != UOCR_OK) return s;
+  CK(cudaMemcpyAsync(ctx->ids_buf, token_ids, rows * 4, cudaMemcpyHostToDevice, ctx->st), "ids copy");
+  CK(cudaMemcpyAsync(ctx->pos_buf, positions, rows * 4, cudaMemcpyHostToDevice, ctx->st), "positions copy");
+  s = run_step(ctx, StepShape{rows, true, true, false, false});
+  if (s != UOCR_OK) return s;
+  CK(cudaMemcpyAsync(next_ids, ctx->next_ids, rows * 4, cudaMemcpyDeviceToHost, ctx->st), "ids copy");
+  CK(cudaStreamSynchronize(ctx->st), "step");
+  return UOCR_OK;
+}
+
+uocr_status uocr_generate(uocr_ctx* ctx, int32_t rows, const int32_t* token_ids, const int32_t* positions,
+                          int32_t n_steps, int32_t* out_ids) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  if (ctx->cfg.vocab <= 0) return ctx->fail(UOCR_E_STATE, "generate needs a vocabulary");
+  if (!token_ids || !positions || !out_ids || n_steps < 0)
+    return ctx->fail(UOCR_E_INVALID_ARG, "NULL device pointer or negative step count");
+  uocr_status s = step_prologue(ctx, rows);
+  if (s != UOCR_OK) return s;
+  CK(cudaMemcpyAsync(ctx->ids_buf, token_ids, rows * 4, cudaMemcpyDeviceToDevice, ctx->st), "ids copy");
+  CK(cudaMemcpyAsync(ctx->pos_buf, positions, rows * 4, cudaMemcpyDeviceToDevice, ctx->st), "positions copy");
+  for (int done = 0; done < n_steps;) {
+    const int n = n_steps - done < kHistCap ? n_steps - done : kHistCap;
+    CK(cudaMemsetAsync(ctx->hist_ctr, 0, 4, ctx->st), "history reset");
+    for (int i = 0; i < n; ++i) {
+      s = run_step(ctx, StepShape{rows, true, true, false, true});
+      if (s != UOCR_OK) return s;
+    }
+    CK(cudaMemcpyAsync(out_ids + (size_t)done * rows, ctx->hist, (size_t)n * rows * 4, cudaMemcpyDeviceToDevice,
+                       ctx->st),
+       "history copy");
+    done += n;
+  }
+  return step_epilogue(ctx);
+}
+
+uocr_status uocr_kv_reset(uocr_ctx* ctx, int32_t row, int32_t keep_prefix) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  const uocr_config& c = ctx->cfg;
+  if (row < -1 || row >= c.max_rows) return ctx->fail(UOCR_E_INVALID_ARG, "row out of range");
+  const int r0 = row < 0 ? 0 : row, r1 = row < 0 ? c.max_rows : row + 1;
+  for (int l = 0; l < c.n_layers; ++l)
+    for (int r = r0; r < r1; ++r) {
+      __half* base = ctx->kv + ctx->kv_layer * l + (size_t)r * 2 * c.n_heads * ctx->SL * c.head_dim;
+      CK(launch_fill_zero_ring(base, c.n_heads, ctx->SL, c.head_dim, keep_prefix ? c.prefix_len : 0, ctx->st),
+         "kv reset");
+    }
+  return UOCR_OK;
+}
+
+uocr_status uocr_sync(uocr_ctx* ctx) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  CK(cudaStreamSynchronize(ctx->st), "sync");
+  int st = 0;
+  CK(cudaMemcpy(&st, ctx->status, 4, cudaMemcpyDeviceToHost), "status read");
+  if (st) {
+    CK(cudaMemset(ctx->status, 0, 4), "status clear");
+    if (st & kStatusToken) return ctx->fail(UOCR_E_TOKEN, "a token id was outside [0, vocab)");
+    return ctx->fail(UOCR_E_POSITION, "a position was negative");
+  }
+  return UOCR_OK;
+}
+
+const char* uocr_last_error(uocr_ctx* ctx) {
+  if (!ctx) return g_create_err.c_str();
+  return ctx->err.c_str();
+}
+
+uocr_status uocr_memory_report(uocr_ctx* ctx, uocr_mem_report* out) {
+  if (!ctx || !out) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  *out = ctx->rep;
+  return UOCR_OK;
+}
+
+uocr_status uocr_debug_hidden(uocr_ctx* ctx, int32_t tap, int32_t rows, float* out) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  const uocr_config& c = ctx->cfg;
+  if (!out || tap < -1 || tap >= 2 * c.n_layers || rows < 1 || rows > c.max_rows)
+    return ctx->fail(UOCR_E_INVALID_ARG, "debug_hidden: bad tap/rows");
+  CK(cudaStreamSynchronize(ctx->st), "sync");
+  CK(cudaMemcpy(out, ctx->hid + (size_t)(tap + 1) * ctx->MR() * c.hidden, (size_t)rows * c.hidden * 4,
+                cudaMemcpyDeviceToHost),
+     "hidden read");
+  return UOCR_OK;
+}
+
+uocr_status uocr_debug_router(uocr_ctx* ctx, int32_t layer, int32_t rows, int32_t* idx, float* w, int32_t* count,
+                              int32_t* offset, int32_t* perm) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  const uocr_config& c = ctx->cfg;
+  if (layer < 0 || layer >= c.n_layers || ctx->layer_dense(layer) || rows < 1 || rows > c.max_rows)
+    return ctx->fail(UOCR_E_INVALID_ARG, "debug_router: not a MoE layer or bad rows");
+  CK(cudaStreamSynchronize(ctx->st), "sync");
+  const size_t MR = ctx->MR(), k = c.top_k, E = c.n_experts;
+  if (idx) CK(cudaMemcpy(idx, ctx->r_idx + layer * MR * k, rows * k * 4, cudaMemcpyDeviceToHost), "router read");
+  if (w) CK(cudaMemcpy(w, ctx->r_w + layer * MR * k, rows * k * 4, cudaMemcpyDeviceToHost), "router read");
+  if (count) CK(cudaMemcpy(count, ctx->r_count + layer * E, E * 4, cudaMemcpyDeviceToHost), "router read");
+  if (offset) CK(cudaMemcpy(offset, ctx->r_offset + layer * (E + 1), (E + 1) * 4, cudaMemcpyDeviceToHost), "router read");
+  if (perm) CK(cudaMemcpy(perm, ctx->r_perm + layer * MR * k, rows * k * 4, cudaMemcpyDeviceToHost), "router read");
+  return UOCR_OK;
+}
+
+uocr_status uocr_profile(uocr_ctx* ctx, int32_t rows, int32_t input_kind, const int32_t* token_ids,
+                         const uint16_t* x, const int32_t* positions, const char** names, float* ms,
+                         int32_t* n_inout) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  if (!positions || !names || !ms || !n_inout) return ctx->fail(UOCR_E_INVALID_ARG, "NULL pointer");
+  const bool ids = input_kind == 0;
+  if (ids && (!token_ids || ctx->cfg.vocab <= 0)) return ctx->fail(UOCR_E_INVALID_ARG, "token ids need a vocabulary");
+  if (!ids && !x) return ctx->fail(UOCR_E_INVALID_ARG, "x is NULL");
+  uocr_status s = step_prologue(ctx, rows);
+  if (s != UOCR_OK) return s;
+  if (ids)
+    CK(cudaMemcpyAsync(ctx->ids_buf, token_ids, rows * 4, cudaMemcpyDeviceToDevice, ctx->st), "ids copy");
+  else
+    CK(cudaMemcpyAsync(ctx->x_in, x, (size_t)rows * ctx->cfg.hidden * 2, cudaMemcpyDeviceToDevice, ctx->st), "x copy");
+  CK(cudaMemcpyAsync(ctx->pos_buf, positions, rows * 4, cudaMemcpyDeviceToDevice, ctx->st), "positions copy");
+  Prof prof;
+  s = enqueue_step(ctx, StepShape{rows, ids, ctx->cfg.vocab > 0, false, false}, &prof);
+  CK(cudaStreamSynchronize(ctx->st), "profile step");
+  std::vector<const char*> nm;
+  std::vector<float> tot;
+  for (auto& e : prof.ev) {
+    float t = 0.f;
+    cudaEventElapsedTime(&t, e.second.first, e.second.second);
+    cudaEventDestroy(e.second.first);
+    cudaEventDestroy(e.second.second);
+    size_t i = 0;
+    while (i < nm.size() && std::strcmp(nm[i], e.first) != 0) ++i;
+    if (i == nm.size()) {
+      nm.push_back(e.first);
+      tot.push_back(0.f);
+    }
+    tot[i] += t;
+  }
+  if (s != UOCR_OK) return s;
+  const int n = (int)nm.size() < *n_inout ? (int)nm.size() : *n_inout;
+  for (int i = 0; i < n; ++i) {
+    names[i] = nm[i];
+    ms[i] = tot[i];
+  }
+  *n_inout = (int)nm.size();
+  return step_epilogue(ctx);
+}
+
+}  // extern "C"

@@ -1,0 +1,100 @@
+"""GPU parity of the decode step against the float64 oracle on small models.
+
+Sizes are chosen so the oracle finishes in seconds while every kernel still
+spans several tiles and a ragged tail: rows that are not a multiple of the
+8-token n-tile, several token groups (40 rows), a vocabulary that is not a
+multiple of the 16-row slab (1000), ring wrap-around (ring of 8 slots), split
+attention with empty splits, every weight format and every (routed, shared)
+expert format pair the library supports.
+"""
+import numpy as np
+import pytest
+
+from quantized_moe_decode_gb300 import synth
+
+from helpers import make_ctx, make_oracle
+from parity import run_parity
+
+pytestmark = pytest.mark.gpu
+
+Q8, Q4, I8 = synth.Q8_0, synth.Q4_0, synth.I8ASYM
+
+
+def _dense(**kw):
+    base = dict(hidden=256, n_heads=4, head_dim=64, n_layers=2, n_dense_layers=2, dense_inter=512,
+                fmt_attn=Q8, fmt_dense=Q8, prefix_len=20, ring_len=8, max_rows=3)
+    base.update(kw)
+    return synth.ModelConfig(**base)
+
+
+def _moe(**kw):
+    base = dict(hidden=256, n_heads=2, head_dim=128, n_layers=3, n_dense_layers=1, dense_inter=512,
+                n_experts=16, top_k=4, n_shared=2, expert_inter=128, vocab=1000, fmt_attn=Q8, fmt_dense=Q8,
+                fmt_shared=Q8, fmt_routed=Q4, prefix_len=12, ring_len=8, max_rows=5)
+    base.update(kw)
+    return synth.ModelConfig(**base)
+
+
+def _run(wl, steps, **kw):
+    ctx = make_ctx(wl)
+    orc = make_oracle(wl)
+    st = run_parity(ctx, wl, steps, orc, **kw)
+    print(f"\n{wl.name}: {st.steps} steps, {st.float_checks} float checks (worst rel-L2 {st.worst_rel:.2e}, "
+          f"max-abs {st.worst_abs:.2e}), router {st.router_checks} ({st.router_near_ties} near ties), "
+          f"ids {st.id_checks} ({st.id_near_ties} near ties), kv {st.kv_checks}")
+    ctx.close()
+    return st
+
+
+def test_dense_q8_ring_wrap(cuda):
+    wl = synth.make_workload("dense_q8", _dense(), 3, 20, 100)
+    st = _run(wl, 20)
+    assert st.kv_checks == 20 * 2 * 3
+
+
+def test_dense_q4_attention_i8asym_mlp_with_sinks(cuda):
+    cfg = _dense(fmt_attn=Q4, fmt_dense=I8, use_sink=1, head_dim=32, n_heads=8, prefix_len=5)
+    wl = synth.make_workload("dense_q4_i8_sink", cfg, 3, 12, 101)
+    _run(wl, 12)
+
+
+def test_dense_i8asym_sink_head_dim_64_single_row(cuda):
+    cfg = _dense(fmt_attn=I8, fmt_dense=I8, use_sink=1, prefix_len=33, max_rows=1, hidden=128,
+                 n_heads=2, dense_inter=256)
+    wl = synth.make_workload("dense_i8_sink", cfg, 1, 12, 102)
+    _run(wl, 12)
+
+
+def test_moe_prefill_by_decode_then_greedy_with_lm_head(cuda):
+    wl = synth.make_workload("moe_lm", _moe(), 5, 12, 103, prefix="prefill", n_prefill_embeds=8,
+                             step_input="ids")
+    st = _run(wl, 12)
+    assert st.id_checks >= 5 * 12
+    assert st.router_checks > 0
+
+
+def test_moe_forty_rows_three_token_groups(cuda):
+    cfg = _moe(max_rows=40, fmt_shared=Q4, fmt_routed=Q8, vocab=0, prefix_len=10)
+    wl = synth.make_workload("moe_40rows", cfg, 40, 10, 104)
+    _run(wl, 10)
+
+
+def test_moe_int8_asym_experts_nine_rows(cuda):
+    cfg = _moe(max_rows=9, fmt_attn=I8, fmt_dense=I8, fmt_shared=I8, fmt_routed=I8, vocab=0, n_shared=1,
+               prefix_len=7)
+    wl = synth.make_workload("moe_i8", cfg, 9, 10, 105)
+    _run(wl, 10)
+
+
+def test_moe_q4_shared_q4_routed_no_shared_dense_free(cuda):
+    cfg = _moe(n_dense_layers=0, n_layers=2, n_shared=0, fmt_routed=Q4, vocab=0, prefix_len=3, max_rows=2,
+               top_k=2, n_experts=8)
+    wl = synth.make_workload("moe_noshared", cfg, 2, 12, 106)
+    _run(wl, 12)
+
+
+def test_moe_q4_both_with_lm_head_rows_12(cuda):
+    cfg = _moe(fmt_shared=Q4, fmt_routed=Q4, max_rows=12, prefix_len=6)
+    wl = synth.make_workload("moe_q4_lm", cfg, 12, 6, 107, prefix="prefill", n_prefill_embeds=3,
+                             step_input="ids")
+    _run(wl, 6)
