@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Decode throughput of the quantized MoE OCR decoder on one GB300.
+
+Workload (one "step" = one decode step of every row through the whole path:
+embedding, 12 layers of RMSNorm/QKV/RoPE/KV append/attention/O-proj and the
+dense MLP or router + experts + combine, final norm, LM head, argmax):
+the 12-layer DeepSeek-V2-style decoder (hidden 1280, 10x128 heads, layer 0
+dense MLP 3584, layers 1-11 with 64 routed top-6 experts + 2 shared of 896),
+Q8_0 attention/dense/shared, Q4_0 routed experts, fp16 LM head over 102400
+tokens, 8 rows, prefix of 256 image embeddings + 32 prompt tokens built by
+decode steps, then greedy decoding through the 128-slot ring.  Weights,
+prefix and prompt are seeded synthetic data (seed 2).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+_CORES = os.cpu_count() or 1
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_moe_decode_gb300 import synth  # noqa: E402
+
+METRIC = "decode tokens/s (rows x steps/s) and achieved HBM GB/s vs GB300 peak, 1 GPU"
+WORKLOAD = "full_b8"
+BPW = {synth.F16: 2.0, synth.Q8_0: 34 / 32, synth.Q4_0: 18 / 32, synth.I8ASYM: 36 / 32}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ algorithmic bytes
+def class_bytes(cfg, rows, positions, distinct):
+    """Bytes the method must move per launch of each kernel class in one step.
+
+    Weights touched (canonical block bytes: Q8_0 34/32, Q4_0 18/32 B per
+    weight, fp16 2 B), KV read/written, and the activation vectors each class
+    reads or writes.  distinct[l] = experts that received a token at layer l.
+    """
+    H, S, V, L = cfg.hidden, cfg.n_heads * cfg.head_dim, cfg.vocab, cfg.n_layers
+    P, R = cfg.prefix_len, cfg.ring_len
+    act = rows * H * 4
+    out = {}
+    out["embed"] = [rows * H * 2 + act]
+    out["qkv"] = [3 * S * H * BPW[cfg.fmt_attn] + act + rows * S * (4 + 2 * 2)] * L
+    kv = 0
+    for p in positions:
+        n_valid = p + 1 if p < P else P + min(p - P + 1, R)
+        kv += n_valid * 2 * S * 2
+    out["attention"] = [kv + rows * S * (4 + 2)] * L
+    out["o_proj"] = [H * S * BPW[cfg.fmt_attn] + rows * S * 2 + 2 * act] * L
+    Ie, Ish = cfg.expert_inter, cfg.n_shared * cfg.expert_inter
+    for l in range(L):
+        if cfg.is_dense(l):
+            I = cfg.dense_inter
+            out.setdefault("mlp_gate_up", []).append(2 * I * H * BPW[cfg.fmt_dense] + act + rows * I * 2)
+            out.setdefault("mlp_down", []).append(H * I * BPW[cfg.fmt_dense] + rows * I * 2 + 2 * act)
+        else:
+            U = distinct[l]
+            out.setdefault("router", []).append(cfg.n_experts * H * 2 + act + rows * H * 2)
+            out.setdefault("expert_gate_up", []).append(
+                U * 2 * Ie * H * BPW[cfg.fmt_routed] + 2 * Ish * H * BPW[cfg.fmt_shared]
+                + rows * H * 2 + rows * (cfg.top_k * Ie + Ish) * 2)
+            out.setdefault("expert_down_combine", []).append(
+                U * H * Ie * BPW[cfg.fmt_routed] + H * Ish * BPW[cfg.fmt_shared]
+                + rows * (cfg.top_k * Ie + Ish) * 2 + 2 * act)
+    if V:
+        out["lm_head_argmax"] = [V * H * 2 + act + rows * 8]
+    return out
+
+
+def sources_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_moe_decode_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_class):
+    """DRAM bytes per launch of a kernel class from the committed ncu summary,
+    valid only while the kernel sources are unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    sha = sources_sha()
+    for line in open(p):
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if f.get("class") == kernel_class and f.get("sources_sha") == sha:
+            return float(f["dram_bytes_per_launch"])
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU / reference arm
+def time_oracle(wl, rows, min_s, max_steps, warm=2):
+    """Oracle decode steps (the prefix's own decode steps, embedding inputs,
+    LM head included) over `rows` rows; returns (steps, seconds)."""
+    import oracle
+
+    m = oracle.OracleModel(wl.cfg, wl.tensors, rows, cache="float64")
+    x = wl.prefill_embeds
+    for p in range(warm):
+        m.step(np.full(rows, p, np.int32), x=x[:rows, p])
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_steps and (time.perf_counter() - t0) < min_s:
+        p = warm + n
+        m.step(np.full(rows, p, np.int32), x=x[:rows, p])
+        n += 1
+    return n, time.perf_counter() - t0
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl = synth.workload(WORKLOAD, steps=0)
+    K, W = args.steps, args.warmup
+    import oracle  # noqa: F401
+
+    rows = 1
+    m_steps = min(K, 40)
+    n, dt = time_oracle(wl, rows, min_s=90.0, max_steps=m_steps, warm=max(W, 2))
+    v = rows * n / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": n, "steps_requested": K, "warmup": W, "ms_per_step": 1e3 * dt / max(n, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": "full 12-layer MoE decoder, 8 rows (oracle sample: 1 row)",
+                                            "rows": 8, "prefix": 288, "ring": 128, "seed": 2},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _CORES, "kind": "oracle",
+                             "sample": f"1 row x {n} decode steps of the workload's prefix positions, float64 "
+                                       f"NumPy oracle, weight cache warmed on {max(W, 2)} steps, capped at 90 s"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world):
+    import torch
+
+    from quantized_moe_decode_gb300 import binding, build
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist_mod.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = dist_mod
+    if rank == 0:
+        build.build()
+    if dist:
+        dist.barrier()
+    t_setup = time.perf_counter()
+    wl = synth.workload(WORKLOAD, steps=0)
+    cfg, rows = wl.cfg, wl.rows
+    stream = torch.cuda.current_stream()
+    ctx = binding.Context(cfg, max_rows=rows, stream=stream.cuda_stream, device=local)
+    binding.load_workload(ctx, wl)
+    dev = torch.device("cuda", local)
+    pos = torch.zeros(rows, dtype=torch.int32, device=dev)
+    ids = torch.zeros(rows, dtype=torch.int32, device=dev)
+    nxt = torch.zeros(rows, dtype=torch.int32, device=dev)
+    x = torch.zeros((rows, cfg.hidden), dtype=torch.int16, device=dev)
+    ne = wl.prefill_embeds.shape[1]
+    emb_all = torch.from_numpy(wl.prefill_embeds.view(np.int16)).to(dev)
+    ids_all = torch.from_numpy(wl.prefill_ids).to(dev)
+    for p in range(cfg.prefix_len):  # prefix built by decode steps (untimed)
+        pos.fill_(p)
+        if p < ne:
+            x.copy_(emb_all[:, p])
+            ctx.uocr_decode_step_embeds(rows, x.data_ptr(), pos.data_ptr())
+        else:
+            ids.copy_(ids_all[:, p - ne])
+            ctx.uocr_decode_step(rows, ids.data_ptr(), pos.data_ptr(), nxt.data_ptr())
+    ctx.uocr_sync()
+    ids.copy_(nxt)
+    start = cfg.prefix_len
+    K, W = args.steps, args.warmup
+    out = torch.zeros((max(K, W, 1), rows), dtype=torch.int32, device=dev)
+    pos.fill_(start)
+    ctx.uocr_generate(rows, ids.data_ptr(), pos.data_ptr(), W, out.data_ptr())
+    ctx.uocr_sync()
+    if W:
+        ids.copy_(out[W - 1])
+    pos.fill_(start + W)
+    torch.cuda.synchronize()
+    log(f"[bench] setup {time.perf_counter() - t_setup:.1f}s")
+
+    # ---- timed region: K greedy steps chained on the device
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    ctx.uocr_generate(rows, ids.data_ptr(), pos.data_ptr(), K, out.data_ptr())
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = clk.stop()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ctx.uocr_sync()
+    gen_ids = out[:K].cpu().numpy()
+    step_pos = start + W + K
+
+    # ---- per-kernel-class durations (un-graphed steps on the library stream, CUDA events)
+    n_prof = 5
+    prof = {}
+    distinct = {}
+    pos.fill_(step_pos)
+    ids.copy_(out[K - 1])
+    for _ in range(n_prof):
+        t = ctx.uocr_profile(rows, 0, ids.data_ptr(), 0, pos.data_ptr())
+        for k_, v_ in t.items():
+            prof[k_] = prof.get(k_, 0.0) + v_ / n_prof
+    for l in range(cfg.n_layers):
+        if not cfg.is_dense(l):
+            distinct[l] = int(np.count_nonzero(ctx.uocr_debug_router(l, rows)["count"]))
+    cb = class_bytes(cfg, rows, [step_pos] * rows, distinct)
+    launches_per_step = sum(len(v) for v in cb.values())
+    hbm_peak, peak_kind = peaks()
+    kernels = {}
+    for name, t_ms in prof.items():
+        b = sum(cb.get(name, [0]))
+        n_l = len(cb.get(name, [1]))
+        kernels[name] = {"ms_per_step": t_ms, "launches_per_step": n_l, "bytes_per_launch": b / n_l,
+                         "gbs": b / (t_ms * 1e-3) / 1e9 if t_ms > 0 else None}
+    dom = max(kernels, key=lambda k_: kernels[k_]["ms_per_step"])
+    dk = kernels[dom]
+    achieved = dk["gbs"]
+    step_bytes = sum(sum(v) for v in cb.values())
+    ms_per_step = ms / K
+    value = world * rows * K / (ms * 1e-3)
+
+    # ---- end to end through the host-buffer entry point (pinned host buffers)
+    K_e2e = min(K, 200)
+    h_ids = torch.empty(rows, dtype=torch.int32, pin_memory=True)
+    h_pos = torch.empty(rows, dtype=torch.int32, pin_memory=True)
+    h_out = torch.empty(rows, dtype=torch.int32, pin_memory=True)
+    h_ids.copy_(torch.from_numpy(gen_ids[-1]))
+    lib = ctx.lib
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(K_e2e):
+        h_pos.fill_(step_pos + s)
+        st_ = lib.uocr_decode_step_host(ctx.h, rows, h_ids.data_ptr(), h_pos.data_ptr(), h_out.data_ptr())
+        if st_ != 0:
+            raise RuntimeError(lib.uocr_last_error(ctx.h).decode())
+        h_ids.copy_(h_out)
+    e2e_s = time.perf_counter() - t0
+    if dist:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": world * rows * K_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": rows * 4 * 2,
+           "d2h_bytes_per_step": rows * 4, "steps": K_e2e}
+
+    if rank != 0:
+        ctx.close()
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        n_c, dt_c = time_oracle(wl, rows, min_s=15.0, max_steps=20)
+        cpu = {"value": rows * n_c / dt_c, "unit": "tokens/s", "cores": _CORES, "kind": "oracle",
+               "sample": f"{rows} rows x {n_c} decode steps of the workload's prefix positions (float64 NumPy "
+                         f"oracle, weight cache warmed on 2 steps)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 activations x Q8_0/Q4_0 weights, f32 accumulate", "data": "synthetic",
+        "config": {"workload": "full 12-layer MoE decoder (hidden 1280, 10x128, 64 routed top-6 + 2 shared, "
+                               "vocab 102400), 8 rows, prefix 256 image embeds + 32 prompt ids, 128-slot ring, "
+                               "greedy", "rows": rows, "global_batch": rows * world, "prefix": cfg.prefix_len,
+                   "ring": cfg.ring_len, "positions": [start + W, step_pos], "seed": 2,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2: %.2f GB touched per step" % (step_bytes / 1e9)},
+        "hbm_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
+        "hbm_frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
+        "bytes_per_step": step_bytes,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak if achieved else None, "traffic": ncu_traffic(dom),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s"},
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    ctx.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()
