@@ -254,6 +254,33 @@ UOCR_API uocr_status uocr_profile(uocr_ctx* ctx, int32_t rows, int32_t input_kin
                          const int32_t* token_ids, const uint16_t* x, const int32_t* positions,
                          const char** names, float* ms, int32_t* n_inout);
 
+/* Final RMSNorm + LM head + greedy argmax on final hidden states the caller
+ * provides, without allocating any memory.  (The pages have no counterpart:
+ * this entry point exists for callers, not for the method.)
+ *
+ * Who needs it: code that may not call cudaMalloc/cudaFree while it runs,
+ * e.g. a serving loop whose device memory is owned by a fixed pool (cudaMalloc
+ * synchronises the device and stalls every other stream), or a host framework
+ * that hands the library only the buffers it already owns.  The regular steps
+ * keep their scratch in the context arena; this call instead keeps the
+ * kernel's scratch (one argmax key per row and a CTA counter, 520 bytes) in a
+ * static device array of the library, which every GPU that loads the library
+ * holds until the process exits.
+ *   hidden    device fp32 [rows][hidden]: residual stream after the last layer
+ *   next_ids  device int32 [rows]: argmax id per row (lowest index on ties)
+ *   logits    device fp32 [rows][vocab] or NULL
+ *   stream    cudaStream_t the work is enqueued on (0 = legacy default stream)
+ * rows must be in [1, 64] (the scratch capacity), else UOCR_E_INVALID_ARG and
+ * nothing is launched.  Uses the context's loaded LM head and final norm.
+ * The first call on a device looks up the scratch address on that device
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the one scratch array and each call clears it first, so
+ * calls whose work overlaps on the GPU (on different streams, or from
+ * different contexts on the same device) race and must be serialised by the
+ * caller.  Asynchronous with respect to the host.                           */
+UOCR_API uocr_status uocr_lm_head_argmax_noalloc(uocr_ctx* ctx, int32_t rows, const float* hidden,
+                                                 int32_t* next_ids, float* logits, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

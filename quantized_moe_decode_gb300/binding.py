@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "OK", 1: "E_INVALID_ARG", 2: "E_OOM", 3: "E_BUDGET", 4: "E_FO
 EXPORTED = ["uocr_create", "uocr_destroy", "uocr_load_weights", "uocr_kv_write_prefix", "uocr_kv_read",
             "uocr_set_sinks", "uocr_decode_step", "uocr_decode_step_embeds", "uocr_decode_step_host",
             "uocr_generate", "uocr_kv_reset", "uocr_sync", "uocr_last_error", "uocr_memory_report",
-            "uocr_debug_hidden", "uocr_debug_router", "uocr_profile"]
+            "uocr_debug_hidden", "uocr_debug_router", "uocr_profile", "uocr_lm_head_argmax_noalloc"]
 
 
 class uocr_config(C.Structure):
@@ -74,6 +74,7 @@ def load(path: str = LIB_PATH):
         "uocr_debug_hidden": ([P, I, I, P], I),
         "uocr_debug_router": ([P, I, I, P, P, P, P, P], I),
         "uocr_profile": ([P, I, I, P, P, P, C.POINTER(C.c_char_p), C.POINTER(C.c_float), C.POINTER(I)], I),
+        "uocr_lm_head_argmax_noalloc": ([P, I, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -179,6 +180,10 @@ class Context:
 
     def uocr_generate(self, rows, ids_ptr, pos_ptr, n_steps, out_ptr):
         self._ck(self.lib.uocr_generate(self.h, rows, ids_ptr, pos_ptr, n_steps, out_ptr))
+
+    def uocr_lm_head_argmax_noalloc(self, rows, hidden_ptr, next_ptr, logits_ptr=0, stream=0):
+        self._ck(self.lib.uocr_lm_head_argmax_noalloc(self.h, rows, hidden_ptr, next_ptr, logits_ptr or None,
+                                                      stream or None))
 
     def uocr_kv_reset(self, row=-1, keep_prefix=1):
         self._ck(self.lib.uocr_kv_reset(self.h, row, keep_prefix))

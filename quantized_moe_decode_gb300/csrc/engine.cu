@@ -796,6 +796,39 @@ static uocr_status check_complete(uocr_ctx* ctx) {
   return UOCR_OK;
 }
 
+// ------------------------------------------------------------------ scratch-free LM head
+// Scratch of uocr_lm_head_argmax_noalloc: one 64-bit argmax key per row (up to
+// kNoAllocMaxRows) followed by the kernel's finished-CTA counter.  It lives in
+// this file-scope device array, so every GPU that loads the library holds these
+// 520 bytes until the process exits and no call ever allocates.  Host code
+// must not pass the symbol itself to a kernel: its device address is fetched
+// per device with cudaGetSymbolAddress.
+constexpr int kNoAllocMaxRows = 64;
+static __device__ __align__(256) unsigned long long g_lm_noalloc_scratch[kNoAllocMaxRows + 1];
+static std::mutex g_noalloc_mu;
+static std::map<int, unsigned long long*> g_noalloc_addr;  // device ordinal -> device address
+
+// Looks the scratch address up once per device, with that device current.
+static cudaError_t noalloc_scratch(int device, unsigned long long** out) {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  auto it = g_noalloc_addr.find(device);
+  if (it != g_noalloc_addr.end()) {
+    *out = it->second;
+    return cudaSuccess;
+  }
+  int prev = 0;
+  cudaError_t e = cudaGetDevice(&prev);
+  if (e != cudaSuccess) return e;
+  if (prev != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_lm_noalloc_scratch);
+  if (prev != device) cudaSetDevice(prev);
+  if (e != cudaSuccess) return e;
+  g_noalloc_addr[device] = reinterpret_cast<unsigned long long*>(p);
+  *out = reinterpret_cast<unsigned long long*>(p);
+  return cudaSuccess;
+}
+
 // ------------------------------------------------------------------ C ABI
 extern "C" {
 
@@ -1165,6 +1198,46 @@ uocr_status uocr_profile(uocr_ctx* ctx, int32_t rows, int32_t input_kind, const 
   }
   *n_inout = (int)nm.size();
   return step_epilogue(ctx);
+}
+
+uocr_status uocr_lm_head_argmax_noalloc(uocr_ctx* ctx, int32_t rows, const float* hidden, int32_t* next_ids,
+                                        float* logits, void* stream) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  const uocr_config& c = ctx->cfg;
+  if (c.vocab <= 0) return ctx->fail(UOCR_E_STATE, "lm_head_argmax_noalloc needs a vocabulary");
+  if (!hidden || !next_ids) return ctx->fail(UOCR_E_INVALID_ARG, "NULL device pointer");
+  if (rows < 1 || rows > kNoAllocMaxRows)
+    return ctx->fail(UOCR_E_INVALID_ARG, "rows %d outside [1, %d], the capacity of the static scratch", rows,
+                     kNoAllocMaxRows);
+  uocr_status s = check_complete(ctx);
+  if (s != UOCR_OK) return s;
+  unsigned long long* scratch = nullptr;
+  CK(noalloc_scratch(c.device, &scratch), "scratch address");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the keys and the counter must start at zero; a previous call leaves them zero
+  // when it completes, but clear them anyway in case it did not
+  CK(cudaMemsetAsync(scratch, 0, sizeof(unsigned long long) * (kNoAllocMaxRows + 1), st), "scratch clear");
+  const int nt = rows <= 8 ? 1 : 2;
+  const int tg = (rows + nt * 8 - 1) / (nt * 8);
+  int gx = 4 * ctx->n_sm / tg;
+  if (gx < 1) gx = 1;
+  if (gx > ctx->lm.n_slabs) gx = ctx->lm.n_slabs;
+  GemvArgs la{};
+  la.w = ctx->lm.view();
+  la.sp = plan_stage(nt, c.hidden, F16);
+  la.ntok = rows;
+  la.xf = hidden;
+  la.ld_src = c.hidden;
+  la.norm_w = ctx->final_norm;
+  la.eps = c.rms_eps;
+  la.out_f = logits;
+  la.n_valid = c.vocab;
+  la.keys = scratch;
+  la.counter = reinterpret_cast<int*>(scratch + kNoAllocMaxRows);
+  la.next_ids = next_ids;
+  CK(launch_gemv(F16, SRC_NORM, EPI_LOGITS, la, gx, tg, st), "lm head launch");
+  return UOCR_OK;
 }
 
 }  // extern "C"
