@@ -13,7 +13,8 @@ import os
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libuocr.so")
+# UOCR_LIB selects another build of the same library (tuning variants)
+LIB_PATH = os.environ.get("UOCR_LIB") or os.path.join(_PKG, "libuocr.so")
 
 UOCR_OK, UOCR_E_INVALID_ARG, UOCR_E_OOM, UOCR_E_BUDGET, UOCR_E_FORMAT = 0, 1, 2, 3, 4
 UOCR_E_STATE, UOCR_E_CUDA, UOCR_E_POSITION, UOCR_E_TOKEN = 5, 6, 7, 8

@@ -18,12 +18,24 @@
 
 namespace uocr {
 
+// Slots per shared-memory stage: 16 KB of keys and 16 KB of values.
+template <int D>
+struct AttnCfg {
+  static constexpr int SUB = 8192 / D;
+  static constexpr int STAGE = 2 * SUB * D * 2;  // K then V
+};
+
+int attn_smem_bytes(int D) { return 2 * (2 * (8192 / D) * D * 2) + 64; }
+
 template <int D>
 __global__ void __launch_bounds__(128) k_attn(const AttnArgs a) {
   constexpr int LPS = D / 8;    // lanes per slot
   constexpr int G = 32 / LPS;   // slots per load instruction
   constexpr int SPI = 4 * G;    // slots per warp iteration
   constexpr int NW = 4;
+  constexpr int SUB = AttnCfg<D>::SUB, STAGE = AttnCfg<D>::STAGE;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * STAGE);
   __shared__ float sm_m[NW], sm_l[NW];
   __shared__ float sm_acc[NW][D];
   __shared__ int s_last;
@@ -31,11 +43,34 @@ __global__ void __launch_bounds__(128) k_attn(const AttnArgs a) {
   const int split = blockIdx.x, head = blockIdx.y, row = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane / LPS, li = lane % LPS;
+  // positions come from a copy that completed before the step's first kernel
   int p = a.pos[row];
   if (p < 0) p = 0;
   const int n_valid = (p < a.P) ? p + 1 : a.P + min(p - a.P + 1, a.R);
   const int s_begin = split * a.chunk;
   const int s_end = min(n_valid, s_begin + a.chunk);
+  const int n_sub = s_end > s_begin ? (s_end - s_begin + SUB - 1) / SUB : 0;
+  const __half* Kg = a.kv + (((size_t)row * 2 + 0) * a.nh + head) * (size_t)a.SL * D;
+  const __half* Vg = a.kv + (((size_t)row * 2 + 1) * a.nh + head) * (size_t)a.SL * D;
+  auto issue = [&](int sb) {
+    const int s0 = s_begin + sb * SUB, n = min(SUB, s_end - s0);
+    uint8_t* st = smem + (sb & 1) * STAGE;
+    uint64_t* b = bar + (sb & 1);
+    mbar_expect_tx(b, 2u * n * D * 2);
+    bulk_g2s(st, Kg + (size_t)s0 * D, n * D * 2, b);
+    bulk_g2s(st + SUB * D * 2, Vg + (size_t)s0 * D, n * D * 2, b);
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    mbar_init(bar + 1, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // every slot but the current token's was written by earlier steps: stream them now
+  if (threadIdx.x == 0)
+    for (int sb = 0; sb < n_sub && sb < 2; ++sb) issue(sb);
+  pdl_launch_dependents();
+  pdl_wait();  // q and the current slot come from the QKV kernel
 
   float qv[8];
   {
@@ -43,68 +78,92 @@ __global__ void __launch_bounds__(128) k_attn(const AttnArgs a) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) qv[i] = qp[i] * a.scale;
   }
-  const __half* Kb = a.kv + (((size_t)row * 2 + 0) * a.nh + head) * (size_t)a.SL * D + 8 * li;
-  const __half* Vb = a.kv + (((size_t)row * 2 + 1) * a.nh + head) * (size_t)a.SL * D + 8 * li;
+  const int cur = p < a.P ? p : a.P + (p - a.P) % a.R;
 
   float m = -INFINITY, l = 0.f;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 
-  for (int base = s_begin + warp * SPI; base < s_end; base += NW * SPI) {
-    uint4 kr[4], vr[4];
-    bool ok[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int slot = base + j * G + grp;
-      ok[j] = slot < s_end;
-      if (ok[j]) {
-        kr[j] = ldg_stream(Kb + (size_t)slot * D);
-        vr[j] = ldg_stream(Vb + (size_t)slot * D);
-      } else {
-        kr[j] = make_uint4(0u, 0u, 0u, 0u);
-        vr[j] = kr[j];
-      }
+  for (int sb = 0; sb < n_sub; ++sb) {
+    const int s0 = s_begin + sb * SUB, n = min(SUB, s_end - s0);
+    int bad = 0;
+    if (threadIdx.x == 0) {
+      bad = !mbar_wait(bar + (sb & 1), (uint32_t)((sb >> 1) & 1));
+      if (bad) atomicOr(a.status, kStatusTimeout);
     }
-    float sc[4];
+    if (__syncthreads_or(bad)) {
+      if (threadIdx.x == 0 && sb + 1 < n_sub) mbar_wait(bar + ((sb + 1) & 1), (uint32_t)(((sb + 1) >> 1) & 1));
+      return;
+    }
+    const __half* Ks = reinterpret_cast<const __half*>(smem + (sb & 1) * STAGE);
+    const __half* Vs = Ks + SUB * D;
+    if (cur >= s0 && cur < s0 + n) {  // the row this step just wrote
+      for (int i = threadIdx.x; i < D / 8; i += blockDim.x) {
+        *reinterpret_cast<uint4*>(const_cast<__half*>(Ks) + (cur - s0) * D + 8 * i) =
+            *reinterpret_cast<const uint4*>(Kg + (size_t)cur * D + 8 * i);
+        *reinterpret_cast<uint4*>(const_cast<__half*>(Vs) + (cur - s0) * D + 8 * i) =
+            *reinterpret_cast<const uint4*>(Vg + (size_t)cur * D + 8 * i);
+      }
+      __syncthreads();
+    }
+    for (int base = warp * SPI; base < n; base += NW * SPI) {
+      uint4 kr[4], vr[4];
+      bool ok[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __half2* kh = reinterpret_cast<const __half2*>(&kr[j]);
-      float d = 0.f;
+      for (int j = 0; j < 4; ++j) {
+        const int slot = base + j * G + grp;
+        ok[j] = slot < n;
+        if (ok[j]) {
+          kr[j] = lds128(Ks + slot * D + 8 * li);
+          vr[j] = lds128(Vs + slot * D + 8 * li);
+        } else {
+          kr[j] = make_uint4(0u, 0u, 0u, 0u);
+          vr[j] = kr[j];
+        }
+      }
+      float sc[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(kh[i]);
-        d = fmaf(qv[2 * i], f.x, d);
-        d = fmaf(qv[2 * i + 1], f.y, d);
+      for (int j = 0; j < 4; ++j) {
+        const __half2* kh = reinterpret_cast<const __half2*>(&kr[j]);
+        float d = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(kh[i]);
+          d = fmaf(qv[2 * i], f.x, d);
+          d = fmaf(qv[2 * i + 1], f.y, d);
+        }
+#pragma unroll
+        for (int o = LPS / 2; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        sc[j] = ok[j] ? d : -INFINITY;
+      }
+      float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+#pragma unroll
+      for (int o = LPS; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float m_new = fmaxf(m, mx);  // finite: slot `base` is valid
+      const float corr = __expf(m - m_new);
+      float ps = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] *= corr;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float pj = ok[j] ? __expf(sc[j] - m_new) : 0.f;
+        ps += pj;
+        const __half2* vh = reinterpret_cast<const __half2*>(&vr[j]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(vh[i]);
+          acc[2 * i] = fmaf(pj, f.x, acc[2 * i]);
+          acc[2 * i + 1] = fmaf(pj, f.y, acc[2 * i + 1]);
+        }
       }
 #pragma unroll
-      for (int o = LPS / 2; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-      sc[j] = ok[j] ? d : -INFINITY;
+      for (int o = LPS; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+      l = l * corr + ps;
+      m = m_new;
     }
-    float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-#pragma unroll
-    for (int o = LPS; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float m_new = fmaxf(m, mx);  // finite: slot `base` is valid
-    const float corr = __expf(m - m_new);
-    float ps = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] *= corr;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float pj = ok[j] ? __expf(sc[j] - m_new) : 0.f;
-      ps += pj;
-      const __half2* vh = reinterpret_cast<const __half2*>(&vr[j]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(vh[i]);
-        acc[2 * i] = fmaf(pj, f.x, acc[2 * i]);
-        acc[2 * i + 1] = fmaf(pj, f.y, acc[2 * i + 1]);
-      }
-    }
-#pragma unroll
-    for (int o = LPS; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-    l = l * corr + ps;
-    m = m_new;
+    __syncthreads();  // stage consumed
+    if (threadIdx.x == 0 && sb + 2 < n_sub) issue(sb + 2);
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -171,23 +230,33 @@ __global__ void __launch_bounds__(128) k_attn(const AttnArgs a) {
   if (threadIdx.x == 0) atomicExch(a.counter + row * a.nh + head, 0);
 }
 
-cudaError_t launch_attn(const AttnArgs& a, int rows, cudaStream_t st) {
+cudaError_t launch_attn(const AttnArgs& a, int rows, cudaStream_t st, bool pdl) {
   const dim3 grid(a.nsplit, a.nh, rows);
+  const size_t sm = attn_smem_bytes(a.D);
   switch (a.D) {
-    case 16: k_attn<16><<<grid, 128, 0, st>>>(a); break;
-    case 32: k_attn<32><<<grid, 128, 0, st>>>(a); break;
-    case 64: k_attn<64><<<grid, 128, 0, st>>>(a); break;
-    case 128: k_attn<128><<<grid, 128, 0, st>>>(a); break;
-    case 256: k_attn<256><<<grid, 128, 0, st>>>(a); break;
-    default: return cudaErrorInvalidValue;
+    case 16: return launch_kernel(k_attn<16>, grid, dim3(128), sm, st, pdl, a);
+    case 32: return launch_kernel(k_attn<32>, grid, dim3(128), sm, st, pdl, a);
+    case 64: return launch_kernel(k_attn<64>, grid, dim3(128), sm, st, pdl, a);
+    case 128: return launch_kernel(k_attn<128>, grid, dim3(128), sm, st, pdl, a);
+    case 256: return launch_kernel(k_attn<256>, grid, dim3(128), sm, st, pdl, a);
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
+}
+
+static cudaError_t init_attn_attributes() {
+  cudaError_t e = cudaSuccess;
+#define UOCR_A(D_) \
+  if (e == cudaSuccess) e = allow_max_dyn_smem(k_attn<D_>);
+  UOCR_A(16) UOCR_A(32) UOCR_A(64) UOCR_A(128) UOCR_A(256)
+#undef UOCR_A
+  return e;
 }
 
 // ------------------------------------------------------------------ embedding
 // Token ids -> fp16 embedding row, or the given fp16 hidden vectors, widened
 // into the fp32 residual stream; validates ids and positions.
 __global__ void k_embed(const EmbedArgs a) {
+  pdl_launch_dependents();  // the next kernel may start streaming its weights
   const int row = blockIdx.x;
   const __half* src;
   if (a.ids) {
@@ -308,7 +377,8 @@ __global__ void k_pack(const PackArgs a) {
   const PackSrcRef r1 = pack_row(a, 16 * slab + g + 8);
   uint32_t w[4] = {0u, 0u, 0u, 0u};
   if (a.fmt == F16) {
-    const int kk = u * 16 + 2 * t;
+    // unit u (32 inputs) = two 512-byte halves of 16 inputs each; thread handles half u % 2
+    const int kk = (u >> 1) * 32 + (u & 1) * 16 + 2 * t;
     w[0] = get_f16(a, r0, kk) | ((uint32_t)get_f16(a, r0, kk + 1) << 16);
     w[1] = get_f16(a, r1, kk) | ((uint32_t)get_f16(a, r1, kk + 1) << 16);
     w[2] = get_f16(a, r0, kk + 8) | ((uint32_t)get_f16(a, r0, kk + 9) << 16);
@@ -333,7 +403,8 @@ __global__ void k_pack(const PackArgs a) {
       w[2 * ks + 1] = c4 | (c5 << 8) | (c6 << 16) | (c7 << 24);
     }
   }
-  uint4* dst = reinterpret_cast<uint4*>(a.q + ((size_t)slab * a.U + u) * kUnitBytes + lane * 16);
+  // F16: a.U counts 16-input halves here (two per 1024-byte unit); others: 512-byte units
+  uint4* dst = reinterpret_cast<uint4*>(a.q + ((size_t)slab * a.U + u) * 512 + lane * 16);
   *dst = make_uint4(w[0], w[1], w[2], w[3]);
   if (t == 0 && a.fmt != F16) {
     const size_t unit = (size_t)slab * a.U + u;
@@ -387,6 +458,7 @@ cudaError_t init_moe_attributes();
 cudaError_t init_kernel_attributes() {
   cudaError_t e = init_gemv_attributes();
   if (e == cudaSuccess) e = init_moe_attributes();
+  if (e == cudaSuccess) e = init_attn_attributes();
   return e;
 }
 

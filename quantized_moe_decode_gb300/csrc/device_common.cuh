@@ -2,13 +2,13 @@
 //
 // Weight layout ("packed"): a matrix W[N][K] is cut into slabs of 16 output
 // rows; a slab is cut into units of 16 rows x KU inputs, KU = 32 (Q8_0,
-// I8ASYM), 64 (Q4_0) or 16 (F16).  A unit is 512 bytes of codes stored in the
-// register order of the m16n8k16 tensor-core A fragment, so lane L of a warp
-// loads bytes [16L, 16L+16) of the unit with one 128-bit load and holds its
-// fragment(s) without any shuffle.  Scales live in a separate plane, per unit
-// and per fragment row group g = lane/4: Q8_0 {d[g], d[g+8]} (4 B),
-// Q4_0 {d[g][b0], d[g+8][b0], d[g][b1], d[g+8][b1]} (8 B),
-// I8ASYM {s[g], s[g+8], z[g], z[g+8]} (8 B).
+// I8ASYM, F16) or 64 (Q4_0).  A unit holds the codes in the register order of
+// the m16n8k16 tensor-core A fragment: lane L reads bytes [16L, 16L+16) of
+// each 512-byte quarter (one quarter for the 8-bit and 4-bit formats, two for
+// fp16) and holds its fragments without any shuffle.  Scales live in a
+// separate plane, per unit and per fragment row group g = lane/4:
+// Q8_0 {d[g], d[g+8]} (4 B), Q4_0 {d[g][b0], d[g+8][b0], d[g][b1], d[g+8][b1]}
+// (8 B), I8ASYM {s[g], s[g+8], z[g], z[g+8]} (8 B).
 //
 // Dequantisation ("Unlimited-OCR on Apple Silicon with C and Metal",
 // "Quantizzazione": no full fp16 copy of the weights, dequantise inside the
@@ -17,6 +17,14 @@
 // tensor core multiplies them with fp16 activations accumulating in fp32,
 // and the block scale is applied to the fp32 block sum, so no weight value is
 // ever rounded.
+//
+// Weight streaming: in every GEMV-like kernel each warp streams its own
+// units through a private shared-memory ring with 16-byte cp.async copies
+// (D units in flight per warp; on GB300 ordinary loads reach the HBM peak
+// with ~64 KB in flight per SM, while one-dimensional bulk copies need about
+// three times as much).  Kernels are chained with programmatic dependent
+// launch: a kernel's first weight copies are issued before it waits for the
+// kernel that produces its activations.
 #pragma once
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -25,18 +33,39 @@ namespace uocr {
 
 enum Fmt : int { F16 = 0, Q8_0 = 1, Q4_0 = 2, I8ASYM = 3 };
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kUnitBytes = 512;
+// Streaming CTAs: kWarps warps, each streaming its own weight units.
+constexpr int kWarps = 8;
+constexpr int kConsumers = kWarps * 32;
+constexpr int kThreads = kConsumers;
+// Build-time tuning (defaults are the measured best on GB300):
+//   UOCR_RING_DEPTH  units in flight per warp (weight ring slots)
+//   UOCR_MIN_BLOCKS  minimum resident CTAs per SM asked of the compiler
+//   UOCR_UNROLL      units consumed per step of the inner loop (1 or 2)
+#ifndef UOCR_RING_DEPTH
+#define UOCR_RING_DEPTH 8
+#endif
+#ifndef UOCR_MIN_BLOCKS
+#define UOCR_MIN_BLOCKS 2
+#endif
+#ifndef UOCR_UNROLL
+#define UOCR_UNROLL 2
+#endif
+constexpr int kRingDepth = UOCR_RING_DEPTH;
+constexpr int kMinBlocks = UOCR_MIN_BLOCKS;
+constexpr int kUnroll = UOCR_UNROLL;
+static_assert(kRingDepth >= 2 && kRingDepth <= 16, "ring depth");
+static_assert(kUnroll == 1 || kUnroll == 2, "unroll");
+constexpr int kSlotBytes = 1024;         // codes (512 or 1024) + lane-private scales (32 x 8 B)
 
-__host__ __device__ constexpr int unit_k(int fmt) { return fmt == Q4_0 ? 64 : (fmt == F16 ? 16 : 32); }
+__host__ __device__ constexpr int unit_k(int fmt) { return fmt == Q4_0 ? 64 : 32; }
+__host__ __device__ constexpr int unit_bytes(int fmt) { return fmt == F16 ? 1024 : 512; }
 __host__ __device__ constexpr int unit_scale_bytes(int fmt) {
   return fmt == Q8_0 ? 32 : (fmt == F16 ? 0 : 64);
 }
 
 // A packed matrix as the kernels see it.
 struct PMat {
-  const uint8_t* q;   // slabs * U * 512 bytes
+  const uint8_t* q;   // slabs * U * unit_bytes
   const uint8_t* s;   // slabs * U * unit_scale_bytes
   int n_slabs;        // ceil(N_packed / 16)
   int U;              // units per slab = K / unit_k
@@ -45,14 +74,13 @@ struct PMat {
   long long s_stride;
 };
 
+// Device status bits (reported by uocr_sync).
+constexpr int kStatusToken = 1;
+constexpr int kStatusPosition = 2;
+constexpr int kStatusTimeout = 4;
+
 // ------------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;  // (a & b) | c
@@ -69,18 +97,87 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
-  uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(a));
+               : "r"(smem_u32(p)));
 }
 
-__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const void* p) {
-  uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r[0]), "=r"(r[1])
-               : "r"(a));
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(smem_u32(p)));
+  return r;
 }
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// ---- per-thread asynchronous copies (cp.async)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---- mbarrier + bulk copy
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false after kSpinLimit polls (each poll may suspend briefly).
+constexpr uint32_t kSpinLimit = 1u << 22;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// barrier 1 among the consumer warps only (the producer warp never joins it)
+
+// ---- programmatic dependent launch
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t h2_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u32_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
@@ -91,10 +188,10 @@ __device__ __forceinline__ __half2 h2_bits(uint16_t b) {
 // ------------------------------------------------------------------ code -> fp16
 // Q8_0: bytes (b0 b1 b2 b3) of signed codes -> (b0,b1), (b2,b3) as fp16 pairs.
 __device__ __forceinline__ void dq_s8x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;                // code + 128, unsigned
+  const uint32_t u = w ^ 0x80808080u;                      // code + 128, unsigned
   const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);  // fp16 1024 + u0, 1024 + u1
   const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
-  const __half2 bias = h2_bits(0x6480);              // 1152 = 1024 + 128
+  const __half2 bias = h2_bits(0x6480);                    // 1152 = 1024 + 128
   lo = h2_u32(__hsub2(u32_h2(a), bias));
   hi = h2_u32(__hsub2(u32_h2(b), bias));
 }
@@ -103,7 +200,7 @@ __device__ __forceinline__ void dq_s8x4(uint32_t w, uint32_t& lo, uint32_t& hi) 
 __device__ __forceinline__ void dq_u8x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t a = __byte_perm(w, 0x64646464u, 0x4140);
   const uint32_t b = __byte_perm(w, 0x64646464u, 0x4342);
-  const __half2 bias = h2_bits(0x6400);              // 1024
+  const __half2 bias = h2_bits(0x6400);  // 1024
   lo = h2_u32(__hsub2(u32_h2(a), bias));
   hi = h2_u32(__hsub2(u32_h2(b), bias));
 }
@@ -112,14 +209,14 @@ __device__ __forceinline__ void dq_u8x4(uint32_t w, uint32_t& lo, uint32_t& hi) 
 // a0@0 a2@4 a4@8 a6@12 a1@16 a3@20 a5@24 a7@28; returns the four A registers
 // (a0,a1) (a2,a3) (a4,a5) (a6,a7) as fp16 pairs of (code - 8).
 __device__ __forceinline__ void dq_q4(uint32_t w, uint32_t (&r)[4]) {
-  const uint32_t x0 = lop_and_or(w, 0x000F000Fu, 0x64006400u);        // 1024 + n
-  const uint32_t x1 = lop_and_or(w, 0x00F000F0u, 0x64006400u);        // 1024 + 16 n
+  const uint32_t x0 = lop_and_or(w, 0x000F000Fu, 0x64006400u);  // 1024 + n
+  const uint32_t x1 = lop_and_or(w, 0x00F000F0u, 0x64006400u);  // 1024 + 16 n
   const uint32_t w8 = w >> 8;
   const uint32_t x2 = lop_and_or(w8, 0x000F000Fu, 0x64006400u);
   const uint32_t x3 = lop_and_or(w8, 0x00F000F0u, 0x64006400u);
-  const __half2 k1032 = h2_bits(0x6408);   // 1024 + 8
-  const __half2 k1_16 = h2_bits(0x2C00);   // 1/16
-  const __half2 km72 = h2_bits(0xD480);    // -(64 + 8)
+  const __half2 k1032 = h2_bits(0x6408);  // 1024 + 8
+  const __half2 k1_16 = h2_bits(0x2C00);  // 1/16
+  const __half2 km72 = h2_bits(0xD480);   // -(64 + 8)
   r[0] = h2_u32(__hsub2(u32_h2(x0), k1032));
   r[1] = h2_u32(__hfma2(u32_h2(x1), k1_16, km72));
   r[2] = h2_u32(__hsub2(u32_h2(x2), k1032));
@@ -129,43 +226,111 @@ __device__ __forceinline__ void dq_q4(uint32_t w, uint32_t (&r)[4]) {
 __device__ __forceinline__ float half_lo(uint32_t u) { return __half2float(__ushort_as_half((uint16_t)(u & 0xFFFF))); }
 __device__ __forceinline__ float half_hi(uint32_t u) { return __half2float(__ushort_as_half((uint16_t)(u >> 16))); }
 
-// ------------------------------------------------------------------ slab compute
-// Shared-memory activation tile: xs[NT*8 tokens][ldx] fp16, ldx = kc + 8
-// (the +8 makes every 8-row ldmatrix phase hit 32 distinct banks).
-//
-// acc[nt][0..3] follows the m16n8 C fragment: (row g, token 2t), (g, 2t+1),
-// (g+8, 2t), (g+8, 2t+1) of n-tile nt.
+// ------------------------------------------------------------------ B operands
+// A B provider returns, for n-tile nt and the 32 inputs starting at kk, the
+// four B registers of two k-steps: (k 2t..2t+1, token g), (k 2t+8.., g),
+// (k 16+2t.., g), (k 24+2t.., g).
 
-template <int FMT>
-__device__ __forceinline__ uint2 load_scales(const uint8_t* __restrict__ ws, int u, int g) {
-  if constexpr (FMT == Q8_0) {
-    uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(ws + (size_t)u * 32 + g * 4));
-    return make_uint2(v, 0u);
-  } else if constexpr (FMT == Q4_0 || FMT == I8ASYM) {
-    return __ldg(reinterpret_cast<const uint2*>(ws + (size_t)u * 64 + g * 8));
-  } else {
-    return make_uint2(0u, 0u);
+// Activations staged in shared memory xs[row][ldx] (fp16), contiguous tokens.
+struct BSmem {
+  const __half* xs;
+  int ldx;
+  __device__ __forceinline__ void operator()(int nt, int kk, int lane, uint32_t (&b)[4]) const {
+    ldsm_x4(b, xs + (nt * 8 + (lane & 7)) * ldx + kk + 8 * (lane >> 3));
   }
+};
+
+// Activations staged in shared memory, tokens gathered through a row list
+// (rows[] holds the staged row of each token of the item, -1 = padding).
+struct BSmemGather {
+  const __half* xs;
+  int ldx;
+  const int* rows;  // [n-tiles * 8]
+  const __half* zero;  // a zero row of at least 32 halves (padding tokens)
+  __device__ __forceinline__ void operator()(int nt, int kk, int lane, uint32_t (&b)[4]) const {
+    const int r = rows[nt * 8 + (lane & 7)];
+    const __half* p = r >= 0 ? xs + r * ldx + kk + 8 * (lane >> 3) : zero + 8 * (lane >> 3);
+    ldsm_x4(b, p);
+  }
+};
+
+// Activations in global memory already in B-fragment order: for tile tl of 8
+// tokens and 32-input unit u, lane L's 16 bytes at ((tl*K32 + u)*32 + L)*16.
+struct BGlobalFrag {
+  const uint8_t* base;  // first tile of this item
+  int k32;              // K / 32
+  __device__ __forceinline__ void operator()(int nt, int kk, int lane, uint32_t (&b)[4]) const {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + (((size_t)nt * k32 + (kk >> 5)) * 32 + lane) * 16));
+    b[0] = v.x;
+    b[1] = v.y;
+    b[2] = v.z;
+    b[3] = v.w;
+  }
+};
+
+// Activations in shared memory in B-fragment order (a bulk copy of the global
+// layout below): lane L's 16 bytes at ((tl*K32 + u)*32 + L)*16.
+struct BSmemFrag {
+  const uint8_t* base;
+  int k32;
+  __device__ __forceinline__ void operator()(int nt, int kk, int lane, uint32_t (&b)[4]) const {
+    const uint4 v = lds128(base + (((size_t)nt * k32 + (kk >> 5)) * 32 + lane) * 16);
+    b[0] = v.x;
+    b[1] = v.y;
+    b[2] = v.z;
+    b[3] = v.w;
+  }
+};
+
+// Byte offset of activation (token n of tile tl, input i) in B-fragment order.
+__host__ __device__ __forceinline__ size_t bfrag_offset(int tl, int n, int i, int k32) {
+  const int u = i >> 5, kk = i & 31;
+  const int ks = kk >> 4, kw = kk & 15;
+  const int hi8 = kw >> 3, t = (kw & 7) >> 1, hf = kw & 1;
+  const int lane = n * 4 + t;
+  return (((size_t)tl * k32 + u) * 32 + lane) * 16 + (ks * 2 + hi8) * 4 + hf * 2;
 }
 
-// One unit (16 rows x unit_k(FMT) inputs) against every n-tile.
-// xs_k: &xs[0][k_local] where k_local is the unit's first input within the
-// staged chunk; xsum: per-token block sums of the staged activations
-// [NT*8][nblk_chunk] (I8ASYM only), blk = the unit's block within the chunk.
-template <int FMT, int NT>
-__device__ __forceinline__ void unit_mma(float (&acc)[NT][4], uint4 q, uint2 sc, const __half* xs_k, int ldx,
-                                         const float* xsum, int nblk, int blk, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  const int r8 = lane & 7, mi = lane >> 3;
+// Sum of the 32 inputs of the current block for tokens 2t and 2t+1 of an
+// n-tile, from the B registers the lanes already hold (I8ASYM zero points).
+__device__ __forceinline__ void block_sums(const uint32_t (&b)[4], int lane, float& s0, float& s1) {
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(u32_h2(b[i]));
+    s += f.x + f.y;
+  }
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);  // token g's block sum in every lane of group g
+  const int t = lane & 3;
+  s0 = __shfl_sync(0xffffffffu, s, (2 * t) * 4);
+  s1 = __shfl_sync(0xffffffffu, s, (2 * t + 1) * 4);
+}
+
+// ------------------------------------------------------------------ unit compute
+// One unit from shared memory (`a` = the unit's bytes, `sc` = this lane's own
+// copy of its row group's scale entry) against NT n-tiles of B.
+// acc[nt][0..3] follows the m16n8 C fragment: (row g, token 2t), (g, 2t+1),
+// (g+8, 2t), (g+8, 2t+1).
+template <int FMT, int NT, class BP>
+__device__ __forceinline__ void unit_mma(float (&acc)[NT][4], const uint8_t* a, const uint8_t* sc, const BP& bp,
+                                         int kk, int lane, int nt_used) {
   if constexpr (FMT == F16) {
-    const uint32_t A[4] = {q.x, q.y, q.z, q.w};
+    const uint4 q0 = lds128(a + lane * 16);
+    const uint4 q1 = lds128(a + 512 + lane * 16);
+    const uint32_t A0[4] = {q0.x, q0.y, q0.z, q0.w};
+    const uint32_t A1[4] = {q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      uint32_t B[2];
-      ldsm_x2(B, xs_k + (nt * 8 + r8) * ldx + 8 * (mi & 1));
-      mma_16816(acc[nt], A, B[0], B[1]);
+      if (nt < nt_used) {
+        uint32_t B[4];
+        bp(nt, kk, lane, B);
+        mma_16816(acc[nt], A0, B[0], B[1]);
+        mma_16816(acc[nt], A1, B[2], B[3]);
+      }
     }
   } else if constexpr (FMT == Q8_0 || FMT == I8ASYM) {
+    const uint4 q = lds128(a + lane * 16);
     uint32_t A0[4], A1[4];
     if constexpr (FMT == Q8_0) {
       dq_s8x4(q.x, A0[0], A0[1]);
@@ -178,197 +343,354 @@ __device__ __forceinline__ void unit_mma(float (&acc)[NT][4], uint4 q, uint2 sc,
       dq_u8x4(q.z, A1[0], A1[1]);
       dq_u8x4(q.w, A1[2], A1[3]);
     }
-    const float d_lo = half_lo(sc.x), d_hi = half_hi(sc.x);
-    float z_lo = 0.f, z_hi = 0.f;
-    if constexpr (FMT == I8ASYM) {
-      z_lo = half_lo(sc.y);
-      z_hi = half_hi(sc.y);
+    float d_lo, d_hi, z_lo = 0.f, z_hi = 0.f;
+    if constexpr (FMT == Q8_0) {
+      const uint32_t s = *reinterpret_cast<const uint32_t*>(sc);
+      d_lo = half_lo(s);
+      d_hi = half_hi(s);
+    } else {
+      const uint2 s = *reinterpret_cast<const uint2*>(sc);
+      d_lo = half_lo(s.x);
+      d_hi = half_hi(s.x);
+      z_lo = half_lo(s.y);
+      z_hi = half_hi(s.y);
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      uint32_t B[4];
-      ldsm_x4(B, xs_k + (nt * 8 + r8) * ldx + 8 * mi);
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_16816(c, A0, B[0], B[1]);
-      mma_16816(c, A1, B[2], B[3]);
-      if constexpr (FMT == I8ASYM) {
-        const float s0 = xsum[(nt * 8 + 2 * t) * nblk + blk];
-        const float s1 = xsum[(nt * 8 + 2 * t + 1) * nblk + blk];
-        c[0] -= z_lo * s0;
-        c[1] -= z_lo * s1;
-        c[2] -= z_hi * s0;
-        c[3] -= z_hi * s1;
+      if (nt < nt_used) {
+        uint32_t B[4];
+        bp(nt, kk, lane, B);
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(c, A0, B[0], B[1]);
+        mma_16816(c, A1, B[2], B[3]);
+        if constexpr (FMT == I8ASYM) {
+          float s0, s1;
+          block_sums(B, lane, s0, s1);
+          c[0] -= z_lo * s0;
+          c[1] -= z_lo * s1;
+          c[2] -= z_hi * s0;
+          c[3] -= z_hi * s1;
+        }
+        acc[nt][0] = fmaf(d_lo, c[0], acc[nt][0]);
+        acc[nt][1] = fmaf(d_lo, c[1], acc[nt][1]);
+        acc[nt][2] = fmaf(d_hi, c[2], acc[nt][2]);
+        acc[nt][3] = fmaf(d_hi, c[3], acc[nt][3]);
       }
-      acc[nt][0] = fmaf(d_lo, c[0], acc[nt][0]);
-      acc[nt][1] = fmaf(d_lo, c[1], acc[nt][1]);
-      acc[nt][2] = fmaf(d_hi, c[2], acc[nt][2]);
-      acc[nt][3] = fmaf(d_hi, c[3], acc[nt][3]);
     }
   } else {  // Q4_0: 4 k-steps, 2 blocks
+    const uint4 q = lds128(a + lane * 16);
     uint32_t A[4][4];
     dq_q4(q.x, A[0]);
     dq_q4(q.y, A[1]);
     dq_q4(q.z, A[2]);
     dq_q4(q.w, A[3]);
-    const float d0_lo = half_lo(sc.x), d0_hi = half_hi(sc.x);
-    const float d1_lo = half_lo(sc.y), d1_hi = half_hi(sc.y);
+    const uint2 s = *reinterpret_cast<const uint2*>(sc);
+    const float d0_lo = half_lo(s.x), d0_hi = half_hi(s.x);
+    const float d1_lo = half_lo(s.y), d1_hi = half_hi(s.y);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      uint32_t B0[4], B1[4];
-      ldsm_x4(B0, xs_k + (nt * 8 + r8) * ldx + 8 * mi);
-      ldsm_x4(B1, xs_k + (nt * 8 + r8) * ldx + 32 + 8 * mi);
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_16816(c, A[0], B0[0], B0[1]);
-      mma_16816(c, A[1], B0[2], B0[3]);
-      acc[nt][0] = fmaf(d0_lo, c[0], acc[nt][0]);
-      acc[nt][1] = fmaf(d0_lo, c[1], acc[nt][1]);
-      acc[nt][2] = fmaf(d0_hi, c[2], acc[nt][2]);
-      acc[nt][3] = fmaf(d0_hi, c[3], acc[nt][3]);
-      float e[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_16816(e, A[2], B1[0], B1[1]);
-      mma_16816(e, A[3], B1[2], B1[3]);
-      acc[nt][0] = fmaf(d1_lo, e[0], acc[nt][0]);
-      acc[nt][1] = fmaf(d1_lo, e[1], acc[nt][1]);
-      acc[nt][2] = fmaf(d1_hi, e[2], acc[nt][2]);
-      acc[nt][3] = fmaf(d1_hi, e[3], acc[nt][3]);
-    }
-  }
-}
-
-// Units [u_begin, u_end) of one slab, split across the CTA's warps
-// (warp w takes units u_begin + w, + w + kWarps, ...; consecutive warps read
-// consecutive 512-byte units), with UNR units of loads in flight per warp.
-// k_chunk0: input index of xs column 0.
-template <int FMT, int NT>
-__device__ __forceinline__ void slab_units(float (&acc)[NT][4], const uint8_t* __restrict__ wq,
-                                           const uint8_t* __restrict__ ws, int u_begin, int u_end,
-                                           const __half* xs, int ldx, int k_chunk0, const float* xsum,
-                                           int nblk) {
-  constexpr int KU = unit_k(FMT);
-  constexpr int UNR = (FMT == F16) ? 8 : 4;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2;
-  for (int u0 = u_begin + warp; u0 < u_end; u0 += kWarps * UNR) {
-    uint4 q[UNR];
-    uint2 s[UNR];
-#pragma unroll
-    for (int i = 0; i < UNR; ++i) {
-      const int u = u0 + i * kWarps;
-      if (u < u_end) {
-        q[i] = ldg_stream(wq + (size_t)u * kUnitBytes + lane * 16);
-        s[i] = load_scales<FMT>(ws, u, g);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < UNR; ++i) {
-      const int u = u0 + i * kWarps;
-      if (u < u_end) {
-        const int kl = u * KU - k_chunk0;
-        unit_mma<FMT, NT>(acc, q[i], s[i], xs + kl, ldx, xsum, nblk, kl / 32, lane);
+      if (nt < nt_used) {
+        uint32_t B0[4], B1[4];
+        bp(nt, kk, lane, B0);
+        bp(nt, kk + 32, lane, B1);
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(c, A[0], B0[0], B0[1]);
+        mma_16816(c, A[1], B0[2], B0[3]);
+        acc[nt][0] = fmaf(d0_lo, c[0], acc[nt][0]);
+        acc[nt][1] = fmaf(d0_lo, c[1], acc[nt][1]);
+        acc[nt][2] = fmaf(d0_hi, c[2], acc[nt][2]);
+        acc[nt][3] = fmaf(d0_hi, c[3], acc[nt][3]);
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(e, A[2], B1[0], B1[1]);
+        mma_16816(e, A[3], B1[2], B1[3]);
+        acc[nt][0] = fmaf(d1_lo, e[0], acc[nt][0]);
+        acc[nt][1] = fmaf(d1_lo, e[1], acc[nt][1]);
+        acc[nt][2] = fmaf(d1_hi, e[2], acc[nt][2]);
+        acc[nt][3] = fmaf(d1_hi, e[3], acc[nt][3]);
       }
     }
   }
 }
 
-// Cross-warp reduction: red[kWarps][NT*8][16] fp32 in shared memory.
 template <int NT>
-__device__ __forceinline__ void slab_store_partial(const float (&acc)[NT][4], float* red) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  float* r = red + warp * (NT * 8 * 16);
+__device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int tok = nt * 8 + 2 * t;
-    r[tok * 16 + g] = acc[nt][0];
-    r[(tok + 1) * 16 + g] = acc[nt][1];
-    r[tok * 16 + g + 8] = acc[nt][2];
-    r[(tok + 1) * 16 + g + 8] = acc[nt][3];
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+}
+
+// ------------------------------------------------------------------ warp weight streams
+// Ring slot layout: codes at [0, unit_bytes), then this lane's scale entry at
+// 512 + 8*lane (the 8-bit and 4-bit formats only).  Every byte of a slot is
+// written and read by the same lane, so a slot needs no barrier.
+template <int FMT>
+__device__ __forceinline__ void fetch_unit(uint8_t* slot, const uint8_t* q_unit, const uint8_t* s_unit, int lane) {
+  cp_async16(slot + lane * 16, q_unit + lane * 16);
+  if constexpr (FMT == F16) {
+    cp_async16(slot + 512 + lane * 16, q_unit + 512 + lane * 16);
+  } else if constexpr (FMT == Q8_0) {
+    cp_async4(slot + 512 + lane * 8, s_unit + (lane >> 2) * 4);
+  } else {
+    cp_async8(slot + 512 + lane * 8, s_unit + (lane >> 2) * 8);
   }
 }
 
+// How a CTA's slabs are shared by its warps.  The CTA owns the slabs
+// first + m*stride, m in [0, n).  Its kWarps warps form G = kWarps/ks groups
+// of ks warps, ks the largest of 8, 4, 2, 1 dividing U, so that every warp
+// gets the same number of units: group j takes m = j, j + G, ... (one slab
+// per round) and warp r of the group the units [r*uw, (r+1)*uw) of each, uw =
+// U/ks.  Only the ks warps of a group meet at a barrier, once per round.
+struct SlabWork {
+  int first, stride, n, U;
+  int ks, uw, G, grp, rank;
+};
+__host__ __device__ __forceinline__ int warps_per_slab(int U) {
+  return (U & 7) == 0 ? 8 : (U & 3) == 0 ? 4 : (U & 1) == 0 ? 2 : 1;
+}
+__device__ __forceinline__ SlabWork slab_work(int first, int stride, int n, int U) {
+  SlabWork w;
+  w.first = first;
+  w.stride = stride;
+  w.n = n;
+  w.U = U;
+  w.ks = warps_per_slab(U);
+  w.uw = U / w.ks;
+  w.G = kWarps / w.ks;
+  const int warp = threadIdx.x >> 5;
+  w.grp = warp / w.ks;
+  w.rank = warp - w.grp * w.ks;
+  return w;
+}
+
+// The next unit a warp fetches: slab m of the CTA's list, unit i of its range.
+template <int FMT>
+struct UnitStream {
+  const uint8_t* q;
+  const uint8_t* sc;
+  int m, i;
+  __device__ __forceinline__ void start(const uint8_t* q_, const uint8_t* sc_, const SlabWork& w) {
+    q = q_;
+    sc = sc_;
+    m = w.grp;
+    i = 0;
+  }
+  __device__ __forceinline__ void fetch_next(uint8_t* slot, const SlabWork& w, int lane) {
+    if (m < w.n) {
+      const size_t unit = (size_t)(w.first + m * w.stride) * w.U + w.rank * w.uw + i;
+      fetch_unit<FMT>(slot, q + unit * unit_bytes(FMT), sc + unit * unit_scale_bytes(FMT), lane);
+      if (++i == w.uw) {
+        i = 0;
+        m += w.G;
+      }
+    }
+    cp_commit();  // one group per call, empty or not, keeps the wait counts uniform
+  }
+  // the first kRingDepth units (weights only: may run before griddepcontrol.wait)
+  __device__ __forceinline__ void prefetch(uint8_t* ring, int slot_bytes, const SlabWork& w, int lane) {
+#pragma unroll
+    for (int d = 0; d < kRingDepth; ++d) fetch_next(ring + d * slot_bytes, w, lane);
+  }
+};
+
+__device__ __forceinline__ void group_sync(int grp, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(grp + 1), "r"(nthreads) : "memory");
+}
+
+// Shared memory of the per-round partials: [G][2][ks][NT*8][16] fp32 =
+// 2*kWarps*NT*512 bytes for any ks.
 template <int NT>
-__device__ __forceinline__ void slab_sum(const float* red, int tok, int pg, float& lo, float& hi) {
+constexpr int red_bytes() { return 2 * kWarps * NT * 8 * 16 * 4; }
+
+// lo/hi = sum over the ks partials of (token tok, rows pg and pg+8).
+template <int NT>
+__device__ __forceinline__ void group_sum(const float* rb, int ks, int tok, int pg, float& lo, float& hi) {
   lo = 0.f;
   hi = 0.f;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    lo += red[w * (NT * 8 * 16) + tok * 16 + pg];
-    hi += red[w * (NT * 8 * 16) + tok * 16 + pg + 8];
+  for (int r = 0; r < ks; ++r) {
+    lo += rb[r * (NT * 128) + tok * 16 + pg];
+    hi += rb[r * (NT * 128) + tok * 16 + pg + 8];
   }
+}
+
+// Stream the CTA's slabs through the warp rings (the first kRingDepth units
+// already issued by us.prefetch).  After each round the group's threads call
+// epi(slab, rb, tid, nthreads): rb holds the ks partials of the slab; thread
+// tid of nthreads = 32*ks takes items tid, tid + nthreads, ... of NT*64.
+template <int FMT, int NT, class BP, class Epi>
+__device__ __forceinline__ void run_stream(UnitStream<FMT>& us, const SlabWork& w, uint8_t* ring, int slot_bytes,
+                                           float* red, const BP& bp, int nt_used, const Epi& epi) {
+  constexpr int KU = unit_k(FMT);
+  const int lane = threadIdx.x & 31;
+  const int nthr = w.ks * 32, tid = threadIdx.x - w.grp * nthr;
+  float* gred = red + (size_t)w.grp * 2 * w.ks * (NT * 128);
+  float acc[NT][4];
+  int si = 0, par = 0;  // ring slot of the next unit to consume; round parity
+  auto next_slot = [&]() {
+    uint8_t* sl = ring + si * slot_bytes;
+    si = si + 1 == kRingDepth ? 0 : si + 1;
+    return sl;
+  };
+  for (int m = w.grp; m < w.n; m += w.G, par ^= 1) {
+    zero_acc<NT>(acc);
+    const int k0 = w.rank * w.uw;
+    int i = 0;
+    if constexpr (kUnroll == 2) {
+      for (; i + 1 < w.uw; i += 2) {
+        cp_wait<kRingDepth - 2>();  // units i and i+1 have landed (this lane's bytes)
+        uint8_t* s0 = next_slot();
+        uint8_t* s1 = next_slot();
+        unit_mma<FMT, NT>(acc, s0, s0 + 512 + lane * 8, bp, (k0 + i) * KU, lane, nt_used);
+        unit_mma<FMT, NT>(acc, s1, s1 + 512 + lane * 8, bp, (k0 + i + 1) * KU, lane, nt_used);
+        us.fetch_next(s0, w, lane);  // refill both with the units kRingDepth ahead
+        us.fetch_next(s1, w, lane);
+      }
+    }
+    for (; i < w.uw; ++i) {
+      cp_wait<kRingDepth - 1>();  // unit i has landed (this lane's bytes)
+      uint8_t* s0 = next_slot();
+      unit_mma<FMT, NT>(acc, s0, s0 + 512 + lane * 8, bp, (k0 + i) * KU, lane, nt_used);
+      us.fetch_next(s0, w, lane);  // refill it with the unit kRingDepth ahead
+    }
+    float* rb = gred + par * w.ks * (NT * 128);
+    {
+      const int g = lane >> 2, t = lane & 3;
+      float* r = rb + w.rank * (NT * 128);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int tok = nt * 8 + 2 * t;
+        r[tok * 16 + g] = acc[nt][0];
+        r[(tok + 1) * 16 + g] = acc[nt][1];
+        r[tok * 16 + g + 8] = acc[nt][2];
+        r[(tok + 1) * 16 + g + 8] = acc[nt][3];
+      }
+    }
+    group_sync(w.grp, nthr);
+    epi(w.first + m * w.stride, rb, tid, nthr);
+  }
+  cp_wait<0>();
 }
 
 // ------------------------------------------------------------------ staging
-// Per-token RMSNorm factor 1/sqrt(mean(x^2)+eps) of fp32 rows (one warp per token).
-__device__ __forceinline__ void stage_rms(float* rs, const float* x, int ldx_g, const int* rows, int ntok,
-                                          int K, float eps) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int tk = warp; tk < ntok; tk += kWarps) {
-    const float* xr = x + (size_t)(rows ? rows[tk] : tk) * ldx_g;
+// All staging loops load first and compute afterwards so that one L2/HBM
+// latency, not one per element, is paid per batch.
+
+// One warp: dst[:] = fp16(src[:] * rsqrt(mean(src^2) + eps) * w[:]).  A row of
+// up to 2048 values is held in registers (16 float4 per lane); longer rows are
+// read twice.
+__device__ __forceinline__ void stage_norm_rows_one(__half* dst, const float* srcf, const __half* w, int K, float eps) {
+  const int lane = threadIdx.x & 31;
+  const int n4 = K / 4;
+  const float4* src = reinterpret_cast<const float4*>(srcf);
+  auto store = [&](int f, const float4& v, float r) {
+    const __half2 w0 = *reinterpret_cast<const __half2*>(w + 4 * f);
+    const __half2 w1 = *reinterpret_cast<const __half2*>(w + 4 * f + 2);
+    __half2* d = reinterpret_cast<__half2*>(dst + 4 * f);
+    d[0] = __floats2half2_rn(v.x * r * __low2float(w0), v.y * r * __high2float(w0));
+    d[1] = __floats2half2_rn(v.z * r * __low2float(w1), v.w * r * __high2float(w1));
+  };
+  if (n4 <= 16 * 32) {
+    float4 v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = (lane + 32 * i < n4) ? src[lane + 32 * i] : make_float4(0.f, 0.f, 0.f, 0.f);
     float ss = 0.f;
-    for (int k = lane * 4; k < K; k += 128) {
-      const float4 v = *reinterpret_cast<const float4*>(xr + k);
-      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = rsqrtf(ss / (float)K + eps);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (lane + 32 * i < n4) store(lane + 32 * i, v[i], r);
+  } else {
+    float ss = 0.f;
+    for (int f0 = 0; f0 < n4; f0 += 8 * 32) {
+      float4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = (f0 + lane + 32 * i < n4) ? src[f0 + lane + 32 * i] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) rs[tk] = rsqrtf(ss / (float)K + eps);
-  }
-}
-
-// xs[tk][j] = fp16(x[row(tk)][k0 + j] * rs[tk] * w[k0 + j]) for j < kc; rows tk >= ntok are zero.
-__device__ __forceinline__ void stage_norm_chunk(__half* xs, int ldx, const float* x, int ldx_g, const int* rows,
-                                                 int ntok, int ntok_pad, const float* rs, const __half* w, int k0,
-                                                 int kc) {
-  const int per_row = kc / 4;
-  for (int i = threadIdx.x; i < ntok_pad * per_row; i += kThreads) {
-    const int tk = i / per_row, j = (i - tk * per_row) * 4;
-    __half2 o0, o1;
-    if (tk < ntok) {
-      const float* xr = x + (size_t)(rows ? rows[tk] : tk) * ldx_g + k0 + j;
-      const float4 v = *reinterpret_cast<const float4*>(xr);
-      const float r = rs[tk];
-      const __half2 w0 = *reinterpret_cast<const __half2*>(w + k0 + j);
-      const __half2 w1 = *reinterpret_cast<const __half2*>(w + k0 + j + 2);
-      o0 = __floats2half2_rn(v.x * r * __low2float(w0), v.y * r * __high2float(w0));
-      o1 = __floats2half2_rn(v.z * r * __low2float(w1), v.w * r * __high2float(w1));
-    } else {
-      o0 = __float2half2_rn(0.f);
-      o1 = o0;
-    }
-    __half2* d = reinterpret_cast<__half2*>(xs + tk * ldx + j);
-    d[0] = o0;
-    d[1] = o1;
-  }
-}
-
-// xs[tk][j] = src[row(tk)][k0 + j] (fp16), rows tk >= ntok zero.  kc % 8 == 0.
-__device__ __forceinline__ void stage_f16_chunk(__half* xs, int ldx, const __half* src, int lds, const int* rows,
-                                                int row0, int ntok, int ntok_pad, int k0, int kc) {
-  const int per_row = kc / 8;
-  for (int i = threadIdx.x; i < ntok_pad * per_row; i += kThreads) {
-    const int tk = i / per_row, j = (i - tk * per_row) * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (tk < ntok) {
-      const int r = rows ? rows[tk] : row0 + tk;
-      v = *reinterpret_cast<const uint4*>(src + (size_t)r * lds + k0 + j);
-    }
-    *reinterpret_cast<uint4*>(xs + tk * ldx + j) = v;
-  }
-}
-
-// Per-token sums of each 32-input block of the staged chunk (I8ASYM zero points).
-__device__ __forceinline__ void stage_block_sums(float* xsum, const __half* xs, int ldx, int ntok_pad, int kc) {
-  const int nblk = kc / 32;
-  for (int i = threadIdx.x; i < ntok_pad * nblk; i += kThreads) {
-    const int tk = i / nblk, b = i - tk * nblk;
-    const __half2* p = reinterpret_cast<const __half2*>(xs + tk * ldx + b * 32);
-    float s = 0.f;
+    const float r = rsqrtf(ss / (float)K + eps);
+    for (int f0 = 0; f0 < n4; f0 += 8 * 32) {
+      float4 v[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float2 f = __half22float2(p[j]);
-      s += f.x + f.y;
+      for (int i = 0; i < 8; ++i) v[i] = (f0 + lane + 32 * i < n4) ? src[f0 + lane + 32 * i] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (f0 + lane + 32 * i < n4) store(f0 + lane + 32 * i, v[i], r);
     }
-    xsum[i] = s;
+  }
+}
+
+// xs[tk][:] = normalised x[tk][:] for tk < ntok, zero rows up to ntok_pad (one warp per row).
+__device__ __forceinline__ void stage_norm_rows(__half* xs, int ldx, const float* x, int ldx_g, int ntok, int ntok_pad,
+                                                const __half* w, int K, float eps) {
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int tk = warp; tk < ntok_pad; tk += nw) {
+    if (tk < ntok)
+      stage_norm_rows_one(xs + tk * ldx, x + (size_t)tk * ldx_g, w, K, eps);
+    else
+      for (int i = (threadIdx.x & 31); i < K / 8; i += 32)
+        *reinterpret_cast<uint4*>(xs + tk * ldx + 8 * i) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// stage_norm_rows over gathered rows: xs[t] = norm(x[rows[t]]) for t < ntok.
+__device__ __forceinline__ void stage_norm_gather(__half* xs, int ldx, const float* x, int ldx_g, const int* rows,
+                                                  int ntok, int ntok_pad, const __half* w, int K, float eps) {
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int tk = warp; tk < ntok_pad; tk += nw) {
+    // one row at a time through the contiguous routine (it handles zero padding)
+    if (tk < ntok)
+      stage_norm_rows_one(xs + tk * ldx, x + (size_t)rows[tk] * ldx_g, w, K, eps);
+    else
+      for (int i = (threadIdx.x & 31); i < K / 8; i += 32)
+        *reinterpret_cast<uint4*>(xs + tk * ldx + 8 * i) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// dst[0, bytes) = src[0, bytes) (16-byte multiples), batched loads.
+__device__ __forceinline__ void stage_bytes(uint8_t* dst, const uint8_t* src, int bytes) {
+  const int n = bytes / 16;
+  for (int i0 = threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      v[u] = i < n ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < n) reinterpret_cast<uint4*>(dst)[i] = v[u];
+    }
+  }
+}
+
+// xs[tk][j] = src[tk][j] (fp16), rows tk in [ntok, ntok_pad) zero.  K % 8 == 0.
+__device__ __forceinline__ void stage_f16(__half* xs, int ldx, const __half* src, int lds, int ntok, int ntok_pad,
+                                          int K) {
+  const int per_row = K / 8;
+  const int total = ntok_pad * per_row;
+  for (int i0 = threadIdx.x; i0 < total; i0 += 8 * blockDim.x) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      const int tk = i / per_row, j = (i - tk * per_row) * 8;
+      v[u] = (i < total && tk < ntok) ? *reinterpret_cast<const uint4*>(src + (size_t)tk * lds + j)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < total) {
+        const int tk = i / per_row, j = (i - tk * per_row) * 8;
+        *reinterpret_cast<uint4*>(xs + tk * ldx + j) = v[u];
+      }
+    }
   }
 }
 
@@ -383,9 +705,5 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
 __device__ __forceinline__ int argmax_key_index(unsigned long long k) {
   return (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
 }
-
-// Device status bits (reported by uocr_sync).
-constexpr int kStatusToken = 1;
-constexpr int kStatusPosition = 2;
 
 }  // namespace uocr

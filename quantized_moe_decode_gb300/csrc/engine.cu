@@ -13,6 +13,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <cstdlib>
 #include <map>
 #include <mutex>
 #include <string>
@@ -45,7 +46,7 @@ struct DMat {
 
 size_t packed_q_bytes(int n_rows_packed, int K, int fmt) {
   const size_t slabs = (size_t)(n_rows_packed + 15) / 16;
-  return slabs * (K / unit_k(fmt)) * kUnitBytes;
+  return slabs * (K / unit_k(fmt)) * unit_bytes(fmt);
 }
 size_t packed_s_bytes(int n_rows_packed, int K, int fmt) {
   const size_t slabs = (size_t)(n_rows_packed + 15) / 16;
@@ -118,14 +119,14 @@ struct uocr_ctx {
   int* attn_counter = nullptr;
   __half* act_dense = nullptr;
   __half* xhat = nullptr;
-  __half* act_r = nullptr;
-  __half* act_s = nullptr;
+  uint8_t* act_r = nullptr;  // B-fragment order, padded expert entries x Ie
+  uint8_t* act_s = nullptr;  // B-fragment order, rows x n_shared*Ie
   float* part_r = nullptr;
   float* part_s = nullptr;
   int* slab_counter = nullptr;
   float* r_logits = nullptr;
   int *r_idx = nullptr, *r_count = nullptr, *r_offset = nullptr, *r_perm = nullptr, *r_inv = nullptr;
-  int *r_active = nullptr, *r_nactive = nullptr, *r_counter = nullptr;
+
   float* r_w = nullptr;
   float* sinks = nullptr;
   float* logits = nullptr;
@@ -138,6 +139,9 @@ struct uocr_ctx {
   bool sinks_set = false;
   // graphs
   std::map<uint64_t, cudaGraphExec_t> graphs;
+  bool pdl = true;  // programmatic dependent launch between the step's kernels
+  int gemv_ctas_per_sm = 2;    // streaming CTAs per SM of a GEMV launch
+  int expert_ctas_per_sm = 2;  // CTAs per SM an expert launch is sized for (active experts only)
 
   int H() const { return cfg.hidden; }
   int MR() const { return cfg.max_rows; }
@@ -178,6 +182,10 @@ static bool expert_pair_ok(int fr, int fs) {
          (fr == Q8_0 && fs == Q4_0) || (fr == I8ASYM && fs == I8ASYM);
 }
 
+// dynamic shared memory a streaming kernel may plan (the device offers 227 KB
+// per block; the kernels' static shared memory is below 13 KB)
+constexpr int kSmemLimit = 214 * 1024;
+
 static uocr_status check_config(uocr_ctx* ctx, const uocr_config& c) {
   auto bad = [&](const char* m) { return ctx->fail(UOCR_E_INVALID_ARG, "invalid config: %s", m); };
   if (c.hidden <= 0 || c.hidden % 64) return bad("hidden must be a positive multiple of 64");
@@ -199,13 +207,19 @@ static uocr_status check_config(uocr_ctx* ctx, const uocr_config& c) {
     const int fs = c.n_shared > 0 ? c.fmt_shared : c.fmt_routed;
     if (!quant_fmt(c.fmt_routed) || !expert_pair_ok(c.fmt_routed, fs))
       return bad("unsupported (routed, shared) expert format pair");
-    const StagePlan sp = plan_stage(2, c.hidden, I8ASYM);
-    if (sp.kc < c.hidden) return bad("hidden too large for the expert kernels");
-    if (plan_stage(2, c.n_shared * c.expert_inter, I8ASYM).kc < c.n_shared * c.expert_inter ||
-        plan_stage(2, c.expert_inter, I8ASYM).kc < c.expert_inter)
-      return bad("expert_inter too large for the expert kernels");
+    if (plan_stream(2, c.fmt_routed, c.hidden, 16).bytes > kSmemLimit)
+      return bad("hidden too large for the expert kernels");
+    const int kmax = c.n_shared * c.expert_inter > c.expert_inter ? c.n_shared * c.expert_inter : c.expert_inter;
+    if (plan_stream(2, c.fmt_routed, 0, 0, 2 * (kmax / 32) * 512).bytes > kSmemLimit)
+      return bad("expert_inter * n_shared too large for the expert kernels");
   }
   if (c.vocab < 0) return bad("vocab must be >= 0");
+  {
+    const int kmax = c.hidden > c.dense_inter ? (c.hidden > c.n_heads * c.head_dim ? c.hidden : c.n_heads * c.head_dim)
+                                              : c.dense_inter;
+    if (plan_stream(2, F16, kmax, 16, c.head_dim / 2 * 8).bytes > kSmemLimit)
+      return bad("a projection input is too long for the shared-memory activation tile");
+  }
   if (c.prefix_len < 0 || c.ring_len < 1) return bad("prefix_len >= 0 and ring_len >= 1 required");
   if ((long long)c.prefix_len + c.ring_len > (1 << 24)) return bad("cache too long");
   if (c.max_rows < 1 || c.max_rows > 64) return bad("max_rows must be in [1, 64]");
@@ -274,8 +288,9 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
   if (c.n_dense_layers > 0 || E == 0) ctx->act_dense = cv.take<__half>((size_t)MR * c.dense_inter, r.activations);
   if (ctx->any_moe()) {
     ctx->xhat = cv.take<__half>((size_t)MR * H, r.activations);
-    ctx->act_r = cv.take<__half>((size_t)MR * k * Ie, r.activations);
-    ctx->act_s = cv.take<__half>((size_t)MR * (Ish > 0 ? Ish : 1), r.activations);
+    const int TG = (MR + 15) / 16;
+    ctx->act_r = cv.take<uint8_t>((size_t)E * TG * 16 * Ie * 2, r.activations);  // 16 tokens per (expert, group)
+    ctx->act_s = cv.take<uint8_t>((size_t)(MR + 7) / 8 * 8 * (Ish > 0 ? Ish : 32) * 2, r.activations);
     ctx->part_r = cv.take<float>((size_t)MR * k * H, r.activations);
     ctx->part_s = cv.take<float>((size_t)MR * H, r.activations);
     ctx->slab_counter = cv.take<int>(H / 16, r.activations);
@@ -286,9 +301,6 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
     ctx->r_offset = cv.take<int>((size_t)Lc * (E + 1), r.routing);
     ctx->r_perm = cv.take<int>((size_t)Lc * MR * k, r.routing);
     ctx->r_inv = cv.take<int>((size_t)Lc * MR * k, r.routing);
-    ctx->r_active = cv.take<int>((size_t)Lc * E, r.routing);
-    ctx->r_nactive = cv.take<int>((size_t)Lc, r.routing);
-    ctx->r_counter = cv.take<int>(1, r.routing);
   }
   if (V > 0) {
     ctx->logits = cv.take<float>((size_t)MR * V, r.logits);
@@ -326,8 +338,11 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
   cudaStream_t st = ctx->st;
   const int H = c.hidden, S = ctx->S, MR = ctx->MR(), rows = sh.rows;
   const int nt = rows <= 8 ? 1 : 2;
-  const int tg = (rows + nt * 8 - 1) / (nt * 8);
-  const int G = 4 * ctx->n_sm;
+  const int tg = (rows + 15) / 16;  // token groups of 16 rows (one n-tile pair)
+  // streaming CTAs per launch
+  const int G = ctx->gemv_ctas_per_sm * ctx->n_sm;
+  const int GE = ctx->expert_ctas_per_sm * ctx->n_sm;
+  const bool pdl = ctx->pdl && !prof;  // timed classes must not overlap
   auto gx_for = [&](int slabs) {
     int g = G / tg;
     if (g < 1) g = 1;
@@ -366,7 +381,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     // QKV + RoPE + in-place KV append
     GemvArgs qa{};
     qa.w = w.qkv.view();
-    qa.sp = plan_stage(nt, H, c.fmt_attn);
+    qa.sp = plan_stream(nt, c.fmt_attn, H, nt * 8, (c.head_dim / 2) * 8);
     qa.ntok = rows;
     qa.xf = hid(2 * l);
     qa.ld_src = H;
@@ -384,7 +399,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     qa.SL = ctx->SL;
     qa.status = ctx->status;
     mark("qkv", true);
-    CK(launch_gemv(c.fmt_attn, SRC_NORM, EPI_QKV, qa, gx_for(w.qkv.n_slabs), tg, st), "qkv launch");
+    CK(launch_gemv(c.fmt_attn, SRC_NORM, EPI_QKV, qa, gx_for(w.qkv.n_slabs), tg, st, pdl), "qkv launch");
     mark("qkv", false);
     // attention
     AttnArgs aa{};
@@ -400,6 +415,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     aa.P = c.prefix_len;
     aa.R = c.ring_len;
     aa.SL = ctx->SL;
+    aa.status = ctx->status;
     {
       int ns = (2 * ctx->n_sm + rows * c.n_heads - 1) / (rows * c.n_heads);
       const int cap = (ctx->SL + 63) / 64;
@@ -411,25 +427,26 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     }
     aa.scale = 1.0f / sqrtf((float)c.head_dim);
     mark("attention", true);
-    CK(launch_attn(aa, rows, st), "attention launch");
+    CK(launch_attn(aa, rows, st, pdl), "attention launch");
     mark("attention", false);
     // O projection + residual
     GemvArgs oa{};
     oa.w = w.o.view();
-    oa.sp = plan_stage(nt, S, c.fmt_attn);
+    oa.sp = plan_stream(nt, c.fmt_attn, S);
     oa.ntok = rows;
     oa.xh = ctx->attn_out;
     oa.ld_src = S;
     oa.res_in = hid(2 * l);
     oa.out_f = hid(2 * l + 1);
     oa.ld_out = H;
+    oa.status = ctx->status;
     mark("o_proj", true);
-    CK(launch_gemv(c.fmt_attn, SRC_F16, EPI_RESID, oa, gx_for(w.o.n_slabs), tg, st), "o_proj launch");
+    CK(launch_gemv(c.fmt_attn, SRC_F16, EPI_RESID, oa, gx_for(w.o.n_slabs), tg, st, pdl), "o_proj launch");
     mark("o_proj", false);
     if (w.dense) {
       GemvArgs ga{};
       ga.w = w.gateup.view();
-      ga.sp = plan_stage(nt, H, c.fmt_dense);
+      ga.sp = plan_stream(nt, c.fmt_dense, H);
       ga.ntok = rows;
       ga.xf = hid(2 * l + 1);
       ga.ld_src = H;
@@ -437,104 +454,124 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       ga.eps = c.rms_eps;
       ga.out_h = ctx->act_dense;
       ga.ld_out = c.dense_inter;
+      ga.status = ctx->status;
       mark("mlp_gate_up", true);
-      CK(launch_gemv(c.fmt_dense, SRC_NORM, EPI_SWIGLU, ga, gx_for(w.gateup.n_slabs), tg, st), "gate/up launch");
+      CK(launch_gemv(c.fmt_dense, SRC_NORM, EPI_SWIGLU, ga, gx_for(w.gateup.n_slabs), tg, st, pdl),
+         "gate/up launch");
       mark("mlp_gate_up", false);
       GemvArgs da{};
       da.w = w.down.view();
-      da.sp = plan_stage(nt, c.dense_inter, c.fmt_dense);
+      da.sp = plan_stream(nt, c.fmt_dense, c.dense_inter);
       da.ntok = rows;
       da.xh = ctx->act_dense;
       da.ld_src = c.dense_inter;
       da.res_in = hid(2 * l + 1);
       da.out_f = hid(2 * l + 2);
       da.ld_out = H;
+      da.status = ctx->status;
       mark("mlp_down", true);
-      CK(launch_gemv(c.fmt_dense, SRC_F16, EPI_RESID, da, gx_for(w.down.n_slabs), tg, st), "down launch");
+      CK(launch_gemv(c.fmt_dense, SRC_F16, EPI_RESID, da, gx_for(w.down.n_slabs), tg, st, pdl), "down launch");
       mark("mlp_down", false);
     } else {
       const int E = c.n_experts, k = c.top_k;
       RouterArgs ra{};
-      ra.w = reinterpret_cast<const __half*>(w.router.q);
-      ra.n_slabs = w.router.n_slabs;
-      ra.U = w.router.U;
-      ra.sp = plan_stage(nt, H, F16);
+      ra.w = w.router.view();
+      ra.sp = plan_stream(nt, F16, H);
       ra.ntok = rows;
       ra.H = H;
       ra.E = E;
-      ra.k = k;
       ra.h = hid(2 * l + 1);
       ra.norm_w = w.mlp_norm;
       ra.eps = c.rms_eps;
-      ra.xhat = ctx->xhat;
       ra.logits = ctx->r_logits + (size_t)l * MR * E;
-      ra.idx = ctx->r_idx + (size_t)l * MR * k;
-      ra.wts = ctx->r_w + (size_t)l * MR * k;
-      ra.count = ctx->r_count + (size_t)l * E;
-      ra.offset = ctx->r_offset + (size_t)l * (E + 1);
-      ra.perm = ctx->r_perm + (size_t)l * MR * k;
-      ra.inv = ctx->r_inv + (size_t)l * MR * k;
-      ra.active = ctx->r_active + (size_t)l * E;
-      ra.n_active = ctx->r_nactive + l;
-      ra.counter = ctx->r_counter;
+      ra.status = ctx->status;
       mark("router", true);
-      CK(launch_router(ra, tg, st), "router launch");
+      CK(launch_router(ra, tg, st, pdl), "router launch");
       mark("router", false);
 
       const int fs = ctx->shared_fmt();
       ExpertArgs xa{};
       xa.ntok = rows;
+      xa.E = E;
       xa.k = k;
       xa.H = H;
       xa.Ie = c.expert_inter;
       xa.Ish = c.n_shared * c.expert_inter;
-      xa.xhat = ctx->xhat;
-      xa.count = ra.count;
-      xa.offset = ra.offset;
-      xa.perm = ra.perm;
-      xa.active = ra.active;
-      xa.n_active = ra.n_active;
+      xa.tg = tg;
+      xa.logits = ra.logits;
+      xa.idx = ctx->r_idx + (size_t)l * MR * k;
+      xa.wts = ctx->r_w + (size_t)l * MR * k;
+      xa.count = ctx->r_count + (size_t)l * E;
+      xa.offset = ctx->r_offset + (size_t)l * (E + 1);
+      xa.perm = ctx->r_perm + (size_t)l * MR * k;
+      xa.inv = ctx->r_inv + (size_t)l * MR * k;
+      xa.h = hid(2 * l + 1);
+      xa.norm_w = w.mlp_norm;
+      xa.eps = c.rms_eps;
       xa.act_r = ctx->act_r;
       xa.act_s = ctx->act_s;
       xa.part_r = ctx->part_r;
       xa.part_s = ctx->part_s;
-      xa.h = hid(2 * l + 1);
-      xa.wts = ra.wts;
-      xa.inv = ra.inv;
       xa.out = hid(2 * l + 2);
       xa.slab_counter = ctx->slab_counter;
+      xa.status = ctx->status;
+      // Routed CTAs by expert id when nearly every expert is expected to
+      // receive a token (they stream before the routing is known, and the grid
+      // is one wave of CTAs that all have work), else by active slot (slots
+      // past the active experts exit at once, after the live ones in launch
+      // order).  Expected experts with a token: E (1 - (1 - k/E)^rows).
       const int max_act = E < rows * k ? E : rows * k;
-      // gate/up
+      const double exp_act = E * (1.0 - pow(1.0 - (double)k / E, rows));
+      xa.by_slot = exp_act < 0.75 * E;
+      xa.n_units = xa.by_slot ? max_act : E;
+      const double units = xa.by_slot ? exp_act : E;
+      // CTAs per routed unit and for the shared experts, in proportion to the
+      // bytes each streams, about GE per token group in all
+      auto split = [&](const DMat& r, const DMat* sh, int rslabs, int sslabs) {
+        const double br = (double)(r.qbytes + r.sbytes), bs = sh ? (double)(sh->qbytes + sh->sbytes) : 0.0;
+        const double tot = units * br + bs;
+        const int gt = GE / tg > 1 ? GE / tg : 1;
+        // parts of whole rounds (G_w slabs); the fewest parts that give the
+        // rounds per CTA the byte-proportional target gives
+        auto parts = [&](double target, int slabs, int U) {
+          const int gw = kWarps / warps_per_slab(U);
+          const int nr = (slabs + gw - 1) / gw;
+          int t = (int)ceil(target);
+          t = t < 1 ? 1 : t > nr ? nr : t;
+          const int per = (nr + t - 1) / t;
+          return (nr + per - 1) / per;
+        };
+        xa.cpe = parts(gt * br / tot, rslabs, r.U);
+        xa.cpes = sh ? parts(gt * bs / tot, sslabs, sh->U) : 0;
+      };
+      const DMat* shg = c.n_shared > 0 ? &w.sh_gateup : nullptr;
+      const DMat* shd = c.n_shared > 0 ? &w.sh_down : nullptr;
+      // gate/up + SwiGLU (and the routing of every row)
       xa.wr = w.ex_gateup.view(1);
-      xa.ws = c.n_shared > 0 ? w.sh_gateup.view() : PMat{};
-      xa.sp = plan_stage(nt, H, I8ASYM);
-      {
-        const int items = max_act * w.ex_gateup.n_slabs + xa.ws.n_slabs;
-        const int grid = items < G ? items : G;
-        mark("expert_gate_up", true);
-        CK(launch_expert_gateup(c.fmt_routed, fs, xa, grid, st), "expert gate/up launch");
-        mark("expert_gate_up", false);
-      }
+      xa.ws = shg ? shg->view() : PMat{};
+      xa.sp = plan_stream(nt, c.fmt_routed, H, 16);
+      split(w.ex_gateup, shg, w.ex_gateup.n_slabs, shg ? shg->n_slabs : 0);
+      mark("expert_gate_up", true);
+      CK(launch_expert_gateup(c.fmt_routed, fs, xa, st, pdl), "expert gate/up launch");
+      mark("expert_gate_up", false);
       // down + combine
       xa.wr = w.ex_down.view(1);
-      xa.ws = c.n_shared > 0 ? w.sh_down.view() : PMat{};
+      xa.ws = shd ? shd->view() : PMat{};
       {
         const int kmax = xa.Ish > xa.Ie ? xa.Ish : xa.Ie;
-        xa.sp = plan_stage(nt, kmax, I8ASYM);
-        const int nS = H / 16;
-        const int items = max_act * nS + (c.n_shared > 0 ? nS : 0);
-        const int grid = items < G ? items : G;
-        mark("expert_down_combine", true);
-        CK(launch_expert_down(c.fmt_routed, fs, xa, grid, st), "expert down launch");
-        mark("expert_down_combine", false);
+        xa.sp = plan_stream(nt, c.fmt_routed, 0, 0, nt * (kmax / 32) * 512);
       }
+      split(w.ex_down, shd, H / 16, H / 16);
+      mark("expert_down_combine", true);
+      CK(launch_expert_down(c.fmt_routed, fs, xa, st, pdl), "expert down launch");
+      mark("expert_down_combine", false);
     }
   }
 
   if (sh.lm) {
     GemvArgs la{};
     la.w = ctx->lm.view();
-    la.sp = plan_stage(nt, H, F16);
+    la.sp = plan_stream(nt, F16, H);
     la.ntok = rows;
     la.xf = hid(2 * c.n_layers);
     la.ld_src = H;
@@ -545,6 +582,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     la.keys = ctx->keys;
     la.counter = ctx->lm_counter;
     la.next_ids = ctx->next_ids;
+    la.status = ctx->status;
     if (sh.chain) {
       la.feed_ids = ctx->ids_buf;
       la.feed_pos = ctx->pos_buf;
@@ -552,7 +590,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       la.hist_ctr = ctx->hist_ctr;
     }
     mark("lm_head_argmax", true);
-    CK(launch_gemv(F16, SRC_NORM, EPI_LOGITS, la, gx_for(ctx->lm.n_slabs), tg, st), "lm head launch");
+    CK(launch_gemv(F16, SRC_NORM, EPI_LOGITS, la, gx_for(ctx->lm.n_slabs), tg, st, pdl), "lm head launch");
     mark("lm_head_argmax", false);
   }
   return UOCR_OK;
@@ -669,7 +707,7 @@ static uocr_status pack_into(uocr_ctx* ctx, const DMat& dst, size_t expert_off_q
   pa.s = dst.s ? dst.s + expert_off_s : nullptr;
   pa.fmt = dst.fmt;
   pa.n_slabs = dst.n_slabs;
-  pa.U = dst.U;
+  pa.U = dst.U * (unit_bytes(dst.fmt) / 512);  // the packer counts 512-byte (sub-)units
   pa.K = dst.K;
   pa.map = map;
   pa.nsrc = (int)srcs.size();
@@ -881,6 +919,18 @@ uocr_status uocr_create(const uocr_config* cfg, uocr_ctx** out) {
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_in, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_out, cudaEventDisableTiming);
   ctx->ust = reinterpret_cast<cudaStream_t>(cfg->stream);
+  {
+    const char* v = std::getenv("UOCR_NO_PDL");  // A/B switch for measuring the launch overlap
+    ctx->pdl = !(v && v[0] == '1');
+    // grid sizing knobs for tuning sweeps (CTAs per SM, 1..8)
+    auto knob = [](const char* name, int def) {
+      const char* e = std::getenv(name);
+      const int x = e ? atoi(e) : def;
+      return x >= 1 && x <= 8 ? x : def;
+    };
+    ctx->gemv_ctas_per_sm = knob("UOCR_GEMV_CTAS_PER_SM", ctx->gemv_ctas_per_sm);
+    ctx->expert_ctas_per_sm = knob("UOCR_EXPERT_CTAS_PER_SM", ctx->expert_ctas_per_sm);
+  }
   // zero everything (KV cache, counters, argmax keys, status)
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->arena, 0, m.off, ctx->st);
   if (e == cudaSuccess) {
@@ -1108,6 +1158,7 @@ uocr_status uocr_sync(uocr_ctx* ctx) {
   CK(cudaMemcpy(&st, ctx->status, 4, cudaMemcpyDeviceToHost), "status read");
   if (st) {
     CK(cudaMemset(ctx->status, 0, 4), "status clear");
+    if (st & kStatusTimeout) return ctx->fail(UOCR_E_CUDA, "a kernel's bounded wait for its weight copies timed out");
     if (st & kStatusToken) return ctx->fail(UOCR_E_TOKEN, "a token id was outside [0, vocab)");
     return ctx->fail(UOCR_E_POSITION, "a position was negative");
   }
@@ -1220,13 +1271,14 @@ uocr_status uocr_lm_head_argmax_noalloc(uocr_ctx* ctx, int32_t rows, const float
   CK(cudaMemsetAsync(scratch, 0, sizeof(unsigned long long) * (kNoAllocMaxRows + 1), st), "scratch clear");
   const int nt = rows <= 8 ? 1 : 2;
   const int tg = (rows + nt * 8 - 1) / (nt * 8);
-  int gx = 4 * ctx->n_sm / tg;
+  int gx = ctx->n_sm / tg;
   if (gx < 1) gx = 1;
   if (gx > ctx->lm.n_slabs) gx = ctx->lm.n_slabs;
   GemvArgs la{};
   la.w = ctx->lm.view();
-  la.sp = plan_stage(nt, c.hidden, F16);
+  la.sp = plan_stream(nt, F16, c.hidden);
   la.ntok = rows;
+  la.status = ctx->status;
   la.xf = hidden;
   la.ld_src = c.hidden;
   la.norm_w = ctx->final_norm;
@@ -1236,7 +1288,7 @@ uocr_status uocr_lm_head_argmax_noalloc(uocr_ctx* ctx, int32_t rows, const float
   la.keys = scratch;
   la.counter = reinterpret_cast<int*>(scratch + kNoAllocMaxRows);
   la.next_ids = next_ids;
-  CK(launch_gemv(F16, SRC_NORM, EPI_LOGITS, la, gx, tg, st), "lm head launch");
+  CK(launch_gemv(F16, SRC_NORM, EPI_LOGITS, la, gx, tg, st, false), "lm head launch");
   return UOCR_OK;
 }
 

@@ -12,126 +12,110 @@
 // il Mixture of Experts": KV append, 128-token ring, argmax over the language
 // head; "Quantizzazione": dequantisation fused into GEMV/SwiGLU/argmax);
 // "Falcon-OCR INT8 OpenVINO IR" intro (the cache is an input written in
-// place; only the new token's K/V are produced).
+// place; only the new token's K/V are produced); "How it is meant to be run"
+// (the rows of a step share one read of the weights).
 //
-// Every CTA stages the (normalised) activations of up to 16 rows in shared
-// memory once, then streams the weight slabs it owns; all rows of the step
-// share that single weight read ("How it is meant to be run": rows share the
-// weight read).
+// Each persistent CTA owns slabs blockIdx.x, +gridDim.x, ...; their chunks
+// stream through a ring of shared-memory stages filled by bulk copies, the
+// first ones issued before the CTA waits for the kernel that produces its
+// activations.  Up to 16 rows (one token group) share each weight read.
 #include "launch.h"
 
 namespace uocr {
 
-StagePlan plan_stage(int nt, int K, int fmt) {
-  StagePlan p{};
+static int round16(int x) { return (x + 15) / 16 * 16; }
+
+StreamPlan plan_stream(int nt, int fmt, int k_stage, int n_rows_list, int extra_bytes) {
+  StreamPlan p{};
   p.nt = nt;
-  const int ntp = nt * 8;
-  const int budget = 80 * 1024;
-  int kcmax = budget / (ntp * 2) - 8;
-  kcmax = (kcmax / 64) * 64;
-  p.kc = K < kcmax ? K : kcmax;
-  p.ldx = p.kc + 8;
-  int off = ((ntp * p.ldx * 2 + 15) / 16) * 16;
-  p.xsum_off = off;
-  if (fmt == I8ASYM) off += ntp * (p.kc / 32) * 4;
+  p.ldx = k_stage > 0 ? k_stage + 8 : 0;
+  p.slot = fmt == F16 ? 1024 : 768;
+  int off = 0;
+  p.xs_off = off;
+  off += k_stage > 0 ? round16(nt * 8 * p.ldx * 2) : 0;
   p.red_off = off;
-  off += kWarps * ntp * 16 * 4;
-  p.rs_off = off;
-  off += 64 * 4;
+  off += 2 * kWarps * nt * 8 * 16 * 4;  // per-round partials, double-buffered (red_bytes<NT>)
   p.rows_off = off;
-  off += 64 * 4;
+  off += round16(n_rows_list * 4);
+  p.zero_off = off;
+  off += 64;
+  p.extra_off = off;
+  off += round16(extra_bytes);
+  off = (off + 127) / 128 * 128;
+  p.ring_off = off;
+  off += kWarps * kRingDepth * p.slot;
   p.bytes = off;
   return p;
 }
 
-template <int FMT, int NT, int SRC>
-__device__ __forceinline__ void stage_chunk(const GemvArgs& a, __half* xs, float* xsum, const float* rs, int tok0,
-                                            int ntok, int k0, int kc) {
-  if constexpr (SRC == SRC_NORM) {
-    stage_norm_chunk(xs, a.sp.ldx, a.xf + (size_t)tok0 * a.ld_src, a.ld_src, nullptr, ntok, NT * 8, rs, a.norm_w,
-                     k0, kc);
-  } else {
-    stage_f16_chunk(xs, a.sp.ldx, a.xh, a.ld_src, nullptr, tok0, ntok, NT * 8, k0, kc);
-  }
-  if constexpr (FMT == I8ASYM) {
-    __syncthreads();
-    stage_block_sums(xsum, xs, a.sp.ldx, NT * 8, kc);
-  }
-}
-
 template <int FMT, int NT, int SRC, int EPI>
-__global__ void __launch_bounds__(kThreads) k_gemv(const GemvArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  __half* xs = reinterpret_cast<__half*>(smem);
-  float* xsum = reinterpret_cast<float*>(smem + a.sp.xsum_off);
-  float* red = reinterpret_cast<float*>(smem + a.sp.red_off);
-  float* rs = reinterpret_cast<float*>(smem + a.sp.rs_off);
+__global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const StreamPlan& p = a.sp;
   __shared__ int s_last;
+  __shared__ unsigned long long s_best[NT * 8];  // EPI_LOGITS: argmax key per token of this CTA
+  __half* xs = reinterpret_cast<__half*>(smem + p.xs_off);
+  float* red = reinterpret_cast<float*>(smem + p.red_off);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = smem + p.ring_off + (size_t)warp * kRingDepth * p.slot;
 
-  constexpr int KU = unit_k(FMT);
-  constexpr int SB = unit_scale_bytes(FMT);
+  pdl_launch_dependents();
   const int tok0 = blockIdx.y * NT * 8;
   const int ntok = min(a.ntok - tok0, NT * 8);
-  const int K = a.w.K, U = a.w.U, kc = a.sp.kc;
-  const bool single = (kc >= K);
+  const int K = a.w.K;
+  const int my_slabs = ((int)blockIdx.x < a.w.n_slabs) ? (a.w.n_slabs - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const SlabWork w = slab_work(blockIdx.x, gridDim.x, my_slabs, a.w.U);
+  // the weights do not depend on the previous kernel: start streaming them now
+  UnitStream<FMT> us;
+  us.start(a.w.q, a.w.s, w);
+  us.prefetch(ring, p.slot, w, lane);
 
+  pdl_wait();  // activations come from the previous kernel
+  int* s_pos = reinterpret_cast<int*>(smem + p.rows_off);
+  double* s_freq = reinterpret_cast<double*>(smem + p.extra_off);
+  if constexpr (EPI == EPI_QKV) {
+    for (int i = threadIdx.x; i < ntok; i += blockDim.x) s_pos[i] = max(a.pos[tok0 + i], 0);
+    for (int i = threadIdx.x; i < a.D / 2; i += blockDim.x) s_freq[i] = a.inv_freq[i];
+  }
+  if constexpr (EPI == EPI_LOGITS) {
+    if (threadIdx.x < NT * 8) s_best[threadIdx.x] = 0ull;
+  }
   if constexpr (SRC == SRC_NORM) {
-    stage_rms(rs, a.xf + (size_t)tok0 * a.ld_src, a.ld_src, nullptr, ntok, K, a.eps);
-    __syncthreads();
+    stage_norm_rows(xs, p.ldx, a.xf + (size_t)tok0 * a.ld_src, a.ld_src, ntok, NT * 8, a.norm_w, K, a.eps);
+  } else {
+    stage_f16(xs, p.ldx, a.xh + (size_t)tok0 * a.ld_src, a.ld_src, ntok, NT * 8, K);
   }
-  if (single) {
-    stage_chunk<FMT, NT, SRC>(a, xs, xsum, rs, tok0, ntok, 0, K);
-    __syncthreads();
-  }
+  __syncthreads();
 
-  unsigned long long best = 0ull;  // EPI_LOGITS: running argmax key of (token, pg)
-
-  for (int s = blockIdx.x; s < a.w.n_slabs; s += gridDim.x) {
-    float acc[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    const uint8_t* wq = a.w.q + (size_t)s * U * kUnitBytes;
-    const uint8_t* ws = a.w.s + (size_t)s * U * SB;
-    if (single) {
-      slab_units<FMT, NT>(acc, wq, ws, 0, U, xs, a.sp.ldx, 0, xsum, K / 32);
-    } else {
-      for (int k0 = 0; k0 < K; k0 += kc) {
-        const int kcc = min(kc, K - k0);
-        __syncthreads();
-        stage_chunk<FMT, NT, SRC>(a, xs, xsum, rs, tok0, ntok, k0, kcc);
-        __syncthreads();
-        slab_units<FMT, NT>(acc, wq, ws, k0 / KU, (k0 + kcc) / KU, xs, a.sp.ldx, k0, xsum, kcc / 32);
-      }
-    }
-    slab_store_partial<NT>(acc, red);
-    __syncthreads();
-    for (int i = threadIdx.x; i < NT * 64; i += kThreads) {
+  const BSmem bp{xs, p.ldx};
+  auto epi = [&](int s, const float* rb, int tid, int nthr) {
+    for (int i = tid; i < NT * 64; i += nthr) {
       const int tok = i >> 3, pg = i & 7;
       if (tok >= ntok) continue;
       float lo, hi;
-      slab_sum<NT>(red, tok, pg, lo, hi);
+      group_sum<NT>(rb, w.ks, tok, pg, lo, hi);
       const int gt = tok0 + tok;
       if constexpr (EPI == EPI_RESID) {
-        const int c = 16 * s + pg;
-        a.out_f[(size_t)gt * a.ld_out + c] = a.res_in[(size_t)gt * a.ld_out + c] + lo;
-        a.out_f[(size_t)gt * a.ld_out + c + 8] = a.res_in[(size_t)gt * a.ld_out + c + 8] + hi;
+        const int col = 16 * s + pg;
+        a.out_f[(size_t)gt * a.ld_out + col] = a.res_in[(size_t)gt * a.ld_out + col] + lo;
+        a.out_f[(size_t)gt * a.ld_out + col + 8] = a.res_in[(size_t)gt * a.ld_out + col + 8] + hi;
       } else if constexpr (EPI == EPI_SWIGLU) {
         a.out_h[(size_t)gt * a.ld_out + 8 * s + pg] = __float2half_rn(silu(lo) * hi);
       } else if constexpr (EPI == EPI_LOGITS) {
         const int r0 = 16 * s + pg, r1 = r0 + 8;
+        unsigned long long best = 0ull;
         if (r0 < a.n_valid) {
           if (a.out_f) a.out_f[(size_t)gt * a.n_valid + r0] = lo;
-          const unsigned long long k0 = argmax_key(lo, r0);
-          best = k0 > best ? k0 : best;
+          best = argmax_key(lo, r0);
         }
         if (r1 < a.n_valid) {
           if (a.out_f) a.out_f[(size_t)gt * a.n_valid + r1] = hi;
           const unsigned long long k1 = argmax_key(hi, r1);
           best = k1 > best ? k1 : best;
         }
+        if (best != 0ull) atomicMax(&s_best[tok], best);
       } else {  // EPI_QKV
-        int p = a.pos[gt];
-        if (p < 0) p = 0;  // reported by the embedding kernel
+        const int pos = s_pos[tok];  // negative positions are reported by the embedding kernel
         const int pr = 16 * s + pg;
         const int sec = pr / a.S;
         const int wi = pr - sec * a.S;
@@ -140,7 +124,7 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const GemvArgs a) {
         const int dlo = 8 * js + pg, dhi = (a.D >> 1) + dlo;
         float vlo = lo, vhi = hi;
         if (sec < 2) {
-          double ang = (double)p * a.inv_freq[dlo];
+          double ang = (double)pos * s_freq[dlo];
           ang -= 6.283185307179586 * rint(ang * 0.15915494309189535);
           float sn, cs;
           sincosf((float)ang, &sn, &cs);
@@ -152,25 +136,19 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const GemvArgs a) {
           qo[dlo] = vlo;
           qo[dhi] = vhi;
         } else {
-          const int slot = p < a.P ? p : a.P + (p - a.P) % a.R;
-          __half* c = a.kv + ((((size_t)gt * 2 + (sec - 1)) * a.nh + head) * a.SL + slot) * a.D;
-          c[dlo] = __float2half_rn(vlo);
-          c[dhi] = __float2half_rn(vhi);
+          const int slot = pos < a.P ? pos : a.P + (pos - a.P) % a.R;
+          __half* c_ = a.kv + ((((size_t)gt * 2 + (sec - 1)) * a.nh + head) * a.SL + slot) * a.D;
+          c_[dlo] = __float2half_rn(vlo);
+          c_[dhi] = __float2half_rn(vhi);
         }
       }
     }
-    __syncthreads();
-  }
+  };
+  run_stream<FMT, NT>(us, w, ring, p.slot, red, bp, NT, epi);
 
   if constexpr (EPI == EPI_LOGITS) {
-    // best over the 8 threads (consecutive lanes) of each token, then one atomic per token
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
-    }
-    const int tok = threadIdx.x >> 3;
-    if ((threadIdx.x & 7) == 0 && tok < ntok && best != 0ull) atomicMax(a.keys + tok0 + tok, best);
+    __syncthreads();
+    if (threadIdx.x < ntok && s_best[threadIdx.x] != 0ull) atomicMax(a.keys + tok0 + threadIdx.x, s_best[threadIdx.x]);
     __syncthreads();
     if (threadIdx.x == 0) {
       __threadfence();
@@ -178,10 +156,10 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const GemvArgs a) {
       s_last = (done == (int)(gridDim.x * gridDim.y) - 1);
     }
     __syncthreads();
-    if (s_last && threadIdx.x == 0) {
+    if (s_last) {  // the last CTA: one thread per row writes (and chains) the ids
       __threadfence();
       const int step = a.hist ? *a.hist_ctr : 0;
-      for (int t = 0; t < a.ntok; ++t) {
+      for (int t = threadIdx.x; t < a.ntok; t += kThreads) {
         const unsigned long long key = atomicExch(a.keys + t, 0ull);
         const int id = argmax_key_index(key);
         a.next_ids[t] = id;
@@ -191,53 +169,54 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const GemvArgs a) {
         }
         if (a.hist) a.hist[(size_t)step * a.ntok + t] = id;
       }
-      if (a.hist) *a.hist_ctr = step + 1;
-      atomicExch(a.counter, 0);
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        if (a.hist) *a.hist_ctr = step + 1;
+        atomicExch(a.counter, 0);
+      }
     }
   }
 }
 
 template <int FMT, int NT, int SRC, int EPI>
-static cudaError_t launch_one(const GemvArgs& a, int gx, int gy, cudaStream_t st) {
-  k_gemv<FMT, NT, SRC, EPI><<<dim3(gx, gy), kThreads, a.sp.bytes, st>>>(a);
-  return cudaGetLastError();
+static cudaError_t launch_one(const GemvArgs& a, int gx, int gy, cudaStream_t st, bool pdl) {
+  return launch_kernel(k_gemv<FMT, NT, SRC, EPI>, dim3(gx, gy), dim3(kThreads), a.sp.bytes, st, pdl, a);
 }
 
 template <int FMT, int NT>
-static cudaError_t dispatch_epi(int src, int epi, const GemvArgs& a, int gx, int gy, cudaStream_t st) {
-  if (src == SRC_NORM && epi == EPI_QKV) return launch_one<FMT, NT, SRC_NORM, EPI_QKV>(a, gx, gy, st);
-  if (src == SRC_F16 && epi == EPI_RESID) return launch_one<FMT, NT, SRC_F16, EPI_RESID>(a, gx, gy, st);
-  if (src == SRC_NORM && epi == EPI_SWIGLU) return launch_one<FMT, NT, SRC_NORM, EPI_SWIGLU>(a, gx, gy, st);
+static cudaError_t dispatch_epi(int src, int epi, const GemvArgs& a, int gx, int gy, cudaStream_t st, bool pdl) {
+  if (src == SRC_NORM && epi == EPI_QKV) return launch_one<FMT, NT, SRC_NORM, EPI_QKV>(a, gx, gy, st, pdl);
+  if (src == SRC_F16 && epi == EPI_RESID) return launch_one<FMT, NT, SRC_F16, EPI_RESID>(a, gx, gy, st, pdl);
+  if (src == SRC_NORM && epi == EPI_SWIGLU) return launch_one<FMT, NT, SRC_NORM, EPI_SWIGLU>(a, gx, gy, st, pdl);
   if constexpr (FMT == F16) {
-    if (src == SRC_NORM && epi == EPI_LOGITS) return launch_one<FMT, NT, SRC_NORM, EPI_LOGITS>(a, gx, gy, st);
+    if (src == SRC_NORM && epi == EPI_LOGITS) return launch_one<FMT, NT, SRC_NORM, EPI_LOGITS>(a, gx, gy, st, pdl);
   }
   return cudaErrorInvalidValue;
 }
 
 template <int NT>
-static cudaError_t dispatch_fmt(int fmt, int src, int epi, const GemvArgs& a, int gx, int gy, cudaStream_t st) {
+static cudaError_t dispatch_fmt(int fmt, int src, int epi, const GemvArgs& a, int gx, int gy, cudaStream_t st,
+                                bool pdl) {
   switch (fmt) {
-    case F16: return dispatch_epi<F16, NT>(src, epi, a, gx, gy, st);
-    case Q8_0: return dispatch_epi<Q8_0, NT>(src, epi, a, gx, gy, st);
-    case Q4_0: return dispatch_epi<Q4_0, NT>(src, epi, a, gx, gy, st);
-    case I8ASYM: return dispatch_epi<I8ASYM, NT>(src, epi, a, gx, gy, st);
+    case F16: return dispatch_epi<F16, NT>(src, epi, a, gx, gy, st, pdl);
+    case Q8_0: return dispatch_epi<Q8_0, NT>(src, epi, a, gx, gy, st, pdl);
+    case Q4_0: return dispatch_epi<Q4_0, NT>(src, epi, a, gx, gy, st, pdl);
+    case I8ASYM: return dispatch_epi<I8ASYM, NT>(src, epi, a, gx, gy, st, pdl);
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gemv(int fmt, int src, int epi, const GemvArgs& a, int gx, int gy, cudaStream_t st) {
-  if (a.sp.nt == 1) return dispatch_fmt<1>(fmt, src, epi, a, gx, gy, st);
-  if (a.sp.nt == 2) return dispatch_fmt<2>(fmt, src, epi, a, gx, gy, st);
+cudaError_t launch_gemv(int fmt, int src, int epi, const GemvArgs& a, int gx, int gy, cudaStream_t st, bool pdl) {
+  if (a.sp.nt == 1) return dispatch_fmt<1>(fmt, src, epi, a, gx, gy, st, pdl);
+  if (a.sp.nt == 2) return dispatch_fmt<2>(fmt, src, epi, a, gx, gy, st, pdl);
   return cudaErrorInvalidValue;
 }
 
 template <int FMT, int NT>
 static cudaError_t set_attr_fmt() {
-  const int mx = 200 * 1024;
   cudaError_t e = cudaSuccess;
-#define UOCR_SET(SRC_, EPI_)                                                                                    \
-  if (e == cudaSuccess)                                                                                         \
-    e = cudaFuncSetAttribute(k_gemv<FMT, NT, SRC_, EPI_>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+#define UOCR_SET(SRC_, EPI_) \
+  if (e == cudaSuccess) e = allow_max_dyn_smem(k_gemv<FMT, NT, SRC_, EPI_>);
   UOCR_SET(SRC_NORM, EPI_QKV)
   UOCR_SET(SRC_F16, EPI_RESID)
   UOCR_SET(SRC_NORM, EPI_SWIGLU)

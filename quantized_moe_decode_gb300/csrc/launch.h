@@ -5,32 +5,32 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "device_common.cuh"
 
 namespace uocr {
 
-// Shared-memory plan of a GEMV-family CTA: activation tile xs[NT*8][ldx]
-// fp16 (kc inputs staged at a time), I8ASYM block sums, cross-warp
-// reduction buffer and per-token norm factors.
-struct StagePlan {
-  int nt;        // n-tiles of 8 tokens per CTA (1 or 2)
-  int kc;        // inputs staged per chunk (multiple of 64, == K when it fits)
-  int ldx;       // kc + 8
-  int xsum_off;  // byte offsets into dynamic shared memory
-  int red_off;
-  int rs_off;
-  int rows_off;
+// Shared-memory plan of a streaming CTA: the activation tile xs[nt*8][ldx]
+// fp16 (ldx = K + 8), the cross-warp reduction buffer (two slabs), a row
+// list, a zero row, a kernel-specific region (extra) and the per-warp weight
+// rings (kWarps x kRingDepth slots of `slot` bytes).
+struct StreamPlan {
+  int nt;
+  int ldx;
+  int slot;
+  int xs_off, red_off, rows_off, zero_off, extra_off, ring_off;
   int bytes;
 };
 
-StagePlan plan_stage(int nt, int K, int fmt);
+StreamPlan plan_stream(int nt, int fmt, int k_stage, int n_rows_list = 0, int extra_bytes = 0);
 
 enum Src : int { SRC_NORM = 0, SRC_F16 = 1 };
 enum Epi : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
 
 struct GemvArgs {
   PMat w;
-  StagePlan sp;
+  StreamPlan sp;
   int ntok;                 // rows of the step
   // source: fp32 residual rows + RMSNorm weight, or fp16 rows
   const float* xf;
@@ -62,47 +62,44 @@ struct GemvArgs {
 };
 
 struct RouterArgs {
-  const __half* w;          // packed F16 router [E][H]
-  int n_slabs, U;
-  StagePlan sp;
-  int ntok, H, E, k;
+  PMat w;                   // packed F16 router [E][H]
+  StreamPlan sp;
+  int ntok, H, E;
   const float* h;           // residual after attention [rows][H]
   const __half* norm_w;
   float eps;
-  __half* xhat;             // out: normed fp16 rows [rows][H]
   float* logits;            // out: [rows][E]
-  int* idx;                 // out: [rows][k]
-  float* wts;               // out: [rows][k]
-  int* count;               // out: [E]
-  int* offset;              // out: [E+1]
-  int* perm;                // out: [rows*k]
-  int* inv;                 // out: [rows*k] position of entry row*k+slot in perm
-  int* active;              // out: [E] experts with count > 0, ascending
-  int* n_active;            // out
-  int* counter;
+  int* status;
 };
 
 struct ExpertArgs {
   PMat wr;                  // routed, expert e at q + e*q_stride
   PMat ws;                  // shared experts packed as one (n_slabs == 0: none)
-  StagePlan sp;
-  int ntok, k, H, Ie, Ish;
-  const __half* xhat;       // gate/up input [rows][H]
-  const int* count;
-  const int* offset;
-  const int* perm;
-  const int* active;
-  const int* n_active;
-  __half* act_r;            // [rows*k][Ie]   (gate/up out, down in)
-  __half* act_s;            // [rows][Ish]
+  StreamPlan sp;
+  int ntok, E, k, H, Ie, Ish;
+  int by_slot;              // routed CTAs by active slot (1) or by expert id (0)
+  int n_units;              // routed units of the grid: max active experts (by slot) or E
+  int cpe, cpes;            // CTAs per routed unit, for the shared experts
+  int tg;                   // token groups of 16 rows (blockIdx.y)
+  const float* logits;      // router logits [rows][E]
+  // routing and grouping: written by the gate/up launch (CTA 0, 0), read by the down launch
+  int* idx;                 // [rows][k] chosen experts
+  float* wts;               // [rows][k] renormalised weights
+  int* count;               // [E]
+  int* offset;              // [E+1]
+  int* perm;                // [rows*k] entries row*k + slot grouped by expert, rows ascending
+  int* inv;                 // [rows*k] position of each entry in perm
+  const float* h;           // residual after attention [rows][H] (gate/up input, combine residual)
+  const __half* norm_w;     // post-attention RMSNorm weight
+  float eps;
+  uint8_t* act_r;           // routed SwiGLU activations, B-fragment order, 16 tokens per (expert, group)
+  uint8_t* act_s;           // shared SwiGLU activations, B-fragment order over rows, K = Ish
   // down + combine
-  float* part_r;            // [rows*k][H]
+  float* part_r;            // [rows*k][H] per entry row*k + slot
   float* part_s;            // [rows][H]
-  const float* h;           // residual after attention
-  const float* wts;         // [rows][k]
-  const int* inv;           // [rows*k]
   float* out;               // layer output residual [rows][H]
   int* slab_counter;        // [H/16]
+  int* status;
 };
 
 struct AttnArgs {
@@ -115,6 +112,7 @@ struct AttnArgs {
   const float* sink;        // [nh] or nullptr
   int nh, D, P, R, SL, nsplit, chunk;
   float scale;
+  int* status;
 };
 
 struct EmbedArgs {
@@ -140,15 +138,50 @@ struct PackArgs {
 };
 enum PackMap : int { MAP_IDENT = 0, MAP_QKV = 1, MAP_SWIGLU = 2, MAP_KCAT = 3 };
 
-// launchers (return cudaGetLastError())
-cudaError_t launch_gemv(int fmt, int src, int epi, const GemvArgs& a, int grid_x, int grid_y, cudaStream_t st);
-cudaError_t launch_router(const RouterArgs& a, int grid_y, cudaStream_t st);
-cudaError_t launch_expert_gateup(int fmt_r, int fmt_s, const ExpertArgs& a, int grid, cudaStream_t st);
-cudaError_t launch_expert_down(int fmt_r, int fmt_s, const ExpertArgs& a, int grid, cudaStream_t st);
-cudaError_t launch_attn(const AttnArgs& a, int rows, cudaStream_t st);
+// Launch with or without programmatic dependent launch (the kernel may start
+// while the previous kernel on the stream finishes; it calls
+// griddepcontrol.wait before touching anything that kernel produces).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Allow a kernel the largest dynamic shared memory the device offers beside
+// its own static shared memory.
+template <typename... KArgs>
+cudaError_t allow_max_dyn_smem(void (*kern)(KArgs...)) {
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa{};
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+  return e;
+}
+
+// launchers (return the launch error)
+cudaError_t launch_gemv(int fmt, int src, int epi, const GemvArgs& a, int grid_x, int grid_y, cudaStream_t st,
+                        bool pdl);
+cudaError_t launch_router(const RouterArgs& a, int grid_y, cudaStream_t st, bool pdl);
+cudaError_t launch_expert_gateup(int fmt_r, int fmt_s, const ExpertArgs& a, cudaStream_t st, bool pdl);
+cudaError_t launch_expert_down(int fmt_r, int fmt_s, const ExpertArgs& a, cudaStream_t st, bool pdl);
+cudaError_t launch_attn(const AttnArgs& a, int rows, cudaStream_t st, bool pdl);
 cudaError_t launch_embed(const EmbedArgs& a, int rows, cudaStream_t st);
 cudaError_t launch_pack(const PackArgs& a, cudaStream_t st);
 cudaError_t launch_fill_zero_ring(__half* kv_layer_row, int nh, int SL, int D, int from_slot, cudaStream_t st);
 cudaError_t init_kernel_attributes();
+int attn_smem_bytes(int D);
 
 }  // namespace uocr

@@ -1,20 +1,25 @@
 // MoE kernels of one decode step.
 //
-//   router   RMSNorm prologue (the normalised fp16 rows are also written out
-//            for the experts) -> fp16 router GEMV (E logits per row); the last
-//            CTA to finish takes, per row, the top-k logits (lowest index wins
-//            a tie), the softmax weights renormalised over them, then the
-//            expert grouping: per-expert counts, exclusive scan, and the
-//            permutation of (row, slot) entries grouped by expert ascending,
-//            rows ascending, plus the list of experts that received a token.
-//   gate/up  one launch over (active expert, slab) items and the shared
-//            experts' slabs: each item gathers the rows routed to its expert,
-//            streams the expert's gate/up slab once for all of them and writes
-//            SwiGLU activations.
-//   down     one launch over (active expert, output slab) items and the
-//            shared slabs; each item writes fp32 partials; the last item of an
-//            output slab (a counter per slab, no waiting) combines them in a
-//            fixed order: residual + sum_j w_j * expert_j + shared.
+//   router   RMSNorm prologue -> fp16 router GEMV: E logits per row.
+//   gate/up  shared-expert CTAs first (they need nothing from the router),
+//            then routed CTAs.  A routed CTA owns one expert, one token group
+//            of 16 rows and a part of the expert's slabs.  It takes the top-k
+//            of its rows' logits itself (lowest index wins a tie) and keeps the
+//            rows that chose its expert: the expert's segment of the token
+//            grouping, as a row mask.  It streams the expert's gate/up slabs
+//            once for those rows and writes SwiGLU activations in the
+//            B-fragment order the down projection reads directly.  CTA (0, 0)
+//            also writes the routing of every row (ids, renormalised weights)
+//            and the grouping arrays (count, offset, perm, inv).
+//   down     the same CTA layout; it streams the expert's down slabs and
+//            writes fp32 partials; the last contribution to an output slab (a
+//            counter per slab, no waiting) combines them in a fixed order:
+//            residual + sum_j w_j * expert_j + shared.
+//
+// Routed CTAs are laid out either by expert id (when most experts are expected
+// to receive a token: the CTA streams the head of its expert's weights before
+// the router has finished, into bandwidth the router leaves idle) or by active
+// slot (few rows: CTA i serves the i-th expert that received a token).
 //
 // Sources: "Unlimited-OCR on Apple Silicon with C and Metal", "Il decoder e
 // il Mixture of Experts" (64 routed experts, top-6, two shared experts;
@@ -33,372 +38,540 @@ __device__ __forceinline__ float argmax_key_value(unsigned long long k) {
   return __uint_as_float(b);
 }
 
-// ------------------------------------------------------------------ router
-template <int NT>
-__global__ void __launch_bounds__(kThreads) k_router(const RouterArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  __half* xs = reinterpret_cast<__half*>(smem);
-  float* red = reinterpret_cast<float*>(smem + a.sp.red_off);
-  float* rs = reinterpret_cast<float*>(smem + a.sp.rs_off);
-  __shared__ int s_last;
-  __shared__ int s_idx[64 * 8];
-  __shared__ int s_cnt[257];
-
-  const int tok0 = blockIdx.y * NT * 8;
-  const int ntok = min(a.ntok - tok0, NT * 8);
-  const int H = a.H, ldx = a.sp.ldx;
-  const float* h = a.h + (size_t)tok0 * H;
-
-  stage_rms(rs, h, H, nullptr, ntok, H, a.eps);
-  __syncthreads();
-  stage_norm_chunk(xs, ldx, h, H, nullptr, ntok, NT * 8, rs, a.norm_w, 0, H);
-  __syncthreads();
-  if (blockIdx.x == 0) {  // the experts read these normalised rows
-    const int per = H / 8;
-    for (int i = threadIdx.x; i < ntok * per; i += kThreads) {
-      const int tk = i / per, j = (i - tk * per) * 8;
-      *reinterpret_cast<uint4*>(a.xhat + (size_t)(tok0 + tk) * H + j) =
-          *reinterpret_cast<const uint4*>(xs + tk * ldx + j);
+// Block-wide exclusive prefix sum of four counters (one value per thread).
+__device__ __forceinline__ int4 block_excl_scan4(int4 v, int4& total, int4* s_warp) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int4 inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, inc.x, o), y = __shfl_up_sync(0xffffffffu, inc.y, o);
+    const int z = __shfl_up_sync(0xffffffffu, inc.z, o), w = __shfl_up_sync(0xffffffffu, inc.w, o);
+    if (lane >= o) {
+      inc.x += x;
+      inc.y += y;
+      inc.z += z;
+      inc.w += w;
     }
   }
-  for (int s = blockIdx.x; s < a.n_slabs; s += gridDim.x) {
-    float acc[NT][4];
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  int4 base = make_int4(0, 0, 0, 0);
+  total = make_int4(0, 0, 0, 0);
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+    const int4 t = s_warp[w];
+    if (w < warp) {
+      base.x += t.x;
+      base.y += t.y;
+      base.z += t.z;
+      base.w += t.w;
+    }
+    total.x += t.x;
+    total.y += t.y;
+    total.z += t.z;
+    total.w += t.w;
+  }
+  __syncthreads();  // s_warp may be reused by the caller's next scan
+  return make_int4(base.x + inc.x - v.x, base.y + inc.y - v.y, base.z + inc.z - v.z, base.w + inc.w - v.w);
+}
+
+// ------------------------------------------------------------------ routing
+// One warp, one row: the E <= 256 logits (8 per lane).
+struct RowLogits {
+  float v[8];
+};
+__device__ __forceinline__ void topk_load(RowLogits& rl, const float* lg, int E, int lane) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    const uint8_t* wq = reinterpret_cast<const uint8_t*>(a.w) + (size_t)s * a.U * kUnitBytes;
-    slab_units<F16, NT>(acc, wq, nullptr, 0, a.U, xs, ldx, 0, nullptr, 0);
-    slab_store_partial<NT>(acc, red);
-    __syncthreads();
-    for (int i = threadIdx.x; i < NT * 64; i += kThreads) {
+  for (int q = 0; q < 8; ++q) {
+    const int e = lane + 32 * q;
+    rl.v[q] = e < E ? __ldcg(lg + e) : -INFINITY;
+  }
+}
+// Top-k by logit, lowest index first among equal logits; lane j < k gets the
+// j-th choice and its softmax weight renormalised over the k choices
+// (exp(l_j - l_0) / sum_i exp(l_i - l_0)).
+__device__ __forceinline__ void topk_select(const RowLogits& rl, int E, int k, int lane, int& e_j, float& w_j) {
+  bool taken[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) taken[q] = lane + 32 * q >= E;
+  float l0 = 0.f, wsum = 0.f, my_l = 0.f;
+  e_j = 0;
+  for (int j = 0; j < k; ++j) {
+    unsigned long long kb = 0ull;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (!taken[q]) {
+        const unsigned long long cc = argmax_key(rl.v[q], lane + 32 * q);
+        kb = cc > kb ? cc : kb;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, kb, o);
+      kb = other > kb ? other : kb;
+    }
+    const int e = argmax_key_index(kb);
+    const float le = argmax_key_value(kb);
+    if ((e & 31) == lane) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q == (e >> 5)) taken[q] = true;
+    }
+    if (j == 0) l0 = le;
+    wsum += expf(le - l0);
+    if (lane == j) {
+      e_j = e;
+      my_l = le;
+    }
+  }
+  w_j = expf(my_l - l0) / wsum;
+}
+
+// Routing state of a CTA in shared memory.
+struct RouteSmem {
+  int idx[64 * 8];                  // [row][k] chosen experts
+  float w[64 * 8];                  // [row][k] weights
+  unsigned long long rowmask[256];  // [E] rows that chose expert e (bit r)
+  int off[256];
+  int4 scan[kWarps];
+  int e, nlast, contrib;
+};
+
+// Top-k of rows [r0, r1) from the logits into rs (rowmask must start at zero).
+__device__ __forceinline__ void route_rows(RouteSmem& rs, const float* logits, int E, int k, int r0, int r1) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = r0 + warp; r < r1; r += kWarps) {
+    RowLogits rl;
+    topk_load(rl, logits + (size_t)r * E, E, lane);
+    int e;
+    float w;
+    topk_select(rl, E, k, lane, e, w);
+    if (lane < k) {
+      rs.idx[r * k + lane] = e;
+      rs.w[r * k + lane] = w;
+      atomicOr(&rs.rowmask[e], 1ull << r);  // a row picks an expert at most once
+    }
+  }
+}
+
+__device__ __forceinline__ void clear_rowmask(RouteSmem& rs, int E) {
+  for (int e = threadIdx.x; e < E; e += kThreads) rs.rowmask[e] = 0ull;
+}
+
+// The i-th expert (ascending) that received a token, or -1.  All threads.
+__device__ __forceinline__ int active_expert(RouteSmem& rs, int E, int i) {
+  const int e = threadIdx.x;
+  const int4 v = make_int4(e < E && rs.rowmask[e] != 0ull, 0, 0, 0);
+  int4 tot;
+  const int4 ex = block_excl_scan4(v, tot, rs.scan);
+  if (threadIdx.x == 0) rs.e = -1;
+  __syncthreads();
+  if (v.x && ex.x == i) rs.e = e;
+  __syncthreads();
+  return rs.e;
+}
+
+// Write every row's routing and the grouping: count[e] (histogram),
+// offset = exclusive scan, perm = entries row*k + slot grouped by expert
+// ascending, rows ascending within an expert; inv = position of each entry in
+// perm.  rs holds the top-k of all rows.  All threads.
+__device__ __forceinline__ void write_routing(RouteSmem& rs, const ExpertArgs& a) {
+  const int rows = a.ntok, E = a.E, k = a.k;
+  for (int i = threadIdx.x; i < rows * k; i += kThreads) {
+    a.idx[i] = rs.idx[i];
+    a.wts[i] = rs.w[i];
+  }
+  const int e = threadIdx.x;
+  const unsigned long long rm = e < E ? rs.rowmask[e] : 0ull;
+  int4 tot;
+  const int4 ex = block_excl_scan4(make_int4(__popcll(rm), 0, 0, 0), tot, rs.scan);
+  if (e < E) {
+    a.count[e] = __popcll(rm);
+    a.offset[e] = ex.x;
+    rs.off[e] = ex.x;
+  }
+  if (threadIdx.x == 0) a.offset[E] = tot.x;
+  __syncthreads();
+  for (int i = threadIdx.x; i < rows * k; i += kThreads) {
+    const int ei = rs.idx[i], r = i / k;
+    const int pos = rs.off[ei] + __popcll(rs.rowmask[ei] & ((1ull << r) - 1ull));
+    a.perm[pos] = i;
+    a.inv[i] = pos;
+  }
+}
+
+// ------------------------------------------------------------------ router
+template <int NT>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) k_router(const RouterArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const StreamPlan& p = a.sp;
+  __half* xs = reinterpret_cast<__half*>(smem + p.xs_off);
+  float* red = reinterpret_cast<float*>(smem + p.red_off);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = smem + p.ring_off + (size_t)warp * kRingDepth * p.slot;
+
+  pdl_launch_dependents();
+  const int tok0 = blockIdx.y * NT * 8;
+  const int ntok = min(a.ntok - tok0, NT * 8);
+  const int H = a.H;
+  const int my_slabs = ((int)blockIdx.x < a.w.n_slabs) ? (a.w.n_slabs - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const SlabWork w = slab_work(blockIdx.x, gridDim.x, my_slabs, a.w.U);
+  UnitStream<F16> us;
+  us.start(a.w.q, a.w.s, w);
+  us.prefetch(ring, p.slot, w, lane);
+  pdl_wait();
+  stage_norm_rows(xs, p.ldx, a.h + (size_t)tok0 * H, H, ntok, NT * 8, a.norm_w, H, a.eps);
+  __syncthreads();
+  const BSmem bp{xs, p.ldx};
+  auto epi = [&](int s, const float* rb, int tid, int nthr) {
+    for (int i = tid; i < NT * 64; i += nthr) {
       const int tok = i >> 3, pg = i & 7;
       if (tok >= ntok) continue;
       float lo, hi;
-      slab_sum<NT>(red, tok, pg, lo, hi);
+      group_sum<NT>(rb, w.ks, tok, pg, lo, hi);
       const int e0 = 16 * s + pg;
       if (e0 < a.E) a.logits[(size_t)(tok0 + tok) * a.E + e0] = lo;
       if (e0 + 8 < a.E) a.logits[(size_t)(tok0 + tok) * a.E + e0 + 8] = hi;
     }
-    __syncthreads();
-  }
+  };
+  run_stream<F16, NT>(us, w, ring, p.slot, red, bp, NT, epi);
+}
 
-  // ---- the last CTA: top-k, weights, grouping
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int done = atomicAdd(a.counter, 1);
-    s_last = (done == (int)(gridDim.x * gridDim.y) - 1);
+// ------------------------------------------------------------------ expert CTAs
+// blockIdx.x < ns (= cpes when there are shared experts, else 0): part x of
+// the shared experts.  Then routed CTAs: unit i = (x - ns) / cpe (expert id i,
+// or active slot i), part (x - ns) % cpe of its slabs.  blockIdx.y: token
+// group of 16 rows.
+struct ExpertCta {
+  bool shared;
+  int i, part, parts;
+};
+__device__ __forceinline__ ExpertCta expert_cta(const ExpertArgs& a) {
+  ExpertCta c;
+  const int ns = a.ws.n_slabs > 0 ? a.cpes : 0;
+  const int x = blockIdx.x;
+  c.shared = x < ns;
+  if (c.shared) {
+    c.i = -1;
+    c.part = x;
+    c.parts = a.cpes;
+  } else {
+    c.i = (x - ns) / a.cpe;
+    c.part = (x - ns) - c.i * a.cpe;
+    c.parts = a.cpe;
   }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+  return c;
+}
+
+// Slabs [lo, hi) of part `part` of `parts`: n slabs cut in runs of gran (the
+// slabs of one round of a CTA) so that every group of warps gets whole rounds.
+__device__ __forceinline__ void part_range(int n, int gran, int part, int parts, int& lo, int& hi) {
+  const int nr = (n + gran - 1) / gran;
+  lo = min(n, gran * (int)(((long long)nr * part) / parts));
+  hi = min(n, gran * (int)(((long long)nr * (part + 1)) / parts));
+}
+__device__ __forceinline__ int groups_of(int U) { return kWarps / warps_per_slab(U); }
+
+// Row mask (bits = rows of token group g) of expert e, from rs.rowmask.
+__device__ __forceinline__ unsigned group_mask(const RouteSmem& rs, int e, int g) {
+  return (unsigned)((rs.rowmask[e] >> (16 * g)) & 0xFFFFull);
+}
+
+// ------------------------------------------------------------------ gate/up
+template <int FR, int FS, int NT>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const ExpertArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ RouteSmem rs;
+  const StreamPlan& p = a.sp;
+  __half* xs = reinterpret_cast<__half*>(smem + p.xs_off);
+  float* red = reinterpret_cast<float*>(smem + p.red_off);
+  int* rows = reinterpret_cast<int*>(smem + p.rows_off);  // staged row of each token of the expert
+  __half* zero = reinterpret_cast<__half*>(smem + p.zero_off);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rows = a.ntok, E = a.E, k = a.k;
-  for (int r = warp; r < rows; r += kWarps) {
-    float v[8];
-    bool taken[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = lane + 32 * j;
-      v[j] = e < E ? __ldcg(a.logits + (size_t)r * E + e) : -INFINITY;
-      taken[j] = e >= E;
+  uint8_t* ring = smem + p.ring_off + (size_t)warp * kRingDepth * p.slot;
+
+  pdl_launch_dependents();
+  const ExpertCta ec = expert_cta(a);
+  const int g = blockIdx.y, tok0 = g * 16;
+  const int ng = min(16, a.ntok - tok0);  // rows of this token group
+  int s0 = 0, s1 = 0;
+  SlabWork w;
+  UnitStream<FS> uss;
+  UnitStream<FR> usr;
+  bool streaming = false;
+  if (ec.shared) {  // the shared experts need nothing from the router: start streaming now
+    part_range(a.ws.n_slabs, groups_of(a.ws.U), ec.part, ec.parts, s0, s1);
+    w = slab_work(s0, 1, s1 - s0, a.ws.U);
+    uss.start(a.ws.q, a.ws.s, w);
+    uss.prefetch(ring, p.slot, w, lane);
+    streaming = true;
+  } else if (!a.by_slot) {  // expert-id layout: the head of this expert's weights, before the routing is known
+    part_range(a.wr.n_slabs, groups_of(a.wr.U), ec.part, ec.parts, s0, s1);
+    w = slab_work(s0, 1, s1 - s0, a.wr.U);
+    usr.start(a.wr.q + (size_t)ec.i * a.wr.q_stride, a.wr.s + (size_t)ec.i * a.wr.s_stride, w);
+    usr.prefetch(ring, p.slot, w, lane);
+    streaming = true;
+  }
+  clear_rowmask(rs, a.E);
+  if (threadIdx.x < 16) zero[threadIdx.x * 2] = zero[threadIdx.x * 2 + 1] = __float2half_rn(0.f);
+  __syncthreads();
+  pdl_wait();
+
+  // routing: CTA (0, 0) and the slot layout need every row, the others their group
+  const bool first = blockIdx.x == 0 && blockIdx.y == 0;
+  const bool all_rows = first || (!ec.shared && a.by_slot);
+  if (all_rows || !ec.shared) {
+    route_rows(rs, a.logits, a.E, a.k, all_rows ? 0 : tok0, all_rows ? a.ntok : tok0 + ng);
+    __syncthreads();
+  }
+  if (first) write_routing(rs, a);
+  // this CTA's rows
+  int e = -1, ntk = ng;
+  if (!ec.shared) {
+    e = a.by_slot ? active_expert(rs, a.E, ec.i) : ec.i;
+    const unsigned mask = e >= 0 ? group_mask(rs, e, g) : 0u;
+    ntk = __popc(mask);
+    if (ntk == 0) {
+      if (streaming) cp_wait<0>();  // copies in flight land before the CTA leaves
+      return;
     }
-    float l0 = 0.f, wsum = 0.f;
-    float lsel[8];
-    int isel[8];
-    for (int j = 0; j < k; ++j) {
-      unsigned long long kb = 0ull;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (!taken[q]) {
-          const unsigned long long c = argmax_key(v[q], lane + 32 * q);
-          kb = c > kb ? c : kb;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const unsigned long long other = __shfl_xor_sync(0xffffffffu, kb, o);
-        kb = other > kb ? other : kb;
-      }
-      const int e = argmax_key_index(kb);
-      const float le = argmax_key_value(kb);
-      if ((e & 31) == lane) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q == (e >> 5)) taken[q] = true;
-      }
-      if (j == 0) l0 = le;
-      isel[j] = e;
-      lsel[j] = le;
-      wsum += expf(le - l0);
-    }
-    if (lane == 0) {
-      for (int j = 0; j < k; ++j) {
-        a.idx[r * k + j] = isel[j];
-        a.wts[r * k + j] = expf(lsel[j] - l0) / wsum;
-        s_idx[r * k + j] = isel[j];
-      }
+    if (threadIdx.x < 16 && ((mask >> threadIdx.x) & 1))
+      rows[__popc(mask & ((1u << threadIdx.x) - 1u))] = threadIdx.x;
+    if (threadIdx.x >= ntk && threadIdx.x < NT * 8) rows[threadIdx.x] = -1;
+    if (a.by_slot) {
+      part_range(a.wr.n_slabs, groups_of(a.wr.U), ec.part, ec.parts, s0, s1);
+      w = slab_work(s0, 1, s1 - s0, a.wr.U);
+      usr.start(a.wr.q + (size_t)e * a.wr.q_stride, a.wr.s + (size_t)e * a.wr.s_stride, w);
+      usr.prefetch(ring, p.slot, w, lane);
     }
   }
+  // the group's rows, normalised (all of them: the expert's rows are gathered by the B operand)
+  stage_norm_rows(xs, p.ldx, a.h + (size_t)tok0 * a.H, a.H, ng, NT * 8, a.norm_w, a.H, a.eps);
   __syncthreads();
-  const int nent = rows * k;
-  for (int e = threadIdx.x; e < E; e += kThreads) {
+  const int nt_used = (ntk + 7) >> 3;
+  if (ec.shared) {
+    auto epi = [&](int sl, const float* rb, int tid, int nthr) {
+      for (int i = tid; i < NT * 64; i += nthr) {
+        const int tok = i >> 3, pg = i & 7;
+        if (tok >= ntk) continue;
+        float lo, hi;
+        group_sum<NT>(rb, w.ks, tok, pg, lo, hi);
+        const int r = tok0 + tok;
+        *reinterpret_cast<__half*>(a.act_s + bfrag_offset(r >> 3, r & 7, 8 * sl + pg, a.Ish >> 5)) =
+            __float2half_rn(silu(lo) * hi);
+      }
+    };
+    run_stream<FS, NT>(uss, w, ring, p.slot, red, BSmem{xs, p.ldx}, nt_used, epi);
+  } else {
+    const int tile0 = (e * a.tg + g) * 2;  // two 8-token tiles per (expert, token group)
+    auto epi = [&](int sl, const float* rb, int tid, int nthr) {
+      for (int i = tid; i < NT * 64; i += nthr) {
+        const int tok = i >> 3, pg = i & 7;
+        if (tok >= ntk) continue;
+        float lo, hi;
+        group_sum<NT>(rb, w.ks, tok, pg, lo, hi);
+        *reinterpret_cast<__half*>(a.act_r + bfrag_offset(tile0 + (tok >> 3), tok & 7, 8 * sl + pg, a.Ie >> 5)) =
+            __float2half_rn(silu(lo) * hi);
+      }
+    };
+    run_stream<FR, NT>(usr, w, ring, p.slot, red, BSmemGather{xs, p.ldx, rows, zero}, nt_used, epi);
+  }
+}
+
+// ------------------------------------------------------------------ down + combine
+template <int FR, int FS, int NT>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const ExpertArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ RouteSmem rs;
+  __shared__ int s_entry[16];  // entry row*k + slot of each token of the expert
+  const StreamPlan& p = a.sp;
+  float* red = reinterpret_cast<float*>(smem + p.red_off);
+  uint8_t* btile = smem + p.extra_off;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = smem + p.ring_off + (size_t)warp * kRingDepth * p.slot;
+
+  pdl_launch_dependents();
+  const ExpertCta ec = expert_cta(a);
+  const int g = blockIdx.y, tok0 = g * 16, H = a.H, E = a.E, k = a.k, rows = a.ntok;
+  int s0 = 0, s1 = 0;
+  SlabWork w;
+  UnitStream<FS> uss;
+  UnitStream<FR> usr;
+  bool streaming = false;
+  if (ec.shared) {
+    part_range(H / 16, groups_of(a.ws.U), ec.part, ec.parts, s0, s1);
+    w = slab_work(s0, 1, s1 - s0, a.ws.U);
+    uss.start(a.ws.q, a.ws.s, w);
+    uss.prefetch(ring, p.slot, w, lane);
+    streaming = true;
+  } else if (!a.by_slot) {
+    part_range(H / 16, groups_of(a.wr.U), ec.part, ec.parts, s0, s1);
+    w = slab_work(s0, 1, s1 - s0, a.wr.U);
+    usr.start(a.wr.q + (size_t)ec.i * a.wr.q_stride, a.wr.s + (size_t)ec.i * a.wr.s_stride, w);
+    usr.prefetch(ring, p.slot, w, lane);
+    streaming = true;
+  }
+  clear_rowmask(rs, E);
+  if (threadIdx.x == 0) rs.contrib = 0;
+  __syncthreads();
+  pdl_wait();
+  // the routing the gate/up launch wrote
+  for (int i = threadIdx.x; i < rows * k; i += kThreads) {
+    const int ei = __ldcg(a.idx + i);
+    rs.idx[i] = ei;
+    rs.w[i] = __ldcg(a.wts + i);
+    atomicOr(&rs.rowmask[ei], 1ull << (i / k));
+  }
+  __syncthreads();
+  // contributions every output slab receives: one per (expert, token group) with rows, one per shared group
+  if (threadIdx.x < E) {
     int c = 0;
-    for (int i = 0; i < nent; ++i) c += (s_idx[i] == e);
-    s_cnt[e] = c;
+    for (int gg = 0; gg < a.tg; ++gg) c += group_mask(rs, threadIdx.x, gg) != 0u;
+    if (c) atomicAdd(&rs.contrib, c);
+  }
+  int e = -1, ntk, k32;
+  const uint8_t* bsrc;
+  if (ec.shared) {
+    ntk = min(16, rows - tok0);
+    k32 = a.Ish >> 5;
+    bsrc = a.act_s + (size_t)(tok0 >> 3) * k32 * 512;
+  } else {
+    e = a.by_slot ? active_expert(rs, E, ec.i) : ec.i;
+    const unsigned mask = e >= 0 ? group_mask(rs, e, g) : 0u;
+    ntk = __popc(mask);
+    if (ntk == 0) {
+      if (streaming) cp_wait<0>();
+      return;
+    }
+    if (threadIdx.x < 16 && ((mask >> threadIdx.x) & 1)) {
+      const int r = tok0 + threadIdx.x;
+      int j = 0;
+      while (j < k - 1 && rs.idx[r * k + j] != e) ++j;
+      s_entry[__popc(mask & ((1u << threadIdx.x) - 1u))] = r * k + j;
+    }
+    k32 = a.Ie >> 5;
+    bsrc = a.act_r + (size_t)((e * a.tg + g) * 2) * k32 * 512;
+    if (a.by_slot) {
+      part_range(H / 16, groups_of(a.wr.U), ec.part, ec.parts, s0, s1);
+      w = slab_work(s0, 1, s1 - s0, a.wr.U);
+      usr.start(a.wr.q + (size_t)e * a.wr.q_stride, a.wr.s + (size_t)e * a.wr.s_stride, w);
+      usr.prefetch(ring, p.slot, w, lane);
+    }
+  }
+  const int tiles = (ntk + 7) >> 3;
+  stage_bytes(btile, bsrc, tiles * k32 * 512);
+  __syncthreads();
+  const int s_contrib = rs.contrib + (a.ws.n_slabs > 0 ? a.tg : 0);
+  const BSmemFrag bp{btile, k32};
+  auto epi = [&](int sl, const float* rb, int tid, int nthr) {
+    for (int i = tid; i < NT * 64; i += nthr) {
+      const int tok = i >> 3, pg = i & 7;
+      if (tok >= ntk) continue;
+      float lo, hi;
+      group_sum<NT>(rb, w.ks, tok, pg, lo, hi);
+      float* dst = ec.shared ? a.part_s + (size_t)(tok0 + tok) * H : a.part_r + (size_t)s_entry[tok] * H;
+      dst[16 * sl + pg] = lo;
+      dst[16 * sl + pg + 8] = hi;
+    }
+  };
+  if (ec.shared)
+    run_stream<FS, NT>(uss, w, ring, p.slot, red, bp, tiles, epi);
+  else
+    run_stream<FR, NT>(usr, w, ring, p.slot, red, bp, tiles, epi);
+
+  // one counter per output slab; the last contribution to a slab combines it.
+  // All of this CTA's slabs are counted at once (one thread per slab), and all
+  // slabs it finishes are combined in one batched pass.
+  int* s_last = reinterpret_cast<int*>(red);  // the partial buffers are free now
+  __syncthreads();
+  if (threadIdx.x == 0) rs.nlast = 0;
+  __syncthreads();
+  for (int t = threadIdx.x; t < s1 - s0; t += kThreads) {
+    __threadfence();
+    const int done = atomicAdd(a.slab_counter + s0 + t, 1);
+    if (done == s_contrib - 1) s_last[atomicAdd(&rs.nlast, 1)] = s0 + t;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0, na = 0;
-    for (int e = 0; e < E; ++e) {
-      const int c = s_cnt[e];
-      a.count[e] = c;
-      a.offset[e] = run;
-      if (c > 0) a.active[na++] = e;
-      s_cnt[e] = run;  // becomes the exclusive offset
-      run += c;
-    }
-    a.offset[E] = run;
-    *a.n_active = na;
-    atomicExch(a.counter, 0);
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += kThreads) {
-    int pos = s_cnt[e];
-    for (int i = 0; i < nent; ++i) {  // entries i = row*k + slot in row order
-      if (s_idx[i] == e) {
-        a.perm[pos] = i;
-        a.inv[i] = pos;
-        ++pos;
-      }
-    }
-  }
-}
-
-// ------------------------------------------------------------------ experts
-// Item of the gate/up launch: (active expert i, slab) for routed experts,
-// then the slabs of the shared experts.
-template <int FMT_R, int FMT_S, int NT>
-__global__ void __launch_bounds__(kThreads) k_expert_gateup(const ExpertArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  __half* xs = reinterpret_cast<__half*>(smem);
-  float* xsum = reinterpret_cast<float*>(smem + a.sp.xsum_off);
-  float* red = reinterpret_cast<float*>(smem + a.sp.red_off);
-  int* srows = reinterpret_cast<int*>(smem + a.sp.rows_off);
-
-  const int n_act = *a.n_active;
-  const int items_r = n_act * a.wr.n_slabs;
-  const int items = items_r + a.ws.n_slabs;
-  const int H = a.H, ldx = a.sp.ldx;
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
-    const bool routed = item < items_r;
-    int s, cnt, off;
-    const uint8_t *wq, *wsc;
-    if (routed) {
-      const int i = item / a.wr.n_slabs;
-      s = item - i * a.wr.n_slabs;
-      const int e = a.active[i];
-      cnt = a.count[e];
-      off = a.offset[e];
-      wq = a.wr.q + (size_t)e * a.wr.q_stride + (size_t)s * a.wr.U * kUnitBytes;
-      wsc = a.wr.s + (size_t)e * a.wr.s_stride + (size_t)s * a.wr.U * unit_scale_bytes(FMT_R);
-    } else {
-      s = item - items_r;
-      cnt = a.ntok;
-      off = 0;
-      wq = a.ws.q + (size_t)s * a.ws.U * kUnitBytes;
-      wsc = a.ws.s + (size_t)s * a.ws.U * unit_scale_bytes(FMT_S);
-    }
-    for (int t0 = 0; t0 < cnt; t0 += NT * 8) {
-      const int ntok = min(NT * 8, cnt - t0);
-      __syncthreads();
-      if (threadIdx.x < ntok) srows[threadIdx.x] = routed ? a.perm[off + t0 + threadIdx.x] / a.k : t0 + threadIdx.x;
-      __syncthreads();
-      stage_f16_chunk(xs, ldx, a.xhat, H, srows, 0, ntok, NT * 8, 0, H);
-      const bool i8 = routed ? (FMT_R == I8ASYM) : (FMT_S == I8ASYM);
-      if (i8) {
-        __syncthreads();
-        stage_block_sums(xsum, xs, ldx, NT * 8, H);
-      }
-      __syncthreads();
-      float acc[NT][4];
+  const int nlast = rs.nlast;
+  if (nlast == 0) return;
+  __threadfence();
+  constexpr int B = 4;  // items per thread per batch: loads first, then sums
+  const int items = nlast * rows * 16;
+  for (int i0 = threadIdx.x; i0 < items; i0 += B * kThreads) {
+    float pr[B][8], ps[B], hv[B];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-      if (routed)
-        slab_units<FMT_R, NT>(acc, wq, wsc, 0, a.wr.U, xs, ldx, 0, xsum, H / 32);
-      else
-        slab_units<FMT_S, NT>(acc, wq, wsc, 0, a.ws.U, xs, ldx, 0, xsum, H / 32);
-      slab_store_partial<NT>(acc, red);
-      __syncthreads();
-      for (int i = threadIdx.x; i < NT * 64; i += kThreads) {
-        const int tok = i >> 3, pg = i & 7;
-        if (tok >= ntok) continue;
-        float lo, hi;
-        slab_sum<NT>(red, tok, pg, lo, hi);
-        const __half v = __float2half_rn(silu(lo) * hi);
-        if (routed)
-          a.act_r[(size_t)(off + t0 + tok) * a.Ie + 8 * s + pg] = v;
-        else
-          a.act_s[(size_t)(t0 + tok) * a.Ish + 8 * s + pg] = v;
-      }
-    }
-  }
-}
-
-template <int FMT_R, int FMT_S, int NT>
-__global__ void __launch_bounds__(kThreads) k_expert_down(const ExpertArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  __half* xs = reinterpret_cast<__half*>(smem);
-  float* xsum = reinterpret_cast<float*>(smem + a.sp.xsum_off);
-  float* red = reinterpret_cast<float*>(smem + a.sp.red_off);
-  __shared__ int s_last;
-
-  const int n_act = *a.n_active;
-  const int nS = a.H / 16;
-  const int items_r = n_act * nS;
-  const bool has_shared = a.ws.n_slabs > 0;
-  const int items = items_r + (has_shared ? nS : 0);
-  const int per_slab = n_act + (has_shared ? 1 : 0);
-  const int H = a.H, ldx = a.sp.ldx;
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
-    const bool routed = item < items_r;
-    int s, cnt, off, K;
-    const uint8_t *wq, *wsc;
-    const __half* src;
-    if (routed) {
-      const int i = item / nS;
-      s = item - i * nS;
-      const int e = a.active[i];
-      cnt = a.count[e];
-      off = a.offset[e];
-      K = a.Ie;
-      src = a.act_r;
-      wq = a.wr.q + (size_t)e * a.wr.q_stride + (size_t)s * a.wr.U * kUnitBytes;
-      wsc = a.wr.s + (size_t)e * a.wr.s_stride + (size_t)s * a.wr.U * unit_scale_bytes(FMT_R);
-    } else {
-      s = item - items_r;
-      cnt = a.ntok;
-      off = 0;
-      K = a.Ish;
-      src = a.act_s;
-      wq = a.ws.q + (size_t)s * a.ws.U * kUnitBytes;
-      wsc = a.ws.s + (size_t)s * a.ws.U * unit_scale_bytes(FMT_S);
-    }
-    for (int t0 = 0; t0 < cnt; t0 += NT * 8) {
-      const int ntok = min(NT * 8, cnt - t0);
-      __syncthreads();
-      stage_f16_chunk(xs, ldx, src, K, nullptr, off + t0, ntok, NT * 8, 0, K);
-      const bool i8 = routed ? (FMT_R == I8ASYM) : (FMT_S == I8ASYM);
-      if (i8) {
-        __syncthreads();
-        stage_block_sums(xsum, xs, ldx, NT * 8, K);
-      }
-      __syncthreads();
-      float acc[NT][4];
+    for (int b = 0; b < B; ++b) {
+      const int i = i0 + b * kThreads;
+      const int it = i < items ? i : 0;
+      const int sl = s_last[it / (rows * 16)], rc = it % (rows * 16);
+      const int r = rc >> 4, col = 16 * sl + (rc & 15);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-      if (routed)
-        slab_units<FMT_R, NT>(acc, wq, wsc, 0, a.wr.U, xs, ldx, 0, xsum, K / 32);
-      else
-        slab_units<FMT_S, NT>(acc, wq, wsc, 0, a.ws.U, xs, ldx, 0, xsum, K / 32);
-      slab_store_partial<NT>(acc, red);
-      __syncthreads();
-      for (int i = threadIdx.x; i < NT * 64; i += kThreads) {
-        const int tok = i >> 3, pg = i & 7;
-        if (tok >= ntok) continue;
-        float lo, hi;
-        slab_sum<NT>(red, tok, pg, lo, hi);
-        float* dst = routed ? a.part_r + (size_t)(off + t0 + tok) * H : a.part_s + (size_t)(t0 + tok) * H;
-        dst[16 * s + pg] = lo;
-        dst[16 * s + pg + 8] = hi;
-      }
+      for (int jj = 0; jj < 8; ++jj)
+        pr[b][jj] = jj < k ? __ldcg(a.part_r + (size_t)(r * k + jj) * H + col) : 0.f;
+      ps[b] = a.ws.n_slabs > 0 ? __ldcg(a.part_s + (size_t)r * H + col) : 0.f;
+      hv[b] = a.h[(size_t)r * H + col];
     }
-    // the last item of this output slab combines it
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      __threadfence();
-      const int done = atomicAdd(a.slab_counter + s, 1);
-      s_last = (done == per_slab - 1);
-    }
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      for (int i = threadIdx.x; i < a.ntok * 16; i += kThreads) {
-        const int r = i >> 4, c = 16 * s + (i & 15);
-        float v = a.h[(size_t)r * H + c];
-        for (int j = 0; j < a.k; ++j)
-          v += a.wts[r * a.k + j] * __ldcg(a.part_r + (size_t)a.inv[r * a.k + j] * H + c);
-        if (has_shared) v += __ldcg(a.part_s + (size_t)r * H + c);
-        a.out[(size_t)r * H + c] = v;
-      }
-      if (threadIdx.x == 0) atomicExch(a.slab_counter + s, 0);
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int i = i0 + b * kThreads;
+      if (i >= items) continue;
+      const int sl = s_last[i / (rows * 16)], rc = i % (rows * 16);
+      const int r = rc >> 4, col = 16 * sl + (rc & 15);
+      float v = hv[b];  // residual + sum_j w_j * expert_j (slot order) + shared
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+        if (jj < k) v += rs.w[r * k + jj] * pr[b][jj];
+      v += ps[b];
+      a.out[(size_t)r * H + col] = v;
     }
   }
+  for (int t = threadIdx.x; t < nlast; t += kThreads) atomicExch(a.slab_counter + s_last[t], 0);
 }
 
 // ------------------------------------------------------------------ launchers
-template <int NT>
-static cudaError_t launch_router_nt(const RouterArgs& a, int gy, cudaStream_t st) {
-  k_router<NT><<<dim3(a.n_slabs, gy), kThreads, a.sp.bytes, st>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_router(const RouterArgs& a, int gy, cudaStream_t st, bool pdl) {
+  const dim3 grid(a.w.n_slabs, gy);
+  if (a.sp.nt == 1) return launch_kernel(k_router<1>, grid, dim3(kThreads), a.sp.bytes, st, pdl, a);
+  return launch_kernel(k_router<2>, grid, dim3(kThreads), a.sp.bytes, st, pdl, a);
 }
 
-cudaError_t launch_router(const RouterArgs& a, int gy, cudaStream_t st) {
-  return a.sp.nt == 1 ? launch_router_nt<1>(a, gy, st) : launch_router_nt<2>(a, gy, st);
+#define UOCR_PAIRS(X, NT_) \
+  X(Q8_0, Q8_0, NT_) X(Q4_0, Q8_0, NT_) X(Q4_0, Q4_0, NT_) X(Q8_0, Q4_0, NT_) X(I8ASYM, I8ASYM, NT_)
+
+static dim3 expert_grid(const ExpertArgs& a) {
+  return dim3((a.ws.n_slabs > 0 ? a.cpes : 0) + a.n_units * a.cpe, a.tg);
 }
 
-template <int FR, int FS, int NT>
-static cudaError_t launch_gu(const ExpertArgs& a, int grid, cudaStream_t st) {
-  k_expert_gateup<FR, FS, NT><<<grid, kThreads, a.sp.bytes, st>>>(a);
-  return cudaGetLastError();
-}
-template <int FR, int FS, int NT>
-static cudaError_t launch_dn(const ExpertArgs& a, int grid, cudaStream_t st) {
-  k_expert_down<FR, FS, NT><<<grid, kThreads, a.sp.bytes, st>>>(a);
-  return cudaGetLastError();
-}
-
-#define UOCR_EXPERT_DISPATCH(FN)                                                           \
-  template <int NT>                                                                        \
-  static cudaError_t FN##_nt(int fr, int fs, const ExpertArgs& a, int grid, cudaStream_t st) { \
-    if (fr == Q8_0 && fs == Q8_0) return FN<Q8_0, Q8_0, NT>(a, grid, st);                  \
-    if (fr == Q4_0 && fs == Q8_0) return FN<Q4_0, Q8_0, NT>(a, grid, st);                  \
-    if (fr == Q4_0 && fs == Q4_0) return FN<Q4_0, Q4_0, NT>(a, grid, st);                  \
-    if (fr == Q8_0 && fs == Q4_0) return FN<Q8_0, Q4_0, NT>(a, grid, st);                  \
-    if (fr == I8ASYM && fs == I8ASYM) return FN<I8ASYM, I8ASYM, NT>(a, grid, st);          \
-    return cudaErrorInvalidValue;                                                          \
-  }
-UOCR_EXPERT_DISPATCH(launch_gu)
-UOCR_EXPERT_DISPATCH(launch_dn)
-#undef UOCR_EXPERT_DISPATCH
-
-cudaError_t launch_expert_gateup(int fr, int fs, const ExpertArgs& a, int grid, cudaStream_t st) {
-  return a.sp.nt == 1 ? launch_gu_nt<1>(fr, fs, a, grid, st) : launch_gu_nt<2>(fr, fs, a, grid, st);
-}
-cudaError_t launch_expert_down(int fr, int fs, const ExpertArgs& a, int grid, cudaStream_t st) {
-  return a.sp.nt == 1 ? launch_dn_nt<1>(fr, fs, a, grid, st) : launch_dn_nt<2>(fr, fs, a, grid, st);
+cudaError_t launch_expert_gateup(int fr, int fs, const ExpertArgs& a, cudaStream_t st, bool pdl) {
+  const dim3 grid = expert_grid(a);
+#define X(FR_, FS_, NT_)                                                                               \
+  if (fr == FR_ && fs == FS_ && a.sp.nt == NT_)                                                        \
+    return launch_kernel(k_expert_gateup<FR_, FS_, NT_>, grid, dim3(kThreads), a.sp.bytes, st, pdl, a);
+  UOCR_PAIRS(X, 1)
+  UOCR_PAIRS(X, 2)
+#undef X
+  return cudaErrorInvalidValue;
 }
 
-template <int FR, int FS, int NT>
-static cudaError_t set_expert_attr() {
-  const int mx = 200 * 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_expert_gateup<FR, FS, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_expert_down<FR, FS, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-  return e;
+cudaError_t launch_expert_down(int fr, int fs, const ExpertArgs& a, cudaStream_t st, bool pdl) {
+  const dim3 grid = expert_grid(a);
+#define X(FR_, FS_, NT_)                                                                             \
+  if (fr == FR_ && fs == FS_ && a.sp.nt == NT_)                                                      \
+    return launch_kernel(k_expert_down<FR_, FS_, NT_>, grid, dim3(kThreads), a.sp.bytes, st, pdl, a);
+  UOCR_PAIRS(X, 1)
+  UOCR_PAIRS(X, 2)
+#undef X
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t init_moe_attributes() {
-  const int mx = 200 * 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_router<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_router<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-#define UOCR_P(FR, FS)                                  \
-  if (e == cudaSuccess) e = set_expert_attr<FR, FS, 1>(); \
-  if (e == cudaSuccess) e = set_expert_attr<FR, FS, 2>();
-  UOCR_P(Q8_0, Q8_0)
-  UOCR_P(Q4_0, Q8_0)
-  UOCR_P(Q4_0, Q4_0)
-  UOCR_P(Q8_0, Q4_0)
-  UOCR_P(I8ASYM, I8ASYM)
-#undef UOCR_P
+  cudaError_t e = allow_max_dyn_smem(k_router<1>);
+  if (e == cudaSuccess) e = allow_max_dyn_smem(k_router<2>);
+#define X(FR_, FS_, NT_)                                                      \
+  if (e == cudaSuccess) e = allow_max_dyn_smem(k_expert_gateup<FR_, FS_, NT_>); \
+  if (e == cudaSuccess) e = allow_max_dyn_smem(k_expert_down<FR_, FS_, NT_>);
+  UOCR_PAIRS(X, 1)
+  UOCR_PAIRS(X, 2)
+#undef X
   return e;
 }
 

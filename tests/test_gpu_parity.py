@@ -98,3 +98,24 @@ def test_moe_q4_both_with_lm_head_rows_12(cuda):
     wl = synth.make_workload("moe_q4_lm", cfg, 12, 6, 107, prefix="prefill", n_prefill_embeds=3,
                              step_input="ids")
     _run(wl, 6)
+
+
+def _wide(**kw):
+    # hidden 2048: every projection needs several 16 KB stages per slab (Q8_0 QKV 2, Q4_0 expert
+    # gate/up 2, shared down 3, LM head 4) and the 78-slot cache spans two attention stages
+    base = dict(hidden=2048, n_heads=16, head_dim=128, n_layers=2, n_dense_layers=1, dense_inter=1024,
+                n_experts=8, top_k=2, n_shared=2, expert_inter=1024, vocab=2000, fmt_attn=Q8, fmt_dense=Q8,
+                fmt_shared=Q8, fmt_routed=Q4, prefix_len=70, ring_len=8, max_rows=3)
+    base.update(kw)
+    return synth.ModelConfig(**base)
+
+
+def test_multi_chunk_slabs_q4_routed_q8_shared(cuda):
+    wl = synth.make_workload("wide_q4r_q8s", _wide(), 3, 10, 108, step_input="ids")
+    st = _run(wl, 10)
+    assert st.id_checks >= 3 * 10
+
+
+def test_multi_chunk_slabs_q8_routed_q4_shared(cuda):
+    wl = synth.make_workload("wide_q8r_q4s", _wide(fmt_routed=Q8, fmt_shared=Q4, vocab=0), 3, 10, 109)
+    _run(wl, 10)
