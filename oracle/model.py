@@ -133,6 +133,32 @@ def route(logits, k):
     return idx.astype(np.int64), w
 
 
+def route_given(logits, idx):
+    """Renormalised softmax weights of a given selection idx[k]."""
+    logits = np.asarray(logits, dtype=np.float64)
+    p = np.exp(logits - logits.max())
+    p /= p.sum()
+    idx = np.asarray(idx, dtype=np.int64)
+    return idx, p[idx] / p[idx].sum()
+
+
+def is_topk_within(logits, idx, k, tol):
+    """True when idx holds k distinct experts and is a top-k of the logits up
+    to tol: no unselected logit exceeds a selected one by more than tol."""
+    logits = np.asarray(logits, dtype=np.float64)
+    sel = sorted({int(e) for e in idx})
+    if len(sel) != k or sel[0] < 0 or sel[-1] >= logits.size:
+        return False
+    rest = np.delete(logits, sel)
+    return rest.size == 0 or rest.max() <= logits[sel].min() + tol
+
+
+# Logit gap under which the top-k set is decided by rounding alone: the k-th
+# and (k+1)-th logits agree to within the accuracy a float32 router GEMV over
+# fp16 activations can promise, so either choice is a correct top-k.
+TIE_TOL = 1e-3
+
+
 def group_by_expert(idx, n_experts):
     """Histogram, exclusive scan and expert-grouped permutation of (row, slot).
 
@@ -199,6 +225,9 @@ class OracleModel:
         # for matrices whose values are exact in float32, see quant.float32_is_exact)
         self._cache = {} if cache else None
         self._cache_dtype = cache
+        # optional tie_choice(layer, row) -> idx[k] or None: consulted only where the
+        # top-k set is a near tie (gap <= TIE_TOL), and only a valid top-k is taken
+        self.tie_choice = None
         self.sinks = None if sinks is None else np.asarray(sinks, dtype=np.float64)
         nh, D, P, R, L = cfg.n_heads, cfg.head_dim, cfg.prefix_len, cfg.ring_len, cfg.n_layers
         self.P, self.R = P, R
@@ -327,10 +356,23 @@ class OracleModel:
         rows, k, E = self.rows, cfg.top_k, cfg.n_experts
         Wr = self.w(T_ROUTER, l)
         logits = Hn @ Wr.T
+        # the k-th vs (k+1)-th logit gap decides whether the selected set is well defined
+        srt = np.sort(logits, axis=-1)[:, ::-1]
+        gap = srt[:, k - 1] - srt[:, k] if k < E else np.full(rows, np.inf)
         idx = np.zeros((rows, k), dtype=np.int64)
         wts = np.zeros((rows, k))
+        tie_taken = np.zeros(rows, dtype=bool)
         for r in range(rows):
             idx[r], wts[r] = route(logits[r], k)
+            if self.tie_choice is not None and gap[r] <= TIE_TOL:
+                # a near tie: another selection is an equally correct top-k; follow the
+                # one the caller observed, provided it is one
+                alt = self.tie_choice(l, r)
+                if alt is not None:
+                    if not is_topk_within(logits[r], alt, k, TIE_TOL):
+                        raise ValueError(f"layer {l} row {r}: {list(alt)} is not a top-{k} within {TIE_TOL}")
+                    idx[r], wts[r] = route_given(logits[r], alt)
+                    tie_taken[r] = True
         Y = Hh.copy()
         for e in range(E):
             sel_r, sel_j = np.nonzero(idx == e)
@@ -344,8 +386,5 @@ class OracleModel:
             Y += swiglu_rows(Hn, self.w(T_SHARED_GATE, l, s), self.w(T_SHARED_UP, l, s),
                              self.w(T_SHARED_DOWN, l, s))
         count, offset, perm = group_by_expert(idx, E)
-        # the k-th vs (k+1)-th logit gap decides whether the selected set is well defined
-        srt = np.sort(logits, axis=-1)[:, ::-1]
-        gap = srt[:, k - 1] - srt[:, k] if k < E else np.full(rows, np.inf)
         return Y, dict(logits=logits, idx=idx, w=wts, count=count, offset=offset,
-                       perm=perm, gap=gap)
+                       perm=perm, gap=gap, tie_taken=tie_taken)
