@@ -228,8 +228,9 @@ def load_workload(ctx: Context, wl, chunk: int = 64):
     for i in range(0, len(ts), chunk):
         ctx.uocr_load_weights(ts[i:i + chunk])
     if wl.kv_prefix is not None:
-        for l, (k, v) in enumerate(wl.kv_prefix):
+        for l in range(wl.cfg.n_layers):
             for r in range(wl.rows):
-                ctx.uocr_kv_write_prefix(r, l, k[r], v[r], 0)
+                k, v = wl.kv_prefix.get(l, r)
+                ctx.uocr_kv_write_prefix(r, l, k, v, 0)
     if wl.sinks is not None:
         ctx.uocr_set_sinks(wl.sinks)

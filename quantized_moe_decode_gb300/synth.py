@@ -107,7 +107,8 @@ class Workload:
     seed: int
     tensors: list = field(default_factory=list)
     # cached prefix: kv_prefix[layer] = (k, v) with k, v fp16 [rows, heads, P, D]
-    kv_prefix: list | None = None
+    # (a KVPrefix: drawn lazily, per (layer, row))
+    kv_prefix: "KVPrefix | None" = None
     sinks: np.ndarray | None = None  # fp32 [layers, heads]
     # prefix built by running decode steps (prefill-by-decode):
     prefill_embeds: np.ndarray | None = None  # fp16 [rows, n_embed, H]
@@ -239,6 +240,63 @@ def _f16_normal(rng, shape) -> np.ndarray:
     return rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
 
 
+class KVPrefix:
+    """Cached prefix keys/values ~ N(0,1) fp16, drawn lazily per (layer, row).
+
+    A pool of 2**24 N(0,1) fp16 samples is drawn once from the workload seed;
+    the keys (values) of one (layer, row) are the window of nh*P*D consecutive
+    pool samples (cyclically) starting at an offset drawn from a generator
+    seeded by (seed, layer, row, 0 or 1).  A (layer, row) therefore never
+    depends on how many rows the workload has, one row can be drawn without the
+    others, and the gigabytes of cache that long prefixes at many rows need
+    cost a copy instead of a fresh draw.
+    """
+
+    POOL = 1 << 24
+
+    def __init__(self, seed: int, n_layers: int, rows: int, nh: int, P: int, D: int):
+        self.seed, self.n_layers, self.rows = seed, n_layers, rows
+        self.shape = (nh, P, D)
+        self._pool = None
+
+    def _window(self, layer: int, row: int, which: int) -> np.ndarray:
+        if self._pool is None:
+            rng = np.random.default_rng([self.seed, 0x4B56])
+            self._pool = _f16_normal(rng, (self.POOL,))
+        n = int(np.prod(self.shape))
+        start = int(np.random.default_rng([self.seed, layer, row, which]).integers(0, self.POOL))
+        idx_end = start + n
+        if idx_end <= self.POOL:
+            flat = self._pool[start:idx_end].copy()
+        else:  # wrap around the pool (as often as needed)
+            reps = (idx_end + self.POOL - 1) // self.POOL
+            flat = np.concatenate([self._pool[start:]] + [self._pool] * (reps - 2) +
+                                  [self._pool[:idx_end - (reps - 1) * self.POOL]])
+        return flat.reshape(self.shape)
+
+    def get(self, layer: int, row: int):
+        """(k, v) fp16 [nh, P, D] of one row of one layer."""
+        return self._window(layer, row, 0), self._window(layer, row, 1)
+
+    def subset(self, rows) -> list:
+        """Per layer (k, v) fp16 [len(rows), nh, P, D] for the given rows."""
+        out = []
+        for l in range(self.n_layers):
+            kv = [self.get(l, r) for r in rows]
+            out.append((np.stack([a for a, _ in kv]), np.stack([b for _, b in kv])))
+        return out
+
+    def __len__(self) -> int:
+        return self.n_layers
+
+    def __getitem__(self, layer: int):
+        kv = [self.get(layer, r) for r in range(self.rows)]
+        return np.stack([a for a, _ in kv]), np.stack([b for _, b in kv])
+
+    def __iter__(self):
+        return (self[l] for l in range(self.n_layers))
+
+
 def make_workload(name: str, cfg: ModelConfig, rows: int, steps: int, seed: int, *,
                   prefix: str = "cached", n_prefill_embeds: int = 0,
                   step_input: str = "x") -> Workload:
@@ -257,11 +315,7 @@ def make_workload(name: str, cfg: ModelConfig, rows: int, steps: int, seed: int,
     wl.tensors = make_weights(cfg, rng)
     P, nh, D, H = cfg.prefix_len, cfg.n_heads, cfg.head_dim, cfg.hidden
     if prefix == "cached":
-        wl.kv_prefix = []
-        for _ in range(cfg.n_layers):
-            k = _f16_normal(rng, (rows, nh, P, D))
-            v = _f16_normal(rng, (rows, nh, P, D))
-            wl.kv_prefix.append((k, v))
+        wl.kv_prefix = KVPrefix(seed, cfg.n_layers, rows, nh, P, D)
     elif prefix == "prefill":
         assert 0 <= n_prefill_embeds <= P
         wl.prefill_embeds = _f16_normal(rng, (rows, n_prefill_embeds, H))

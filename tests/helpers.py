@@ -15,5 +15,5 @@ def make_ctx(wl, **kw):
 
 def make_oracle(wl, rows=None, cache="float64"):
     rows = list(range(wl.rows)) if rows is None else list(rows)
-    kv = None if wl.kv_prefix is None else [(k[rows], v[rows]) for k, v in wl.kv_prefix]
+    kv = None if wl.kv_prefix is None else wl.kv_prefix.subset(rows)
     return oracle.OracleModel(wl.cfg, wl.tensors, len(rows), kv_prefix=kv, sinks=wl.sinks, cache=cache)

@@ -145,6 +145,8 @@ def compare_step(ctx, cfg, res, lib_rows, stats, hist_bad, row_map=None, check_k
                 want = sorted(int(e) for e in info["idx"][i])
                 got = sorted(int(e) for e in gr["idx"][r])
                 stats.router_checks += 1
+                if info.get("tie_taken") is not None and info["tie_taken"][i]:
+                    stats.router_near_ties += 1  # the oracle took the library's set (a valid top-k)
                 if want != got:
                     router_all_equal = False
                     assert info["gap"][i] <= ROUTER_GAP, \
@@ -180,6 +182,17 @@ def compare_step(ctx, cfg, res, lib_rows, stats, hist_bad, row_map=None, check_k
     return in_bad
 
 
+def _tie_choice(ctx, lib_rows, row_map):
+    """The library's top-k set of oracle row i at layer l (read once per layer)."""
+    cache = {}
+
+    def choice(layer, i):
+        if layer not in cache:
+            cache[layer] = ctx.uocr_debug_router(layer, lib_rows)["idx"]
+        return cache[layer][row_map[i]]
+    return choice
+
+
 def run_parity(ctx, wl, steps, oracle_model, rows=None, row_map=None, check_kv=True, log=None):
     """Run `steps` decode steps (plus the prefill-by-decode prefix when the
     workload has one) on both sides and compare.  Returns Stats."""
@@ -209,13 +222,19 @@ def run_parity(ctx, wl, steps, oracle_model, rows=None, row_map=None, check_kv=T
         opos = np.full(n_or, p, np.int32)
         is_last_prefill = wl.prefill_embeds is not None and p == cfg.prefix_len - 1
         want_lm = cfg.vocab > 0 and (kind == "greedy" or is_last_prefill)
+        # the library steps first, so that at a near tie of the router the oracle can
+        # follow the library's (equally correct) top-k set
         if kind == "x":
-            res = oracle_model.step(opos, x=data[row_map], want_logits=want_lm)
             g = runner.step(gpos, x=data[:runner.rows], want_logits=want_lm)
         else:
             ids = data if kind == "ids" else last_ids
-            res = oracle_model.step(opos, ids=ids[row_map], want_logits=want_lm)
             g = runner.step(gpos, ids=ids[:runner.rows], want_logits=want_lm)
+        oracle_model.tie_choice = _tie_choice(ctx, runner.rows, row_map)
+        if kind == "x":
+            res = oracle_model.step(opos, x=data[row_map], want_logits=want_lm)
+        else:
+            res = oracle_model.step(opos, ids=ids[row_map], want_logits=want_lm)
+        oracle_model.tie_choice = None
         in_bad = compare_step(ctx, cfg, res, runner.rows, stats, hist_bad, row_map=row_map, check_kv=check_kv)
         clean = [i for i in range(n_or) if in_bad[i] >= 10 ** 9]
         if "y" in g and clean:
@@ -239,6 +258,7 @@ def run_parity(ctx, wl, steps, oracle_model, rows=None, row_map=None, check_kv=T
                 nxt[r] = res.next_ids[i]
             last_ids = nxt
         stats.steps += 1
+        stats.last_ids = last_ids  # the ids the next greedy step takes
         if log and (si % 50 == 0):
             log(f"step {si}/{len(plan)} worst rel {stats.worst_rel:.2e}")
     return stats
