@@ -1,6 +1,8 @@
 """A second, independent statement of the decode step in scalar Python.
 
-Used only to pin the oracle on tiny shapes.  It parses the weight blocks with
+Used only to pin the oracle on tiny shapes.  Activations are rounded to fp16
+where the method stores them (normalised matmul inputs, cached keys and
+values, attention output, SwiGLU activations).  It parses the weight blocks with
 ``struct`` byte by byte, keeps the KV history as a dict keyed by absolute
 position (no slots, no ring arithmetic), applies the ring rule as a mask on
 absolute positions, and spells every sum as a loop.  It shares nothing with
@@ -51,6 +53,11 @@ def decode_rows(t):
     return out
 
 
+def h16(v):
+    """Round a Python float to fp16 (nearest even) through struct's half format."""
+    return struct.unpack("<e", struct.pack("<e", v))[0]
+
+
 def matvec(W, x):
     return [sum(W[n][k] * x[k] for k in range(len(x))) for n in range(len(W))]
 
@@ -77,7 +84,7 @@ def mlp(x, g, u, d):
     a = [0.0] * len(g)
     gx, ux = matvec(g, x), matvec(u, x)
     for i in range(len(g)):
-        a[i] = gx[i] / (1.0 + math.exp(-gx[i])) * ux[i]
+        a[i] = h16(gx[i] / (1.0 + math.exp(-gx[i])) * ux[i])  # activations stored in fp16
     return matvec(d, a)
 
 
@@ -107,13 +114,13 @@ class BruteModel:
         nh, D, P, R = cfg.n_heads, cfg.head_dim, cfg.prefix_len, cfg.ring_len
         layers_out = []
         for l in range(cfg.n_layers):
-            xn = norm(x, self.vec(3, l), cfg.rms_eps)
+            xn = [h16(a) for a in norm(x, self.vec(3, l), cfg.rms_eps)]
             q = matvec(self.mat(4, l), xn)
             k = matvec(self.mat(5, l), xn)
             v = matvec(self.mat(6, l), xn)
             qh = [rot(q[h * D:(h + 1) * D], p, cfg.rope_theta) for h in range(nh)]
-            kh = [rot(k[h * D:(h + 1) * D], p, cfg.rope_theta) for h in range(nh)]
-            vh = [v[h * D:(h + 1) * D] for h in range(nh)]
+            kh = [[h16(a) for a in rot(k[h * D:(h + 1) * D], p, cfg.rope_theta)] for h in range(nh)]
+            vh = [[h16(a) for a in v[h * D:(h + 1) * D]] for h in range(nh)]
             self.hist[r][l][p] = (kh, vh)
             keep = [pp for pp in sorted(self.hist[r][l]) if pp <= p and (pp < P or pp > p - R)]
             att = []
@@ -127,10 +134,10 @@ class BruteModel:
                 m = max(logits)
                 e = [math.exp(a - m) for a in logits]
                 z = sum(e)
-                att += [sum(e[j] * vals[j][i] for j in range(len(e))) / z for i in range(D)]
+                att += [h16(sum(e[j] * vals[j][i] for j in range(len(e))) / z) for i in range(D)]
             o = matvec(self.mat(7, l), att)
             hh = [x[i] + o[i] for i in range(len(x))]
-            hn = norm(hh, self.vec(8, l), cfg.rms_eps)
+            hn = [h16(a) for a in norm(hh, self.vec(8, l), cfg.rms_eps)]
             if l < cfg.n_dense_layers or cfg.n_experts == 0:
                 m = mlp(hn, self.mat(9, l), self.mat(10, l), self.mat(11, l))
                 y = [hh[i] + m[i] for i in range(len(hh))]
@@ -164,7 +171,7 @@ class BruteModel:
             x = y
         logits = None
         if cfg.vocab:
-            xn = norm(x, self.vec(1), cfg.rms_eps)
+            xn = [h16(a) for a in norm(x, self.vec(1), cfg.rms_eps)]
             logits = matvec(self.mat(2), xn)
         return layers_out, logits
 

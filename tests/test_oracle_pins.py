@@ -233,13 +233,19 @@ def test_top_all_experts_equals_dense_softmax_mixture():
     m = oracle.OracleModel(cfg, wl.tensors, 2, kv_prefix=wl.kv_prefix)
     res = m.step(wl.positions(0), x=wl.step_x[0])
     Hh = res.h_attn[0]
-    Hn = om.rmsnorm(Hh, m.w(om.T_MLP_NORM, 0), cfg.rms_eps)
+    # the method stores the normalised input and the SwiGLU activations in fp16
+    Hn = om.rmsnorm(Hh, m.w(om.T_MLP_NORM, 0), cfg.rms_eps).astype(np.float16).astype(np.float64)
+
+    def expert(x, e):
+        g, u = m.w(om.T_EXPERT_GATE, 0, e) @ x, m.w(om.T_EXPERT_UP, 0, e) @ x
+        a = (g / (1 + np.exp(-g)) * u).astype(np.float16).astype(np.float64)
+        return m.w(om.T_EXPERT_DOWN, 0, e) @ a
+
     for r in range(2):
         lg = m.w(om.T_ROUTER, 0) @ Hn[r]
         p = np.exp(lg - lg.max())
         p /= p.sum()
-        mix = sum(p[e] * om.swiglu(Hn[r], m.w(om.T_EXPERT_GATE, 0, e), m.w(om.T_EXPERT_UP, 0, e),
-                                   m.w(om.T_EXPERT_DOWN, 0, e)) for e in range(4))
+        mix = sum(p[e] * expert(Hn[r], e) for e in range(4))
         assert np.allclose(res.hidden[1][r], Hh[r] + mix, atol=1e-12)
 
 
@@ -252,6 +258,17 @@ def test_two_shared_experts_equal_one_concatenated_expert():
     two = om.swiglu(x, g[0], u[0], d[0]) + om.swiglu(x, g[1], u[1], d[1])
     one = om.swiglu(x, np.vstack(g), np.vstack(u), np.hstack(d))
     assert np.allclose(two, one, atol=1e-12)
+
+
+def test_fp16_storage_rounds_to_nearest_even():
+    u = 2.0 ** -10  # fp16 spacing at 1
+    assert om.f16(1 + u / 2) == 1.0                  # tie -> even mantissa
+    assert om.f16(1 + 3 * u / 2) == 1 + 2 * u        # tie -> even mantissa (up)
+    assert om.f16(1 + 0.51 * u) == 1 + u
+    assert om.f16(65504.0) == 65504.0 and np.isinf(om.f16(65520.0))
+    assert om.f16(-2.0 ** -24) == -2.0 ** -24        # smallest subnormal survives
+    x = np.random.default_rng(13).standard_normal(1000)
+    assert np.all(np.abs(om.f16(x) - x) <= np.abs(x) * 2.0 ** -11 + 2.0 ** -25)
 
 
 def test_argmax_first_maximum():
