@@ -245,6 +245,10 @@ UOCR_API uocr_status uocr_memory_report(uocr_ctx* ctx, uocr_mem_report* out);
 UOCR_API uocr_status uocr_debug_hidden(uocr_ctx* ctx, int32_t tap, int32_t rows, float* out);
 UOCR_API uocr_status uocr_debug_router(uocr_ctx* ctx, int32_t layer, int32_t rows, int32_t* idx,
                               float* w, int32_t* count, int32_t* offset, int32_t* perm);
+/* The fp32 router logits [rows][E] of MoE layer `layer` from the last step
+ * (the values the top-k was taken on).  Host output buffer; E_INVALID_ARG for
+ * a dense layer or bad rows. */
+UOCR_API uocr_status uocr_debug_router_logits(uocr_ctx* ctx, int32_t layer, int32_t rows, float* logits);
 
 /* Per-kernel-class device time (ms) of one un-graphed step with the given
  * rows and input kind (0 = token ids, 1 = hidden vectors), measured with CUDA

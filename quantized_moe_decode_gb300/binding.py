@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "OK", 1: "E_INVALID_ARG", 2: "E_OOM", 3: "E_BUDGET", 4: "E_FO
 EXPORTED = ["uocr_create", "uocr_destroy", "uocr_load_weights", "uocr_kv_write_prefix", "uocr_kv_read",
             "uocr_set_sinks", "uocr_decode_step", "uocr_decode_step_embeds", "uocr_decode_step_host",
             "uocr_generate", "uocr_kv_reset", "uocr_sync", "uocr_last_error", "uocr_memory_report",
-            "uocr_debug_hidden", "uocr_debug_router", "uocr_profile", "uocr_lm_head_argmax_noalloc"]
+            "uocr_debug_hidden", "uocr_debug_router", "uocr_debug_router_logits", "uocr_profile",
+            "uocr_lm_head_argmax_noalloc"]
 
 
 class uocr_config(C.Structure):
@@ -74,6 +75,7 @@ def load(path: str = LIB_PATH):
         "uocr_memory_report": ([P, C.POINTER(uocr_mem_report)], I),
         "uocr_debug_hidden": ([P, I, I, P], I),
         "uocr_debug_router": ([P, I, I, P, P, P, P, P], I),
+        "uocr_debug_router_logits": ([P, I, I, P], I),
         "uocr_profile": ([P, I, I, P, P, P, C.POINTER(C.c_char_p), C.POINTER(C.c_float), C.POINTER(I)], I),
         "uocr_lm_head_argmax_noalloc": ([P, I, P, P, P, P], I),
     }
@@ -212,6 +214,11 @@ class Context:
         self._ck(self.lib.uocr_debug_router(self.h, layer, rows, idx.ctypes.data, w.ctypes.data,
                                             count.ctypes.data, offset.ctypes.data, perm.ctypes.data))
         return dict(idx=idx, w=w, count=count, offset=offset, perm=perm)
+
+    def uocr_debug_router_logits(self, layer, rows):
+        out = np.empty((rows, self.cfg.n_experts), np.float32)
+        self._ck(self.lib.uocr_debug_router_logits(self.h, layer, rows, out.ctypes.data))
+        return out
 
     def uocr_profile(self, rows, input_kind, ids_ptr, x_ptr, pos_ptr, cap=32):
         names = (C.c_char_p * cap)()

@@ -1207,6 +1207,18 @@ uocr_status uocr_debug_router(uocr_ctx* ctx, int32_t layer, int32_t rows, int32_
   return UOCR_OK;
 }
 
+uocr_status uocr_debug_router_logits(uocr_ctx* ctx, int32_t layer, int32_t rows, float* logits) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  const uocr_config& c = ctx->cfg;
+  if (layer < 0 || layer >= c.n_layers || ctx->layer_dense(layer) || rows < 1 || rows > c.max_rows || !logits)
+    return ctx->fail(UOCR_E_INVALID_ARG, "debug_router_logits: not a MoE layer, bad rows or NULL output");
+  CK(cudaStreamSynchronize(ctx->st), "sync");
+  const size_t MR = ctx->MR(), E = c.n_experts;
+  CK(cudaMemcpy(logits, ctx->r_logits + layer * MR * E, rows * E * 4, cudaMemcpyDeviceToHost), "router read");
+  return UOCR_OK;
+}
+
 uocr_status uocr_profile(uocr_ctx* ctx, int32_t rows, int32_t input_kind, const int32_t* token_ids,
                          const uint16_t* x, const int32_t* positions, const char** names, float* ms,
                          int32_t* n_inout) {

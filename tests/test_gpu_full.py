@@ -42,7 +42,7 @@ def _cache():
 def _report(name, st):
     print(f"\n{name}: {st.steps} steps, {st.float_checks} float checks (worst rel-L2 {st.worst_rel:.2e}, "
           f"max-abs {st.worst_abs:.2e}), router {st.router_checks} ({st.router_near_ties} near ties), "
-          f"ids {st.id_checks} ({st.id_near_ties} near ties), kv {st.kv_checks}")
+          f"ids {st.id_checks} ({st.id_near_ties} near ties), kv {st.kv_checks}; worst: {st.worst_name}")
 
 
 def test_dense_layer_b1_full(cuda):
@@ -88,7 +88,7 @@ def test_full_b8_prefill_then_generate_sampled_rows(cuda):
     ctx.uocr_generate(wl.rows, ids.data_ptr(), pos.data_ptr(), n_gen, out.data_ptr())
     ctx.uocr_sync()
     hist = out.cpu().numpy()
-    assert (pos.cpu().numpy() == p0 + n_gen).all()
+    assert (pos.cpu().numpy() == p0).all()  # the caller's inputs are not modified
     checked = ties = 0
     prev = ids0
     for s in range(n_gen):
@@ -101,9 +101,10 @@ def test_full_b8_prefill_then_generate_sampled_rows(cuda):
                 ties += 1
         prev = hist[s]
     # the hidden taps hold the last generated step
-    for tap in (2 * cfg.n_layers - 2, 2 * cfg.n_layers - 1):
-        got = ctx.uocr_debug_hidden(tap, wl.rows)[sample]
-        check_close(f"generate tap {tap}", got, res.hidden[tap + 1])
+    L = cfg.n_layers
+    check_close("generate: last layer after attention", ctx.uocr_debug_hidden(2 * L - 2, wl.rows)[sample],
+                res.h_attn[L - 1])
+    check_close("generate: last layer output", ctx.uocr_debug_hidden(2 * L - 1, wl.rows)[sample], res.hidden[L])
     print(f"generate: {n_gen} steps, {checked} ids checked, {ties} near ties")
     assert checked >= n_gen
     ctx.close()

@@ -265,7 +265,8 @@ def test_fp16_storage_rounds_to_nearest_even():
     assert om.f16(1 + u / 2) == 1.0                  # tie -> even mantissa
     assert om.f16(1 + 3 * u / 2) == 1 + 2 * u        # tie -> even mantissa (up)
     assert om.f16(1 + 0.51 * u) == 1 + u
-    assert om.f16(65504.0) == 65504.0 and np.isinf(om.f16(65520.0))
+    with np.errstate(over="ignore"):
+        assert om.f16(65504.0) == 65504.0 and np.isinf(om.f16(65520.0))
     assert om.f16(-2.0 ** -24) == -2.0 ** -24        # smallest subnormal survives
     x = np.random.default_rng(13).standard_normal(1000)
     assert np.all(np.abs(om.f16(x) - x) <= np.abs(x) * 2.0 ** -11 + 2.0 ** -25)
