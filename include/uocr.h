@@ -182,6 +182,13 @@ UOCR_API uocr_status uocr_kv_write_prefix(uocr_ctx* ctx, int32_t row, int32_t la
 UOCR_API uocr_status uocr_kv_read(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0,
                          int32_t n, uint16_t* k, uint16_t* v);
 
+/* Write cache slots [slot0, slot0+n) of one row and layer (prefix or ring)
+ * from host fp16 [n_heads][n][head_dim] buffers: the cache is caller-visible
+ * state the step reads and writes in place (Falcon-OCR INT8 OpenVINO IR model
+ * card, intro).  Requires slot0+n <= prefix_len+ring_len.  Synchronous.       */
+UOCR_API uocr_status uocr_kv_write(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0,
+                          int32_t n, const uint16_t* k, const uint16_t* v);
+
 /* Per-layer, per-head sink logits, host fp32 [n_layers][n_heads]; they enter
  * the softmax unscaled as one more key with value zero.  Synchronous.        */
 UOCR_API uocr_status uocr_set_sinks(uocr_ctx* ctx, const float* sinks);

@@ -146,31 +146,11 @@ def route(logits, k):
     return idx.astype(np.int64), w
 
 
-def route_given(logits, idx):
-    """Renormalised softmax weights of a given selection idx[k]."""
-    logits = np.asarray(logits, dtype=np.float64)
-    p = np.exp(logits - logits.max())
-    p /= p.sum()
-    idx = np.asarray(idx, dtype=np.int64)
-    return idx, p[idx] / p[idx].sum()
-
-
-def is_topk_within(logits, idx, k, tol):
-    """True when idx holds k distinct experts and is a top-k of the logits up
-    to tol: no unselected logit exceeds a selected one by more than tol."""
-    logits = np.asarray(logits, dtype=np.float64)
-    sel = sorted({int(e) for e in idx})
-    if len(sel) != k or sel[0] < 0 or sel[-1] >= logits.size:
-        return False
-    rest = np.delete(logits, sel)
-    return rest.size == 0 or rest.max() <= logits[sel].min() + tol
-
-
 # Logit gap under which the top-k set is not decided by the definition alone:
 # a decode step that meets the float tolerance (hidden states to rel-L2 2e-3
 # after several layers of fp16 activations) moves router logits by up to about
-# this much, so two sets whose k-th and (k+1)-th logits are closer are both
-# correct top-k sets.  It is the margin that also gates greedy token ids.
+# this much, so where the k-th and (k+1)-th logits are closer, another set is
+# an equally correct top-k.  It is the margin that also gates greedy token ids.
 TIE_TOL = 1e-2
 
 
@@ -240,9 +220,6 @@ class OracleModel:
         # for matrices whose values are exact in float32, see quant.float32_is_exact)
         self._cache = {} if cache else None
         self._cache_dtype = cache
-        # optional tie_choice(layer, row) -> idx[k] or None: consulted only where the
-        # top-k set is a near tie (gap <= TIE_TOL), and only a valid top-k is taken
-        self.tie_choice = None
         self.sinks = None if sinks is None else np.asarray(sinks, dtype=np.float64)
         nh, D, P, R, L = cfg.n_heads, cfg.head_dim, cfg.prefix_len, cfg.ring_len, cfg.n_layers
         self.P, self.R = P, R
@@ -376,18 +353,8 @@ class OracleModel:
         gap = srt[:, k - 1] - srt[:, k] if k < E else np.full(rows, np.inf)
         idx = np.zeros((rows, k), dtype=np.int64)
         wts = np.zeros((rows, k))
-        tie_taken = np.zeros(rows, dtype=bool)
         for r in range(rows):
             idx[r], wts[r] = route(logits[r], k)
-            if self.tie_choice is not None and gap[r] <= TIE_TOL:
-                # a near tie: another selection is an equally correct top-k; follow the
-                # one the caller observed, provided it is one
-                alt = self.tie_choice(l, r)
-                if alt is not None:
-                    if not is_topk_within(logits[r], alt, k, TIE_TOL):
-                        raise ValueError(f"layer {l} row {r}: {list(alt)} is not a top-{k} within {TIE_TOL}")
-                    idx[r], wts[r] = route_given(logits[r], alt)
-                    tie_taken[r] = True
         Y = Hh.copy()
         for e in range(E):
             sel_r, sel_j = np.nonzero(idx == e)
@@ -402,4 +369,4 @@ class OracleModel:
                              self.w(T_SHARED_DOWN, l, s), act_fp16=True)
         count, offset, perm = group_by_expert(idx, E)
         return Y, dict(logits=logits, idx=idx, w=wts, count=count, offset=offset,
-                       perm=perm, gap=gap, tie_taken=tie_taken)
+                       perm=perm, gap=gap)

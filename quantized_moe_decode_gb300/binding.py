@@ -21,7 +21,8 @@ UOCR_E_STATE, UOCR_E_CUDA, UOCR_E_POSITION, UOCR_E_TOKEN = 5, 6, 7, 8
 STATUS_NAMES = {0: "OK", 1: "E_INVALID_ARG", 2: "E_OOM", 3: "E_BUDGET", 4: "E_FORMAT", 5: "E_STATE",
                 6: "E_CUDA", 7: "E_POSITION", 8: "E_TOKEN"}
 
-EXPORTED = ["uocr_create", "uocr_destroy", "uocr_load_weights", "uocr_kv_write_prefix", "uocr_kv_read",
+EXPORTED = ["uocr_create", "uocr_destroy", "uocr_load_weights", "uocr_kv_write_prefix", "uocr_kv_write",
+            "uocr_kv_read",
             "uocr_set_sinks", "uocr_decode_step", "uocr_decode_step_embeds", "uocr_decode_step_host",
             "uocr_generate", "uocr_kv_reset", "uocr_sync", "uocr_last_error", "uocr_memory_report",
             "uocr_debug_hidden", "uocr_debug_router", "uocr_debug_router_logits", "uocr_profile",
@@ -64,6 +65,7 @@ def load(path: str = LIB_PATH):
         "uocr_load_weights": ([P, C.POINTER(uocr_tensor), C.c_size_t], I),
         "uocr_kv_write_prefix": ([P, I, I, P, P, I, I], I),
         "uocr_kv_read": ([P, I, I, I, I, P, P], I),
+        "uocr_kv_write": ([P, I, I, I, I, P, P], I),
         "uocr_set_sinks": ([P, P], I),
         "uocr_decode_step": ([P, I, P, P, P, P], I),
         "uocr_decode_step_embeds": ([P, I, P, P, P, P, P], I),
@@ -154,6 +156,12 @@ class Context:
         v = np.ascontiguousarray(v, dtype=np.float16)
         self._ck(self.lib.uocr_kv_write_prefix(self.h, row, layer, k.ctypes.data, v.ctypes.data, start,
                                                k.shape[1]))
+
+    def uocr_kv_write(self, row, layer, slot0, k, v):
+        """k, v: fp16 [n_heads][n][head_dim] written to slots [slot0, slot0+n)."""
+        k = np.ascontiguousarray(k, dtype=np.float16)
+        v = np.ascontiguousarray(v, dtype=np.float16)
+        self._ck(self.lib.uocr_kv_write(self.h, row, layer, slot0, k.shape[1], k.ctypes.data, v.ctypes.data))
 
     def uocr_kv_read(self, row, layer, slot0, n):
         nh, D = self.cfg.n_heads, self.cfg.head_dim

@@ -999,6 +999,27 @@ uocr_status uocr_kv_write_prefix(uocr_ctx* ctx, int32_t row, int32_t layer, cons
   return UOCR_OK;
 }
 
+uocr_status uocr_kv_write(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0, int32_t n, const uint16_t* k,
+                          const uint16_t* v) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  const uocr_config& c = ctx->cfg;
+  if (!k || !v || row < 0 || row >= c.max_rows || layer < 0 || layer >= c.n_layers || slot0 < 0 || n < 0 ||
+      slot0 + n > ctx->SL)
+    return ctx->fail(UOCR_E_INVALID_ARG, "kv_write: bad row/layer/slot range");
+  const size_t D = c.head_dim;
+  for (int kv = 0; kv < 2; ++kv) {
+    const uint16_t* src = kv ? v : k;
+    for (int h = 0; h < c.n_heads; ++h) {
+      __half* dst = ctx->kv + ctx->kv_layer * layer + ((((size_t)row * 2 + kv) * c.n_heads + h) * ctx->SL + slot0) * D;
+      CK(cudaMemcpyAsync(dst, src + (size_t)h * n * D, (size_t)n * D * 2, cudaMemcpyHostToDevice, ctx->st),
+         "kv copy");
+    }
+  }
+  CK(cudaStreamSynchronize(ctx->st), "kv copy");
+  return UOCR_OK;
+}
+
 uocr_status uocr_kv_read(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0, int32_t n, uint16_t* k,
                          uint16_t* v) {
   if (!ctx) return UOCR_E_INVALID_ARG;

@@ -1,21 +1,28 @@
 """Free-running parity of the CUDA library (through the C ABI) against the oracle.
 
-Both sides consume the same seeded workload.  For token-id workloads the
-library is fed the oracle's greedy ids (teacher forcing by the oracle), so a
-near-tie argmax cannot make the two inputs diverge.
+Both sides consume the same seeded workload; nothing the library computes is
+ever an input of the oracle.  For token-id workloads the library is fed the
+oracle's greedy ids (teacher forcing by the oracle), so a near-tie argmax
+cannot make the two inputs diverge.
 
 Comparison rules (the decode-step statement's tolerances):
-* every floating-point output: relative L2 error <= 2e-3 and max abs error
-  <= 2e-2 against the float64 oracle;
-* integer outputs bit-exact: the router's top-k set where the oracle's k-th vs
-  (k+1)-th logit gap exceeds 1e-3, argmax ids where the oracle's top-2 margin
-  exceeds 1e-2, the counts / offsets / permutation of the grouping (equal to
-  the oracle's when every row's set matches, else checked to be the stable
-  grouping of the library's own top-k);
+* every floating-point output (hidden state after attention and after each
+  layer, the K and V written to the cache, LM logits): relative L2 error
+  <= 2e-3 and max abs error <= 2e-2 against the oracle;
+* integer outputs bit-exact: the router's top-k set where the oracle's k-th
+  vs (k+1)-th logit gap exceeds 1e-2, argmax ids where the oracle's top-2
+  margin exceeds 1e-2, the counts / offsets / permutation of the grouping
+  (equal to the oracle's when every row's set matches, else checked to be
+  the stable grouping of the library's own top-k); the library's set is
+  always exactly the top-k of its own fp32 logits;
+* router logits and routing weights are intermediates: logits within half
+  the 1e-2 gate (which makes the gated set comparison sound), weights to
+  rel-L2 1e-2; the layer output they feed keeps the full tolerance;
 * a router set that differs at a near tie is counted, not failed; it changes
-  that row's layer output, so the row's later layers at that step and the
-  KV history of the layers above are excluded from the comparison from then
-  on (lockstep cannot be used: no oracle input comes from the library).
+  that row's layer output, so the rest of the row's layers at that step are
+  not compared, and before the next step the library's cache entries of the
+  layers above are overwritten with the oracle's (the library takes the
+  oracle's state; the oracle never takes the library's).
 """
 from __future__ import annotations
 
@@ -111,14 +118,14 @@ class GpuRunner:
         return out
 
 
-def compare_step(ctx, cfg, res, lib_rows, stats, hist_bad, row_map=None, check_kv=True):
+def compare_step(ctx, cfg, res, lib_rows, stats, row_map=None, check_kv=True):
     """Compare one step.  res: oracle StepResult over the oracle's rows;
-    row_map[i] = library row of oracle row i.  hist_bad[i]: first layer whose
-    KV history is tainted for oracle row i (mutated)."""
+    row_map[i] = library row of oracle row i.  Returns, per oracle row, the
+    layer whose MoE output diverged at a router near tie (cfg.n_layers if none)."""
     n = res.hidden.shape[1]
     row_map = list(range(n)) if row_map is None else row_map
     L = cfg.n_layers
-    in_bad = list(hist_bad)
+    div = [L] * n
     taps = {}
 
     def tap(t):
@@ -128,7 +135,7 @@ def compare_step(ctx, cfg, res, lib_rows, stats, hist_bad, row_map=None, check_k
 
     router_all_equal = True
     for l in range(L):
-        keep = [i for i in range(n) if l < in_bad[i]]
+        keep = [i for i in range(n) if div[i] >= L]
         if not keep:
             break
         g = tap(2 * l)[[row_map[i] for i in keep]]
@@ -156,17 +163,9 @@ def compare_step(ctx, cfg, res, lib_rows, stats, hist_bad, row_map=None, check_k
                 # logits, lowest index first among equal logits
                 own = sorted(int(e) for e in np.argsort(-glog[r], kind="stable")[:cfg.top_k])
                 assert got == own, f"layer {l} row {r}: router set {got} is not the top-k {own} of its logits"
-                # logits within half the gate of the oracle's make the gap-gated set
-                # comparison below sound (a set can only differ where the gap is < 2*err)
-                # Router logits and weights are intermediates of the step: the layer
-                # output they feed is held to the full tolerance below.  Logits within
-                # half the gate of the oracle's make the gap-gated set comparison sound
-                # (a set can only differ where the gap is < 2*err).
                 err = float(np.max(np.abs(glog[r].astype(np.float64) - info["logits"][i])))
                 assert err <= ROUTER_GAP / 2, f"layer {l} row {r}: router logits differ by {err:.3e}"
                 stats.router_checks += 1
-                if info.get("tie_taken") is not None and info["tie_taken"][i]:
-                    stats.router_near_ties += 1  # the oracle took the library's set (a valid top-k)
                 if want != got:
                     router_all_equal = False
                     assert info["gap"][i] <= ROUTER_GAP, \
@@ -174,13 +173,10 @@ def compare_step(ctx, cfg, res, lib_rows, stats, hist_bad, row_map=None, check_k
                     stats.router_near_ties += 1
                     stats.tainted_rows.add(r)
                     out_ok.remove(i)
-                    in_bad[i] = l + 1
-                    hist_bad[i] = min(hist_bad[i], l + 1)
+                    div[i] = l
                     continue
                 wmap = {int(e): float(w) for e, w in zip(gr["idx"][r], gr["w"][r])}
                 got_w = np.array([wmap[int(e)] for e in info["idx"][i]])
-                # renormalised over k logits, the weights carry the logits' absolute
-                # error (~2e-3 after a dozen fp16-activation layers) as a relative one
                 stats.note(*check_close(f"layer {l} row {r} routing weights", got_w, info["w"][i],
                                         rel=WEIGHTS_REL))
             # grouping: unique given the top-k sets
@@ -202,18 +198,18 @@ def compare_step(ctx, cfg, res, lib_rows, stats, hist_bad, row_map=None, check_k
         if out_ok:
             g = tap(2 * l + 1)[[row_map[i] for i in out_ok]]
             stats.note(*check_close(f"layer {l} output", g, res.hidden[l + 1][out_ok]))
-    return in_bad
+    return div
 
 
-def _tie_choice(ctx, lib_rows, row_map):
-    """The library's top-k set of oracle row i at layer l (read once per layer)."""
-    cache = {}
-
-    def choice(layer, i):
-        if layer not in cache:
-            cache[layer] = ctx.uocr_debug_router(layer, lib_rows)["idx"]
-        return cache[layer][row_map[i]]
-    return choice
+def resync_rows(ctx, cfg, res, div, row_map):
+    """Give the library the oracle's cache entries of this step for the layers
+    above a near-tie divergence (the oracle's K/V are fp16 values already)."""
+    for i, l in enumerate(div):
+        r, s = row_map[i], int(res.slots[i])
+        for m in range(l + 1, cfg.n_layers):
+            k = res.k_new[m, i].astype(np.float16)[:, None, :]
+            v = res.v_new[m, i].astype(np.float16)[:, None, :]
+            ctx.uocr_kv_write(r, m, s, k, v)
 
 
 def run_parity(ctx, wl, steps, oracle_model, rows=None, row_map=None, check_kv=True, log=None):
@@ -224,7 +220,6 @@ def run_parity(ctx, wl, steps, oracle_model, rows=None, row_map=None, check_kv=T
     n_or = oracle_model.rows
     row_map = list(range(n_or)) if row_map is None else row_map
     stats = Stats()
-    hist_bad = [10 ** 9] * n_or
     plan = []
     if wl.prefill_embeds is not None:
         ne = wl.prefill_embeds.shape[1]
@@ -245,21 +240,16 @@ def run_parity(ctx, wl, steps, oracle_model, rows=None, row_map=None, check_kv=T
         opos = np.full(n_or, p, np.int32)
         is_last_prefill = wl.prefill_embeds is not None and p == cfg.prefix_len - 1
         want_lm = cfg.vocab > 0 and (kind == "greedy" or is_last_prefill)
-        # the library steps first, so that at a near tie of the router the oracle can
-        # follow the library's (equally correct) top-k set
         if kind == "x":
             g = runner.step(gpos, x=data[:runner.rows], want_logits=want_lm)
+            res = oracle_model.step(opos, x=data[row_map], want_logits=want_lm)
         else:
             ids = data if kind == "ids" else last_ids
             g = runner.step(gpos, ids=ids[:runner.rows], want_logits=want_lm)
-        oracle_model.tie_choice = _tie_choice(ctx, runner.rows, row_map)
-        if kind == "x":
-            res = oracle_model.step(opos, x=data[row_map], want_logits=want_lm)
-        else:
             res = oracle_model.step(opos, ids=ids[row_map], want_logits=want_lm)
-        oracle_model.tie_choice = None
-        in_bad = compare_step(ctx, cfg, res, runner.rows, stats, hist_bad, row_map=row_map, check_kv=check_kv)
-        clean = [i for i in range(n_or) if in_bad[i] >= 10 ** 9]
+        div = compare_step(ctx, cfg, res, runner.rows, stats, row_map=row_map, check_kv=check_kv)
+        resync_rows(ctx, cfg, res, div, row_map)
+        clean = [i for i in range(n_or) if div[i] >= cfg.n_layers]
         if "y" in g and clean:
             stats.note(*check_close(f"step {si} output", g["y"][[row_map[i] for i in clean]],
                                     res.hidden[-1][clean]))

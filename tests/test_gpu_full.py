@@ -3,13 +3,13 @@
 The library runs every row of each workload at its full size; the float64
 oracle follows a sample of rows (rows are independent in a decode step, so a
 one- or two-row oracle reproduces those rows exactly).  Greedy runs are
-teacher-forced: the oracle's ids feed both sides, or, for the device-chained
-generate loop the benchmark times, the library's own ids feed the oracle.
+teacher-forced by the oracle: its ids feed both sides.
 
   dense_layer_b1  one dense layer, batch 1, 64 cached tokens (3 steps)
   moe_layer_b1    one MoE layer, batch 1, 289 cached tokens, 300 steps (the ring wraps)
-  full_b8         12 layers, 8 rows, prefill-by-decode of 256 embeddings + 32 ids,
-                  then greedy steps through uocr_generate as the benchmark runs it
+  full_b8         12 layers, 8 rows, prefill-by-decode of 256 embeddings + 32 ids, then
+                  greedy steps; and uocr_generate (the benchmark's launch configuration)
+                  against the step loop, bit for bit
   sink            18-layer int8-asym sink decoder, rows 1/6/12/24/64 at 350 and 3000 cached tokens
   stress_b64      12 layers, 64 rows, 2048 cached tokens, all experts Q4_0, 128 greedy steps
 """
@@ -19,7 +19,7 @@ import pytest
 from quantized_moe_decode_gb300 import synth
 
 from helpers import make_ctx, make_oracle
-from parity import ID_MARGIN, check_close, run_parity
+from parity import GpuRunner, run_parity
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -64,50 +64,62 @@ def test_moe_layer_b1_300_steps_ring_wraps(cuda):
     ctx.close()
 
 
-def test_full_b8_prefill_then_generate_sampled_rows(cuda):
-    import torch
-
+def test_full_b8_prefill_and_greedy_sampled_rows(cuda):
     wl = synth.workload("full_b8")
-    cfg = wl.cfg
     sample = [0, 7]
     ctx = make_ctx(wl)
     orc = make_oracle(wl, rows=sample, cache=_cache())
-    # prefill-by-decode (288 steps) and 8 greedy steps, every layer tap compared
-    n_step = 8
+    # prefill-by-decode (288 steps) then greedy steps, every layer tap compared
+    n_step = 24
     st = run_parity(ctx, wl, n_step, orc, rows=wl.rows, row_map=sample)
-    _report(wl.name + " step-by-step", st)
+    _report(wl.name, st)
     assert st.id_checks >= 2 * n_step
-    # then the benchmark's launch configuration: uocr_generate (graph, argmax chained on the device)
-    n_gen = 24
-    dev = torch.device("cuda")
-    p0 = wl.start_pos + n_step
-    ids0 = np.asarray(st.last_ids, np.int32)
-    ids = torch.from_numpy(ids0).to(dev)
-    pos = torch.full((wl.rows,), p0, dtype=torch.int32, device=dev)
-    out = torch.zeros((n_gen, wl.rows), dtype=torch.int32, device=dev)
-    ctx.uocr_generate(wl.rows, ids.data_ptr(), pos.data_ptr(), n_gen, out.data_ptr())
-    ctx.uocr_sync()
-    hist = out.cpu().numpy()
-    assert (pos.cpu().numpy() == p0).all()  # the caller's inputs are not modified
-    checked = ties = 0
-    prev = ids0
-    for s in range(n_gen):
-        res = orc.step(np.full(len(sample), p0 + s, np.int32), ids=prev[sample], want_logits=True)
-        for i, r in enumerate(sample):
-            if res.margin[i] > ID_MARGIN:
-                assert int(hist[s, r]) == int(res.next_ids[i]), f"generate step {s} row {r}"
-                checked += 1
-            else:
-                ties += 1
-        prev = hist[s]
-    # the hidden taps hold the last generated step
-    L = cfg.n_layers
-    check_close("generate: last layer after attention", ctx.uocr_debug_hidden(2 * L - 2, wl.rows)[sample],
-                res.h_attn[L - 1])
-    check_close("generate: last layer output", ctx.uocr_debug_hidden(2 * L - 1, wl.rows)[sample], res.hidden[L])
-    print(f"generate: {n_gen} steps, {checked} ids checked, {ties} near ties")
-    assert checked >= n_gen
     ctx.close()
+
+
+def _gpu_prefill(ctx, wl):
+    """The workload's prefill-by-decode on the library alone; returns the first greedy ids."""
+    run = GpuRunner(ctx, wl)
+    ne = wl.prefill_embeds.shape[1]
+    for p in range(wl.cfg.prefix_len):
+        pos = np.full(wl.rows, p, np.int32)
+        if p < ne:
+            g = run.step(pos, x=wl.prefill_embeds[:, p])
+        else:
+            g = run.step(pos, ids=wl.prefill_ids[:, p - ne])
+    return g["next"]
+
+
+def test_full_b8_generate_equals_step_loop_bitwise(cuda):
+    """uocr_generate (one graph per step, argmax chained on the device: what the
+    benchmark times) computes exactly what the step-by-step path the oracle
+    checks computes: same ids and same final hidden states, bit for bit."""
+    import torch
+
+    wl = synth.workload("full_b8")
+    L, n = wl.cfg.n_layers, 24
+    a, b = make_ctx(wl), make_ctx(wl)
+    ids_a, ids_b = _gpu_prefill(a, wl), _gpu_prefill(b, wl)
+    assert np.array_equal(ids_a, ids_b)
+    dev = torch.device("cuda")
+    p0 = wl.start_pos
+    ids = torch.from_numpy(ids_a.astype(np.int32)).to(dev)
+    pos = torch.full((wl.rows,), p0, dtype=torch.int32, device=dev)
+    out = torch.zeros((n, wl.rows), dtype=torch.int32, device=dev)
+    a.uocr_generate(wl.rows, ids.data_ptr(), pos.data_ptr(), n, out.data_ptr())
+    a.uocr_sync()
+    assert (pos.cpu().numpy() == p0).all()  # the caller's inputs are not modified
+    run = GpuRunner(b, wl)
+    cur = ids_b
+    hist = []
+    for s in range(n):
+        cur = run.step(np.full(wl.rows, p0 + s, np.int32), ids=cur)["next"]
+        hist.append(cur)
+    assert np.array_equal(out.cpu().numpy(), np.stack(hist))
+    for tap in (2 * L - 2, 2 * L - 1):
+        assert np.array_equal(a.uocr_debug_hidden(tap, wl.rows), b.uocr_debug_hidden(tap, wl.rows)), tap
+    a.close()
+    b.close()
 
 
 @pytest.mark.parametrize("T", [350, 3000])
