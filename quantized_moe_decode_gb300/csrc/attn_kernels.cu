@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(128) k_attn(const AttnArgs a) {
   // every slot but the current token's was written by earlier steps: stream them now
   if (threadIdx.x == 0)
     for (int sb = 0; sb < n_sub && sb < 2; ++sb) issue(sb);
-  pdl_launch_dependents();
+  if (!(kPdlLate & PDL_ATTN)) pdl_launch_dependents();
   pdl_wait();  // q and the current slot come from the QKV kernel
 
   float qv[8];
@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(128) k_attn(const AttnArgs a) {
     __syncthreads();  // stage consumed
     if (threadIdx.x == 0 && sb + 2 < n_sub) issue(sb + 2);
   }
+  if (kPdlLate & PDL_ATTN) pdl_launch_dependents();
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
 #pragma unroll

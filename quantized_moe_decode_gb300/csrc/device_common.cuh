@@ -50,9 +50,17 @@ constexpr int kThreads = kConsumers;
 #ifndef UOCR_UNROLL
 #define UOCR_UNROLL 2
 #endif
+//   UOCR_PDL_LATE    kernels that let their dependents launch only after their
+//                    weight stream instead of at their start (bit mask:
+//                    1 GEMV, 2 router, 4 expert kernels, 8 attention)
+#ifndef UOCR_PDL_LATE
+#define UOCR_PDL_LATE 8
+#endif
 constexpr int kRingDepth = UOCR_RING_DEPTH;
 constexpr int kMinBlocks = UOCR_MIN_BLOCKS;
 constexpr int kUnroll = UOCR_UNROLL;
+constexpr int kPdlLate = UOCR_PDL_LATE;
+enum PdlKernel : int { PDL_GEMV = 1, PDL_ROUTER = 2, PDL_EXPERT = 4, PDL_ATTN = 8 };
 static_assert(kRingDepth >= 2 && kRingDepth <= 16, "ring depth");
 static_assert(kUnroll == 1 || kUnroll == 2, "unroll");
 constexpr int kSlotBytes = 1024;         // codes (512 or 1024) + lane-private scales (32 x 8 B)

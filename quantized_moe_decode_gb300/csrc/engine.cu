@@ -126,6 +126,7 @@ struct uocr_ctx {
   int* slab_counter = nullptr;
   float* r_logits = nullptr;
   int *r_idx = nullptr, *r_count = nullptr, *r_offset = nullptr, *r_perm = nullptr, *r_inv = nullptr;
+  int4* r_rec = nullptr;  // [L][token groups][E] routing records
 
   float* r_w = nullptr;
   float* sinks = nullptr;
@@ -301,6 +302,7 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
     ctx->r_offset = cv.take<int>((size_t)Lc * (E + 1), r.routing);
     ctx->r_perm = cv.take<int>((size_t)Lc * MR * k, r.routing);
     ctx->r_inv = cv.take<int>((size_t)Lc * MR * k, r.routing);
+    ctx->r_rec = cv.take<int4>((size_t)Lc * TG * E, r.routing);
   }
   if (V > 0) {
     ctx->logits = cv.take<float>((size_t)MR * V, r.logits);
@@ -474,19 +476,36 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       mark("mlp_down", false);
     } else {
       const int E = c.n_experts, k = c.top_k;
+      // Routed units: active slots when few experts are expected to receive a
+      // token (one token group only), else expert ids (their CTAs stream before
+      // the routing is known; the grid is one wave of CTAs that all have work).
+      // Expected experts with a token: E (1 - (1 - k/E)^rows).
+      const int max_act = E < rows * k ? E : rows * k;
+      const double exp_act = E * (1.0 - pow(1.0 - (double)k / E, rows));
+      const int by_slot = exp_act < 0.75 * E && tg == 1;
+      const int n_units = by_slot ? max_act : E;
+      int4* rec = ctx->r_rec + (size_t)l * ((MR + 15) / 16) * E;
+
       RouterArgs ra{};
       ra.w = w.router.view();
       ra.sp = plan_stream(nt, F16, H);
       ra.ntok = rows;
       ra.H = H;
       ra.E = E;
+      ra.k = k;
       ra.h = hid(2 * l + 1);
       ra.norm_w = w.mlp_norm;
       ra.eps = c.rms_eps;
       ra.logits = ctx->r_logits + (size_t)l * MR * E;
+      ra.tg = tg;
+      ra.by_slot = by_slot;
+      ra.n_units = n_units;
+      ra.idx = ctx->r_idx + (size_t)l * MR * k;
+      ra.wts = ctx->r_w + (size_t)l * MR * k;
+      ra.rec = rec;
       ra.status = ctx->status;
       mark("router", true);
-      CK(launch_router(ra, tg, st, pdl), "router launch");
+      CK(launch_router(ra, st, pdl), "router launch");
       mark("router", false);
 
       const int fs = ctx->shared_fmt();
@@ -498,9 +517,9 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       xa.Ie = c.expert_inter;
       xa.Ish = c.n_shared * c.expert_inter;
       xa.tg = tg;
-      xa.logits = ra.logits;
-      xa.idx = ctx->r_idx + (size_t)l * MR * k;
-      xa.wts = ctx->r_w + (size_t)l * MR * k;
+      xa.rec = rec;
+      xa.idx = ra.idx;
+      xa.wts = ra.wts;
       xa.count = ctx->r_count + (size_t)l * E;
       xa.offset = ctx->r_offset + (size_t)l * (E + 1);
       xa.perm = ctx->r_perm + (size_t)l * MR * k;
@@ -515,16 +534,9 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       xa.out = hid(2 * l + 2);
       xa.slab_counter = ctx->slab_counter;
       xa.status = ctx->status;
-      // Routed CTAs by expert id when nearly every expert is expected to
-      // receive a token (they stream before the routing is known, and the grid
-      // is one wave of CTAs that all have work), else by active slot (slots
-      // past the active experts exit at once, after the live ones in launch
-      // order).  Expected experts with a token: E (1 - (1 - k/E)^rows).
-      const int max_act = E < rows * k ? E : rows * k;
-      const double exp_act = E * (1.0 - pow(1.0 - (double)k / E, rows));
-      xa.by_slot = exp_act < 0.75 * E;
-      xa.n_units = xa.by_slot ? max_act : E;
-      const double units = xa.by_slot ? exp_act : E;
+      xa.by_slot = by_slot;
+      xa.n_units = n_units;
+      const double units = by_slot ? exp_act : E;
       // CTAs per routed unit and for the shared experts, in proportion to the
       // bytes each streams, about GE per token group in all
       auto split = [&](const DMat& r, const DMat* sh, int rslabs, int sslabs) {

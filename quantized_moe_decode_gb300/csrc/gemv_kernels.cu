@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = smem + p.ring_off + (size_t)warp * kRingDepth * p.slot;
 
-  pdl_launch_dependents();
+  if (!(kPdlLate & PDL_GEMV)) pdl_launch_dependents();
   const int tok0 = blockIdx.y * NT * 8;
   const int ntok = min(a.ntok - tok0, NT * 8);
   const int K = a.w.K;
@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
     }
   };
   run_stream<FMT, NT>(us, w, ring, p.slot, red, bp, NT, epi);
+  if (kPdlLate & PDL_GEMV) pdl_launch_dependents();
 
   if constexpr (EPI == EPI_LOGITS) {
     __syncthreads();

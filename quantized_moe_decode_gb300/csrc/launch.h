@@ -64,11 +64,18 @@ struct GemvArgs {
 struct RouterArgs {
   PMat w;                   // packed F16 router [E][H]
   StreamPlan sp;
-  int ntok, H, E;
+  int ntok, H, E, k;
   const float* h;           // residual after attention [rows][H]
   const __half* norm_w;
   float eps;
   float* logits;            // out: [rows][E]
+  // routing (rank 0 of each cluster, one cluster per token group of 16 rows)
+  int tg;                   // token groups
+  int by_slot;              // records per active slot (1) or per expert id (0)
+  int n_units;              // records per token group
+  int* idx;                 // out: [rows][k] chosen experts
+  float* wts;               // out: [rows][k] renormalised weights
+  int4* rec;                // out: [tg][n_units] {expert or -1, 16-row mask, slot bits 0-31, slot bits 32-47}
   int* status;
 };
 
@@ -81,10 +88,10 @@ struct ExpertArgs {
   int n_units;              // routed units of the grid: max active experts (by slot) or E
   int cpe, cpes;            // CTAs per routed unit, for the shared experts
   int tg;                   // token groups of 16 rows (blockIdx.y)
-  const float* logits;      // router logits [rows][E]
-  // routing and grouping: written by the gate/up launch (CTA 0, 0), read by the down launch
-  int* idx;                 // [rows][k] chosen experts
-  float* wts;               // [rows][k] renormalised weights
+  const int4* rec;          // [tg][n_units] routing records written by the router
+  const int* idx;           // [rows][k] chosen experts (router)
+  const float* wts;         // [rows][k] renormalised weights (router)
+  // grouping: written by the gate/up launch (CTA 0, 0) from idx
   int* count;               // [E]
   int* offset;              // [E+1]
   int* perm;                // [rows*k] entries row*k + slot grouped by expert, rows ascending
@@ -157,6 +164,27 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// The same as a thread-block cluster launch of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                  bool pdl, int cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster_x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // Allow a kernel the largest dynamic shared memory the device offers beside
 // its own static shared memory.
 template <typename... KArgs>
@@ -174,7 +202,9 @@ cudaError_t allow_max_dyn_smem(void (*kern)(KArgs...)) {
 // launchers (return the launch error)
 cudaError_t launch_gemv(int fmt, int src, int epi, const GemvArgs& a, int grid_x, int grid_y, cudaStream_t st,
                         bool pdl);
-cudaError_t launch_router(const RouterArgs& a, int grid_y, cudaStream_t st, bool pdl);
+// grid (cluster, token groups); cluster = min(8, router slabs) CTAs per token group
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t st, bool pdl);
+int router_cluster(int n_slabs);
 cudaError_t launch_expert_gateup(int fmt_r, int fmt_s, const ExpertArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_expert_down(int fmt_r, int fmt_s, const ExpertArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_attn(const AttnArgs& a, int rows, cudaStream_t st, bool pdl);

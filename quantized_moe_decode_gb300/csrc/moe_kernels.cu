@@ -1,31 +1,37 @@
 // MoE kernels of one decode step.
 //
-//   router   RMSNorm prologue -> fp16 router GEMV: E logits per row.
+//   router   one thread-block cluster per token group of 16 rows: its CTAs
+//            share the E/16 slabs of the fp16 router GEMV (RMSNorm prologue)
+//            and keep their logits in shared memory; after a cluster barrier
+//            rank 0 reads all E logits of each row through distributed shared
+//            memory, takes the top-k (lowest index wins a tie) and the softmax
+//            weights renormalised over them, and writes one record per routed
+//            unit (active slot or expert id): the expert, the rows of the group
+//            that chose it (its segment of the token grouping, a 16-bit mask)
+//            and each row's slot in its top-k (3 bits per row).
 //   gate/up  shared-expert CTAs first (they need nothing from the router),
-//            then routed CTAs.  A routed CTA owns one expert, one token group
-//            of 16 rows and a part of the expert's slabs.  It takes the top-k
-//            of its rows' logits itself (lowest index wins a tie) and keeps the
-//            rows that chose its expert: the expert's segment of the token
-//            grouping, as a row mask.  It streams the expert's gate/up slabs
-//            once for those rows and writes SwiGLU activations in the
-//            B-fragment order the down projection reads directly.  CTA (0, 0)
-//            also writes the routing of every row (ids, renormalised weights)
-//            and the grouping arrays (count, offset, perm, inv).
+//            then routed CTAs, one per (unit, token group, part of the
+//            expert's slabs).  A routed CTA reads its record, stages its rows,
+//            streams the expert's gate/up slabs once for them and writes SwiGLU
+//            activations in the B-fragment order the down projection reads
+//            directly.  CTA (0, 0) also writes the grouping arrays (count,
+//            offset, perm, inv) from the router's choices.
 //   down     the same CTA layout; it streams the expert's down slabs and
 //            writes fp32 partials; the last contribution to an output slab (a
 //            counter per slab, no waiting) combines them in a fixed order:
 //            residual + sum_j w_j * expert_j + shared.
 //
-// Routed CTAs are laid out either by expert id (when most experts are expected
-// to receive a token: the CTA streams the head of its expert's weights before
-// the router has finished, into bandwidth the router leaves idle) or by active
-// slot (few rows: CTA i serves the i-th expert that received a token).
+// Routed units are expert ids when most experts are expected to receive a
+// token (the CTA streams the head of its expert's weights before the routing
+// is known, into bandwidth the router leaves idle), else active slots (few
+// rows: unit i is the i-th expert that received a token).
 //
 // Sources: "Unlimited-OCR on Apple Silicon with C and Metal", "Il decoder e
 // il Mixture of Experts" (64 routed experts, top-6, two shared experts;
 // compute the routing, group the tokens by expert, run the projections,
 // recompose without useless copies) and "Quantizzazione" (dequantisation
 // fused into GEMV/GEMM, SwiGLU and the expert combine).
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "launch.h"
@@ -136,50 +142,24 @@ struct RouteSmem {
   int e, nlast, contrib;
 };
 
-// Top-k of rows [r0, r1) from the logits into rs (rowmask must start at zero).
-__device__ __forceinline__ void route_rows(RouteSmem& rs, const float* logits, int E, int k, int r0, int r1) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = r0 + warp; r < r1; r += kWarps) {
-    RowLogits rl;
-    topk_load(rl, logits + (size_t)r * E, E, lane);
-    int e;
-    float w;
-    topk_select(rl, E, k, lane, e, w);
-    if (lane < k) {
-      rs.idx[r * k + lane] = e;
-      rs.w[r * k + lane] = w;
-      atomicOr(&rs.rowmask[e], 1ull << r);  // a row picks an expert at most once
-    }
-  }
-}
-
 __device__ __forceinline__ void clear_rowmask(RouteSmem& rs, int E) {
   for (int e = threadIdx.x; e < E; e += kThreads) rs.rowmask[e] = 0ull;
 }
 
-// The i-th expert (ascending) that received a token, or -1.  All threads.
-__device__ __forceinline__ int active_expert(RouteSmem& rs, int E, int i) {
-  const int e = threadIdx.x;
-  const int4 v = make_int4(e < E && rs.rowmask[e] != 0ull, 0, 0, 0);
-  int4 tot;
-  const int4 ex = block_excl_scan4(v, tot, rs.scan);
-  if (threadIdx.x == 0) rs.e = -1;
-  __syncthreads();
-  if (v.x && ex.x == i) rs.e = e;
-  __syncthreads();
-  return rs.e;
-}
-
-// Write every row's routing and the grouping: count[e] (histogram),
-// offset = exclusive scan, perm = entries row*k + slot grouped by expert
-// ascending, rows ascending within an expert; inv = position of each entry in
-// perm.  rs holds the top-k of all rows.  All threads.
-__device__ __forceinline__ void write_routing(RouteSmem& rs, const ExpertArgs& a) {
+// The grouping of the step: count[e] (histogram), offset = exclusive scan,
+// perm = entries row*k + slot grouped by expert ascending, rows ascending
+// within an expert; inv = position of each entry in perm.  From the router's
+// choices idx[rows][k].  All threads.
+__device__ __forceinline__ void write_grouping(RouteSmem& rs, const ExpertArgs& a) {
   const int rows = a.ntok, E = a.E, k = a.k;
+  clear_rowmask(rs, E);
+  __syncthreads();
   for (int i = threadIdx.x; i < rows * k; i += kThreads) {
-    a.idx[i] = rs.idx[i];
-    a.wts[i] = rs.w[i];
+    const int ei = __ldcg(a.idx + i);
+    rs.idx[i] = ei;
+    atomicOr(&rs.rowmask[ei], 1ull << (i / k));  // a row picks an expert at most once
   }
+  __syncthreads();
   const int e = threadIdx.x;
   const unsigned long long rm = e < E ? rs.rowmask[e] : 0ull;
   int4 tot;
@@ -201,20 +181,27 @@ __device__ __forceinline__ void write_routing(RouteSmem& rs, const ExpertArgs& a
 
 // ------------------------------------------------------------------ router
 template <int NT>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) k_router(const RouterArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ float s_lg[16][256];             // this CTA's logits, by expert index
+  __shared__ unsigned s_mask[256];            // rank 0: rows of the group that chose expert e
+  __shared__ unsigned long long s_jbits[256]; // rank 0: 3-bit slot of each such row
+  __shared__ int4 s_scan[kWarps];
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
   const StreamPlan& p = a.sp;
   __half* xs = reinterpret_cast<__half*>(smem + p.xs_off);
   float* red = reinterpret_cast<float*>(smem + p.red_off);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = smem + p.ring_off + (size_t)warp * kRingDepth * p.slot;
 
-  pdl_launch_dependents();
-  const int tok0 = blockIdx.y * NT * 8;
+  if (!(kPdlLate & PDL_ROUTER)) pdl_launch_dependents();
+  const int cs = gridDim.x, rank = blockIdx.x;  // the cluster spans x
+  const int g = blockIdx.y, tok0 = g * 16;
   const int ntok = min(a.ntok - tok0, NT * 8);
-  const int H = a.H;
-  const int my_slabs = ((int)blockIdx.x < a.w.n_slabs) ? (a.w.n_slabs - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const SlabWork w = slab_work(blockIdx.x, gridDim.x, my_slabs, a.w.U);
+  const int H = a.H, E = a.E;
+  const int my_slabs = (rank < a.w.n_slabs) ? (a.w.n_slabs - 1 - rank) / cs + 1 : 0;
+  const SlabWork w = slab_work(rank, cs, my_slabs, a.w.U);
   UnitStream<F16> us;
   us.start(a.w.q, a.w.s, w);
   us.prefetch(ring, p.slot, w, lane);
@@ -222,18 +209,70 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_router(const RouterArg
   stage_norm_rows(xs, p.ldx, a.h + (size_t)tok0 * H, H, ntok, NT * 8, a.norm_w, H, a.eps);
   __syncthreads();
   const BSmem bp{xs, p.ldx};
-  auto epi = [&](int s, const float* rb, int tid, int nthr) {
+  auto epi = [&](int sl, const float* rb, int tid, int nthr) {
     for (int i = tid; i < NT * 64; i += nthr) {
       const int tok = i >> 3, pg = i & 7;
       if (tok >= ntok) continue;
       float lo, hi;
       group_sum<NT>(rb, w.ks, tok, pg, lo, hi);
-      const int e0 = 16 * s + pg;
-      if (e0 < a.E) a.logits[(size_t)(tok0 + tok) * a.E + e0] = lo;
-      if (e0 + 8 < a.E) a.logits[(size_t)(tok0 + tok) * a.E + e0 + 8] = hi;
+      const int e0 = 16 * sl + pg;
+      if (e0 < E) {
+        s_lg[tok][e0] = lo;
+        a.logits[(size_t)(tok0 + tok) * E + e0] = lo;
+      }
+      if (e0 + 8 < E) {
+        s_lg[tok][e0 + 8] = hi;
+        a.logits[(size_t)(tok0 + tok) * E + e0 + 8] = hi;
+      }
     }
   };
   run_stream<F16, NT>(us, w, ring, p.slot, red, bp, NT, epi);
+  if (kPdlLate & PDL_ROUTER) pdl_launch_dependents();
+  cluster.sync();  // every CTA's logits are in its shared memory
+
+  if (rank == 0) {
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+      s_mask[e] = 0u;
+      s_jbits[e] = 0ull;
+    }
+    __syncthreads();
+    const int k = a.k;
+    for (int r = warp; r < ntok; r += kWarps) {
+      RowLogits rl;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int e = lane + 32 * q;
+        rl.v[q] = -INFINITY;
+        if (e < E) {
+          const float* peer = cluster.map_shared_rank(&s_lg[0][0], (e >> 4) % cs);
+          rl.v[q] = peer[r * 256 + e];
+        }
+      }
+      int ej;
+      float wj;
+      topk_select(rl, E, k, lane, ej, wj);
+      if (lane < k) {
+        a.idx[(tok0 + r) * k + lane] = ej;
+        a.wts[(tok0 + r) * k + lane] = wj;
+        atomicOr(&s_mask[ej], 1u << r);  // a row picks an expert at most once
+        atomicOr(&s_jbits[ej], (unsigned long long)lane << (3 * r));
+      }
+    }
+    __syncthreads();
+    const int e = threadIdx.x;
+    const unsigned mk = e < E ? s_mask[e] : 0u;
+    const unsigned long long jb = e < E ? s_jbits[e] : 0ull;
+    int4* rec = a.rec + (size_t)g * a.n_units;
+    if (a.by_slot) {  // one token group: unit i = the i-th expert that received a token
+      int4 tot;
+      const int4 ex = block_excl_scan4(make_int4(mk != 0u, 0, 0, 0), tot, s_scan);
+      if (mk) rec[ex.x] = make_int4(e, (int)mk, (int)(uint32_t)jb, (int)(uint32_t)(jb >> 32));
+      for (int i = tot.x + threadIdx.x; i < a.n_units; i += kThreads) rec[i] = make_int4(-1, 0, 0, 0);
+    } else if (e < E) {
+      rec[e] = make_int4(mk ? e : -1, (int)mk, (int)(uint32_t)jb, (int)(uint32_t)(jb >> 32));
+    }
+  }
+  cluster.sync();  // peers keep their shared memory until rank 0 has read it
 }
 
 // ------------------------------------------------------------------ expert CTAs
@@ -271,11 +310,6 @@ __device__ __forceinline__ void part_range(int n, int gran, int part, int parts,
 }
 __device__ __forceinline__ int groups_of(int U) { return kWarps / warps_per_slab(U); }
 
-// Row mask (bits = rows of token group g) of expert e, from rs.rowmask.
-__device__ __forceinline__ unsigned group_mask(const RouteSmem& rs, int e, int g) {
-  return (unsigned)((rs.rowmask[e] >> (16 * g)) & 0xFFFFull);
-}
-
 // ------------------------------------------------------------------ gate/up
 template <int FR, int FS, int NT>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const ExpertArgs a) {
@@ -284,12 +318,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
   const StreamPlan& p = a.sp;
   __half* xs = reinterpret_cast<__half*>(smem + p.xs_off);
   float* red = reinterpret_cast<float*>(smem + p.red_off);
-  int* rows = reinterpret_cast<int*>(smem + p.rows_off);  // staged row of each token of the expert
-  __half* zero = reinterpret_cast<__half*>(smem + p.zero_off);
+  int* rows = reinterpret_cast<int*>(smem + p.rows_off);  // global row of each token of the expert
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = smem + p.ring_off + (size_t)warp * kRingDepth * p.slot;
 
-  pdl_launch_dependents();
+  if (!(kPdlLate & PDL_EXPERT)) pdl_launch_dependents();
   const ExpertCta ec = expert_cta(a);
   const int g = blockIdx.y, tok0 = g * 16;
   const int ng = min(16, a.ntok - tok0);  // rows of this token group
@@ -311,32 +344,24 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
     usr.prefetch(ring, p.slot, w, lane);
     streaming = true;
   }
-  clear_rowmask(rs, a.E);
-  if (threadIdx.x < 16) zero[threadIdx.x * 2] = zero[threadIdx.x * 2 + 1] = __float2half_rn(0.f);
-  __syncthreads();
   pdl_wait();
 
-  // routing: CTA (0, 0) and the slot layout need every row, the others their group
-  const bool first = blockIdx.x == 0 && blockIdx.y == 0;
-  const bool all_rows = first || (!ec.shared && a.by_slot);
-  if (all_rows || !ec.shared) {
-    route_rows(rs, a.logits, a.E, a.k, all_rows ? 0 : tok0, all_rows ? a.ntok : tok0 + ng);
-    __syncthreads();
-  }
-  if (first) write_routing(rs, a);
+  if (blockIdx.x == 0 && blockIdx.y == 0) write_grouping(rs, a);
   // this CTA's rows
   int e = -1, ntk = ng;
-  if (!ec.shared) {
-    e = a.by_slot ? active_expert(rs, a.E, ec.i) : ec.i;
-    const unsigned mask = e >= 0 ? group_mask(rs, e, g) : 0u;
-    ntk = __popc(mask);
+  if (ec.shared) {
+    for (int t = threadIdx.x; t < ng; t += kThreads) rows[t] = tok0 + t;
+  } else {
+    const int4 r = a.rec[(size_t)g * a.n_units + ec.i];  // {expert, row mask, slot bits}
+    e = r.x;
+    const unsigned mask = (unsigned)r.y;
+    ntk = e >= 0 ? __popc(mask) : 0;
     if (ntk == 0) {
       if (streaming) cp_wait<0>();  // copies in flight land before the CTA leaves
       return;
     }
     if (threadIdx.x < 16 && ((mask >> threadIdx.x) & 1))
-      rows[__popc(mask & ((1u << threadIdx.x) - 1u))] = threadIdx.x;
-    if (threadIdx.x >= ntk && threadIdx.x < NT * 8) rows[threadIdx.x] = -1;
+      rows[__popc(mask & ((1u << threadIdx.x) - 1u))] = tok0 + threadIdx.x;
     if (a.by_slot) {
       part_range(a.wr.n_slabs, groups_of(a.wr.U), ec.part, ec.parts, s0, s1);
       w = slab_work(s0, 1, s1 - s0, a.wr.U);
@@ -344,10 +369,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
       usr.prefetch(ring, p.slot, w, lane);
     }
   }
-  // the group's rows, normalised (all of them: the expert's rows are gathered by the B operand)
-  stage_norm_rows(xs, p.ldx, a.h + (size_t)tok0 * a.H, a.H, ng, NT * 8, a.norm_w, a.H, a.eps);
+  __syncthreads();
+  // the expert's rows, normalised, packed into consecutive tokens
+  stage_norm_gather(xs, p.ldx, a.h, a.H, rows, ntk, NT * 8, a.norm_w, a.H, a.eps);
   __syncthreads();
   const int nt_used = (ntk + 7) >> 3;
+  const BSmem bp{xs, p.ldx};
   if (ec.shared) {
     auto epi = [&](int sl, const float* rb, int tid, int nthr) {
       for (int i = tid; i < NT * 64; i += nthr) {
@@ -360,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
             __float2half_rn(silu(lo) * hi);
       }
     };
-    run_stream<FS, NT>(uss, w, ring, p.slot, red, BSmem{xs, p.ldx}, nt_used, epi);
+    run_stream<FS, NT>(uss, w, ring, p.slot, red, bp, nt_used, epi);
   } else {
     const int tile0 = (e * a.tg + g) * 2;  // two 8-token tiles per (expert, token group)
     auto epi = [&](int sl, const float* rb, int tid, int nthr) {
@@ -373,8 +400,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
             __float2half_rn(silu(lo) * hi);
       }
     };
-    run_stream<FR, NT>(usr, w, ring, p.slot, red, BSmemGather{xs, p.ldx, rows, zero}, nt_used, epi);
+    run_stream<FR, NT>(usr, w, ring, p.slot, red, bp, nt_used, epi);
   }
+  if (kPdlLate & PDL_EXPERT) pdl_launch_dependents();
 }
 
 // ------------------------------------------------------------------ down + combine
@@ -389,9 +417,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = smem + p.ring_off + (size_t)warp * kRingDepth * p.slot;
 
-  pdl_launch_dependents();
+  if (!(kPdlLate & PDL_EXPERT)) pdl_launch_dependents();
   const ExpertCta ec = expert_cta(a);
-  const int g = blockIdx.y, tok0 = g * 16, H = a.H, E = a.E, k = a.k, rows = a.ntok;
+  const int g = blockIdx.y, tok0 = g * 16, H = a.H, k = a.k, rows = a.ntok;
   int s0 = 0, s1 = 0;
   SlabWork w;
   UnitStream<FS> uss;
@@ -410,24 +438,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
     usr.prefetch(ring, p.slot, w, lane);
     streaming = true;
   }
-  clear_rowmask(rs, E);
   if (threadIdx.x == 0) rs.contrib = 0;
   __syncthreads();
   pdl_wait();
-  // the routing the gate/up launch wrote
-  for (int i = threadIdx.x; i < rows * k; i += kThreads) {
-    const int ei = __ldcg(a.idx + i);
-    rs.idx[i] = ei;
-    rs.w[i] = __ldcg(a.wts + i);
-    atomicOr(&rs.rowmask[ei], 1ull << (i / k));
-  }
-  __syncthreads();
-  // contributions every output slab receives: one per (expert, token group) with rows, one per shared group
-  if (threadIdx.x < E) {
+  // contributions every output slab receives: one per routed record with rows, one per shared group
+  {
     int c = 0;
-    for (int gg = 0; gg < a.tg; ++gg) c += group_mask(rs, threadIdx.x, gg) != 0u;
+    for (int i = threadIdx.x; i < a.n_units * a.tg; i += kThreads) c += __ldcg(&a.rec[i].y) != 0;
     if (c) atomicAdd(&rs.contrib, c);
   }
+  for (int i = threadIdx.x; i < rows * k; i += kThreads) rs.w[i] = __ldcg(a.wts + i);  // combine weights
   int e = -1, ntk, k32;
   const uint8_t* bsrc;
   if (ec.shared) {
@@ -435,18 +455,18 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
     k32 = a.Ish >> 5;
     bsrc = a.act_s + (size_t)(tok0 >> 3) * k32 * 512;
   } else {
-    e = a.by_slot ? active_expert(rs, E, ec.i) : ec.i;
-    const unsigned mask = e >= 0 ? group_mask(rs, e, g) : 0u;
-    ntk = __popc(mask);
+    const int4 r = a.rec[(size_t)g * a.n_units + ec.i];  // {expert, row mask, slot bits}
+    e = r.x;
+    const unsigned mask = (unsigned)r.y;
+    ntk = e >= 0 ? __popc(mask) : 0;
     if (ntk == 0) {
       if (streaming) cp_wait<0>();
       return;
     }
     if (threadIdx.x < 16 && ((mask >> threadIdx.x) & 1)) {
-      const int r = tok0 + threadIdx.x;
-      int j = 0;
-      while (j < k - 1 && rs.idx[r * k + j] != e) ++j;
-      s_entry[__popc(mask & ((1u << threadIdx.x) - 1u))] = r * k + j;
+      const unsigned long long jb = (unsigned long long)(uint32_t)r.z | ((unsigned long long)(uint32_t)r.w << 32);
+      const int j = (int)((jb >> (3 * threadIdx.x)) & 7ull);
+      s_entry[__popc(mask & ((1u << threadIdx.x) - 1u))] = (tok0 + threadIdx.x) * k + j;
     }
     k32 = a.Ie >> 5;
     bsrc = a.act_r + (size_t)((e * a.tg + g) * 2) * k32 * 512;
@@ -477,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
     run_stream<FS, NT>(uss, w, ring, p.slot, red, bp, tiles, epi);
   else
     run_stream<FR, NT>(usr, w, ring, p.slot, red, bp, tiles, epi);
+  if (kPdlLate & PDL_EXPERT) pdl_launch_dependents();
 
   // one counter per output slab; the last contribution to a slab combines it.
   // All of this CTA's slabs are counted at once (one thread per slab), and all
@@ -528,10 +549,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
 }
 
 // ------------------------------------------------------------------ launchers
-cudaError_t launch_router(const RouterArgs& a, int gy, cudaStream_t st, bool pdl) {
-  const dim3 grid(a.w.n_slabs, gy);
-  if (a.sp.nt == 1) return launch_kernel(k_router<1>, grid, dim3(kThreads), a.sp.bytes, st, pdl, a);
-  return launch_kernel(k_router<2>, grid, dim3(kThreads), a.sp.bytes, st, pdl, a);
+int router_cluster(int n_slabs) { return n_slabs < 8 ? n_slabs : 8; }
+
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t st, bool pdl) {
+  const int cs = router_cluster(a.w.n_slabs);
+  const dim3 grid(cs, a.tg);
+  if (a.sp.nt == 1) return launch_kernel_cluster(k_router<1>, grid, dim3(kThreads), a.sp.bytes, st, pdl, cs, a);
+  return launch_kernel_cluster(k_router<2>, grid, dim3(kThreads), a.sp.bytes, st, pdl, cs, a);
 }
 
 #define UOCR_PAIRS(X, NT_) \
