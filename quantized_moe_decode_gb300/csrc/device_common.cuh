@@ -42,13 +42,13 @@ constexpr int kThreads = kConsumers;
 //   UOCR_MIN_BLOCKS  minimum resident CTAs per SM asked of the compiler
 //   UOCR_UNROLL      units consumed per step of the inner loop (1 or 2)
 #ifndef UOCR_RING_DEPTH
-#define UOCR_RING_DEPTH 8
+#define UOCR_RING_DEPTH 6
 #endif
 #ifndef UOCR_MIN_BLOCKS
 #define UOCR_MIN_BLOCKS 2
 #endif
 #ifndef UOCR_UNROLL
-#define UOCR_UNROLL 2
+#define UOCR_UNROLL 1
 #endif
 //   UOCR_PDL_LATE    kernels that let their dependents launch only after their
 //                    weight stream instead of at their start (bit mask:
@@ -330,7 +330,7 @@ __device__ __forceinline__ void unit_mma(float (&acc)[NT][4], const uint8_t* a, 
     const uint32_t A1[4] = {q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      if (nt < nt_used) {
+      if (NT == 1 || nt < nt_used) {
         uint32_t B[4];
         bp(nt, kk, lane, B);
         mma_16816(acc[nt], A0, B[0], B[1]);
@@ -365,7 +365,7 @@ __device__ __forceinline__ void unit_mma(float (&acc)[NT][4], const uint8_t* a, 
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      if (nt < nt_used) {
+      if (NT == 1 || nt < nt_used) {
         uint32_t B[4];
         bp(nt, kk, lane, B);
         float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -397,7 +397,7 @@ __device__ __forceinline__ void unit_mma(float (&acc)[NT][4], const uint8_t* a, 
     const float d1_lo = half_lo(s.y), d1_hi = half_hi(s.y);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      if (nt < nt_used) {
+      if (NT == 1 || nt < nt_used) {
         uint32_t B0[4], B1[4];
         bp(nt, kk, lane, B0);
         bp(nt, kk + 32, lane, B1);
@@ -430,17 +430,6 @@ __device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
 // Ring slot layout: codes at [0, unit_bytes), then this lane's scale entry at
 // 512 + 8*lane (the 8-bit and 4-bit formats only).  Every byte of a slot is
 // written and read by the same lane, so a slot needs no barrier.
-template <int FMT>
-__device__ __forceinline__ void fetch_unit(uint8_t* slot, const uint8_t* q_unit, const uint8_t* s_unit, int lane) {
-  cp_async16(slot + lane * 16, q_unit + lane * 16);
-  if constexpr (FMT == F16) {
-    cp_async16(slot + 512 + lane * 16, q_unit + 512 + lane * 16);
-  } else if constexpr (FMT == Q8_0) {
-    cp_async4(slot + 512 + lane * 8, s_unit + (lane >> 2) * 4);
-  } else {
-    cp_async8(slot + 512 + lane * 8, s_unit + (lane >> 2) * 8);
-  }
-}
 
 // How a CTA's slabs are shared by its warps.  The CTA owns the slabs
 // first + m*stride, m in [0, n).  Its kWarps warps form G = kWarps/ks groups
@@ -470,22 +459,40 @@ __device__ __forceinline__ SlabWork slab_work(int first, int stride, int n, int 
   return w;
 }
 
-// The next unit a warp fetches: slab m of the CTA's list, unit i of its range.
+// The units a warp fetches, in the order it consumes them: for each of its
+// group's slabs (first + m*stride, m = grp, grp + G, ...) the run of uw units
+// starting at rank*uw.  Running pointers to this lane's 16 code bytes and its
+// scale entry; at the end of a run they jump to the next slab's run.
+// The units a warp fetches, in the order it consumes them: for each of its
+// group's slabs (first + m*stride, m = grp, grp + G, ...) the run of uw units
+// starting at rank*uw.  The unit index is recomputed from warp-uniform counters
+// (measured faster than per-lane running pointers).
 template <int FMT>
 struct UnitStream {
   const uint8_t* q;
   const uint8_t* sc;
   int m, i;
+  const SlabWork* wp;
   __device__ __forceinline__ void start(const uint8_t* q_, const uint8_t* sc_, const SlabWork& w) {
     q = q_;
     sc = sc_;
     m = w.grp;
     i = 0;
+    wp = &w;
   }
-  __device__ __forceinline__ void fetch_next(uint8_t* slot, const SlabWork& w, int lane) {
+  __device__ __forceinline__ void fetch_next(uint8_t* slot, int lane) {
+    const SlabWork& w = *wp;
     if (m < w.n) {
       const size_t unit = (size_t)(w.first + m * w.stride) * w.U + w.rank * w.uw + i;
-      fetch_unit<FMT>(slot, q + unit * unit_bytes(FMT), sc + unit * unit_scale_bytes(FMT), lane);
+      const uint8_t* qu = q + unit * unit_bytes(FMT);
+      cp_async16(slot + lane * 16, qu + lane * 16);
+      if constexpr (FMT == F16) {
+        cp_async16(slot + 512 + lane * 16, qu + 512 + lane * 16);
+      } else if constexpr (FMT == Q8_0) {
+        cp_async4(slot + 512 + lane * 8, sc + unit * unit_scale_bytes(FMT) + (lane >> 2) * 4);
+      } else {
+        cp_async8(slot + 512 + lane * 8, sc + unit * unit_scale_bytes(FMT) + (lane >> 2) * 8);
+      }
       if (++i == w.uw) {
         i = 0;
         m += w.G;
@@ -494,9 +501,9 @@ struct UnitStream {
     cp_commit();  // one group per call, empty or not, keeps the wait counts uniform
   }
   // the first kRingDepth units (weights only: may run before griddepcontrol.wait)
-  __device__ __forceinline__ void prefetch(uint8_t* ring, int slot_bytes, const SlabWork& w, int lane) {
+  __device__ __forceinline__ void prefetch(uint8_t* ring, int slot_bytes, const SlabWork&, int lane) {
 #pragma unroll
-    for (int d = 0; d < kRingDepth; ++d) fetch_next(ring + d * slot_bytes, w, lane);
+    for (int d = 0; d < kRingDepth; ++d) fetch_next(ring + d * slot_bytes, lane);
   }
 };
 
@@ -549,15 +556,15 @@ __device__ __forceinline__ void run_stream(UnitStream<FMT>& us, const SlabWork& 
         uint8_t* s1 = next_slot();
         unit_mma<FMT, NT>(acc, s0, s0 + 512 + lane * 8, bp, (k0 + i) * KU, lane, nt_used);
         unit_mma<FMT, NT>(acc, s1, s1 + 512 + lane * 8, bp, (k0 + i + 1) * KU, lane, nt_used);
-        us.fetch_next(s0, w, lane);  // refill both with the units kRingDepth ahead
-        us.fetch_next(s1, w, lane);
+        us.fetch_next(s0, lane);  // refill both with the units kRingDepth ahead
+        us.fetch_next(s1, lane);
       }
     }
     for (; i < w.uw; ++i) {
       cp_wait<kRingDepth - 1>();  // unit i has landed (this lane's bytes)
       uint8_t* s0 = next_slot();
       unit_mma<FMT, NT>(acc, s0, s0 + 512 + lane * 8, bp, (k0 + i) * KU, lane, nt_used);
-      us.fetch_next(s0, w, lane);  // refill it with the unit kRingDepth ahead
+      us.fetch_next(s0, lane);  // refill it with the unit kRingDepth ahead
     }
     float* rb = gred + par * w.ks * (NT * 128);
     {
