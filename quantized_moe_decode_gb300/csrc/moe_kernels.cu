@@ -34,15 +34,11 @@
 #include <cooperative_groups.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "launch.h"
 
 namespace uocr {
-
-__device__ __forceinline__ float argmax_key_value(unsigned long long k) {
-  const uint32_t u = (uint32_t)(k >> 32);
-  const uint32_t b = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
-  return __uint_as_float(b);
-}
 
 // Block-wide exclusive prefix sum of four counters (one value per thread).
 __device__ __forceinline__ int4 block_excl_scan4(int4 v, int4& total, int4* s_warp) {
@@ -92,44 +88,45 @@ __device__ __forceinline__ void topk_load(RowLogits& rl, const float* lg, int E,
     rl.v[q] = e < E ? __ldcg(lg + e) : -INFINITY;
   }
 }
-// Top-k by logit, lowest index first among equal logits; lane j < k gets the
-// j-th choice and its softmax weight renormalised over the k choices
-// (exp(l_j - l_0) / sum_i exp(l_i - l_0)).
-__device__ __forceinline__ void topk_select(const RowLogits& rl, int E, int k, int lane, int& e_j, float& w_j) {
-  bool taken[8];
+// Top-k by logit, lowest index first among equal logits, by ranking: the
+// rank of logit e is the number of logits that beat it (greater, or equal
+// with a lower index); e is chosen iff rank < k, and its slot is its rank.
+// All lanes compare their QN logits (experts lane + 32q) against every logit
+// broadcast from the other lanes: independent work, no serial argmax rounds.
+// Weights: exp(l_e - l_max) / sum over the chosen of exp(l - l_max).
+// Returns, per held logit q, its rank (>= k: not chosen) and weight.
+template <int QN>
+__device__ __forceinline__ void topk_rank(const RowLogits& rl, int E, int k, int lane, int (&rank)[QN],
+                                          float (&wt)[QN]) {
 #pragma unroll
-  for (int q = 0; q < 8; ++q) taken[q] = lane + 32 * q >= E;
-  float l0 = 0.f, wsum = 0.f, my_l = 0.f;
-  e_j = 0;
-  for (int j = 0; j < k; ++j) {
-    unsigned long long kb = 0ull;
+  for (int q = 0; q < QN; ++q) rank[q] = 0;
+  for (int src = 0; src < 32; ++src) {  // kept rolled: this code runs once per launch, cold
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (!taken[q]) {
-        const unsigned long long cc = argmax_key(rl.v[q], lane + 32 * q);
-        kb = cc > kb ? cc : kb;
+    for (int qs = 0; qs < QN; ++qs) {
+      const float o = __shfl_sync(0xffffffffu, rl.v[qs], src);
+      const int eo = src + 32 * qs;
+#pragma unroll
+      for (int q = 0; q < QN; ++q) {
+        const int em = lane + 32 * q;
+        rank[q] += (o > rl.v[q]) || (o == rl.v[q] && eo < em);
       }
     }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, kb, o);
-      kb = other > kb ? other : kb;
-    }
-    const int e = argmax_key_index(kb);
-    const float le = argmax_key_value(kb);
-    if ((e & 31) == lane) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (q == (e >> 5)) taken[q] = true;
-    }
-    if (j == 0) l0 = le;
-    wsum += expf(le - l0);
-    if (lane == j) {
-      e_j = e;
-      my_l = le;
-    }
   }
-  w_j = expf(my_l - l0) / wsum;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < QN; ++q) mx = fmaxf(mx, rl.v[q]);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float ex[QN], sum = 0.f;
+#pragma unroll
+  for (int q = 0; q < QN; ++q) {
+    ex[q] = (rank[q] < k && lane + 32 * q < E) ? expf(rl.v[q] - mx) : 0.f;
+    sum += ex[q];
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+#pragma unroll
+  for (int q = 0; q < QN; ++q) wt[q] = ex[q] / sum;
 }
 
 // Routing state of a CTA in shared memory.
@@ -237,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
     }
     __syncthreads();
     const int k = a.k;
+    const int qn = (E + 31) / 32;
     for (int r = warp; r < ntok; r += kWarps) {
       RowLogits rl;
 #pragma unroll
@@ -248,15 +246,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
           rl.v[q] = peer[r * 256 + e];
         }
       }
-      int ej;
-      float wj;
-      topk_select(rl, E, k, lane, ej, wj);
-      if (lane < k) {
-        a.idx[(tok0 + r) * k + lane] = ej;
-        a.wts[(tok0 + r) * k + lane] = wj;
-        atomicOr(&s_mask[ej], 1u << r);  // a row picks an expert at most once
-        atomicOr(&s_jbits[ej], (unsigned long long)lane << (3 * r));
-      }
+      auto emit = [&](auto qn_tag) {
+        constexpr int QN = decltype(qn_tag)::value;
+        int rk[QN];
+        float wt[QN];
+        topk_rank<QN>(rl, E, k, lane, rk, wt);
+#pragma unroll
+        for (int q = 0; q < QN; ++q) {
+          const int e = lane + 32 * q;
+          if (e < E && rk[q] < k) {
+            a.idx[(tok0 + r) * k + rk[q]] = e;
+            a.wts[(tok0 + r) * k + rk[q]] = wt[q];
+            atomicOr(&s_mask[e], 1u << r);  // a row picks an expert at most once
+            atomicOr(&s_jbits[e], (unsigned long long)rk[q] << (3 * r));
+          }
+        }
+      };
+      if (qn <= 2) emit(std::integral_constant<int, 2>{});
+      else if (qn <= 4) emit(std::integral_constant<int, 4>{});
+      else emit(std::integral_constant<int, 8>{});
     }
     __syncthreads();
     const int e = threadIdx.x;
