@@ -8,10 +8,13 @@
 // place).  For a row at position p the valid slots are a contiguous range:
 // [0, p] while p < P, else [0, P + min(p - P + 1, R)) (every ring slot
 // written for this sequence; softmax does not care about their order).  CTA
-// (split, head, row) takes one chunk of that range; each warp streams 4*G
-// slots per iteration with 16-byte loads (D/8 lanes per slot) and keeps an
-// online softmax; the last CTA of a (row, head) merges the splits with their
-// log-sum-exp weights and the sink, and writes the fp16 output.
+// (split, head, row) takes one chunk of that range, staged by TMA bulk copies;
+// each warp reads 4*G slots per iteration (D/8 lanes per slot) and keeps an
+// online softmax.  The splits of a (row, head) form a thread-block cluster:
+// each keeps its partial in shared memory, and after a cluster barrier every
+// CTA merges one slice of D from all partials with their log-sum-exp weights
+// and the sink, and writes the fp16 output.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "launch.h"
@@ -38,7 +41,7 @@ __global__ void __launch_bounds__(128) k_attn(const AttnArgs a) {
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * STAGE);
   __shared__ float sm_m[NW], sm_l[NW];
   __shared__ float sm_acc[NW][D];
-  __shared__ int s_last;
+  __shared__ float s_part[D + 2];
 
   const int split = blockIdx.x, head = blockIdx.y, row = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -93,8 +96,10 @@ __global__ void __launch_bounds__(128) k_attn(const AttnArgs a) {
       if (bad) atomicOr(a.status, kStatusTimeout);
     }
     if (__syncthreads_or(bad)) {
+      // the status word reports it; wait (bounded) for the copy still in flight, then
+      // join the cluster merge with what has been accumulated
       if (threadIdx.x == 0 && sb + 1 < n_sub) mbar_wait(bar + ((sb + 1) & 1), (uint32_t)(((sb + 1) >> 1) & 1));
-      return;
+      break;
     }
     const __half* Ks = reinterpret_cast<const __half*>(smem + (sb & 1) * STAGE);
     const __half* Vs = Ks + SUB * D;
@@ -181,11 +186,10 @@ __global__ void __launch_bounds__(128) k_attn(const AttnArgs a) {
   }
   __syncthreads();
 
-  // CTA merge -> split partial {m, l, acc[D]}
+  // CTA merge -> this split's partial {m, l, acc[D]} in shared memory
   float M = -INFINITY;
 #pragma unroll
   for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w]);
-  float* part = a.part + (((size_t)row * a.nh + head) * a.nsplit + split) * (D + 2);
   float wsc[NW];
 #pragma unroll
   for (int w = 0; w < NW; ++w) wsc[w] = (M == -INFINITY) ? 0.f : __expf(sm_m[w] - M);
@@ -193,53 +197,50 @@ __global__ void __launch_bounds__(128) k_attn(const AttnArgs a) {
     float L = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) L += sm_l[w] * wsc[w];
-    part[0] = M;
-    part[1] = L;
+    s_part[0] = M;
+    s_part[1] = L;
   }
   for (int d = threadIdx.x; d < D; d += blockDim.x) {
     float v = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) v += sm_acc[w][d] * wsc[w];
-    part[2 + d] = v;
+    s_part[2 + d] = v;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    int* ctr = a.counter + row * a.nh + head;
-    const int done = atomicAdd(ctr, 1);
-    s_last = (done == a.nsplit - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const float* pbase = a.part + ((size_t)row * a.nh + head) * a.nsplit * (D + 2);
+  // The splits of one (row, head) form a thread-block cluster: after the cluster
+  // barrier every CTA merges its slice of D from all splits' partials (distributed
+  // shared memory) with their log-sum-exp weights and the sink.
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  const int ns = a.nsplit;
   float Mt = a.sink ? a.sink[head] : -INFINITY;
-  for (int sp = 0; sp < a.nsplit; ++sp) Mt = fmaxf(Mt, __ldcg(pbase + (size_t)sp * (D + 2)));
+  for (int sp = 0; sp < ns; ++sp) Mt = fmaxf(Mt, cluster.map_shared_rank(s_part, sp)[0]);
   float Lt = a.sink ? __expf(a.sink[head] - Mt) : 0.f;
-  for (int sp = 0; sp < a.nsplit; ++sp) {
-    const float ms = __ldcg(pbase + (size_t)sp * (D + 2));
-    if (ms != -INFINITY) Lt += __ldcg(pbase + (size_t)sp * (D + 2) + 1) * __expf(ms - Mt);
+  for (int sp = 0; sp < ns; ++sp) {
+    const float* pp = cluster.map_shared_rank(s_part, sp);
+    if (pp[0] != -INFINITY) Lt += pp[1] * __expf(pp[0] - Mt);
   }
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+  const int d0 = split * D / ns, d1 = (split + 1) * D / ns;
+  for (int d = d0 + threadIdx.x; d < d1; d += blockDim.x) {
     float v = 0.f;
-    for (int sp = 0; sp < a.nsplit; ++sp) {
-      const float ms = __ldcg(pbase + (size_t)sp * (D + 2));
-      if (ms != -INFINITY) v += __ldcg(pbase + (size_t)sp * (D + 2) + 2 + d) * __expf(ms - Mt);
+    for (int sp = 0; sp < ns; ++sp) {
+      const float* pp = cluster.map_shared_rank(s_part, sp);
+      if (pp[0] != -INFINITY) v += pp[2 + d] * __expf(pp[0] - Mt);
     }
     a.out[(size_t)row * a.nh * D + head * D + d] = __float2half_rn(v / Lt);
   }
-  if (threadIdx.x == 0) atomicExch(a.counter + row * a.nh + head, 0);
+  cluster.sync();  // every CTA keeps its partial until all slices are merged
 }
 
 cudaError_t launch_attn(const AttnArgs& a, int rows, cudaStream_t st, bool pdl) {
   const dim3 grid(a.nsplit, a.nh, rows);
   const size_t sm = attn_smem_bytes(a.D);
   switch (a.D) {
-    case 16: return launch_kernel(k_attn<16>, grid, dim3(128), sm, st, pdl, a);
-    case 32: return launch_kernel(k_attn<32>, grid, dim3(128), sm, st, pdl, a);
-    case 64: return launch_kernel(k_attn<64>, grid, dim3(128), sm, st, pdl, a);
-    case 128: return launch_kernel(k_attn<128>, grid, dim3(128), sm, st, pdl, a);
-    case 256: return launch_kernel(k_attn<256>, grid, dim3(128), sm, st, pdl, a);
+    case 16: return launch_kernel_cluster(k_attn<16>, grid, dim3(128), sm, st, pdl, a.nsplit, a);
+    case 32: return launch_kernel_cluster(k_attn<32>, grid, dim3(128), sm, st, pdl, a.nsplit, a);
+    case 64: return launch_kernel_cluster(k_attn<64>, grid, dim3(128), sm, st, pdl, a.nsplit, a);
+    case 128: return launch_kernel_cluster(k_attn<128>, grid, dim3(128), sm, st, pdl, a.nsplit, a);
+    case 256: return launch_kernel_cluster(k_attn<256>, grid, dim3(128), sm, st, pdl, a.nsplit, a);
   }
   return cudaErrorInvalidValue;
 }

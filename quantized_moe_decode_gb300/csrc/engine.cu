@@ -80,7 +80,7 @@ struct Carver {
   }
 };
 
-constexpr int kMaxSplits = 32;
+constexpr int kMaxSplits = 8;  // attention splits of a (row, head): one portable thread-block cluster
 thread_local std::string g_create_err;  // text of the last failed uocr_create on this thread
 constexpr int kHistCap = 1024;
 
@@ -115,8 +115,6 @@ struct uocr_ctx {
   __half* x_in = nullptr;
   float* q = nullptr;
   __half* attn_out = nullptr;
-  float* attn_part = nullptr;
-  int* attn_counter = nullptr;
   __half* act_dense = nullptr;
   __half* xhat = nullptr;
   uint8_t* act_r = nullptr;  // B-fragment order, padded expert entries x Ie
@@ -284,8 +282,6 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
   ctx->x_in = cv.take<__half>((size_t)MR * H, r.activations);
   ctx->q = cv.take<float>((size_t)MR * S, r.activations);
   ctx->attn_out = cv.take<__half>((size_t)MR * S, r.activations);
-  ctx->attn_part = cv.take<float>((size_t)MR * c.n_heads * kMaxSplits * (c.head_dim + 2), r.activations);
-  ctx->attn_counter = cv.take<int>((size_t)MR * c.n_heads, r.activations);
   if (c.n_dense_layers > 0 || E == 0) ctx->act_dense = cv.take<__half>((size_t)MR * c.dense_inter, r.activations);
   if (ctx->any_moe()) {
     ctx->xhat = cv.take<__half>((size_t)MR * H, r.activations);
@@ -408,8 +404,6 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     aa.q = ctx->q;
     aa.kv = kvl;
     aa.pos = ctx->pos_buf;
-    aa.part = ctx->attn_part;
-    aa.counter = ctx->attn_counter;
     aa.out = ctx->attn_out;
     aa.sink = c.use_sink ? ctx->sinks + (size_t)l * c.n_heads : nullptr;
     aa.nh = c.n_heads;

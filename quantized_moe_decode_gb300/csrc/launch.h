@@ -113,8 +113,6 @@ struct AttnArgs {
   const float* q;           // [rows][nh][D]
   const __half* kv;         // layer base [rows][2][nh][SL][D]
   const int* pos;
-  float* part;              // [rows][nh][nsplit][D+2]
-  int* counter;             // [rows][nh]
   __half* out;              // [rows][nh*D]
   const float* sink;        // [nh] or nullptr
   int nh, D, P, R, SL, nsplit, chunk;
