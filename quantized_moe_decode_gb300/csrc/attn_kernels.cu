@@ -277,6 +277,16 @@ __global__ void k_embed(const EmbedArgs a) {
     a.out[(size_t)row * a.H + k] = f.x;
     a.out[(size_t)row * a.H + k + 1] = f.y;
   }
+  // rotary angles of this row's position (rotate-half RoPE): the angle is formed
+  // and reduced modulo 2 pi in double precision, then its cosine and sine in float
+  const int pos = max(a.pos[row], 0);
+  for (int j = threadIdx.x; j < a.half_d; j += blockDim.x) {
+    double ang = (double)pos * a.inv_freq[j];
+    ang -= 6.283185307179586 * rint(ang * 0.15915494309189535);
+    float sn, cs;
+    sincosf((float)ang, &sn, &cs);
+    a.rope[(size_t)row * a.half_d + j] = make_float2(cs, sn);
+  }
 }
 
 cudaError_t launch_embed(const EmbedArgs& a, int rows, cudaStream_t st) {

@@ -53,6 +53,14 @@ constexpr int kThreads = kConsumers;
 //   UOCR_PDL_LATE    kernels that let their dependents launch only after their
 //                    weight stream instead of at their start (bit mask:
 //                    1 GEMV, 2 router, 4 expert kernels, 8 attention)
+//   UOCR_KS_MAX      most warps that share one slab (8, 4, 2 or 1)
+#ifndef UOCR_KS_MAX
+#define UOCR_KS_MAX 8
+#endif
+//   UOCR_WARM_TOPK   1 = the router runs its top-k once before waiting (code warm-up)
+#ifndef UOCR_WARM_TOPK
+#define UOCR_WARM_TOPK 1
+#endif
 #ifndef UOCR_PDL_LATE
 #define UOCR_PDL_LATE 8
 #endif
@@ -60,6 +68,8 @@ constexpr int kRingDepth = UOCR_RING_DEPTH;
 constexpr int kMinBlocks = UOCR_MIN_BLOCKS;
 constexpr int kUnroll = UOCR_UNROLL;
 constexpr int kPdlLate = UOCR_PDL_LATE;
+constexpr int kKsMax = UOCR_KS_MAX;
+constexpr int kWarmTopk = UOCR_WARM_TOPK;
 enum PdlKernel : int { PDL_GEMV = 1, PDL_ROUTER = 2, PDL_EXPERT = 4, PDL_ATTN = 8 };
 static_assert(kRingDepth >= 2 && kRingDepth <= 16, "ring depth");
 static_assert(kUnroll == 1 || kUnroll == 2, "unroll");
@@ -442,7 +452,8 @@ struct SlabWork {
   int ks, uw, G, grp, rank;
 };
 __host__ __device__ __forceinline__ int warps_per_slab(int U) {
-  return (U & 7) == 0 ? 8 : (U & 3) == 0 ? 4 : (U & 1) == 0 ? 2 : 1;
+  const int ks = (U & 7) == 0 ? 8 : (U & 3) == 0 ? 4 : (U & 1) == 0 ? 2 : 1;
+  return ks < kKsMax ? ks : kKsMax;
 }
 __device__ __forceinline__ SlabWork slab_work(int first, int stride, int n, int U) {
   SlabWork w;

@@ -108,6 +108,7 @@ struct uocr_ctx {
   __half* final_norm = nullptr;
   DMat lm;
   double* inv_freq = nullptr;
+  float2* rope = nullptr;  // [max_rows][head_dim/2] (cos, sin) of the step's positions
   __half* kv = nullptr;
   size_t kv_layer = 0;  // elements per layer
   int S = 0, SL = 0;
@@ -216,7 +217,7 @@ static uocr_status check_config(uocr_ctx* ctx, const uocr_config& c) {
   {
     const int kmax = c.hidden > c.dense_inter ? (c.hidden > c.n_heads * c.head_dim ? c.hidden : c.n_heads * c.head_dim)
                                               : c.dense_inter;
-    if (plan_stream(2, F16, kmax, 16, c.head_dim / 2 * 8).bytes > kSmemLimit)
+    if (plan_stream(2, F16, kmax, 16, 16 * (c.head_dim / 2) * 8).bytes > kSmemLimit)
       return bad("a projection input is too long for the shared-memory activation tile");
   }
   if (c.prefix_len < 0 || c.ring_len < 1) return bad("prefix_len >= 0 and ring_len >= 1 required");
@@ -271,6 +272,7 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
     mat(ctx->lm, V, H, F16);
   }
   ctx->inv_freq = cv.take<double>(c.head_dim / 2, r.weights);
+  ctx->rope = cv.take<float2>((size_t)c.max_rows * (c.head_dim / 2), r.activations);
   ctx->sinks = cv.take<float>((size_t)Lc * c.n_heads, r.weights);
   // KV cache [L][MR][2][nh][SL][D]
   ctx->S = S;
@@ -368,6 +370,9 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
   ea.out = hid(0);
   ea.H = H;
   ea.V = c.vocab;
+  ea.inv_freq = ctx->inv_freq;
+  ea.rope = ctx->rope;
+  ea.half_d = c.head_dim / 2;
   ea.status = ctx->status;
   mark("embed", true);
   CK(launch_embed(ea, rows, st), "embed launch");
@@ -379,7 +384,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     // QKV + RoPE + in-place KV append
     GemvArgs qa{};
     qa.w = w.qkv.view();
-    qa.sp = plan_stream(nt, c.fmt_attn, H, nt * 8, (c.head_dim / 2) * 8);
+    qa.sp = plan_stream(nt, c.fmt_attn, H, nt * 8, nt * 8 * (c.head_dim / 2) * 8);
     qa.ntok = rows;
     qa.xf = hid(2 * l);
     qa.ld_src = H;
@@ -388,7 +393,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     qa.pos = ctx->pos_buf;
     qa.q_out = ctx->q;
     qa.kv = kvl;
-    qa.inv_freq = ctx->inv_freq;
+    qa.rope = ctx->rope;
     qa.nh = c.n_heads;
     qa.D = c.head_dim;
     qa.S = S;

@@ -72,10 +72,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
 
   pdl_wait();  // activations come from the previous kernel
   int* s_pos = reinterpret_cast<int*>(smem + p.rows_off);
-  double* s_freq = reinterpret_cast<double*>(smem + p.extra_off);
+  float2* s_rope = reinterpret_cast<float2*>(smem + p.extra_off);  // [NT*8][D/2] (cos, sin)
   if constexpr (EPI == EPI_QKV) {
     for (int i = threadIdx.x; i < ntok; i += blockDim.x) s_pos[i] = max(a.pos[tok0 + i], 0);
-    for (int i = threadIdx.x; i < a.D / 2; i += blockDim.x) s_freq[i] = a.inv_freq[i];
+    for (int i = threadIdx.x; i < ntok * (a.D / 2); i += blockDim.x) s_rope[i] = a.rope[(size_t)tok0 * (a.D / 2) + i];
   }
   if constexpr (EPI == EPI_LOGITS) {
     if (threadIdx.x < NT * 8) s_best[threadIdx.x] = 0ull;
@@ -124,12 +124,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
         const int dlo = 8 * js + pg, dhi = (a.D >> 1) + dlo;
         float vlo = lo, vhi = hi;
         if (sec < 2) {
-          double ang = (double)pos * s_freq[dlo];
-          ang -= 6.283185307179586 * rint(ang * 0.15915494309189535);
-          float sn, cs;
-          sincosf((float)ang, &sn, &cs);
-          vlo = lo * cs - hi * sn;
-          vhi = hi * cs + lo * sn;
+          const float2 r = s_rope[tok * (a.D / 2) + dlo];  // (cos, sin) of this position's angle
+          vlo = lo * r.x - hi * r.y;
+          vhi = hi * r.x + lo * r.y;
         }
         if (sec == 0) {
           float* qo = a.q_out + ((size_t)gt * a.nh + head) * a.D;

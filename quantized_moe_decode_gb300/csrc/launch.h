@@ -47,7 +47,7 @@ struct GemvArgs {
   const int* pos;
   float* q_out;             // [rows][nh][D]
   __half* kv;               // layer base [rows][2][nh][SL][D]
-  const double* inv_freq;   // [D/2]
+  const float2* rope;       // [rows][D/2] (cos, sin) of the step's positions
   int nh, D, S, P, R, SL;
   // EPI_LOGITS
   int n_valid;              // vocab
@@ -127,6 +127,10 @@ struct EmbedArgs {
   const int* pos;
   float* out;               // [rows][H]
   int H, V;
+  // the step's rotary table: rope[row][j] = (cos, sin) of pos * inv_freq[j]
+  const double* inv_freq;   // [half_d]
+  float2* rope;             // [rows][half_d]
+  int half_d;
   int* status;
 };
 

@@ -202,6 +202,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
   UnitStream<F16> us;
   us.start(a.w.q, a.w.s, w);
   us.prefetch(ring, p.slot, w, lane);
+  if (kWarmTopk && rank == 0 && E <= 64) {
+    // run the top-k once on placeholder logits while the previous kernel drains:
+    // it pulls the (once-per-launch, otherwise cold) code into the instruction cache
+    RowLogits rl;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) rl.v[q] = (float)((lane * 37 + q * 11) & 63);
+    int rk[2];
+    float wt[2];
+    topk_rank<2>(rl, E, a.k, lane, rk, wt);
+    if (wt[0] < -1.f) s_mask[lane] = (unsigned)rk[0];  // never true; keeps the work
+  }
   pdl_wait();
   stage_norm_rows(xs, p.ldx, a.h + (size_t)tok0 * H, H, ntok, NT * 8, a.norm_w, H, a.eps);
   __syncthreads();
