@@ -31,11 +31,11 @@ struct AttnCfg {
 int attn_smem_bytes(int D) { return 2 * (2 * (8192 / D) * D * 2) + 64; }
 
 template <int D>
-__global__ void __launch_bounds__(128) k_attn(const AttnArgs a) {
+__global__ void __launch_bounds__(UOCR_ATTN_WARPS * 32) k_attn(const AttnArgs a) {
   constexpr int LPS = D / 8;    // lanes per slot
   constexpr int G = 32 / LPS;   // slots per load instruction
   constexpr int SPI = 4 * G;    // slots per warp iteration
-  constexpr int NW = 4;
+  constexpr int NW = UOCR_ATTN_WARPS;
   constexpr int SUB = AttnCfg<D>::SUB, STAGE = AttnCfg<D>::STAGE;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * STAGE);
@@ -236,11 +236,11 @@ cudaError_t launch_attn(const AttnArgs& a, int rows, cudaStream_t st, bool pdl) 
   const dim3 grid(a.nsplit, a.nh, rows);
   const size_t sm = attn_smem_bytes(a.D);
   switch (a.D) {
-    case 16: return launch_kernel_cluster(k_attn<16>, grid, dim3(128), sm, st, pdl, a.nsplit, a);
-    case 32: return launch_kernel_cluster(k_attn<32>, grid, dim3(128), sm, st, pdl, a.nsplit, a);
-    case 64: return launch_kernel_cluster(k_attn<64>, grid, dim3(128), sm, st, pdl, a.nsplit, a);
-    case 128: return launch_kernel_cluster(k_attn<128>, grid, dim3(128), sm, st, pdl, a.nsplit, a);
-    case 256: return launch_kernel_cluster(k_attn<256>, grid, dim3(128), sm, st, pdl, a.nsplit, a);
+    case 16: return launch_kernel_cluster(k_attn<16>, grid, dim3(UOCR_ATTN_WARPS * 32), sm, st, pdl, a.nsplit, a);
+    case 32: return launch_kernel_cluster(k_attn<32>, grid, dim3(UOCR_ATTN_WARPS * 32), sm, st, pdl, a.nsplit, a);
+    case 64: return launch_kernel_cluster(k_attn<64>, grid, dim3(UOCR_ATTN_WARPS * 32), sm, st, pdl, a.nsplit, a);
+    case 128: return launch_kernel_cluster(k_attn<128>, grid, dim3(UOCR_ATTN_WARPS * 32), sm, st, pdl, a.nsplit, a);
+    case 256: return launch_kernel_cluster(k_attn<256>, grid, dim3(UOCR_ATTN_WARPS * 32), sm, st, pdl, a.nsplit, a);
   }
   return cudaErrorInvalidValue;
 }

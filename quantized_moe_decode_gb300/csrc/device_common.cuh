@@ -61,6 +61,10 @@ constexpr int kThreads = kConsumers;
 #ifndef UOCR_WARM_TOPK
 #define UOCR_WARM_TOPK 1
 #endif
+//   UOCR_ATTN_WARPS  warps per attention CTA (4 or 8)
+#ifndef UOCR_ATTN_WARPS
+#define UOCR_ATTN_WARPS 4
+#endif
 #ifndef UOCR_PDL_LATE
 #define UOCR_PDL_LATE 8
 #endif
@@ -251,10 +255,12 @@ __device__ __forceinline__ float half_hi(uint32_t u) { return __half2float(__ush
 
 // Activations staged in shared memory xs[row][ldx] (fp16), contiguous tokens.
 struct BSmem {
-  const __half* xs;
-  int ldx;
-  __device__ __forceinline__ void operator()(int nt, int kk, int lane, uint32_t (&b)[4]) const {
-    ldsm_x4(b, xs + (nt * 8 + (lane & 7)) * ldx + kk + 8 * (lane >> 3));
+  const __half* base;  // this lane's ldmatrix row address at kk = 0, n-tile 0
+  int nt_stride;       // halves between n-tiles (8 rows)
+  __device__ __forceinline__ BSmem(const __half* xs, int ldx)
+      : base(xs + (threadIdx.x & 7) * ldx + 8 * ((threadIdx.x & 31) >> 3)), nt_stride(8 * ldx) {}
+  __device__ __forceinline__ void operator()(int nt, int kk, int, uint32_t (&b)[4]) const {
+    ldsm_x4(b, base + nt * nt_stride + kk);
   }
 };
 

@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
   }
   __syncthreads();
 
-  const BSmem bp{xs, p.ldx};
+  const BSmem bp(xs, p.ldx);
   auto epi = [&](int s, const float* rb, int tid, int nthr) {
     for (int i = tid; i < NT * 64; i += nthr) {
       const int tok = i >> 3, pg = i & 7;

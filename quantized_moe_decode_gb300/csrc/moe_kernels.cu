@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
   pdl_wait();
   stage_norm_rows(xs, p.ldx, a.h + (size_t)tok0 * H, H, ntok, NT * 8, a.norm_w, H, a.eps);
   __syncthreads();
-  const BSmem bp{xs, p.ldx};
+  const BSmem bp(xs, p.ldx);
   auto epi = [&](int sl, const float* rb, int tid, int nthr) {
     for (int i = tid; i < NT * 64; i += nthr) {
       const int tok = i >> 3, pg = i & 7;
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
   stage_norm_gather(xs, p.ldx, a.h, a.H, rows, ntk, NT * 8, a.norm_w, a.H, a.eps);
   __syncthreads();
   const int nt_used = (ntk + 7) >> 3;
-  const BSmem bp{xs, p.ldx};
+  const BSmem bp(xs, p.ldx);
   if (ec.shared) {
     auto epi = [&](int sl, const float* rb, int tid, int nthr) {
       for (int i = tid; i < NT * 64; i += nthr) {
