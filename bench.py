@@ -200,6 +200,26 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ replicas
+# With N GPUs the path runs as N independent replicas (rows need no exchange):
+# every rank times its own steps, the job's time is the slowest rank's, and
+# the job processed world x rows x steps tokens in it.
+def max_over_ranks(x, dist, device):
+    """The maximum of a per-rank float over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, rows, steps, seconds):
+    """Whole-job tokens/s of `world` replicas of `rows` rows over `steps` steps."""
+    return world * rows * steps / seconds
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, rank, world):
     import torch
@@ -271,11 +291,7 @@ def run_ours(args, rank, world):
     if dist:
         dist.barrier()
     clocks = clk.stop()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     ctx.uocr_sync()
     gen_ids = out[:K].cpu().numpy()
     step_pos = start + W + K
@@ -307,7 +323,7 @@ def run_ours(args, rank, world):
     achieved = dk["gbs"]
     step_bytes = sum(sum(v) for v in cb.values())
     ms_per_step = ms / K
-    value = world * rows * K / (ms * 1e-3)
+    value = replica_throughput(world, rows, K, ms * 1e-3)
 
     # ---- end to end through the host-buffer entry point (pinned host buffers)
     K_e2e = min(K, 200)
@@ -326,12 +342,9 @@ def run_ours(args, rank, world):
         if st_ != 0:
             raise RuntimeError(lib.uocr_last_error(ctx.h).decode())
         h_ids.copy_(h_out)
-    e2e_s = time.perf_counter() - t0
-    if dist:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": world * rows * K_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": rows * 4 * 2,
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
+    e2e = {"value": replica_throughput(world, rows, K_e2e, e2e_s), "unit": "tokens/s",
+           "h2d_bytes_per_step": rows * 4 * 2,
            "d2h_bytes_per_step": rows * 4, "steps": K_e2e}
 
     if rank != 0:
