@@ -65,6 +65,10 @@ constexpr int kThreads = kConsumers;
 #ifndef UOCR_ATTN_WARPS
 #define UOCR_ATTN_WARPS 4
 #endif
+//   UOCR_COMBINE_B   outputs per thread per batch of loads in the expert combine
+#ifndef UOCR_COMBINE_B
+#define UOCR_COMBINE_B 6
+#endif
 #ifndef UOCR_PDL_LATE
 #define UOCR_PDL_LATE 8
 #endif

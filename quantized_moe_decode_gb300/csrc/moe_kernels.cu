@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
   const int nlast = rs.nlast;
   if (nlast == 0) return;
   __threadfence();
-  constexpr int B = 4;  // items per thread per batch: loads first, then sums
+  constexpr int B = UOCR_COMBINE_B;  // items per thread per batch: loads first, then sums
   const int items = nlast * rows * 16;
   for (int i0 = threadIdx.x; i0 < items; i0 += B * kThreads) {
     float pr[B][8], ps[B], hv[B];
