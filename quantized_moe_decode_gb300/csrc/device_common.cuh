@@ -66,8 +66,13 @@ constexpr int kThreads = kConsumers;
 #define UOCR_ATTN_WARPS 4
 #endif
 //   UOCR_COMBINE_B   outputs per thread per batch of loads in the expert combine
+//                    (fewer when more CTAs per SM leave fewer registers per thread)
 #ifndef UOCR_COMBINE_B
+#if UOCR_MIN_BLOCKS >= 3
+#define UOCR_COMBINE_B 3
+#else
 #define UOCR_COMBINE_B 6
+#endif
 #endif
 #ifndef UOCR_PDL_LATE
 #define UOCR_PDL_LATE 8
@@ -120,6 +125,16 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// d = a * b (a zero accumulator operand instead of a zeroed register quad)
+__device__ __forceinline__ void mma_16816_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  const float z = 0.f;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
@@ -388,8 +403,8 @@ __device__ __forceinline__ void unit_mma(float (&acc)[NT][4], const uint8_t* a, 
       if (NT == 1 || nt < nt_used) {
         uint32_t B[4];
         bp(nt, kk, lane, B);
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_16816(c, A0, B[0], B[1]);
+        float c[4];
+        mma_16816_z(c, A0, B[0], B[1]);
         mma_16816(c, A1, B[2], B[3]);
         if constexpr (FMT == I8ASYM) {
           float s0, s1;
@@ -421,15 +436,15 @@ __device__ __forceinline__ void unit_mma(float (&acc)[NT][4], const uint8_t* a, 
         uint32_t B0[4], B1[4];
         bp(nt, kk, lane, B0);
         bp(nt, kk + 32, lane, B1);
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_16816(c, A[0], B0[0], B0[1]);
+        float c[4];
+        mma_16816_z(c, A[0], B0[0], B0[1]);
         mma_16816(c, A[1], B0[2], B0[3]);
         acc[nt][0] = fmaf(d0_lo, c[0], acc[nt][0]);
         acc[nt][1] = fmaf(d0_lo, c[1], acc[nt][1]);
         acc[nt][2] = fmaf(d0_hi, c[2], acc[nt][2]);
         acc[nt][3] = fmaf(d0_hi, c[3], acc[nt][3]);
-        float e[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_16816(e, A[2], B1[0], B1[1]);
+        float e[4];
+        mma_16816_z(e, A[2], B1[0], B1[1]);
         mma_16816(e, A[3], B1[2], B1[3]);
         acc[nt][0] = fmaf(d1_lo, e[0], acc[nt][0]);
         acc[nt][1] = fmaf(d1_lo, e[1], acc[nt][1]);
@@ -611,8 +626,9 @@ __device__ __forceinline__ void run_stream(UnitStream<FMT>& us, const SlabWork& 
 // latency, not one per element, is paid per batch.
 
 // One warp: dst[:] = fp16(src[:] * rsqrt(mean(src^2) + eps) * w[:]).  A row of
-// up to 2048 values is held in registers (16 float4 per lane); longer rows are
-// read twice.
+// up to 32*4*kNormRegs values (1280 for the decoders here) is held in
+// registers; longer rows are read twice.
+constexpr int kNormRegs = 10;
 __device__ __forceinline__ void stage_norm_rows_one(__half* dst, const float* srcf, const __half* w, int K, float eps) {
   const int lane = threadIdx.x & 31;
   const int n4 = K / 4;
@@ -624,18 +640,18 @@ __device__ __forceinline__ void stage_norm_rows_one(__half* dst, const float* sr
     d[0] = __floats2half2_rn(v.x * r * __low2float(w0), v.y * r * __high2float(w0));
     d[1] = __floats2half2_rn(v.z * r * __low2float(w1), v.w * r * __high2float(w1));
   };
-  if (n4 <= 16 * 32) {
-    float4 v[16];
+  if (n4 <= kNormRegs * 32) {
+    float4 v[kNormRegs];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = (lane + 32 * i < n4) ? src[lane + 32 * i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < kNormRegs; ++i) v[i] = (lane + 32 * i < n4) ? src[lane + 32 * i] : make_float4(0.f, 0.f, 0.f, 0.f);
     float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    for (int i = 0; i < kNormRegs; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
 #pragma unroll
     for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float r = rsqrtf(ss / (float)K + eps);
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < kNormRegs; ++i)
       if (lane + 32 * i < n4) store(lane + 32 * i, v[i], r);
   } else {
     float ss = 0.f;

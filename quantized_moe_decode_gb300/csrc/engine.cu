@@ -126,6 +126,7 @@ struct uocr_ctx {
   float* r_logits = nullptr;
   int *r_idx = nullptr, *r_count = nullptr, *r_offset = nullptr, *r_perm = nullptr, *r_inv = nullptr;
   int4* r_rec = nullptr;  // [L][token groups][E] routing records
+  int* r_nact = nullptr;  // [L][token groups] experts that received a token (records by active slot)
 
   float* r_w = nullptr;
   float* sinks = nullptr;
@@ -301,6 +302,7 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
     ctx->r_perm = cv.take<int>((size_t)Lc * MR * k, r.routing);
     ctx->r_inv = cv.take<int>((size_t)Lc * MR * k, r.routing);
     ctx->r_rec = cv.take<int4>((size_t)Lc * TG * E, r.routing);
+    ctx->r_nact = cv.take<int>((size_t)Lc * TG, r.routing);
   }
   if (V > 0) {
     ctx->logits = cv.take<float>((size_t)MR * V, r.logits);
@@ -502,6 +504,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       ra.idx = ctx->r_idx + (size_t)l * MR * k;
       ra.wts = ctx->r_w + (size_t)l * MR * k;
       ra.rec = rec;
+      ra.n_act = ctx->r_nact + (size_t)l * ((MR + 15) / 16);
       ra.status = ctx->status;
       mark("router", true);
       CK(launch_router(ra, st, pdl), "router launch");
@@ -517,6 +520,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       xa.Ish = c.n_shared * c.expert_inter;
       xa.tg = tg;
       xa.rec = rec;
+      xa.n_act = ra.n_act;
       xa.idx = ra.idx;
       xa.wts = ra.wts;
       xa.count = ctx->r_count + (size_t)l * E;
@@ -554,6 +558,10 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
         };
         xa.cpe = parts(gt * br / tot, rslabs, r.U);
         xa.cpes = sh ? parts(gt * bs / tot, sslabs, sh->U) : 0;
+        // active-slot units: the routed CTAs fill the rest of the wave and are
+        // dealt out over the experts that did receive a token (at least one each)
+        const int rest = gt - xa.cpes;
+        xa.n_rctas = by_slot ? (rest > n_units ? rest : n_units) : 0;
       };
       const DMat* shg = c.n_shared > 0 ? &w.sh_gateup : nullptr;
       const DMat* shd = c.n_shared > 0 ? &w.sh_down : nullptr;

@@ -76,6 +76,7 @@ struct RouterArgs {
   int* idx;                 // out: [rows][k] chosen experts
   float* wts;               // out: [rows][k] renormalised weights
   int4* rec;                // out: [tg][n_units] {expert or -1, 16-row mask, slot bits 0-31, slot bits 32-47}
+  int* n_act;               // out: [tg] experts that received a token (records by active slot)
   int* status;
 };
 
@@ -86,9 +87,11 @@ struct ExpertArgs {
   int ntok, E, k, H, Ie, Ish;
   int by_slot;              // routed CTAs by active slot (1) or by expert id (0)
   int n_units;              // routed units of the grid: max active experts (by slot) or E
-  int cpe, cpes;            // CTAs per routed unit, for the shared experts
+  int cpe, cpes;            // CTAs per routed unit (expert ids), for the shared experts
+  int n_rctas;              // routed CTAs of the grid when units are active slots (>= n_units)
   int tg;                   // token groups of 16 rows (blockIdx.y)
   const int4* rec;          // [tg][n_units] routing records written by the router
+  const int* n_act;         // [tg] active slots (written by the router when units are active slots)
   const int* idx;           // [rows][k] chosen experts (router)
   const float* wts;         // [rows][k] renormalised weights (router)
   // grouping: written by the gate/up launch (CTA 0, 0) from idx
@@ -198,6 +201,9 @@ cudaError_t allow_max_dyn_smem(void (*kern)(KArgs...)) {
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+  // all of the unified L1/shared array as shared memory: the streaming kernels
+  // keep their weight rings there and bypass L1 for the weights
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   return e;
 }
 

@@ -287,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
       const int4 ex = block_excl_scan4(make_int4(mk != 0u, 0, 0, 0), tot, s_scan);
       if (mk) rec[ex.x] = make_int4(e, (int)mk, (int)(uint32_t)jb, (int)(uint32_t)(jb >> 32));
       for (int i = tot.x + threadIdx.x; i < a.n_units; i += kThreads) rec[i] = make_int4(-1, 0, 0, 0);
+      if (threadIdx.x == 0) a.n_act[g] = tot.x;
     } else if (e < E) {
       rec[e] = make_int4(mk ? e : -1, (int)mk, (int)(uint32_t)jb, (int)(uint32_t)(jb >> 32));
     }
@@ -296,9 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
 
 // ------------------------------------------------------------------ expert CTAs
 // blockIdx.x < ns (= cpes when there are shared experts, else 0): part x of
-// the shared experts.  Then routed CTAs: unit i = (x - ns) / cpe (expert id i,
-// or active slot i), part (x - ns) % cpe of its slabs.  blockIdx.y: token
-// group of 16 rows.
+// the shared experts.  Then routed CTAs.  With expert-id units: unit i =
+// (x - ns) / cpe, part (x - ns) % cpe of its slabs.  With active-slot units
+// the n_rctas routed CTAs are dealt out over the n active slots once the
+// router has counted them (slot_assign): every routed CTA has work and the
+// grid is one wave whatever the number of experts that received a token.
+// blockIdx.y: token group of 16 rows.
 struct ExpertCta {
   bool shared;
   int i, part, parts;
@@ -312,6 +316,10 @@ __device__ __forceinline__ ExpertCta expert_cta(const ExpertArgs& a) {
     c.i = -1;
     c.part = x;
     c.parts = a.cpes;
+  } else if (a.by_slot) {  // known after the router: slot_assign
+    c.i = -1;
+    c.part = 0;
+    c.parts = 1;
   } else {
     c.i = (x - ns) / a.cpe;
     c.part = (x - ns) - c.i * a.cpe;
@@ -320,12 +328,45 @@ __device__ __forceinline__ ExpertCta expert_cta(const ExpertArgs& a) {
   return c;
 }
 
+// R routed CTAs over n active slots (1 <= n <= R, which the host guarantees by
+// launching at least as many routed CTAs as experts can receive a token): the
+// first R % n slots get R / n + 1 CTAs, the others R / n, in slot order.
+__device__ __forceinline__ void slot_assign(int xr, int R, int n, ExpertCta& c) {
+  const int base = R / n, rem = R - base * n;
+  const int cut = rem * (base + 1);
+  if (xr < cut) {
+    c.i = xr / (base + 1);
+    c.part = xr - c.i * (base + 1);
+    c.parts = base + 1;
+  } else {
+    const int y = xr - cut;
+    c.i = rem + y / base;
+    c.part = y - (c.i - rem) * base;
+    c.parts = base;
+  }
+}
+__device__ __forceinline__ void assign_routed(const ExpertArgs& a, int g, ExpertCta& c) {
+  if (c.shared || !a.by_slot) return;
+  const int n = __ldcg(a.n_act + g);
+  const int ns = a.ws.n_slabs > 0 ? a.cpes : 0;
+  if (n < 1 || n > a.n_rctas) {  // cannot happen (n_rctas >= most experts a group can pick)
+    c.i = -1;
+    return;
+  }
+  slot_assign((int)blockIdx.x - ns, a.n_rctas, n, c);
+}
+
 // Slabs [lo, hi) of part `part` of `parts`: n slabs cut in runs of gran (the
 // slabs of one round of a CTA) so that every group of warps gets whole rounds.
+// Each part takes ceil(rounds / parts) rounds; the parts this leaves without
+// a round (e.g. the 8th of 8 parts of 20 rounds) get none, which keeps the
+// longest part as short as an even split would and leaves their SM to the
+// CTAs that have work.
 __device__ __forceinline__ void part_range(int n, int gran, int part, int parts, int& lo, int& hi) {
   const int nr = (n + gran - 1) / gran;
-  lo = min(n, gran * (int)(((long long)nr * part) / parts));
-  hi = min(n, gran * (int)(((long long)nr * (part + 1)) / parts));
+  const int per = (nr + parts - 1) / parts;
+  lo = min(n, gran * min(nr, part * per));
+  hi = min(n, gran * min(nr, (part + 1) * per));
 }
 __device__ __forceinline__ int groups_of(int U) { return kWarps / warps_per_slab(U); }
 
@@ -342,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
   uint8_t* ring = smem + p.ring_off + (size_t)warp * kRingDepth * p.slot;
 
   if (!(kPdlLate & PDL_EXPERT)) pdl_launch_dependents();
-  const ExpertCta ec = expert_cta(a);
+  ExpertCta ec = expert_cta(a);
   const int g = blockIdx.y, tok0 = g * 16;
   const int ng = min(16, a.ntok - tok0);  // rows of this token group
   int s0 = 0, s1 = 0;
@@ -366,12 +407,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
   pdl_wait();
 
   if (blockIdx.x == 0 && blockIdx.y == 0) write_grouping(rs, a);
+  assign_routed(a, g, ec);
   // this CTA's rows
   int e = -1, ntk = ng;
   if (ec.shared) {
     for (int t = threadIdx.x; t < ng; t += kThreads) rows[t] = tok0 + t;
   } else {
-    const int4 r = a.rec[(size_t)g * a.n_units + ec.i];  // {expert, row mask, slot bits}
+    const int4 r = ec.i >= 0 ? a.rec[(size_t)g * a.n_units + ec.i] : make_int4(-1, 0, 0, 0);  // {expert, row mask, slot bits}
     e = r.x;
     const unsigned mask = (unsigned)r.y;
     ntk = e >= 0 ? __popc(mask) : 0;
@@ -383,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
       rows[__popc(mask & ((1u << threadIdx.x) - 1u))] = tok0 + threadIdx.x;
     if (a.by_slot) {
       part_range(a.wr.n_slabs, groups_of(a.wr.U), ec.part, ec.parts, s0, s1);
+      if (s0 == s1) return;  // a part without a round (nothing in flight yet)
       w = slab_work(s0, 1, s1 - s0, a.wr.U);
       usr.start(a.wr.q + (size_t)e * a.wr.q_stride, a.wr.s + (size_t)e * a.wr.s_stride, w);
       usr.prefetch(ring, p.slot, w, lane);
@@ -437,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
   uint8_t* ring = smem + p.ring_off + (size_t)warp * kRingDepth * p.slot;
 
   if (!(kPdlLate & PDL_EXPERT)) pdl_launch_dependents();
-  const ExpertCta ec = expert_cta(a);
+  ExpertCta ec = expert_cta(a);
   const int g = blockIdx.y, tok0 = g * 16, H = a.H, k = a.k, rows = a.ntok;
   int s0 = 0, s1 = 0;
   SlabWork w;
@@ -467,6 +510,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
     if (c) atomicAdd(&rs.contrib, c);
   }
   for (int i = threadIdx.x; i < rows * k; i += kThreads) rs.w[i] = __ldcg(a.wts + i);  // combine weights
+  assign_routed(a, g, ec);
   int e = -1, ntk, k32;
   const uint8_t* bsrc;
   if (ec.shared) {
@@ -474,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
     k32 = a.Ish >> 5;
     bsrc = a.act_s + (size_t)(tok0 >> 3) * k32 * 512;
   } else {
-    const int4 r = a.rec[(size_t)g * a.n_units + ec.i];  // {expert, row mask, slot bits}
+    const int4 r = ec.i >= 0 ? a.rec[(size_t)g * a.n_units + ec.i] : make_int4(-1, 0, 0, 0);  // {expert, row mask, slot bits}
     e = r.x;
     const unsigned mask = (unsigned)r.y;
     ntk = e >= 0 ? __popc(mask) : 0;
@@ -491,6 +535,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
     bsrc = a.act_r + (size_t)((e * a.tg + g) * 2) * k32 * 512;
     if (a.by_slot) {
       part_range(H / 16, groups_of(a.wr.U), ec.part, ec.parts, s0, s1);
+      if (s0 == s1) return;  // a part without a round (nothing in flight yet)
       w = slab_work(s0, 1, s1 - s0, a.wr.U);
       usr.start(a.wr.q + (size_t)e * a.wr.q_stride, a.wr.s + (size_t)e * a.wr.s_stride, w);
       usr.prefetch(ring, p.slot, w, lane);
@@ -581,7 +626,7 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t st, bool pdl) {
   X(Q8_0, Q8_0, NT_) X(Q4_0, Q8_0, NT_) X(Q4_0, Q4_0, NT_) X(Q8_0, Q4_0, NT_) X(I8ASYM, I8ASYM, NT_)
 
 static dim3 expert_grid(const ExpertArgs& a) {
-  return dim3((a.ws.n_slabs > 0 ? a.cpes : 0) + a.n_units * a.cpe, a.tg);
+  return dim3((a.ws.n_slabs > 0 ? a.cpes : 0) + (a.by_slot ? a.n_rctas : a.n_units * a.cpe), a.tg);
 }
 
 cudaError_t launch_expert_gateup(int fr, int fs, const ExpertArgs& a, cudaStream_t st, bool pdl) {
