@@ -629,16 +629,35 @@ __device__ __forceinline__ void run_stream(UnitStream<FMT>& us, const SlabWork& 
 // up to 32*4*kNormRegs values (1280 for the decoders here) is held in
 // registers; longer rows are read twice.
 constexpr int kNormRegs = 10;
-__device__ __forceinline__ void stage_norm_rows_one(__half* dst, const float* srcf, const __half* w, int K, float eps) {
+
+// This lane's norm weights for the register path (elements 4f..4f+3 for f =
+// lane + 32 i).  The norm weights never change during a step, so kernels load
+// them before griddepcontrol.wait and the staging after it waits for the
+// activations alone.
+struct NormW {
+  uint2 v[kNormRegs];
+};
+__device__ __forceinline__ void load_norm_w(NormW& nw, const __half* w, int K) {
+  const int lane = threadIdx.x & 31, n4 = K / 4;
+#pragma unroll
+  for (int i = 0; i < kNormRegs; ++i)
+    nw.v[i] = (n4 <= kNormRegs * 32 && lane + 32 * i < n4) ? *reinterpret_cast<const uint2*>(w + 4 * (lane + 32 * i))
+                                                           : make_uint2(0u, 0u);
+}
+
+__device__ __forceinline__ void stage_norm_rows_one(__half* dst, const float* srcf, const __half* w, const NormW& nw,
+                                                    int K, float eps) {
   const int lane = threadIdx.x & 31;
   const int n4 = K / 4;
   const float4* src = reinterpret_cast<const float4*>(srcf);
-  auto store = [&](int f, const float4& v, float r) {
-    const __half2 w0 = *reinterpret_cast<const __half2*>(w + 4 * f);
-    const __half2 w1 = *reinterpret_cast<const __half2*>(w + 4 * f + 2);
+  auto store_w = [&](int f, const float4& v, float r, uint2 wv) {
+    const __half2 w0 = u32_h2(wv.x), w1 = u32_h2(wv.y);
     __half2* d = reinterpret_cast<__half2*>(dst + 4 * f);
     d[0] = __floats2half2_rn(v.x * r * __low2float(w0), v.y * r * __high2float(w0));
     d[1] = __floats2half2_rn(v.z * r * __low2float(w1), v.w * r * __high2float(w1));
+  };
+  auto store = [&](int f, const float4& v, float r) {
+    store_w(f, v, r, *reinterpret_cast<const uint2*>(w + 4 * f));
   };
   if (n4 <= kNormRegs * 32) {
     float4 v[kNormRegs];
@@ -652,7 +671,7 @@ __device__ __forceinline__ void stage_norm_rows_one(__half* dst, const float* sr
     const float r = rsqrtf(ss / (float)K + eps);
 #pragma unroll
     for (int i = 0; i < kNormRegs; ++i)
-      if (lane + 32 * i < n4) store(lane + 32 * i, v[i], r);
+      if (lane + 32 * i < n4) store_w(lane + 32 * i, v[i], r, nw.v[i]);
   } else {
     float ss = 0.f;
     for (int f0 = 0; f0 < n4; f0 += 8 * 32) {
@@ -678,11 +697,11 @@ __device__ __forceinline__ void stage_norm_rows_one(__half* dst, const float* sr
 
 // xs[tk][:] = normalised x[tk][:] for tk < ntok, zero rows up to ntok_pad (one warp per row).
 __device__ __forceinline__ void stage_norm_rows(__half* xs, int ldx, const float* x, int ldx_g, int ntok, int ntok_pad,
-                                                const __half* w, int K, float eps) {
+                                                const __half* w, const NormW& nwr, int K, float eps) {
   const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   for (int tk = warp; tk < ntok_pad; tk += nw) {
     if (tk < ntok)
-      stage_norm_rows_one(xs + tk * ldx, x + (size_t)tk * ldx_g, w, K, eps);
+      stage_norm_rows_one(xs + tk * ldx, x + (size_t)tk * ldx_g, w, nwr, K, eps);
     else
       for (int i = (threadIdx.x & 31); i < K / 8; i += 32)
         *reinterpret_cast<uint4*>(xs + tk * ldx + 8 * i) = make_uint4(0u, 0u, 0u, 0u);
@@ -691,12 +710,13 @@ __device__ __forceinline__ void stage_norm_rows(__half* xs, int ldx, const float
 
 // stage_norm_rows over gathered rows: xs[t] = norm(x[rows[t]]) for t < ntok.
 __device__ __forceinline__ void stage_norm_gather(__half* xs, int ldx, const float* x, int ldx_g, const int* rows,
-                                                  int ntok, int ntok_pad, const __half* w, int K, float eps) {
+                                                  int ntok, int ntok_pad, const __half* w, const NormW& nwr, int K,
+                                                  float eps) {
   const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   for (int tk = warp; tk < ntok_pad; tk += nw) {
     // one row at a time through the contiguous routine (it handles zero padding)
     if (tk < ntok)
-      stage_norm_rows_one(xs + tk * ldx, x + (size_t)rows[tk] * ldx_g, w, K, eps);
+      stage_norm_rows_one(xs + tk * ldx, x + (size_t)rows[tk] * ldx_g, w, nwr, K, eps);
     else
       for (int i = (threadIdx.x & 31); i < K / 8; i += 32)
         *reinterpret_cast<uint4*>(xs + tk * ldx + 8 * i) = make_uint4(0u, 0u, 0u, 0u);

@@ -69,6 +69,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
   UnitStream<FMT> us;
   us.start(a.w.q, a.w.s, w);
   us.prefetch(ring, p.slot, w, lane);
+  NormW nw;
+  if constexpr (SRC == SRC_NORM) load_norm_w(nw, a.norm_w, K);
 
   pdl_wait();  // activations come from the previous kernel
   int* s_pos = reinterpret_cast<int*>(smem + p.rows_off);
@@ -81,7 +83,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
     if (threadIdx.x < NT * 8) s_best[threadIdx.x] = 0ull;
   }
   if constexpr (SRC == SRC_NORM) {
-    stage_norm_rows(xs, p.ldx, a.xf + (size_t)tok0 * a.ld_src, a.ld_src, ntok, NT * 8, a.norm_w, K, a.eps);
+    stage_norm_rows(xs, p.ldx, a.xf + (size_t)tok0 * a.ld_src, a.ld_src, ntok, NT * 8, a.norm_w, nw, K, a.eps);
   } else {
     stage_f16(xs, p.ldx, a.xh + (size_t)tok0 * a.ld_src, a.ld_src, ntok, NT * 8, K);
   }

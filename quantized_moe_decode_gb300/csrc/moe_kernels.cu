@@ -213,8 +213,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
     topk_rank<2>(rl, E, a.k, lane, rk, wt);
     if (wt[0] < -1.f) s_mask[lane] = (unsigned)rk[0];  // never true; keeps the work
   }
+  NormW nw;
+  load_norm_w(nw, a.norm_w, H);
   pdl_wait();
-  stage_norm_rows(xs, p.ldx, a.h + (size_t)tok0 * H, H, ntok, NT * 8, a.norm_w, H, a.eps);
+  stage_norm_rows(xs, p.ldx, a.h + (size_t)tok0 * H, H, ntok, NT * 8, a.norm_w, nw, H, a.eps);
   __syncthreads();
   const BSmem bp(xs, p.ldx);
   auto epi = [&](int sl, const float* rb, int tid, int nthr) {
@@ -404,6 +406,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
     usr.prefetch(ring, p.slot, w, lane);
     streaming = true;
   }
+  NormW nw;
+  load_norm_w(nw, a.norm_w, a.H);
   pdl_wait();
 
   if (blockIdx.x == 0 && blockIdx.y == 0) write_grouping(rs, a);
@@ -433,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
   }
   __syncthreads();
   // the expert's rows, normalised, packed into consecutive tokens
-  stage_norm_gather(xs, p.ldx, a.h, a.H, rows, ntk, NT * 8, a.norm_w, a.H, a.eps);
+  stage_norm_gather(xs, p.ldx, a.h, a.H, rows, ntk, NT * 8, a.norm_w, nw, a.H, a.eps);
   __syncthreads();
   const int nt_used = (ntk + 7) >> 3;
   const BSmem bp(xs, p.ldx);
