@@ -126,7 +126,6 @@ struct uocr_ctx {
   float* r_logits = nullptr;
   int *r_idx = nullptr, *r_count = nullptr, *r_offset = nullptr, *r_perm = nullptr, *r_inv = nullptr;
   int4* r_rec = nullptr;  // [L][token groups][E] routing records
-  int* r_nact = nullptr;  // [L][token groups] experts that received a token (records by active slot)
 
   float* r_w = nullptr;
   float* sinks = nullptr;
@@ -302,7 +301,6 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
     ctx->r_perm = cv.take<int>((size_t)Lc * MR * k, r.routing);
     ctx->r_inv = cv.take<int>((size_t)Lc * MR * k, r.routing);
     ctx->r_rec = cv.take<int4>((size_t)Lc * TG * E, r.routing);
-    ctx->r_nact = cv.take<int>((size_t)Lc * TG, r.routing);
   }
   if (V > 0) {
     ctx->logits = cv.take<float>((size_t)MR * V, r.logits);
@@ -504,7 +502,6 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       ra.idx = ctx->r_idx + (size_t)l * MR * k;
       ra.wts = ctx->r_w + (size_t)l * MR * k;
       ra.rec = rec;
-      ra.n_act = ctx->r_nact + (size_t)l * ((MR + 15) / 16);
       ra.status = ctx->status;
       mark("router", true);
       CK(launch_router(ra, st, pdl), "router launch");
@@ -520,7 +517,6 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       xa.Ish = c.n_shared * c.expert_inter;
       xa.tg = tg;
       xa.rec = rec;
-      xa.n_act = ra.n_act;
       xa.idx = ra.idx;
       xa.wts = ra.wts;
       xa.count = ctx->r_count + (size_t)l * E;

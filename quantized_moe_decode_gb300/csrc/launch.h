@@ -76,7 +76,6 @@ struct RouterArgs {
   int* idx;                 // out: [rows][k] chosen experts
   float* wts;               // out: [rows][k] renormalised weights
   int4* rec;                // out: [tg][n_units] {expert or -1, 16-row mask, slot bits 0-31, slot bits 32-47}
-  int* n_act;               // out: [tg] experts that received a token (records by active slot)
   int* status;
 };
 
@@ -91,7 +90,6 @@ struct ExpertArgs {
   int n_rctas;              // routed CTAs of the grid when units are active slots (>= n_units)
   int tg;                   // token groups of 16 rows (blockIdx.y)
   const int4* rec;          // [tg][n_units] routing records written by the router
-  const int* n_act;         // [tg] active slots (written by the router when units are active slots)
   const int* idx;           // [rows][k] chosen experts (router)
   const float* wts;         // [rows][k] renormalised weights (router)
   // grouping: written by the gate/up launch (CTA 0, 0) from idx

@@ -136,6 +136,7 @@ struct RouteSmem {
   unsigned long long rowmask[256];  // [E] rows that chose expert e (bit r)
   int off[256];
   int4 scan[kWarps];
+  int4 rec;                         // this CTA's routing record
   int e, nlast, contrib;
 };
 
@@ -289,7 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
       const int4 ex = block_excl_scan4(make_int4(mk != 0u, 0, 0, 0), tot, s_scan);
       if (mk) rec[ex.x] = make_int4(e, (int)mk, (int)(uint32_t)jb, (int)(uint32_t)(jb >> 32));
       for (int i = tot.x + threadIdx.x; i < a.n_units; i += kThreads) rec[i] = make_int4(-1, 0, 0, 0);
-      if (threadIdx.x == 0) a.n_act[g] = tot.x;
     } else if (e < E) {
       rec[e] = make_int4(mk ? e : -1, (int)mk, (int)(uint32_t)jb, (int)(uint32_t)(jb >> 32));
     }
@@ -347,15 +347,25 @@ __device__ __forceinline__ void slot_assign(int xr, int R, int n, ExpertCta& c) 
     c.parts = base;
   }
 }
-__device__ __forceinline__ void assign_routed(const ExpertArgs& a, int g, ExpertCta& c) {
+__device__ __forceinline__ void assign_routed(const ExpertArgs& a, int n, ExpertCta& c) {
   if (c.shared || !a.by_slot) return;
-  const int n = __ldcg(a.n_act + g);
   const int ns = a.ws.n_slabs > 0 ? a.cpes : 0;
   if (n < 1 || n > a.n_rctas) {  // cannot happen (n_rctas >= most experts a group can pick)
     c.i = -1;
     return;
   }
   slot_assign((int)blockIdx.x - ns, a.n_rctas, n, c);
+}
+// Active-slot units (one token group, at most kThreads records): thread t
+// holds record t (`mine`).  The records with rows are the active slots, in
+// slot order, so their count deals the routed CTAs out (slot_assign) without a
+// separate load of the count, and the thread holding this CTA's record passes
+// it on through shared memory.  All threads of the CTA; two barriers.
+__device__ __forceinline__ int4 record_by_slot(const ExpertArgs& a, int4 mine, ExpertCta& c, RouteSmem& rs) {
+  assign_routed(a, __syncthreads_count(mine.y != 0), c);
+  if (c.i >= 0 && (int)threadIdx.x == c.i) rs.rec = mine;
+  __syncthreads();
+  return c.i >= 0 ? rs.rec : make_int4(-1, 0, 0, 0);
 }
 
 // Slabs [lo, hi) of part `part` of `parts`: n slabs cut in runs of gran (the
@@ -411,13 +421,19 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
   pdl_wait();
 
   if (blockIdx.x == 0 && blockIdx.y == 0) write_grouping(rs, a);
-  assign_routed(a, g, ec);
   // this CTA's rows
   int e = -1, ntk = ng;
   if (ec.shared) {
     for (int t = threadIdx.x; t < ng; t += kThreads) rows[t] = tok0 + t;
   } else {
-    const int4 r = ec.i >= 0 ? a.rec[(size_t)g * a.n_units + ec.i] : make_int4(-1, 0, 0, 0);  // {expert, row mask, slot bits}
+    int4 r;  // {expert, row mask, slot bits}
+    if (a.by_slot) {
+      const int t = threadIdx.x;
+      r = record_by_slot(a, t < a.n_units ? __ldcg(a.rec + (size_t)g * a.n_units + t) : make_int4(-1, 0, 0, 0), ec,
+                         rs);
+    } else {
+      r = __ldcg(a.rec + (size_t)g * a.n_units + ec.i);
+    }
     e = r.x;
     const unsigned mask = (unsigned)r.y;
     ntk = e >= 0 ? __popc(mask) : 0;
@@ -508,13 +524,17 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
   __syncthreads();
   pdl_wait();
   // contributions every output slab receives: one per routed record with rows, one per shared group
+  int4 mine = make_int4(-1, 0, 0, 0);  // active-slot units: record threadIdx.x of the (single) group
   {
     int c = 0;
-    for (int i = threadIdx.x; i < a.n_units * a.tg; i += kThreads) c += __ldcg(&a.rec[i].y) != 0;
+    for (int i = threadIdx.x; i < a.n_units * a.tg; i += kThreads) {
+      const int4 v = __ldcg(a.rec + i);
+      c += v.y != 0;
+      if (i == (int)threadIdx.x) mine = v;
+    }
     if (c) atomicAdd(&rs.contrib, c);
   }
   for (int i = threadIdx.x; i < rows * k; i += kThreads) rs.w[i] = __ldcg(a.wts + i);  // combine weights
-  assign_routed(a, g, ec);
   int e = -1, ntk, k32;
   const uint8_t* bsrc;
   if (ec.shared) {
@@ -522,7 +542,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
     k32 = a.Ish >> 5;
     bsrc = a.act_s + (size_t)(tok0 >> 3) * k32 * 512;
   } else {
-    const int4 r = ec.i >= 0 ? a.rec[(size_t)g * a.n_units + ec.i] : make_int4(-1, 0, 0, 0);  // {expert, row mask, slot bits}
+    const int4 r = a.by_slot ? record_by_slot(a, mine, ec, rs)
+                             : __ldcg(a.rec + (size_t)g * a.n_units + ec.i);  // {expert, row mask, slot bits}
     e = r.x;
     const unsigned mask = (unsigned)r.y;
     ntk = e >= 0 ? __popc(mask) : 0;
