@@ -383,6 +383,89 @@ def run_ours(args, rank, world):
     ctx.close()
 
 
+# ------------------------------------------------------------------ other workloads
+def run_sweep(args):
+    """One extra JSON line per workload (not the benchmark line): the 12-layer decoder
+    at 1 row and at 64 rows with 2048 cached tokens, and the sink decoder at 1 and
+    64 rows with 350 and 3000 cached tokens.  Each times `--steps` decode steps
+    (capped at 24) after 4 warm-up steps with CUDA events on the caller's stream;
+    inputs are resident on the device."""
+    import torch
+
+    from quantized_moe_decode_gb300 import binding, build
+
+    build.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    hbm_peak, _ = peaks()
+    K, W = min(args.steps, 24), 4
+    cases = [("full_b8", dict(rows=1)), ("stress_b64", {}), ("sink", dict(rows=1, T=350)),
+             ("sink", dict(rows=64, T=350)), ("sink", dict(rows=1, T=3000)), ("sink", dict(rows=64, T=3000))]
+    for name, kw in cases:
+        t0 = time.perf_counter()
+        wl = synth.workload(name, steps=K + W, **kw)
+        cfg, rows = wl.cfg, wl.rows
+        ctx = binding.Context(cfg, max_rows=rows, stream=stream.cuda_stream, device=0)
+        binding.load_workload(ctx, wl)
+        start = cfg.prefix_len
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if wl.step_x is not None:  # hidden-vector inputs each step, no LM head
+            x_all = torch.from_numpy(np.ascontiguousarray(wl.step_x).view(np.int16)).to(dev)
+            pos_all = torch.tensor([[start + s] * rows for s in range(K + W)], dtype=torch.int32, device=dev)
+            for s in range(W):
+                ctx.uocr_decode_step_embeds(rows, x_all[s].data_ptr(), pos_all[s].data_ptr())
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for s in range(W, W + K):
+                ctx.uocr_decode_step_embeds(rows, x_all[s].data_ptr(), pos_all[s].data_ptr())
+            e1.record(stream)
+        else:  # token ids, greedy steps chained on the device
+            ids = torch.zeros(rows, dtype=torch.int32, device=dev)
+            pos = torch.zeros(rows, dtype=torch.int32, device=dev)
+            if wl.prefill_embeds is not None:  # prefix built by decode steps
+                nxt = torch.zeros(rows, dtype=torch.int32, device=dev)
+                x = torch.zeros((rows, cfg.hidden), dtype=torch.int16, device=dev)
+                ne = wl.prefill_embeds.shape[1]
+                emb_all = torch.from_numpy(wl.prefill_embeds.view(np.int16)).to(dev)
+                ids_all = torch.from_numpy(wl.prefill_ids).to(dev)
+                for p in range(start):
+                    pos.fill_(p)
+                    if p < ne:
+                        x.copy_(emb_all[:, p])
+                        ctx.uocr_decode_step_embeds(rows, x.data_ptr(), pos.data_ptr())
+                    else:
+                        ids.copy_(ids_all[:, p - ne])
+                        ctx.uocr_decode_step(rows, ids.data_ptr(), pos.data_ptr(), nxt.data_ptr())
+                ids.copy_(nxt)
+            else:
+                ids.copy_(torch.from_numpy(wl.first_ids))
+            out = torch.zeros((K + W, rows), dtype=torch.int32, device=dev)
+            pos.fill_(start)
+            ctx.uocr_generate(rows, ids.data_ptr(), pos.data_ptr(), W, out.data_ptr())
+            ids.copy_(out[W - 1])
+            pos.fill_(start + W)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            ctx.uocr_generate(rows, ids.data_ptr(), pos.data_ptr(), K, out.data_ptr())
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ctx.uocr_sync()
+        ms = e0.elapsed_time(e1) / K
+        last = start + W + K - 1
+        distinct = {l: int(np.count_nonzero(ctx.uocr_debug_router(l, rows)["count"]))
+                    for l in range(cfg.n_layers) if not cfg.is_dense(l)}
+        step_bytes = sum(sum(v) for v in class_bytes(cfg, rows, [last] * rows, distinct).values())
+        gbs = step_bytes / (ms * 1e-3) / 1e9
+        print(json.dumps({"sweep": wl.name, "rows": rows, "cached_prefix": cfg.prefix_len, "steps": K,
+                          "positions": [start + W, last], "ms_per_step": ms, "tokens_per_s": rows / (ms * 1e-3),
+                          "bytes_per_step": step_bytes, "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak,
+                          "setup_s": round(time.perf_counter() - t0, 1)}), flush=True)
+        ctx.close()
+        del ctx
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -390,7 +473,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="time the other workloads (extra JSON lines) instead")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
