@@ -214,7 +214,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-// barrier 1 among the consumer warps only (the producer warp never joins it)
 
 // ---- programmatic dependent launch
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -311,7 +310,7 @@ struct BGlobalFrag {
   }
 };
 
-// Activations in shared memory in B-fragment order (a bulk copy of the global
+// Activations in shared memory in B-fragment order (a copy of the global
 // layout below): lane L's 16 bytes at ((tl*K32 + u)*32 + L)*16.
 struct BSmemFrag {
   const uint8_t* base;
@@ -495,10 +494,6 @@ __device__ __forceinline__ SlabWork slab_work(int first, int stride, int n, int 
   return w;
 }
 
-// The units a warp fetches, in the order it consumes them: for each of its
-// group's slabs (first + m*stride, m = grp, grp + G, ...) the run of uw units
-// starting at rank*uw.  Running pointers to this lane's 16 code bytes and its
-// scale entry; at the end of a run they jump to the next slab's run.
 // The units a warp fetches, in the order it consumes them: for each of its
 // group's slabs (first + m*stride, m = grp, grp + G, ...) the run of uw units
 // starting at rank*uw.  The unit index is recomputed from warp-uniform counters

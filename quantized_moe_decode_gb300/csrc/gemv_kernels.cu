@@ -15,10 +15,11 @@
 // place; only the new token's K/V are produced); "How it is meant to be run"
 // (the rows of a step share one read of the weights).
 //
-// Each persistent CTA owns slabs blockIdx.x, +gridDim.x, ...; their chunks
-// stream through a ring of shared-memory stages filled by bulk copies, the
-// first ones issued before the CTA waits for the kernel that produces its
-// activations.  Up to 16 rows (one token group) share each weight read.
+// Each persistent CTA owns slabs blockIdx.x, +gridDim.x, ...; each warp streams
+// its units through its own shared-memory ring filled by 16-byte cp.async
+// copies, the first ones issued before the CTA waits for the kernel that
+// produces its activations.  Up to 16 rows (one token group) share each
+// weight read.
 #include "launch.h"
 
 namespace uocr {
