@@ -135,6 +135,7 @@ struct uocr_ctx {
   int *hist = nullptr, *hist_ctr = nullptr, *status = nullptr;
   // loading
   std::map<std::vector<int>, bool> loaded;  // (kind, layer, expert) -> present
+  bool complete = false;  // every tensor the config needs has been loaded (set once checked; loads only add)
   std::map<std::vector<int>, Pending> pending;
   bool sinks_set = false;
   // graphs
@@ -821,6 +822,7 @@ static uocr_status load_one(uocr_ctx* ctx, const uocr_tensor& t) {
 }
 
 static uocr_status check_complete(uocr_ctx* ctx) {
+  if (ctx->complete) return UOCR_OK;  // the walk below costs hundreds of µs of host time per step
   const uocr_config& c = ctx->cfg;
   auto has = [&](int k, int l, int e) { return ctx->loaded.count({k, l, e}) > 0; };
   auto miss = [&](int k, int l, int e) {
@@ -846,6 +848,7 @@ static uocr_status check_complete(uocr_ctx* ctx) {
     }
   }
   if (c.use_sink && !ctx->sinks_set) return ctx->fail(UOCR_E_STATE, "use_sink = 1 but uocr_set_sinks was not called");
+  ctx->complete = true;
   return UOCR_OK;
 }
 
