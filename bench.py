@@ -1,17 +1,23 @@
 #!/usr/bin/env python3
 """Decode throughput of the quantized MoE OCR decoder on one GB300.
 
-Workload (one "step" = one decode step of every row through the whole path:
-embedding, 12 layers of RMSNorm/QKV/RoPE/KV append/attention/O-proj and the
-dense MLP or router + experts + combine, final norm, LM head, argmax):
-the 12-layer DeepSeek-V2-style decoder (hidden 1280, 10x128 heads, layer 0
-dense MLP 3584, layers 1-11 with 64 routed top-6 experts + 2 shared of 896),
-Q8_0 attention/dense/shared, Q4_0 routed experts, fp16 LM head over 102400
-tokens, 8 rows, prefix of 256 image embeddings + 32 prompt tokens built by
-decode steps, then greedy decoding through the 128-slot ring.  Weights,
-prefix and prompt are seeded synthetic data (seed 2).
+Headline workload (one "step" = one decode step of every row through the
+whole path: embedding, 12 layers of RMSNorm/QKV/RoPE/KV append/attention/
+O-proj and the dense MLP or router + experts + combine, final norm, LM head,
+argmax): the throughput stress configuration, i.e. the 12-layer
+DeepSeek-V2-style decoder (hidden 1280, 10x128 heads, layer 0 dense MLP 3584,
+layers 1-11 with 64 routed top-6 experts + 2 shared of 896, fp16 LM head over
+102400 tokens) at 64 rows with 2048 cached prefix tokens per row plus the
+128-slot ring, all experts Q4_0, greedy decoding.  Weights, cache and first
+ids are seeded synthetic data (seed 4).
+
+The same line carries the full decoder at 8 rows and at 1 row (256 image
+embeddings + 32 prompt ids per row, built by uocr_prefill), the per-kernel
+table with the dominant kernel's roofline, the end-to-end host-buffer figure
+and the float64 oracle timed on the host cores (all threads, and 6 threads).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--no-side-configs] [--no-cpu-baseline] [--sweep]
 
 Prints one JSON line on rank 0.
 """
@@ -38,7 +44,12 @@ sys.path.insert(0, ROOT)
 from quantized_moe_decode_gb300 import synth  # noqa: E402
 
 METRIC = "decode tokens/s (rows x steps/s) and achieved HBM GB/s vs GB300 peak, 1 GPU"
-WORKLOAD = "full_b8"
+WORKLOAD = "stress_b64"
+HEADLINE_CONFIG = {
+    "workload": "throughput stress: full 12-layer MoE decoder (hidden 1280, 10x128 heads, layer 0 dense MLP 3584, "
+                "layers 1-11 64 routed top-6 + 2 shared experts of 896, vocab 102400 fp16 LM head), 64 rows, "
+                "2048 cached prefix tokens + 128-slot ring, all experts Q4_0, Q8_0 attention/dense, greedy",
+    "rows": 64, "prefix": 2048, "ring": 128, "seed": 4}
 BPW = {synth.F16: 2.0, synth.Q8_0: 34 / 32, synth.Q4_0: 18 / 32, synth.I8ASYM: 36 / 32}
 
 
@@ -159,22 +170,62 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU / reference arm
+ORACLE_ROWS = 2  # rows of the headline workload the oracle steps through in its timed sample
+
+
 def time_oracle(wl, rows, min_s, max_steps, warm=2):
-    """Oracle decode steps (the prefix's own decode steps, embedding inputs,
-    LM head included) over `rows` rows; returns (steps, seconds)."""
+    """Oracle decode steps of the workload's first `rows` rows, from its own
+    starting state (cached prefix, or the prefix embeddings' positions), LM
+    head included; returns (steps, seconds).  Weight dequantisation is cached
+    on the warm-up steps."""
     import oracle
 
-    m = oracle.OracleModel(wl.cfg, wl.tensors, rows, cache="float64")
-    x = wl.prefill_embeds
+    kv = None if wl.kv_prefix is None else wl.kv_prefix.subset(list(range(rows)))
+    m = oracle.OracleModel(wl.cfg, wl.tensors, rows, kv_prefix=kv, sinks=wl.sinks, cache="float64")
+    if wl.prefill_embeds is not None:  # positions of the prefix, embedding inputs
+        step = lambda p: m.step(np.full(rows, p, np.int32), x=wl.prefill_embeds[:rows, p])
+        p0 = 0
+    else:  # greedy decoding from the cached prefix
+        ids = [wl.first_ids[:rows].copy()]
+
+        def step(p):
+            r = m.step(np.full(rows, p, np.int32), ids=ids[0])
+            ids[0] = r.next_ids.astype(np.int32)
+        p0 = wl.start_pos
     for p in range(warm):
-        m.step(np.full(rows, p, np.int32), x=x[:rows, p])
+        step(p0 + p)
     t0 = time.perf_counter()
     n = 0
     while n < max_steps and (time.perf_counter() - t0) < min_s:
-        p = warm + n
-        m.step(np.full(rows, p, np.int32), x=x[:rows, p])
+        step(p0 + warm + n)
         n += 1
     return n, time.perf_counter() - t0
+
+
+def cpu_sample_desc(rows, n, warm, cores):
+    return (f"{rows} rows x {n} greedy decode steps of the 64-row stress workload from its 2048-token cached "
+            f"prefix (float64 NumPy oracle on {cores} host threads, weight dequantisation cached on {warm} "
+            f"warm-up steps)")
+
+
+def cpu_baseline_threads(threads, min_s=15.0, max_steps=20):
+    """The oracle sample in a child process whose BLAS / OpenMP pools have `threads` threads."""
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(threads)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", str(min_s), str(max_steps)],
+                       env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else f"rc {r.returncode}"}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": ORACLE_ROWS * d["steps"] / d["seconds"], "unit": "tokens/s", "cores": threads,
+            "kind": "oracle", "sample": cpu_sample_desc(ORACLE_ROWS, d["steps"], 2, threads)}
+
+
+def run_cpu_sample(min_s, max_steps):
+    wl = synth.workload(WORKLOAD, steps=0)
+    n, dt = time_oracle(wl, ORACLE_ROWS, min_s=min_s, max_steps=max_steps)
+    print(json.dumps({"steps": n, "seconds": dt}), flush=True)
 
 
 def run_reference(args, rank, world):
@@ -182,20 +233,15 @@ def run_reference(args, rank, world):
         return
     wl = synth.workload(WORKLOAD, steps=0)
     K, W = args.steps, args.warmup
-    import oracle  # noqa: F401
-
-    rows = 1
-    m_steps = min(K, 40)
-    n, dt = time_oracle(wl, rows, min_s=90.0, max_steps=m_steps, warm=max(W, 2))
-    v = rows * n / dt
+    n, dt = time_oracle(wl, ORACLE_ROWS, min_s=90.0, max_steps=min(K, 40), warm=max(min(W, 3), 2))
+    v = ORACLE_ROWS * n / dt
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": n, "steps_requested": K, "warmup": W, "ms_per_step": 1e3 * dt / max(n, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": "full 12-layer MoE decoder, 8 rows (oracle sample: 1 row)",
-                                            "rows": 8, "prefix": 288, "ring": 128, "seed": 2},
+            "data": "synthetic", "config": dict(HEADLINE_CONFIG, oracle_rows=ORACLE_ROWS),
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _CORES, "kind": "oracle",
-                             "sample": f"1 row x {n} decode steps of the workload's prefix positions, float64 "
-                                       f"NumPy oracle, weight cache warmed on {max(W, 2)} steps, capped at 90 s"},
+                             "sample": cpu_sample_desc(ORACLE_ROWS, n, max(min(W, 3), 2), _CORES) +
+                             ", capped at 90 s"},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -221,10 +267,124 @@ def replica_throughput(world, rows, steps, seconds):
 
 
 # ------------------------------------------------------------------ our arm
+def open_workload(name, dev, stream, **kw):
+    """Context with the workload loaded and its prefix in the cache (cached
+    prefixes written, image + prompt prefixes built by uocr_prefill).  Returns
+    (ctx, wl, first ids on the device, prefill seconds or None)."""
+    import torch
+
+    from quantized_moe_decode_gb300 import binding
+
+    wl = synth.workload(name, steps=0, **kw)
+    cfg, rows = wl.cfg, wl.rows
+    ctx = binding.Context(cfg, max_rows=rows, stream=stream.cuda_stream, device=dev.index or 0)
+    binding.load_workload(ctx, wl)
+    ids = torch.zeros(rows, dtype=torch.int32, device=dev)
+    t_pre = None
+    if wl.prefill_embeds is not None:
+        ne = wl.prefill_embeds.shape[1]
+        emb = torch.from_numpy(np.ascontiguousarray(wl.prefill_embeds).view(np.int16)).to(dev)
+        pids = torch.from_numpy(np.ascontiguousarray(wl.prefill_ids)).to(dev)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for r in range(rows):
+            ctx.uocr_prefill(r, ne, 0, x_ptr=emb[r].data_ptr())
+            ctx.uocr_prefill(r, cfg.prefix_len - ne, ne, ids_ptr=pids[r].data_ptr(), next_ptr=ids[r:].data_ptr())
+        ctx.uocr_sync()
+        t_pre = time.perf_counter() - t0
+    else:
+        ids.copy_(torch.from_numpy(wl.first_ids))
+    return ctx, wl, ids, t_pre
+
+
+def time_greedy(ctx, wl, ids, dev, stream, K, W, dist=None):
+    """W untimed then K timed greedy steps chained on the device (one graph
+    replay per step), CUDA events on the caller's stream.  Returns (ms, first
+    timed position, last ids)."""
+    import torch
+
+    rows, start = wl.rows, wl.start_pos
+    out = torch.zeros((max(K, W, 1), rows), dtype=torch.int32, device=dev)
+    pos = torch.full((rows,), start, dtype=torch.int32, device=dev)
+    if W:
+        ctx.uocr_generate(rows, ids.data_ptr(), pos.data_ptr(), W, out.data_ptr())
+        ctx.uocr_sync()
+        ids = out[W - 1].clone()
+    pos.fill_(start + W)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    ctx.uocr_generate(rows, ids.data_ptr(), pos.data_ptr(), K, out.data_ptr())
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ctx.uocr_sync()
+    return e0.elapsed_time(e1), start + W, out[K - 1].clone()
+
+
+def kernel_table(ctx, wl, ids, dev, position):
+    """Per kernel class: its launches of one step replayed alone in a graph
+    (uocr_profile, CUDA events on the library stream), algorithmic bytes, GB/s."""
+    import torch
+
+    cfg, rows = wl.cfg, wl.rows
+    pos = torch.full((rows,), position, dtype=torch.int32, device=dev)
+    prof = {}
+    n_prof = 3
+    for _ in range(n_prof):
+        t = ctx.uocr_profile(rows, 0, ids.data_ptr(), 0, pos.data_ptr())
+        for k_, v_ in t.items():
+            prof[k_] = prof.get(k_, 0.0) + v_ / n_prof
+    distinct = {l: int(np.count_nonzero(ctx.uocr_debug_router(l, rows)["count"]))
+                for l in range(cfg.n_layers) if not cfg.is_dense(l)}
+    cb = class_bytes(cfg, rows, [position] * rows, distinct)
+    kernels = {}
+    for name, t_ms in prof.items():
+        b = sum(cb.get(name, [0]))
+        n_l = len(cb.get(name, [1]))
+        kernels[name] = {"ms_per_step": t_ms, "launches_per_step": n_l, "ms_per_launch": t_ms / n_l,
+                         "bytes_per_launch": b / n_l, "gbs": b / (t_ms * 1e-3) / 1e9 if t_ms > 0 else None}
+    return kernels, distinct
+
+
+def step_bytes_over(cfg, rows, positions, distinct):
+    """Mean algorithmic bytes per step over the timed steps' positions."""
+    tot = 0.0
+    for p in positions:
+        tot += sum(sum(v) for v in class_bytes(cfg, rows, [p] * rows, distinct).values())
+    return tot / len(positions)
+
+
+def side_config(name, dev, stream, K, W, hbm_peak, **kw):
+    """One extra configuration of the same line: time K greedy steps, report
+    tokens/s, bytes and the HBM fraction, and the uocr_prefill time."""
+    ctx, wl, ids, t_pre = open_workload(name, dev, stream, **kw)
+    cfg, rows = wl.cfg, wl.rows
+    ms, p0, last = time_greedy(ctx, wl, ids, dev, stream, K, W)
+    kernels, distinct = kernel_table(ctx, wl, last, dev, p0 + K)
+    sb = step_bytes_over(cfg, rows, range(p0, p0 + K), distinct)
+    ms_step = ms / K
+    d = {"workload": wl.name, "rows": rows, "prefix": cfg.prefix_len, "steps": K, "warmup": W,
+         "positions": [p0, p0 + K - 1], "ms_per_step": ms_step, "tokens_per_s": rows / (ms_step * 1e-3),
+         "bytes_per_step": sb, "hbm_gbs": sb / (ms_step * 1e-3) / 1e9,
+         "hbm_frac": sb / (ms_step * 1e-3) / 1e9 / hbm_peak,
+         "kernels": {k_: {"ms_per_launch": round(v_["ms_per_launch"], 5), "gbs": round(v_["gbs"] or 0, 1)}
+                     for k_, v_ in kernels.items()}}
+    if t_pre is not None:
+        d["prefill"] = {"tokens": rows * cfg.prefix_len, "seconds": t_pre,
+                        "tokens_per_s": rows * cfg.prefix_len / t_pre,
+                        "how": "uocr_prefill per row: 256 image embeddings (4 chunks of 64) + 32 prompt ids, "
+                               "host wall clock around the calls and one uocr_sync"}
+    ctx.close()
+    return d
+
+
 def run_ours(args, rank, world):
     import torch
 
-    from quantized_moe_decode_gb300 import binding, build
+    from quantized_moe_decode_gb300 import build
 
     local = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(local)
@@ -239,155 +399,108 @@ def run_ours(args, rank, world):
     if dist:
         dist.barrier()
     t_setup = time.perf_counter()
-    wl = synth.workload(WORKLOAD, steps=0)
-    cfg, rows = wl.cfg, wl.rows
-    stream = torch.cuda.current_stream()
-    ctx = binding.Context(cfg, max_rows=rows, stream=stream.cuda_stream, device=local)
-    binding.load_workload(ctx, wl)
     dev = torch.device("cuda", local)
-    pos = torch.zeros(rows, dtype=torch.int32, device=dev)
-    ids = torch.zeros(rows, dtype=torch.int32, device=dev)
-    nxt = torch.zeros(rows, dtype=torch.int32, device=dev)
-    x = torch.zeros((rows, cfg.hidden), dtype=torch.int16, device=dev)
-    ne = wl.prefill_embeds.shape[1]
-    emb_all = torch.from_numpy(wl.prefill_embeds.view(np.int16)).to(dev)
-    ids_all = torch.from_numpy(wl.prefill_ids).to(dev)
-    for p in range(cfg.prefix_len):  # prefix built by decode steps (untimed)
-        pos.fill_(p)
-        if p < ne:
-            x.copy_(emb_all[:, p])
-            ctx.uocr_decode_step_embeds(rows, x.data_ptr(), pos.data_ptr())
-        else:
-            ids.copy_(ids_all[:, p - ne])
-            ctx.uocr_decode_step(rows, ids.data_ptr(), pos.data_ptr(), nxt.data_ptr())
-    ctx.uocr_sync()
-    ids.copy_(nxt)
-    start = cfg.prefix_len
+    stream = torch.cuda.current_stream()
+    ctx, wl, ids, _ = open_workload(WORKLOAD, dev, stream)
+    cfg, rows = wl.cfg, wl.rows
     K, W = args.steps, args.warmup
-    out = torch.zeros((max(K, W, 1), rows), dtype=torch.int32, device=dev)
-    pos.fill_(start)
-    ctx.uocr_generate(rows, ids.data_ptr(), pos.data_ptr(), W, out.data_ptr())
-    ctx.uocr_sync()
-    if W:
-        ids.copy_(out[W - 1])
-    pos.fill_(start + W)
-    torch.cuda.synchronize()
     log(f"[bench] setup {time.perf_counter() - t_setup:.1f}s")
 
     # ---- timed region: K greedy steps chained on the device
     clk = ClockSampler(local)
     clk.start()
     time.sleep(0.3)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
     torch.cuda.profiler.start()  # a profiler run with --profile-from-start off sees the timed steps only
-    torch.cuda.synchronize()
-    e0.record(stream)
-    ctx.uocr_generate(rows, ids.data_ptr(), pos.data_ptr(), K, out.data_ptr())
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms, p0, last = time_greedy(ctx, wl, ids, dev, stream, K, W, dist)
     torch.cuda.profiler.stop()
     if dist:
         dist.barrier()
     clocks = clk.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
-    ctx.uocr_sync()
-    gen_ids = out[:K].cpu().numpy()
-    step_pos = start + W + K
+    ms = max_over_ranks(ms, dist, dev)
 
-    # ---- per-kernel-class durations (un-graphed steps on the library stream, CUDA events)
-    n_prof = 5
-    prof = {}
-    distinct = {}
-    pos.fill_(step_pos)
-    ids.copy_(out[K - 1])
-    for _ in range(n_prof):
-        t = ctx.uocr_profile(rows, 0, ids.data_ptr(), 0, pos.data_ptr())
-        for k_, v_ in t.items():
-            prof[k_] = prof.get(k_, 0.0) + v_ / n_prof
-    for l in range(cfg.n_layers):
-        if not cfg.is_dense(l):
-            distinct[l] = int(np.count_nonzero(ctx.uocr_debug_router(l, rows)["count"]))
-    cb = class_bytes(cfg, rows, [step_pos] * rows, distinct)
-    launches_per_step = sum(len(v) for v in cb.values())
+    # ---- per-kernel-class durations and the roofline of the dominant class
+    kernels, distinct = kernel_table(ctx, wl, last, dev, p0 + K)
     hbm_peak, peak_kind = peaks()
-    kernels = {}
-    for name, t_ms in prof.items():
-        b = sum(cb.get(name, [0]))
-        n_l = len(cb.get(name, [1]))
-        kernels[name] = {"ms_per_step": t_ms, "launches_per_step": n_l, "bytes_per_launch": b / n_l,
-                         "gbs": b / (t_ms * 1e-3) / 1e9 if t_ms > 0 else None}
     dom = max(kernels, key=lambda k_: kernels[k_]["ms_per_step"])
     dk = kernels[dom]
-    achieved = dk["gbs"]
-    step_bytes = sum(sum(v) for v in cb.values())
+    step_bytes = step_bytes_over(cfg, rows, range(p0, p0 + K), distinct)
+    launches_per_step = sum(len(v) for v in class_bytes(cfg, rows, [p0] * rows, distinct).values())
     ms_per_step = ms / K
     value = replica_throughput(world, rows, K, ms * 1e-3)
 
     # ---- end to end through the host-buffer entry point (pinned host buffers)
-    K_e2e = min(K, 200)
+    K_e2e = min(K, 100)
     h_ids = torch.empty(rows, dtype=torch.int32, pin_memory=True)
     h_pos = torch.empty(rows, dtype=torch.int32, pin_memory=True)
     h_out = torch.empty(rows, dtype=torch.int32, pin_memory=True)
-    h_ids.copy_(torch.from_numpy(gen_ids[-1]))
+    h_ids.copy_(last.cpu())
     lib = ctx.lib
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for s in range(K_e2e):
-        h_pos.fill_(step_pos + s)
+        h_pos.fill_(p0 + K + 1 + s)
         st_ = lib.uocr_decode_step_host(ctx.h, rows, h_ids.data_ptr(), h_pos.data_ptr(), h_out.data_ptr())
         if st_ != 0:
             raise RuntimeError(lib.uocr_last_error(ctx.h).decode())
         h_ids.copy_(h_out)
     e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
     e2e = {"value": replica_throughput(world, rows, K_e2e, e2e_s), "unit": "tokens/s",
-           "h2d_bytes_per_step": rows * 4 * 2,
-           "d2h_bytes_per_step": rows * 4, "steps": K_e2e}
+           "h2d_bytes_per_step": rows * 4 * 2, "d2h_bytes_per_step": rows * 4, "steps": K_e2e,
+           "how": "uocr_decode_step_host (host ids/positions in, host ids out, synchronous) per step"}
+    ctx.close()
+    del ctx
+    torch.cuda.empty_cache()
 
     if rank != 0:
-        ctx.close()
         return
-    cpu = None
+    # ---- the other configurations of the statement, as fields of the same line
+    others = {}
+    if not args.no_side_configs:
+        K2 = min(K, 200)
+        others["full_b8"] = side_config("full_b8", dev, stream, K2, W, hbm_peak)
+        others["full_b1"] = side_config("full_b8", dev, stream, K2, W, hbm_peak, rows=1)
+    cpu = cpu6 = None
     if not args.no_cpu_baseline:
-        n_c, dt_c = time_oracle(wl, rows, min_s=15.0, max_steps=20)
-        cpu = {"value": rows * n_c / dt_c, "unit": "tokens/s", "cores": _CORES, "kind": "oracle",
-               "sample": f"{rows} rows x {n_c} decode steps of the workload's prefix positions (float64 NumPy "
-                         f"oracle, weight cache warmed on 2 steps)"}
+        n_c, dt_c = time_oracle(wl, ORACLE_ROWS, min_s=15.0, max_steps=20)
+        cpu = {"value": ORACLE_ROWS * n_c / dt_c, "unit": "tokens/s", "cores": _CORES, "kind": "oracle",
+               "sample": cpu_sample_desc(ORACLE_ROWS, n_c, 2, _CORES)}
+        cpu6 = cpu_baseline_threads(6)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 activations x Q8_0/Q4_0 weights, f32 accumulate", "data": "synthetic",
-        "config": {"workload": "full 12-layer MoE decoder (hidden 1280, 10x128, 64 routed top-6 + 2 shared, "
-                               "vocab 102400), 8 rows, prefix 256 image embeds + 32 prompt ids, 128-slot ring, "
-                               "greedy", "rows": rows, "global_batch": rows * world, "prefix": cfg.prefix_len,
-                   "ring": cfg.ring_len, "positions": [start + W, step_pos], "seed": 2,
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "inputs larger than L2: %.2f GB touched per step" % (step_bytes / 1e9)},
+        "config": dict(HEADLINE_CONFIG, global_batch=rows * world, positions=[p0, p0 + K - 1],
+                       parallelism="replicas" if world > 1 else "single",
+                       l2="inputs larger than L2: %.2f GB touched per step" % (step_bytes / 1e9)),
         "hbm_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
         "hbm_frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
         "bytes_per_step": step_bytes,
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak if achieved else None, "traffic": ncu_traffic(dom),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": dk["gbs"], "peak": hbm_peak, "unit": "GB/s",
+                     "frac": dk["gbs"] / hbm_peak if dk["gbs"] else None, "traffic": ncu_traffic(dom),
+                     "algorithmic_bytes_per_launch": dk["bytes_per_launch"],
+                     "ms_per_launch": dk["ms_per_launch"],
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                     else "fallback 6.8 TB/s"},
+                     else "fallback 6.8 TB/s",
+                     "timing": "the class's launches of one step replayed alone in a CUDA graph (every layer, "
+                               "programmatic dependent launch between them), CUDA events on the launching "
+                               "stream, 5 replays x 3"},
         "kernels": kernels,
+        "other_configs": others,
         "cpu_baseline": cpu,
+        "cpu_baseline_6_threads": cpu6,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
-    ctx.close()
 
 
 # ------------------------------------------------------------------ other workloads
 def run_sweep(args):
-    """One extra JSON line per workload (not the benchmark line): the 12-layer decoder
-    at 1 row and at 64 rows with 2048 cached tokens, and the sink decoder at 1 and
-    64 rows with 350 and 3000 cached tokens.  Each times `--steps` decode steps
+    """One extra JSON line per workload (not the benchmark line): the sink decoder at
+    1 and 64 rows with 350 and 3000 cached tokens.  Each times `--steps` decode steps
     (capped at 24) after 4 warm-up steps with CUDA events on the caller's stream;
     inputs are resident on the device."""
     import torch
@@ -400,8 +513,8 @@ def run_sweep(args):
     stream = torch.cuda.current_stream()
     hbm_peak, _ = peaks()
     K, W = min(args.steps, 24), 4
-    cases = [("full_b8", dict(rows=1)), ("stress_b64", {}), ("sink", dict(rows=1, T=350)),
-             ("sink", dict(rows=64, T=350)), ("sink", dict(rows=1, T=3000)), ("sink", dict(rows=64, T=3000))]
+    cases = [("sink", dict(rows=1, T=350)), ("sink", dict(rows=64, T=350)), ("sink", dict(rows=1, T=3000)),
+             ("sink", dict(rows=64, T=3000))]
     for name, kw in cases:
         t0 = time.perf_counter()
         wl = synth.workload(name, steps=K + W, **kw)
@@ -469,12 +582,17 @@ def run_sweep(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side-configs", action="store_true", help="only the headline configuration")
+    ap.add_argument("--cpu-sample", nargs=2, type=float, help=argparse.SUPPRESS)
     ap.add_argument("--sweep", action="store_true", help="time the other workloads (extra JSON lines) instead")
     args = ap.parse_args()
+    if args.cpu_sample:
+        run_cpu_sample(args.cpu_sample[0], int(args.cpu_sample[1]))
+        return
     if args.sweep:
         run_sweep(args)
         return

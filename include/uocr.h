@@ -24,6 +24,11 @@
  *      rebuilt); "How it is meant to be run" (dynamic batch: rows share one
  *      weight read; lengths are explicit, never inferred from shapes).
  *
+ * Each declaration below names the passage that defines what it computes or
+ * enforces ("Source:").  Page titles are abbreviated as
+ *   [Metal]  "Unlimited-OCR on Apple Silicon with C and Metal"
+ *   [Falcon] "Falcon-OCR INT8 OpenVINO IR" model card
+ *
  * Conventions
  *  - Every call returns a uocr_status; uocr_last_error() gives the text of
  *    the last failure on that context.  Calls on one context are serialised
@@ -65,10 +70,16 @@ typedef enum {
   UOCR_E_STATE = 5,       /* call not valid in the context's current state */
   UOCR_E_CUDA = 6,        /* a CUDA runtime error (text in uocr_last_error) */
   UOCR_E_POSITION = 7,    /* a device-side position was invalid */
-  UOCR_E_TOKEN = 8        /* a device-side token id was outside [0, vocab) */
+  UOCR_E_TOKEN = 8,       /* a device-side token id was outside [0, vocab) */
+  UOCR_E_TIMEOUT = 9      /* a kernel's bounded wait for its asynchronous copies ran out;
+                             the kernel returned without the data, the context stays usable */
 } uocr_status;
 
-/* Canonical weight formats.  Blocks hold 32 consecutive values of one row;
+/* Canonical weight formats.  Source: [Metal] "Quantizzazione: Q8 prima, Q4
+ * dove conviene" (Q8_0 / Q4_0 block formats dequantised inside the kernels);
+ * [Falcon] "How it is meant to be run" (INT8_ASYM weights, u8 codes); the block
+ * size 32 and the value formulas are the decode-step statement's definitions.
+ * Blocks hold 32 consecutive values of one row;
  * blocks run along the row (K), rows follow each other.  fp16 little endian.
  *   UOCR_F16     plain fp16 [rows][cols]
  *   UOCR_Q8_0    {fp16 d; int8 q[32]}           34 B   value = d*q
@@ -77,7 +88,9 @@ typedef enum {
  *   UOCR_I8ASYM  {fp16 s; fp16 z; uint8 q[32]}  36 B   value = s*(q-z)      */
 typedef enum { UOCR_F16 = 0, UOCR_Q8_0 = 1, UOCR_Q4_0 = 2, UOCR_I8ASYM = 3 } uocr_format;
 
-/* Weight tensor kinds.  Shapes use H = hidden, S = n_heads*head_dim,
+/* Weight tensor kinds.  Source: [Metal] "Il decoder e il Mixture of Experts"
+ * (attention, one dense MLP layer, MoE layers with a router, 64 routed and 2
+ * shared SwiGLU experts, embedding and language head).  Shapes use H = hidden, S = n_heads*head_dim,
  * I = dense_inter, Ie = expert_inter, E = n_experts, V = vocab.
  * Matrices are [out_features][in_features] (y = W x).                       */
 typedef enum {
@@ -102,6 +115,9 @@ typedef enum {
   UOCR_T_EXPERT_DOWN = 18   /* [H][Ie]  fmt_routed                           */
 } uocr_tensor_kind;
 
+/* Source: [Metal] "Il decoder e il Mixture of Experts" (model constants, the
+ * 128-token ring for generated tokens); [Falcon] intro (the sink, the cache
+ * as an input); "Dall'ABI C all'API Python" (one engine per execution lane). */
 typedef struct {
   /* model */
   int32_t hidden;          /* H, multiple of 64                                  */
@@ -141,7 +157,9 @@ typedef struct {
   uint64_t bytes;   /* byte size of data                                  */
 } uocr_tensor;
 
-/* Bytes per category (the Metal page's memory categories). */
+/* Bytes per category.  Source: [Metal] "Memoria: il vincolo principale"
+ * (every buffer belongs to a category; the working set is estimated per
+ * category before running). */
 typedef struct {
   uint64_t weights;      /* packed weights, norms, router, embedding, LM head  */
   uint64_t kv_cache;     /* [layer][row][K|V][head][P+R][D] fp16               */
@@ -153,16 +171,22 @@ typedef struct {
 
 typedef struct uocr_ctx uocr_ctx;
 
-/* Validate cfg, size the arena per category, compare it with cfg->mem_budget
+/* Source: [Metal] "Memoria: il vincolo principale" (estimate, compare with the
+ * budget, refuse with a detailed error) and "Dall'ABI C all'API Python" (engine
+ * open).
+ * Validate cfg, size the arena per category, compare it with cfg->mem_budget
  * (UOCR_E_BUDGET with a per-category message when it does not fit), allocate
  * it, zero the KV cache.  Launches no compute kernel.  *out receives the
  * context (NULL on failure).  cfg is copied.                                 */
 UOCR_API uocr_status uocr_create(const uocr_config* cfg, uocr_ctx** out);
 
-/* Release everything; NULL-safe; the context must not be used afterwards.   */
+/* Source: [Metal] "Dall'ABI C all'API Python" (engine close).
+ * Release everything; NULL-safe; the context must not be used afterwards.   */
 UOCR_API void uocr_destroy(uocr_ctx* ctx);
 
-/* Copy and pack weight tensors (host pointers, caller keeps ownership and may
+/* Source: [Metal] "Quantizzazione" (no fp16 copy of the weights: the packed
+ * quantised blocks are what the kernels read).
+ * Copy and pack weight tensors (host pointers, caller keeps ownership and may
  * free them on return).  Tensors may come in any order and over several
  * calls; a group (Q/K/V of a layer, gate/up of an MLP or expert, the shared
  * experts of a layer) is packed once all its members have arrived.  Wrong
@@ -170,14 +194,17 @@ UOCR_API void uocr_destroy(uocr_ctx* ctx);
  * tensor is kept).  Synchronous.                                             */
 UOCR_API uocr_status uocr_load_weights(uocr_ctx* ctx, const uocr_tensor* t, size_t n);
 
-/* Write n cached prefix positions [start, start+n) of one row and layer.
+/* Source: [Falcon] intro (the KV cache is an input the caller owns; lengths
+ * are explicit).
+ * Write n cached prefix positions [start, start+n) of one row and layer.
  * k, v: host fp16 [n_heads][n][head_dim].  Requires start+n <= prefix_len.
  * Synchronous.                                                               */
 UOCR_API uocr_status uocr_kv_write_prefix(uocr_ctx* ctx, int32_t row, int32_t layer,
                                  const uint16_t* k, const uint16_t* v,
                                  int32_t start, int32_t n);
 
-/* Read back cache slots [slot0, slot0+n) of one row and layer into host fp16
+/* Source: [Falcon] intro (the cache is caller-visible state).
+ * Read back cache slots [slot0, slot0+n) of one row and layer into host fp16
  * [n_heads][n][head_dim] buffers.  Synchronous.                               */
 UOCR_API uocr_status uocr_kv_read(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0,
                          int32_t n, uint16_t* k, uint16_t* v);
@@ -189,11 +216,19 @@ UOCR_API uocr_status uocr_kv_read(uocr_ctx* ctx, int32_t row, int32_t layer, int
 UOCR_API uocr_status uocr_kv_write(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0,
                           int32_t n, const uint16_t* k, const uint16_t* v);
 
-/* Per-layer, per-head sink logits, host fp32 [n_layers][n_heads]; they enter
+/* Source: [Falcon] intro (the sink is one more key whose logit is the sink and
+ * whose value is zero; equivalent to rescaling by sigmoid(lse - sink)).
+ * Per-layer, per-head sink logits, host fp32 [n_layers][n_heads]; they enter
  * the softmax unscaled as one more key with value zero.  Synchronous.        */
 UOCR_API uocr_status uocr_set_sinks(uocr_ctx* ctx, const float* sinks);
 
-/* One decode step for rows 0..rows-1 (row i uses KV row i).
+/* Source: [Metal] "Il decoder e il Mixture of Experts" (the decode loop:
+ * append to the KV cache, generated tokens in a 128-token ring, argmax over the
+ * language head; route, group tokens by expert, recompose) and
+ * "Quantizzazione" (dequantisation inside GEMV/SwiGLU/combine/argmax, fp16
+ * activations); [Falcon] "How it is meant to be run" (the rows of a step share
+ * one read of the weights).
+ * One decode step for rows 0..rows-1 (row i uses KV row i).
  *   token_ids  device int32 [rows]  (embedding lookup; requires vocab > 0)
  *   positions  device int32 [rows]  absolute positions; slot(p) is written
  *              with the new key/value, then attention reads every slot whose
@@ -204,45 +239,84 @@ UOCR_API uocr_status uocr_set_sinks(uocr_ctx* ctx, const float* sinks);
 UOCR_API uocr_status uocr_decode_step(uocr_ctx* ctx, int32_t rows, const int32_t* token_ids,
                              const int32_t* positions, int32_t* next_ids, float* logits);
 
-/* The same step fed with hidden vectors instead of token ids.
+/* Source: as uocr_decode_step; [Metal] "Il modello: una pipeline
+ * vision-language completa" (visual tokens enter the decoder as embeddings).
+ * The same step fed with hidden vectors instead of token ids.
  *   x         device fp16 [rows][hidden]
  *   y         device fp32 [rows][hidden] or NULL: residual stream after the
  *             last layer (before the final norm)
+ *   y_f16     device fp16 [rows][hidden] or NULL: the same, rounded to fp16
+ *             (the activation precision of [Metal] "Quantizzazione")
  *   next_ids  device int32 [rows] or NULL (requires vocab > 0 when given)
  *   logits    device fp32 [rows][vocab] or NULL                              */
 UOCR_API uocr_status uocr_decode_step_embeds(uocr_ctx* ctx, int32_t rows, const uint16_t* x,
-                                    const int32_t* positions, float* y,
+                                    const int32_t* positions, float* y, uint16_t* y_f16,
                                     int32_t* next_ids, float* logits);
 
-/* uocr_decode_step with HOST buffers: copies token_ids/positions to the
+/* Source: [Metal] intro and "Il modello" (prefill of the prompt, with the
+ * visual tokens in the placeholder span, before token-by-token decoding);
+ * [Falcon] file table (a separate prompt pass over the whole prompt).
+ * Prefill of one row: n consecutive positions [start_pos, start_pos + n) of
+ * cache row `row`, all layers, in chunks of up to 64 tokens.  Each chunk runs
+ * the decode-step kernels once over its tokens (every weight read serves all
+ * of them, on the tensor cores), writes their keys and values, and attends
+ * causally (position p sees the slots of positions <= p).  The result is the
+ * one n decode steps of this row would give.
+ *   token_ids  device int32 [n] or NULL   exactly one of token_ids, x
+ *   x          device fp16 [n][hidden] or NULL
+ *   next_id    device int32 [1] or NULL: greedy argmax after the last token
+ *   logits     device fp32 [vocab] or NULL: logits of the last token
+ * Requires 0 <= start_pos and start_pos + n <= prefix_len + ring_len (no ring
+ * wrap inside one call).  Invalid ids / positions are reported by uocr_sync as
+ * for a step.  Asynchronous (see conventions); not captured in a graph.      */
+UOCR_API uocr_status uocr_prefill(uocr_ctx* ctx, int32_t row, const int32_t* token_ids, const uint16_t* x,
+                                  int32_t n, int32_t start_pos, int32_t* next_id, float* logits);
+
+/* Source: as uocr_decode_step; [Metal] "Dall'ABI C all'API Python" (token
+ * results returned to the host).
+ * uocr_decode_step with HOST buffers: copies token_ids/positions to the
  * device, runs the step, copies next_ids back, and returns when they are on
  * the host.                                                                  */
 UOCR_API uocr_status uocr_decode_step_host(uocr_ctx* ctx, int32_t rows, const int32_t* token_ids,
                                   const int32_t* positions, int32_t* next_ids);
 
-/* n_steps greedy steps chained on the device: step s uses positions+s and
+/* Source: as uocr_decode_step ([Metal]: the decode loop generates token by
+ * token, greedy argmax).
+ * n_steps greedy steps chained on the device: step s uses positions+s and
  * the ids produced by step s-1 (token_ids for s = 0).  out_ids: device int32
  * [n_steps][rows].  Asynchronous.                                            */
 UOCR_API uocr_status uocr_generate(uocr_ctx* ctx, int32_t rows, const int32_t* token_ids,
                           const int32_t* positions, int32_t n_steps, int32_t* out_ids);
 
-/* Zero the ring slots (and the prefix when keep_prefix == 0) of one row
+/* Source: [Metal] "Il decoder e il Mixture of Experts" (the ring bounds the
+ * memory of generated tokens).
+ * Zero the ring slots (and the prefix when keep_prefix == 0) of one row
  * (row = -1: all rows).  Attention never reads a slot not written for the
  * current sequence, so this is hygiene, not a correctness requirement.      */
 UOCR_API uocr_status uocr_kv_reset(uocr_ctx* ctx, int32_t row, int32_t keep_prefix);
 
-/* Wait for the context's work; report a device-side status raised since the
- * last uocr_sync (UOCR_E_TOKEN, UOCR_E_POSITION) and clear it.               */
+/* Source: [Metal] "Dall'ABI C all'API Python" (errors reported through the
+ * ABI, never by aborting).
+ * Wait for the context's work; report a device-side status raised since the
+ * last uocr_sync (UOCR_E_TIMEOUT, UOCR_E_TOKEN, UOCR_E_POSITION, in that order
+ * of precedence) and clear it.                                               */
 UOCR_API uocr_status uocr_sync(uocr_ctx* ctx);
 
-/* Text of the last failure on ctx ("" if none); valid until the next call.
+/* Source: [Metal] "Memoria" (refusals carry a detailed message).
+ * Text of the last failure on ctx ("" if none); valid until the next call.
  * uocr_last_error(NULL) gives the text of the last failed uocr_create on the
  * calling thread.                                                            */
 UOCR_API const char* uocr_last_error(uocr_ctx* ctx);
 
+/* Source: [Metal] "Dall'ABI C all'API Python" (memory report) and "Memoria".
+ * The bytes of each category of the context's arena (host output).         */
 UOCR_API uocr_status uocr_memory_report(uocr_ctx* ctx, uocr_mem_report* out);
 
-/* Debug taps of the last completed step (synchronous, host outputs).
+/* Source: as uocr_decode_step (the intermediate values it defines: residual
+ * after attention and after each layer; the router's choice, weights and
+ * grouping of [Metal] "Il decoder e il Mixture of Experts").
+ * Debug taps of the last completed step or prefill chunk (synchronous, host
+ * outputs; rows up to 64, the tokens of the last pass).
  *   uocr_debug_hidden: fp32 [rows][hidden] residual stream at tap `layer`:
  *     2*l   = after attention of layer l, 2*l+1 = output of layer l,
  *     -1    = input of layer 0.
@@ -252,15 +326,21 @@ UOCR_API uocr_status uocr_memory_report(uocr_ctx* ctx, uocr_mem_report* out);
 UOCR_API uocr_status uocr_debug_hidden(uocr_ctx* ctx, int32_t tap, int32_t rows, float* out);
 UOCR_API uocr_status uocr_debug_router(uocr_ctx* ctx, int32_t layer, int32_t rows, int32_t* idx,
                               float* w, int32_t* count, int32_t* offset, int32_t* perm);
-/* The fp32 router logits [rows][E] of MoE layer `layer` from the last step
+/* Source: as uocr_debug_router.
+ * The fp32 router logits [rows][E] of MoE layer `layer` from the last step
  * (the values the top-k was taken on).  Host output buffer; E_INVALID_ARG for
  * a dense layer or bad rows. */
 UOCR_API uocr_status uocr_debug_router_logits(uocr_ctx* ctx, int32_t layer, int32_t rows, float* logits);
 
-/* Per-kernel-class device time (ms) of one un-graphed step with the given
- * rows and input kind (0 = token ids, 1 = hidden vectors), measured with CUDA
- * events; names[i] points into static storage.  n_inout: in = capacity,
- * out = number of classes.  The step mutates the KV cache like a real step. */
+/* Source: [Metal] "Dall'ABI C all'API Python" (profiling through the ABI).
+ * Per-kernel-class device time (ms per step).  One whole step runs first with
+ * the given rows, input kind and inputs; then, for each kernel class, that
+ * class's launches of one step (every layer, with the step's real arguments
+ * and programmatic dependent launch between them) are captured alone in a
+ * CUDA graph and replayed 5 times, timed with CUDA events on the library
+ * stream.  names[i] points into static storage.  n_inout: in = capacity, out
+ * = number of classes.  The step mutates the KV cache like a real step (the
+ * replays rewrite the current slot with the same values).                  */
 UOCR_API uocr_status uocr_profile(uocr_ctx* ctx, int32_t rows, int32_t input_kind,
                          const int32_t* token_ids, const uint16_t* x, const int32_t* positions,
                          const char** names, float* ms, int32_t* n_inout);
@@ -288,9 +368,22 @@ UOCR_API uocr_status uocr_profile(uocr_ctx* ctx, int32_t rows, int32_t input_kin
  * All calls share the one scratch array and each call clears it first, so
  * calls whose work overlaps on the GPU (on different streams, or from
  * different contexts on the same device) race and must be serialised by the
- * caller.  Asynchronous with respect to the host.                           */
+ * caller.  The launch goes to the context's device (cfg.device), whatever
+ * device the calling thread has current; the thread's current device is left
+ * as it was.  The kernel raises no device-side status of its own (the ids
+ * and positions it would check belong to the step that produced `hidden`).
+ * Asynchronous with respect to the host.                                    */
 UOCR_API uocr_status uocr_lm_head_argmax_noalloc(uocr_ctx* ctx, int32_t rows, const float* hidden,
                                                  int32_t* next_ids, float* logits, void* stream);
+
+/* Source: [Falcon] intro and [Metal] "Dall'ABI C all'API Python" (failures are
+ * reported, never fatal); the kernels' TMA waits poll an mbarrier with an
+ * iteration limit and report UOCR_E_TIMEOUT through uocr_sync.
+ * Runs that bounded wait alone, with a short limit, on a 16-byte bulk copy
+ * that is issued (issue_copy = 1: the wait succeeds and no status is raised)
+ * or never issued (issue_copy = 0: the wait runs out, and the next uocr_sync
+ * returns UOCR_E_TIMEOUT).  Asynchronous; no copy is left in flight.        */
+UOCR_API uocr_status uocr_debug_wait_probe(uocr_ctx* ctx, int32_t issue_copy);
 
 #ifdef __cplusplus
 }

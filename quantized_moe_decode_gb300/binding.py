@@ -17,16 +17,16 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.environ.get("UOCR_LIB") or os.path.join(_PKG, "libuocr.so")
 
 UOCR_OK, UOCR_E_INVALID_ARG, UOCR_E_OOM, UOCR_E_BUDGET, UOCR_E_FORMAT = 0, 1, 2, 3, 4
-UOCR_E_STATE, UOCR_E_CUDA, UOCR_E_POSITION, UOCR_E_TOKEN = 5, 6, 7, 8
+UOCR_E_STATE, UOCR_E_CUDA, UOCR_E_POSITION, UOCR_E_TOKEN, UOCR_E_TIMEOUT = 5, 6, 7, 8, 9
 STATUS_NAMES = {0: "OK", 1: "E_INVALID_ARG", 2: "E_OOM", 3: "E_BUDGET", 4: "E_FORMAT", 5: "E_STATE",
-                6: "E_CUDA", 7: "E_POSITION", 8: "E_TOKEN"}
+                6: "E_CUDA", 7: "E_POSITION", 8: "E_TOKEN", 9: "E_TIMEOUT"}
 
 EXPORTED = ["uocr_create", "uocr_destroy", "uocr_load_weights", "uocr_kv_write_prefix", "uocr_kv_write",
             "uocr_kv_read",
             "uocr_set_sinks", "uocr_decode_step", "uocr_decode_step_embeds", "uocr_decode_step_host",
-            "uocr_generate", "uocr_kv_reset", "uocr_sync", "uocr_last_error", "uocr_memory_report",
+            "uocr_prefill", "uocr_generate", "uocr_kv_reset", "uocr_sync", "uocr_last_error", "uocr_memory_report",
             "uocr_debug_hidden", "uocr_debug_router", "uocr_debug_router_logits", "uocr_profile",
-            "uocr_lm_head_argmax_noalloc"]
+            "uocr_lm_head_argmax_noalloc", "uocr_debug_wait_probe"]
 
 
 class uocr_config(C.Structure):
@@ -68,7 +68,8 @@ def load(path: str = LIB_PATH):
         "uocr_kv_write": ([P, I, I, I, I, P, P], I),
         "uocr_set_sinks": ([P, P], I),
         "uocr_decode_step": ([P, I, P, P, P, P], I),
-        "uocr_decode_step_embeds": ([P, I, P, P, P, P, P], I),
+        "uocr_decode_step_embeds": ([P, I, P, P, P, P, P, P], I),
+        "uocr_prefill": ([P, I, P, P, I, I, P, P], I),
         "uocr_decode_step_host": ([P, I, P, P, P], I),
         "uocr_generate": ([P, I, P, P, I, P], I),
         "uocr_kv_reset": ([P, I, I], I),
@@ -80,6 +81,7 @@ def load(path: str = LIB_PATH):
         "uocr_debug_router_logits": ([P, I, I, P], I),
         "uocr_profile": ([P, I, I, P, P, P, C.POINTER(C.c_char_p), C.POINTER(C.c_float), C.POINTER(I)], I),
         "uocr_lm_head_argmax_noalloc": ([P, I, P, P, P, P], I),
+        "uocr_debug_wait_probe": ([P, I], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -178,9 +180,17 @@ class Context:
     def uocr_decode_step(self, rows, ids_ptr, pos_ptr, next_ptr, logits_ptr=0):
         self._ck(self.lib.uocr_decode_step(self.h, rows, ids_ptr, pos_ptr, next_ptr, logits_ptr or None))
 
-    def uocr_decode_step_embeds(self, rows, x_ptr, pos_ptr, y_ptr=0, next_ptr=0, logits_ptr=0):
-        self._ck(self.lib.uocr_decode_step_embeds(self.h, rows, x_ptr, pos_ptr, y_ptr or None, next_ptr or None,
-                                                  logits_ptr or None))
+    def uocr_decode_step_embeds(self, rows, x_ptr, pos_ptr, y_ptr=0, next_ptr=0, logits_ptr=0, y_f16_ptr=0):
+        self._ck(self.lib.uocr_decode_step_embeds(self.h, rows, x_ptr, pos_ptr, y_ptr or None, y_f16_ptr or None,
+                                                  next_ptr or None, logits_ptr or None))
+
+    def uocr_prefill(self, row, n, start_pos, ids_ptr=0, x_ptr=0, next_ptr=0, logits_ptr=0):
+        """Prefill n positions of cache row `row` from device token ids or fp16 hidden vectors."""
+        self._ck(self.lib.uocr_prefill(self.h, row, ids_ptr or None, x_ptr or None, n, start_pos, next_ptr or None,
+                                       logits_ptr or None))
+
+    def uocr_debug_wait_probe(self, issue_copy):
+        self._ck(self.lib.uocr_debug_wait_probe(self.h, int(issue_copy)))
 
     def uocr_decode_step_host(self, rows, ids, pos):
         ids = np.ascontiguousarray(ids, dtype=np.int32)

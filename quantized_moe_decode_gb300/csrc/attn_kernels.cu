@@ -53,8 +53,9 @@ __global__ void __launch_bounds__(UOCR_ATTN_WARPS * 32) k_attn(const AttnArgs a)
   const int s_begin = split * a.chunk;
   const int s_end = min(n_valid, s_begin + a.chunk);
   const int n_sub = s_end > s_begin ? (s_end - s_begin + SUB - 1) / SUB : 0;
-  const __half* Kg = a.kv + (((size_t)row * 2 + 0) * a.nh + head) * (size_t)a.SL * D;
-  const __half* Vg = a.kv + (((size_t)row * 2 + 1) * a.nh + head) * (size_t)a.SL * D;
+  const int kvr = a.kv_row0 + row * a.kv_rstep;
+  const __half* Kg = a.kv + (((size_t)kvr * 2 + 0) * a.nh + head) * (size_t)a.SL * D;
+  const __half* Vg = a.kv + (((size_t)kvr * 2 + 1) * a.nh + head) * (size_t)a.SL * D;
   auto issue = [&](int sb) {
     const int s0 = s_begin + sb * SUB, n = min(SUB, s_end - s0);
     uint8_t* st = smem + (sb & 1) * STAGE;
@@ -69,11 +70,15 @@ __global__ void __launch_bounds__(UOCR_ATTN_WARPS * 32) k_attn(const AttnArgs a)
     fence_mbar_init();
   }
   __syncthreads();
-  // every slot but the current token's was written by earlier steps: stream them now
-  if (threadIdx.x == 0)
+  // decode: every slot but the current token's was written by earlier steps, so
+  // stream them now (the current slot is re-read below); a prefill chunk writes
+  // many slots, so its copies start once the QKV kernel has finished
+  if (a.early && threadIdx.x == 0)
     for (int sb = 0; sb < n_sub && sb < 2; ++sb) issue(sb);
   if (!(kPdlLate & PDL_ATTN)) pdl_launch_dependents();
   pdl_wait();  // q and the current slot come from the QKV kernel
+  if (!a.early && threadIdx.x == 0)
+    for (int sb = 0; sb < n_sub && sb < 2; ++sb) issue(sb);
 
   float qv[8];
   {
@@ -271,6 +276,10 @@ __global__ void k_embed(const EmbedArgs a) {
   } else {
     src = a.x + (size_t)row * a.H;
   }
+  if (a.pos_base >= 0) {  // prefill: consecutive positions from pos_base
+    if (threadIdx.x == 0) a.pos[row] = a.pos_base + row;
+    __syncthreads();
+  }
   if (threadIdx.x == 0 && a.pos[row] < 0) atomicOr(a.status, kStatusPosition);
   for (int k = threadIdx.x * 2; k < a.H; k += blockDim.x * 2) {
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(src + k));
@@ -444,6 +453,43 @@ cudaError_t launch_pack(const PackArgs& a, cudaStream_t st) {
   const long long total = (long long)a.n_slabs * a.U * 32;
   const int blocks = (int)((total + 255) / 256);
   k_pack<<<blocks, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ fp32 -> fp16
+__global__ void k_f32_to_f16(const float* src, __half* dst, long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    dst[i] = __float2half_rn(src[i]);
+}
+
+cudaError_t launch_f32_to_f16(const float* src, __half* dst, long long n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const long long b = (n + 255) / 256;
+  k_f32_to_f16<<<(int)(b < 1024 ? b : 1024), 256, 0, st>>>(src, dst, n);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ bounded-wait probe
+// The pattern every TMA wait of the step follows (arm the barrier with the
+// bytes expected, issue the copy, poll with an iteration limit, report a
+// timeout through the status word), with a short limit and the copy issued
+// only when `issue` is set: without it the barrier's phase never completes
+// and the wait must give up and report.  No copy is left in flight either way.
+constexpr uint32_t kProbeSpinLimit = 1u << 12;
+
+__global__ void k_wait_probe(const void* src, int issue, int* status) {
+  __shared__ __align__(16) unsigned char buf[16];
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  mbar_expect_tx(&bar, 16);
+  if (issue) bulk_g2s(buf, src, 16, &bar);
+  if (!mbar_wait<kProbeSpinLimit>(&bar, 0)) atomicOr(status, kStatusTimeout);
+}
+
+cudaError_t launch_wait_probe(const void* src, int issue, int* status, cudaStream_t st) {
+  k_wait_probe<<<1, 32, 0, st>>>(src, issue, status);
   return cudaGetLastError();
 }
 

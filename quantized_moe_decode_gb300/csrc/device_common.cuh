@@ -205,8 +205,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 // Bounded wait: false after kSpinLimit polls (each poll may suspend briefly).
 constexpr uint32_t kSpinLimit = 1u << 22;
+template <uint32_t Limit = kSpinLimit>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
+  for (uint32_t i = 0; i < Limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }

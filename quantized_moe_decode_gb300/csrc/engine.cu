@@ -81,6 +81,10 @@ struct Carver {
 };
 
 constexpr int kMaxSplits = 8;  // attention splits of a (row, head): one portable thread-block cluster
+// Tokens one pass of the kernels can carry (four token groups of 16): the rows
+// of a decode step (max_rows <= 64) or one chunk of a prefill.  Activation and
+// routing buffers are sized for it; the KV cache is sized by max_rows.
+constexpr int kTokCap = 64;
 thread_local std::string g_create_err;  // text of the last failed uocr_create on this thread
 constexpr int kHistCap = 1024;
 
@@ -112,7 +116,7 @@ struct uocr_ctx {
   __half* kv = nullptr;
   size_t kv_layer = 0;  // elements per layer
   int S = 0, SL = 0;
-  float* hid = nullptr;  // [2L+1][MR][H]
+  float* hid = nullptr;  // [2L+1][kTokCap][H]
   __half* x_in = nullptr;
   float* q = nullptr;
   __half* attn_out = nullptr;
@@ -146,6 +150,7 @@ struct uocr_ctx {
 
   int H() const { return cfg.hidden; }
   int MR() const { return cfg.max_rows; }
+  int TC() const { return kTokCap; }
   bool layer_dense(int l) const { return l < cfg.n_dense_layers || cfg.n_experts == 0; }
   bool any_moe() const {
     for (int l = 0; l < cfg.n_layers; ++l)
@@ -236,6 +241,7 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
   r = uocr_mem_report{};
   const int H = c.hidden, S = c.n_heads * c.head_dim, MR = c.max_rows, Lc = c.n_layers, V = c.vocab;
   const int E = c.n_experts, k = c.top_k, Ie = c.expert_inter, Ish = c.n_shared * c.expert_inter;
+  const int TC = kTokCap;  // tokens of one pass (decode rows or a prefill chunk)
   auto mat = [&](DMat& m, int rows_packed, int K, int fmt, int count = 1) {
     m.fmt = fmt;
     m.K = K;
@@ -273,7 +279,7 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
     mat(ctx->lm, V, H, F16);
   }
   ctx->inv_freq = cv.take<double>(c.head_dim / 2, r.weights);
-  ctx->rope = cv.take<float2>((size_t)c.max_rows * (c.head_dim / 2), r.activations);
+  ctx->rope = cv.take<float2>((size_t)TC * (c.head_dim / 2), r.activations);
   ctx->sinks = cv.take<float>((size_t)Lc * c.n_heads, r.weights);
   // KV cache [L][MR][2][nh][SL][D]
   ctx->S = S;
@@ -281,26 +287,26 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
   ctx->kv_layer = (size_t)MR * 2 * c.n_heads * ctx->SL * c.head_dim;
   ctx->kv = cv.take<__half>(ctx->kv_layer * Lc, r.kv_cache);
   // activations
-  ctx->hid = cv.take<float>((size_t)(2 * Lc + 1) * MR * H, r.activations);
-  ctx->x_in = cv.take<__half>((size_t)MR * H, r.activations);
-  ctx->q = cv.take<float>((size_t)MR * S, r.activations);
-  ctx->attn_out = cv.take<__half>((size_t)MR * S, r.activations);
-  if (c.n_dense_layers > 0 || E == 0) ctx->act_dense = cv.take<__half>((size_t)MR * c.dense_inter, r.activations);
+  ctx->hid = cv.take<float>((size_t)(2 * Lc + 1) * TC * H, r.activations);
+  ctx->x_in = cv.take<__half>((size_t)TC * H, r.activations);
+  ctx->q = cv.take<float>((size_t)TC * S, r.activations);
+  ctx->attn_out = cv.take<__half>((size_t)TC * S, r.activations);
+  if (c.n_dense_layers > 0 || E == 0) ctx->act_dense = cv.take<__half>((size_t)TC * c.dense_inter, r.activations);
   if (ctx->any_moe()) {
-    ctx->xhat = cv.take<__half>((size_t)MR * H, r.activations);
-    const int TG = (MR + 15) / 16;
+    ctx->xhat = cv.take<__half>((size_t)TC * H, r.activations);
+    const int TG = (TC + 15) / 16;
     ctx->act_r = cv.take<uint8_t>((size_t)E * TG * 16 * Ie * 2, r.activations);  // 16 tokens per (expert, group)
-    ctx->act_s = cv.take<uint8_t>((size_t)(MR + 7) / 8 * 8 * (Ish > 0 ? Ish : 32) * 2, r.activations);
-    ctx->part_r = cv.take<float>((size_t)MR * k * H, r.activations);
-    ctx->part_s = cv.take<float>((size_t)MR * H, r.activations);
+    ctx->act_s = cv.take<uint8_t>((size_t)(TC + 7) / 8 * 8 * (Ish > 0 ? Ish : 32) * 2, r.activations);
+    ctx->part_r = cv.take<float>((size_t)TC * k * H, r.activations);
+    ctx->part_s = cv.take<float>((size_t)TC * H, r.activations);
     ctx->slab_counter = cv.take<int>(H / 16, r.activations);
-    ctx->r_logits = cv.take<float>((size_t)Lc * MR * E, r.routing);
-    ctx->r_idx = cv.take<int>((size_t)Lc * MR * k, r.routing);
-    ctx->r_w = cv.take<float>((size_t)Lc * MR * k, r.routing);
+    ctx->r_logits = cv.take<float>((size_t)Lc * TC * E, r.routing);
+    ctx->r_idx = cv.take<int>((size_t)Lc * TC * k, r.routing);
+    ctx->r_w = cv.take<float>((size_t)Lc * TC * k, r.routing);
     ctx->r_count = cv.take<int>((size_t)Lc * E, r.routing);
     ctx->r_offset = cv.take<int>((size_t)Lc * (E + 1), r.routing);
-    ctx->r_perm = cv.take<int>((size_t)Lc * MR * k, r.routing);
-    ctx->r_inv = cv.take<int>((size_t)Lc * MR * k, r.routing);
+    ctx->r_perm = cv.take<int>((size_t)Lc * TC * k, r.routing);
+    ctx->r_inv = cv.take<int>((size_t)Lc * TC * k, r.routing);
     ctx->r_rec = cv.take<int4>((size_t)Lc * TG * E, r.routing);
   }
   if (V > 0) {
@@ -309,8 +315,8 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
     ctx->lm_counter = cv.take<int>(1, r.logits);
   }
   ctx->next_ids = cv.take<int>(MR, r.activations);
-  ctx->ids_buf = cv.take<int>(MR, r.activations);
-  ctx->pos_buf = cv.take<int>(MR, r.activations);
+  ctx->ids_buf = cv.take<int>(TC, r.activations);
+  ctx->pos_buf = cv.take<int>(TC, r.activations);
   ctx->hist = cv.take<int>((size_t)kHistCap * MR, r.activations);
   ctx->hist_ctr = cv.take<int>(1, r.activations);
   ctx->status = cv.take<int>(1, r.activations);
@@ -320,9 +326,16 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
 // ------------------------------------------------------------------ step
 namespace {
 
+// A step that launches the kernels of one class only (`only`), for timing that
+// class on its own; `launches` counts them.
 struct Prof {
-  std::vector<std::pair<const char*, std::pair<cudaEvent_t, cudaEvent_t>>> ev;
+  const char* only = nullptr;
+  int launches = 0;
 };
+
+// kernel classes of a step, in launch order
+const char* const kClasses[] = {"embed",  "qkv",    "attention",      "o_proj",              "mlp_gate_up",
+                                "mlp_down", "router", "expert_gate_up", "expert_down_combine", "lm_head_argmax"};
 
 struct StepShape {
   int rows;
@@ -330,6 +343,11 @@ struct StepShape {
   bool lm;      // run the LM head + argmax
   bool logits;  // store logits
   bool chain;   // feed the argmax into the next step (uocr_generate)
+  // prefill chunk: every token belongs to cache row `kv_row`, at positions
+  // pos_base + t; the LM head (when lm) runs on the last token only
+  bool prefill = false;
+  int kv_row = 0;
+  int pos_base = -1;
 };
 
 }  // namespace
@@ -337,37 +355,34 @@ struct StepShape {
 static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) {
   const uocr_config& c = ctx->cfg;
   cudaStream_t st = ctx->st;
-  const int H = c.hidden, S = ctx->S, MR = ctx->MR(), rows = sh.rows;
+  const int H = c.hidden, S = ctx->S, TC = ctx->TC(), rows = sh.rows;
+  const int kv_row0 = sh.prefill ? sh.kv_row : 0, kv_rstep = sh.prefill ? 0 : 1;
   const int nt = rows <= 8 ? 1 : 2;
   const int tg = (rows + 15) / 16;  // token groups of 16 rows (one n-tile pair)
   // streaming CTAs per launch
   const int G = ctx->gemv_ctas_per_sm * ctx->n_sm;
   const int GE = ctx->expert_ctas_per_sm * ctx->n_sm;
-  const bool pdl = ctx->pdl && !prof;  // timed classes must not overlap
+  const bool pdl = ctx->pdl;
   auto gx_for = [&](int slabs) {
     int g = G / tg;
     if (g < 1) g = 1;
     return slabs < g ? slabs : g;
   };
-  auto mark = [&](const char* name, bool begin) {
-    if (!prof) return;
-    if (begin) {
-      cudaEvent_t a, b;
-      cudaEventCreate(&a);
-      cudaEventCreate(&b);
-      cudaEventRecord(a, st);
-      prof->ev.push_back({name, {a, b}});
-    } else {
-      cudaEventRecord(prof->ev.back().second.second, st);
-    }
+  // with prof->only set, only that class's kernels are launched
+  auto want = [&](const char* name) {
+    if (!prof || !prof->only) return true;
+    if (std::strcmp(prof->only, name) != 0) return false;
+    ++prof->launches;
+    return true;
   };
-  auto hid = [&](int idx) { return ctx->hid + (size_t)idx * MR * H; };
+  auto hid = [&](int idx) { return ctx->hid + (size_t)idx * TC * H; };
 
   EmbedArgs ea{};
   ea.ids = sh.ids ? ctx->ids_buf : nullptr;
   ea.x = ctx->x_in;
   ea.emb = ctx->emb;
   ea.pos = ctx->pos_buf;
+  ea.pos_base = sh.prefill ? sh.pos_base : -1;
   ea.out = hid(0);
   ea.H = H;
   ea.V = c.vocab;
@@ -375,9 +390,9 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
   ea.rope = ctx->rope;
   ea.half_d = c.head_dim / 2;
   ea.status = ctx->status;
-  mark("embed", true);
-  CK(launch_embed(ea, rows, st), "embed launch");
-  mark("embed", false);
+  if (want("embed")) {
+    CK(launch_embed(ea, rows, st), "embed launch");
+  }
 
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& w = ctx->L[l];
@@ -401,10 +416,12 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     qa.P = c.prefix_len;
     qa.R = c.ring_len;
     qa.SL = ctx->SL;
+    qa.kv_row0 = kv_row0;
+    qa.kv_rstep = kv_rstep;
     qa.status = ctx->status;
-    mark("qkv", true);
-    CK(launch_gemv(c.fmt_attn, SRC_NORM, EPI_QKV, qa, gx_for(w.qkv.n_slabs), tg, st, pdl), "qkv launch");
-    mark("qkv", false);
+    if (want("qkv")) {
+      CK(launch_gemv(c.fmt_attn, SRC_NORM, EPI_QKV, qa, gx_for(w.qkv.n_slabs), tg, st, pdl), "qkv launch");
+    }
     // attention
     AttnArgs aa{};
     aa.q = ctx->q;
@@ -417,6 +434,9 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     aa.P = c.prefix_len;
     aa.R = c.ring_len;
     aa.SL = ctx->SL;
+    aa.kv_row0 = kv_row0;
+    aa.kv_rstep = kv_rstep;
+    aa.early = sh.prefill ? 0 : 1;
     aa.status = ctx->status;
     {
       int ns = (2 * ctx->n_sm + rows * c.n_heads - 1) / (rows * c.n_heads);
@@ -428,9 +448,9 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       aa.chunk = (ctx->SL + ns - 1) / ns;
     }
     aa.scale = 1.0f / sqrtf((float)c.head_dim);
-    mark("attention", true);
-    CK(launch_attn(aa, rows, st, pdl), "attention launch");
-    mark("attention", false);
+    if (want("attention")) {
+      CK(launch_attn(aa, rows, st, pdl), "attention launch");
+    }
     // O projection + residual
     GemvArgs oa{};
     oa.w = w.o.view();
@@ -442,9 +462,9 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     oa.out_f = hid(2 * l + 1);
     oa.ld_out = H;
     oa.status = ctx->status;
-    mark("o_proj", true);
-    CK(launch_gemv(c.fmt_attn, SRC_F16, EPI_RESID, oa, gx_for(w.o.n_slabs), tg, st, pdl), "o_proj launch");
-    mark("o_proj", false);
+    if (want("o_proj")) {
+      CK(launch_gemv(c.fmt_attn, SRC_F16, EPI_RESID, oa, gx_for(w.o.n_slabs), tg, st, pdl), "o_proj launch");
+    }
     if (w.dense) {
       GemvArgs ga{};
       ga.w = w.gateup.view();
@@ -457,10 +477,10 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       ga.out_h = ctx->act_dense;
       ga.ld_out = c.dense_inter;
       ga.status = ctx->status;
-      mark("mlp_gate_up", true);
-      CK(launch_gemv(c.fmt_dense, SRC_NORM, EPI_SWIGLU, ga, gx_for(w.gateup.n_slabs), tg, st, pdl),
-         "gate/up launch");
-      mark("mlp_gate_up", false);
+      if (want("mlp_gate_up")) {
+        CK(launch_gemv(c.fmt_dense, SRC_NORM, EPI_SWIGLU, ga, gx_for(w.gateup.n_slabs), tg, st, pdl),
+           "gate/up launch");
+      }
       GemvArgs da{};
       da.w = w.down.view();
       da.sp = plan_stream(nt, c.fmt_dense, c.dense_inter);
@@ -471,9 +491,9 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       da.out_f = hid(2 * l + 2);
       da.ld_out = H;
       da.status = ctx->status;
-      mark("mlp_down", true);
-      CK(launch_gemv(c.fmt_dense, SRC_F16, EPI_RESID, da, gx_for(w.down.n_slabs), tg, st, pdl), "down launch");
-      mark("mlp_down", false);
+      if (want("mlp_down")) {
+        CK(launch_gemv(c.fmt_dense, SRC_F16, EPI_RESID, da, gx_for(w.down.n_slabs), tg, st, pdl), "down launch");
+      }
     } else {
       const int E = c.n_experts, k = c.top_k;
       // Routed units: active slots when few experts are expected to receive a
@@ -484,7 +504,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       const double exp_act = E * (1.0 - pow(1.0 - (double)k / E, rows));
       const int by_slot = exp_act < 0.75 * E && tg == 1;
       const int n_units = by_slot ? max_act : E;
-      int4* rec = ctx->r_rec + (size_t)l * ((MR + 15) / 16) * E;
+      int4* rec = ctx->r_rec + (size_t)l * ((TC + 15) / 16) * E;
 
       RouterArgs ra{};
       ra.w = w.router.view();
@@ -496,17 +516,17 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       ra.h = hid(2 * l + 1);
       ra.norm_w = w.mlp_norm;
       ra.eps = c.rms_eps;
-      ra.logits = ctx->r_logits + (size_t)l * MR * E;
+      ra.logits = ctx->r_logits + (size_t)l * TC * E;
       ra.tg = tg;
       ra.by_slot = by_slot;
       ra.n_units = n_units;
-      ra.idx = ctx->r_idx + (size_t)l * MR * k;
-      ra.wts = ctx->r_w + (size_t)l * MR * k;
+      ra.idx = ctx->r_idx + (size_t)l * TC * k;
+      ra.wts = ctx->r_w + (size_t)l * TC * k;
       ra.rec = rec;
       ra.status = ctx->status;
-      mark("router", true);
-      CK(launch_router(ra, st, pdl), "router launch");
-      mark("router", false);
+      if (want("router")) {
+        CK(launch_router(ra, st, pdl), "router launch");
+      }
 
       const int fs = ctx->shared_fmt();
       ExpertArgs xa{};
@@ -522,8 +542,8 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       xa.wts = ra.wts;
       xa.count = ctx->r_count + (size_t)l * E;
       xa.offset = ctx->r_offset + (size_t)l * (E + 1);
-      xa.perm = ctx->r_perm + (size_t)l * MR * k;
-      xa.inv = ctx->r_inv + (size_t)l * MR * k;
+      xa.perm = ctx->r_perm + (size_t)l * TC * k;
+      xa.inv = ctx->r_inv + (size_t)l * TC * k;
       xa.h = hid(2 * l + 1);
       xa.norm_w = w.mlp_norm;
       xa.eps = c.rms_eps;
@@ -567,9 +587,9 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       xa.ws = shg ? shg->view() : PMat{};
       xa.sp = plan_stream(nt, c.fmt_routed, H, 16);
       split(w.ex_gateup, shg, w.ex_gateup.n_slabs, shg ? shg->n_slabs : 0);
-      mark("expert_gate_up", true);
-      CK(launch_expert_gateup(c.fmt_routed, fs, xa, st, pdl), "expert gate/up launch");
-      mark("expert_gate_up", false);
+      if (want("expert_gate_up")) {
+        CK(launch_expert_gateup(c.fmt_routed, fs, xa, st, pdl), "expert gate/up launch");
+      }
       // down + combine
       xa.wr = w.ex_down.view(1);
       xa.ws = shd ? shd->view() : PMat{};
@@ -578,18 +598,21 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
         xa.sp = plan_stream(nt, c.fmt_routed, 0, 0, nt * (kmax / 32) * 512);
       }
       split(w.ex_down, shd, H / 16, H / 16);
-      mark("expert_down_combine", true);
-      CK(launch_expert_down(c.fmt_routed, fs, xa, st, pdl), "expert down launch");
-      mark("expert_down_combine", false);
+      if (want("expert_down_combine")) {
+        CK(launch_expert_down(c.fmt_routed, fs, xa, st, pdl), "expert down launch");
+      }
     }
   }
 
   if (sh.lm) {
+    // a prefill chunk needs the next id after its last token only
+    const int lm_rows = sh.prefill ? 1 : rows;
+    const int lm_nt = lm_rows <= 8 ? 1 : 2, lm_tg = (lm_rows + 15) / 16;
     GemvArgs la{};
     la.w = ctx->lm.view();
-    la.sp = plan_stream(nt, F16, H);
-    la.ntok = rows;
-    la.xf = hid(2 * c.n_layers);
+    la.sp = plan_stream(lm_nt, F16, H);
+    la.ntok = lm_rows;
+    la.xf = hid(2 * c.n_layers) + (size_t)(rows - lm_rows) * H;
     la.ld_src = H;
     la.norm_w = ctx->final_norm;
     la.eps = c.rms_eps;
@@ -605,9 +628,11 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       la.hist = ctx->hist;
       la.hist_ctr = ctx->hist_ctr;
     }
-    mark("lm_head_argmax", true);
-    CK(launch_gemv(F16, SRC_NORM, EPI_LOGITS, la, gx_for(ctx->lm.n_slabs), tg, st, pdl), "lm head launch");
-    mark("lm_head_argmax", false);
+    if (want("lm_head_argmax")) {
+      int lgx = G / lm_tg;
+      lgx = lgx < 1 ? 1 : lgx > ctx->lm.n_slabs ? ctx->lm.n_slabs : lgx;
+      CK(launch_gemv(F16, SRC_NORM, EPI_LOGITS, la, lgx, lm_tg, st, pdl), "lm head launch");
+    }
   }
   return UOCR_OK;
 }
@@ -885,6 +910,9 @@ static cudaError_t noalloc_scratch(int device, unsigned long long** out) {
   return cudaSuccess;
 }
 
+static uocr_status noalloc_launch(uocr_ctx* ctx, int rows, const float* hidden, int32_t* next_ids, float* logits,
+                                  unsigned long long* scratch, cudaStream_t st);
+
 // ------------------------------------------------------------------ C ABI
 extern "C" {
 
@@ -1106,7 +1134,7 @@ uocr_status uocr_decode_step(uocr_ctx* ctx, int32_t rows, const int32_t* token_i
 }
 
 uocr_status uocr_decode_step_embeds(uocr_ctx* ctx, int32_t rows, const uint16_t* x, const int32_t* positions,
-                                    float* y, int32_t* next_ids, float* logits) {
+                                    float* y, uint16_t* y_f16, int32_t* next_ids, float* logits) {
   if (!ctx) return UOCR_E_INVALID_ARG;
   std::lock_guard<std::mutex> lk(ctx->mu);
   if (!x || !positions) return ctx->fail(UOCR_E_INVALID_ARG, "NULL device pointer");
@@ -1119,10 +1147,9 @@ uocr_status uocr_decode_step_embeds(uocr_ctx* ctx, int32_t rows, const uint16_t*
   CK(cudaMemcpyAsync(ctx->pos_buf, positions, rows * 4, cudaMemcpyDeviceToDevice, ctx->st), "positions copy");
   s = run_step(ctx, StepShape{rows, false, lm, logits != nullptr, false});
   if (s != UOCR_OK) return s;
-  if (y)
-    CK(cudaMemcpyAsync(y, ctx->hid + (size_t)2 * ctx->cfg.n_layers * ctx->MR() * H, (size_t)rows * H * 4,
-                       cudaMemcpyDeviceToDevice, ctx->st),
-       "y copy");
+  const float* last = ctx->hid + (size_t)2 * ctx->cfg.n_layers * ctx->TC() * H;
+  if (y) CK(cudaMemcpyAsync(y, last, (size_t)rows * H * 4, cudaMemcpyDeviceToDevice, ctx->st), "y copy");
+  if (y_f16) CK(launch_f32_to_f16(last, reinterpret_cast<__half*>(y_f16), (long long)rows * H, ctx->st), "y_f16");
   if (next_ids) CK(cudaMemcpyAsync(next_ids, ctx->next_ids, rows * 4, cudaMemcpyDeviceToDevice, ctx->st), "ids copy");
   if (logits)
     CK(cudaMemcpyAsync(logits, ctx->logits, (size_t)rows * ctx->cfg.vocab * 4, cudaMemcpyDeviceToDevice, ctx->st),
@@ -1145,6 +1172,55 @@ uocr_status uocr_decode_step_host(uocr_ctx* ctx, int32_t rows, const int32_t* to
   if (s != UOCR_OK) return s;
   CK(cudaMemcpyAsync(next_ids, ctx->next_ids, rows * 4, cudaMemcpyDeviceToHost, ctx->st), "ids copy");
   CK(cudaStreamSynchronize(ctx->st), "step");
+  return UOCR_OK;
+}
+
+uocr_status uocr_prefill(uocr_ctx* ctx, int32_t row, const int32_t* token_ids, const uint16_t* x, int32_t n,
+                         int32_t start_pos, int32_t* next_id, float* logits) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  const uocr_config& c = ctx->cfg;
+  if ((token_ids == nullptr) == (x == nullptr))
+    return ctx->fail(UOCR_E_INVALID_ARG, "prefill: give exactly one of token_ids and x");
+  if (token_ids && c.vocab <= 0) return ctx->fail(UOCR_E_STATE, "prefill from token ids needs a vocabulary");
+  if ((next_id || logits) && c.vocab <= 0) return ctx->fail(UOCR_E_STATE, "next_id/logits need a vocabulary");
+  if (row < 0 || row >= c.max_rows) return ctx->fail(UOCR_E_INVALID_ARG, "prefill: row %d outside [0, %d)", row,
+                                                     c.max_rows);
+  if (n < 1 || start_pos < 0 || (long long)start_pos + n > (long long)ctx->SL)
+    return ctx->fail(UOCR_E_INVALID_ARG,
+                     "prefill: positions [%d, %d) must lie in [0, prefix_len + ring_len = %d) (no ring wrap)",
+                     start_pos, start_pos + n, ctx->SL);
+  uocr_status s = check_complete(ctx);
+  if (s != UOCR_OK) return s;
+  CK(cudaEventRecord(ctx->ev_in, ctx->ust), "event record");
+  CK(cudaStreamWaitEvent(ctx->st, ctx->ev_in, 0), "stream wait");
+  const int H = c.hidden, TC = ctx->TC();
+  for (int off = 0; off < n; off += TC) {
+    const int m = n - off < TC ? n - off : TC;
+    const bool last = off + m == n;
+    if (token_ids)
+      CK(cudaMemcpyAsync(ctx->ids_buf, token_ids + off, (size_t)m * 4, cudaMemcpyDeviceToDevice, ctx->st), "ids copy");
+    else
+      CK(cudaMemcpyAsync(ctx->x_in, x + (size_t)off * H, (size_t)m * H * 2, cudaMemcpyDeviceToDevice, ctx->st),
+         "x copy");
+    StepShape sh{m, token_ids != nullptr, last && (next_id || logits), last && logits != nullptr, false};
+    sh.prefill = true;
+    sh.kv_row = row;
+    sh.pos_base = start_pos + off;
+    s = enqueue_step(ctx, sh, nullptr);
+    if (s != UOCR_OK) return s;
+  }
+  if (next_id) CK(cudaMemcpyAsync(next_id, ctx->next_ids, 4, cudaMemcpyDeviceToDevice, ctx->st), "id copy");
+  if (logits)
+    CK(cudaMemcpyAsync(logits, ctx->logits, (size_t)c.vocab * 4, cudaMemcpyDeviceToDevice, ctx->st), "logits copy");
+  return step_epilogue(ctx);
+}
+
+uocr_status uocr_debug_wait_probe(uocr_ctx* ctx, int32_t issue_copy) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  // the 16-byte source is the (256-byte aligned) history buffer of the arena
+  CK(launch_wait_probe(ctx->hist, issue_copy ? 1 : 0, ctx->status, ctx->st), "wait probe launch");
   return UOCR_OK;
 }
 
@@ -1197,7 +1273,8 @@ uocr_status uocr_sync(uocr_ctx* ctx) {
   CK(cudaMemcpy(&st, ctx->status, 4, cudaMemcpyDeviceToHost), "status read");
   if (st) {
     CK(cudaMemset(ctx->status, 0, 4), "status clear");
-    if (st & kStatusTimeout) return ctx->fail(UOCR_E_CUDA, "a kernel's bounded wait for its weight copies timed out");
+    if (st & kStatusTimeout)
+      return ctx->fail(UOCR_E_TIMEOUT, "a kernel's bounded wait for its asynchronous copies ran out");
     if (st & kStatusToken) return ctx->fail(UOCR_E_TOKEN, "a token id was outside [0, vocab)");
     return ctx->fail(UOCR_E_POSITION, "a position was negative");
   }
@@ -1220,10 +1297,10 @@ uocr_status uocr_debug_hidden(uocr_ctx* ctx, int32_t tap, int32_t rows, float* o
   if (!ctx) return UOCR_E_INVALID_ARG;
   std::lock_guard<std::mutex> lk(ctx->mu);
   const uocr_config& c = ctx->cfg;
-  if (!out || tap < -1 || tap >= 2 * c.n_layers || rows < 1 || rows > c.max_rows)
+  if (!out || tap < -1 || tap >= 2 * c.n_layers || rows < 1 || rows > ctx->TC())
     return ctx->fail(UOCR_E_INVALID_ARG, "debug_hidden: bad tap/rows");
   CK(cudaStreamSynchronize(ctx->st), "sync");
-  CK(cudaMemcpy(out, ctx->hid + (size_t)(tap + 1) * ctx->MR() * c.hidden, (size_t)rows * c.hidden * 4,
+  CK(cudaMemcpy(out, ctx->hid + (size_t)(tap + 1) * ctx->TC() * c.hidden, (size_t)rows * c.hidden * 4,
                 cudaMemcpyDeviceToHost),
      "hidden read");
   return UOCR_OK;
@@ -1234,10 +1311,10 @@ uocr_status uocr_debug_router(uocr_ctx* ctx, int32_t layer, int32_t rows, int32_
   if (!ctx) return UOCR_E_INVALID_ARG;
   std::lock_guard<std::mutex> lk(ctx->mu);
   const uocr_config& c = ctx->cfg;
-  if (layer < 0 || layer >= c.n_layers || ctx->layer_dense(layer) || rows < 1 || rows > c.max_rows)
+  if (layer < 0 || layer >= c.n_layers || ctx->layer_dense(layer) || rows < 1 || rows > ctx->TC())
     return ctx->fail(UOCR_E_INVALID_ARG, "debug_router: not a MoE layer or bad rows");
   CK(cudaStreamSynchronize(ctx->st), "sync");
-  const size_t MR = ctx->MR(), k = c.top_k, E = c.n_experts;
+  const size_t MR = ctx->TC(), k = c.top_k, E = c.n_experts;
   if (idx) CK(cudaMemcpy(idx, ctx->r_idx + layer * MR * k, rows * k * 4, cudaMemcpyDeviceToHost), "router read");
   if (w) CK(cudaMemcpy(w, ctx->r_w + layer * MR * k, rows * k * 4, cudaMemcpyDeviceToHost), "router read");
   if (count) CK(cudaMemcpy(count, ctx->r_count + layer * E, E * 4, cudaMemcpyDeviceToHost), "router read");
@@ -1250,10 +1327,10 @@ uocr_status uocr_debug_router_logits(uocr_ctx* ctx, int32_t layer, int32_t rows,
   if (!ctx) return UOCR_E_INVALID_ARG;
   std::lock_guard<std::mutex> lk(ctx->mu);
   const uocr_config& c = ctx->cfg;
-  if (layer < 0 || layer >= c.n_layers || ctx->layer_dense(layer) || rows < 1 || rows > c.max_rows || !logits)
+  if (layer < 0 || layer >= c.n_layers || ctx->layer_dense(layer) || rows < 1 || rows > ctx->TC() || !logits)
     return ctx->fail(UOCR_E_INVALID_ARG, "debug_router_logits: not a MoE layer, bad rows or NULL output");
   CK(cudaStreamSynchronize(ctx->st), "sync");
-  const size_t MR = ctx->MR(), E = c.n_experts;
+  const size_t MR = ctx->TC(), E = c.n_experts;
   CK(cudaMemcpy(logits, ctx->r_logits + layer * MR * E, rows * E * 4, cudaMemcpyDeviceToHost), "router read");
   return UOCR_OK;
 }
@@ -1274,31 +1351,60 @@ uocr_status uocr_profile(uocr_ctx* ctx, int32_t rows, int32_t input_kind, const 
   else
     CK(cudaMemcpyAsync(ctx->x_in, x, (size_t)rows * ctx->cfg.hidden * 2, cudaMemcpyDeviceToDevice, ctx->st), "x copy");
   CK(cudaMemcpyAsync(ctx->pos_buf, positions, rows * 4, cudaMemcpyDeviceToDevice, ctx->st), "positions copy");
-  Prof prof;
-  s = enqueue_step(ctx, StepShape{rows, ids, ctx->cfg.vocab > 0, false, false}, &prof);
-  CK(cudaStreamSynchronize(ctx->st), "profile step");
-  std::vector<const char*> nm;
-  std::vector<float> tot;
-  for (auto& e : prof.ev) {
-    float t = 0.f;
-    cudaEventElapsedTime(&t, e.second.first, e.second.second);
-    cudaEventDestroy(e.second.first);
-    cudaEventDestroy(e.second.second);
-    size_t i = 0;
-    while (i < nm.size() && std::strcmp(nm[i], e.first) != 0) ++i;
-    if (i == nm.size()) {
-      nm.push_back(e.first);
-      tot.push_back(0.f);
-    }
-    tot[i] += t;
-  }
+  const StepShape sh{rows, ids, ctx->cfg.vocab > 0, false, false};
+  // one whole step, so that every buffer a class reads holds a real step's values
+  s = enqueue_step(ctx, sh, nullptr);
   if (s != UOCR_OK) return s;
-  const int n = (int)nm.size() < *n_inout ? (int)nm.size() : *n_inout;
-  for (int i = 0; i < n; ++i) {
-    names[i] = nm[i];
-    ms[i] = tot[i];
+  // then each class alone: its launches of one step (every layer, real arguments,
+  // programmatic dependent launch between them) captured in a graph and replayed
+  constexpr int kReps = 5;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  CK(cudaEventCreate(&e0), "event");
+  CK(cudaEventCreate(&e1), "event");
+  int n = 0;
+  uocr_status out = UOCR_OK;
+  for (const char* cls : kClasses) {
+    Prof pf;
+    pf.only = cls;
+    cudaGraph_t g = nullptr;
+    cudaGraphExec_t ge = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(ctx->st, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) {
+      out = ctx->cuda(e, "profile capture");
+      break;
+    }
+    s = enqueue_step(ctx, sh, &pf);
+    e = cudaStreamEndCapture(ctx->st, &g);
+    if (s == UOCR_OK && e != cudaSuccess) s = ctx->cuda(e, "profile capture");
+    if (s == UOCR_OK && pf.launches > 0) s = ctx->cuda(cudaGraphInstantiate(&ge, g, 0), "profile instantiate");
+    if (g) cudaGraphDestroy(g);
+    if (s != UOCR_OK) {
+      out = s;
+      break;
+    }
+    if (pf.launches == 0) continue;
+    float t = 0.f;
+    e = cudaGraphLaunch(ge, ctx->st);  // warm-up replay
+    if (e == cudaSuccess) e = cudaEventRecord(e0, ctx->st);
+    for (int r = 0; r < kReps && e == cudaSuccess; ++r) e = cudaGraphLaunch(ge, ctx->st);
+    if (e == cudaSuccess) e = cudaEventRecord(e1, ctx->st);
+    if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, e0, e1);
+    cudaGraphExecDestroy(ge);
+    if (e != cudaSuccess) {
+      out = ctx->cuda(e, "profile replay");
+      break;
+    }
+    if (n < *n_inout) {
+      names[n] = cls;
+      ms[n] = t / kReps;
+    }
+    ++n;
   }
-  *n_inout = (int)nm.size();
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (out != UOCR_OK) return out;
+  *n_inout = n;
   return step_epilogue(ctx);
 }
 
@@ -1317,12 +1423,26 @@ uocr_status uocr_lm_head_argmax_noalloc(uocr_ctx* ctx, int32_t rows, const float
   unsigned long long* scratch = nullptr;
   CK(noalloc_scratch(c.device, &scratch), "scratch address");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // launch on the context's device, whatever device the calling thread has current
+  int prev = 0;
+  CK(cudaGetDevice(&prev), "current device");
+  if (prev != c.device) CK(cudaSetDevice(c.device), "set device");
+  const uocr_status ls = noalloc_launch(ctx, rows, hidden, next_ids, logits, scratch, st);
+  if (prev != c.device) CK(cudaSetDevice(prev), "restore device");
+  return ls;
+}
+
+}  // extern "C"
+
+static uocr_status noalloc_launch(uocr_ctx* ctx, int rows, const float* hidden, int32_t* next_ids, float* logits,
+                                  unsigned long long* scratch, cudaStream_t st) {
+  const uocr_config& c = ctx->cfg;
   // the keys and the counter must start at zero; a previous call leaves them zero
   // when it completes, but clear them anyway in case it did not
   CK(cudaMemsetAsync(scratch, 0, sizeof(unsigned long long) * (kNoAllocMaxRows + 1), st), "scratch clear");
   const int nt = rows <= 8 ? 1 : 2;
-  const int tg = (rows + nt * 8 - 1) / (nt * 8);
-  int gx = ctx->n_sm / tg;
+  const int tg = (rows + 15) / 16;
+  int gx = ctx->gemv_ctas_per_sm * ctx->n_sm / tg;  // the grid of the step's LM-head launch
   if (gx < 1) gx = 1;
   if (gx > ctx->lm.n_slabs) gx = ctx->lm.n_slabs;
   GemvArgs la{};
@@ -1342,5 +1462,3 @@ uocr_status uocr_lm_head_argmax_noalloc(uocr_ctx* ctx, int32_t rows, const float
   CK(launch_gemv(F16, SRC_NORM, EPI_LOGITS, la, gx, tg, st, false), "lm head launch");
   return UOCR_OK;
 }
-
-}  // extern "C"

@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
           qo[dhi] = vhi;
         } else {
           const int slot = pos < a.P ? pos : a.P + (pos - a.P) % a.R;
-          __half* c_ = a.kv + ((((size_t)gt * 2 + (sec - 1)) * a.nh + head) * a.SL + slot) * a.D;
+          const int kvr = a.kv_row0 + gt * a.kv_rstep;
+          __half* c_ = a.kv + ((((size_t)kvr * 2 + (sec - 1)) * a.nh + head) * a.SL + slot) * a.D;
           c_[dlo] = __float2half_rn(vlo);
           c_[dhi] = __float2half_rn(vhi);
         }

@@ -49,6 +49,7 @@ struct GemvArgs {
   __half* kv;               // layer base [rows][2][nh][SL][D]
   const float2* rope;       // [rows][D/2] (cos, sin) of the step's positions
   int nh, D, S, P, R, SL;
+  int kv_row0, kv_rstep;    // token t writes cache row kv_row0 + t * kv_rstep (decode: 0, 1; prefill: row, 0)
   // EPI_LOGITS
   int n_valid;              // vocab
   unsigned long long* keys; // [rows]
@@ -117,6 +118,9 @@ struct AttnArgs {
   __half* out;              // [rows][nh*D]
   const float* sink;        // [nh] or nullptr
   int nh, D, P, R, SL, nsplit, chunk;
+  int kv_row0, kv_rstep;    // token t reads cache row kv_row0 + t * kv_rstep
+  int early;                // 1: stage the first K/V blocks before waiting for the QKV kernel
+                            //    (decode: only the current slot changes, and it is re-read)
   float scale;
   int* status;
 };
@@ -125,7 +129,8 @@ struct EmbedArgs {
   const int* ids;           // nullable (hidden-vector input)
   const __half* x;          // [rows][H] when ids == nullptr
   const __half* emb;        // [V][H]
-  const int* pos;
+  int* pos;                 // [rows]; written as pos_base + row when pos_base >= 0 (prefill)
+  int pos_base;
   float* out;               // [rows][H]
   int H, V;
   // the step's rotary table: rope[row][j] = (cos, sin) of pos * inv_freq[j]
@@ -217,6 +222,10 @@ cudaError_t launch_attn(const AttnArgs& a, int rows, cudaStream_t st, bool pdl);
 cudaError_t launch_embed(const EmbedArgs& a, int rows, cudaStream_t st);
 cudaError_t launch_pack(const PackArgs& a, cudaStream_t st);
 cudaError_t launch_fill_zero_ring(__half* kv_layer_row, int nh, int SL, int D, int from_slot, cudaStream_t st);
+cudaError_t launch_f32_to_f16(const float* src, __half* dst, long long n, cudaStream_t st);
+// A bounded mbarrier wait on a copy of 16 bytes from src that is issued only
+// when `issue` is set; a wait that runs out sets kStatusTimeout in *status.
+cudaError_t launch_wait_probe(const void* src, int issue, int* status, cudaStream_t st);
 cudaError_t init_kernel_attributes();
 int attn_smem_bytes(int D);
 

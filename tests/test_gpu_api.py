@@ -144,3 +144,61 @@ def test_kv_reset_keeps_prefix_and_clears_ring(cuda):
     assert np.array_equal(k_after[:, :P], k_before[:, :P])
     assert not np.any(k_after[:, P:]) and not np.any(v_after[:, P:])
     ctx.close()
+
+
+def test_bounded_wait_reports_timeout_and_context_stays_usable(cuda):
+    """The TMA waits poll an mbarrier with an iteration limit.  The probe runs
+    that wait with a short limit: with its 16-byte copy issued the wait
+    succeeds; with the copy never issued it runs out, uocr_sync reports
+    UOCR_E_TIMEOUT once, and the context still decodes."""
+    torch = cuda
+    wl = _wl(seed=205)
+    ctx = make_ctx(wl)
+    ctx.uocr_debug_wait_probe(1)
+    ctx.uocr_sync()  # the copy landed: no status
+    ctx.uocr_debug_wait_probe(0)
+    with pytest.raises(binding.UocrError) as e:
+        ctx.uocr_sync()
+    assert e.value.status == binding.UOCR_E_TIMEOUT
+    ctx.uocr_sync()  # cleared
+    ref = make_ctx(wl)
+    assert np.array_equal(_greedy_steps(ctx, torch, wl, 3), _greedy_steps(ref, torch, wl, 3))
+    ctx.close()
+    ref.close()
+
+
+def test_embeds_step_fp16_output_is_the_rounded_fp32_output(cuda):
+    torch = cuda
+    cfg = _cfg(vocab=0)
+    wl = synth.make_workload("api_x", cfg, 4, 2, 206)
+    ctx = make_ctx(wl)
+    x = torch.from_numpy(np.ascontiguousarray(wl.step_x[0]).view(np.int16)).cuda()
+    pos = torch.full((4,), wl.start_pos, dtype=torch.int32, device="cuda")
+    y = torch.zeros((4, cfg.hidden), dtype=torch.float32, device="cuda")
+    y16 = torch.zeros((4, cfg.hidden), dtype=torch.int16, device="cuda")
+    ctx.uocr_decode_step_embeds(4, x.data_ptr(), pos.data_ptr(), y_ptr=y.data_ptr(), y_f16_ptr=y16.data_ptr())
+    ctx.uocr_sync()
+    got = y16.cpu().numpy().view(np.float16)
+    assert np.array_equal(got, y.cpu().numpy().astype(np.float16))
+    ctx.close()
+
+
+def test_prefill_refusals(cuda):
+    torch = cuda
+    wl = _wl(seed=207)
+    ctx = make_ctx(wl)
+    ids = torch.zeros(8, dtype=torch.int32, device="cuda")
+    x = torch.zeros((8, wl.cfg.hidden), dtype=torch.int16, device="cuda")
+    SL = wl.cfg.prefix_len + wl.cfg.ring_len
+    for kw, st in ((dict(ids_ptr=ids.data_ptr(), x_ptr=x.data_ptr()), binding.UOCR_E_INVALID_ARG),
+                   (dict(), binding.UOCR_E_INVALID_ARG)):
+        with pytest.raises(binding.UocrError) as e:
+            ctx.uocr_prefill(0, 4, 0, **kw)
+        assert e.value.status == st
+    for row, n, start in ((-1, 4, 0), (4, 4, 0), (0, 0, 0), (0, 4, -1), (0, 4, SL - 3)):
+        with pytest.raises(binding.UocrError) as e:
+            ctx.uocr_prefill(row, n, start, ids_ptr=ids.data_ptr())
+        assert e.value.status == binding.UOCR_E_INVALID_ARG, (row, n, start)
+    ctx.uocr_prefill(0, 3, SL - 3, ids_ptr=ids.data_ptr())  # the last ring slots, no wrap
+    ctx.uocr_sync()
+    ctx.close()

@@ -42,7 +42,8 @@ def _cache():
 def _report(name, st):
     print(f"\n{name}: {st.steps} steps, {st.float_checks} float checks (worst rel-L2 {st.worst_rel:.2e}, "
           f"max-abs {st.worst_abs:.2e}), router {st.router_checks} ({st.router_near_ties} near ties), "
-          f"ids {st.id_checks} ({st.id_near_ties} near ties), kv {st.kv_checks}; worst: {st.worst_name}")
+          f"ids {st.id_checks} ({st.id_near_ties} near ties), kv {st.kv_checks}, grouping rows "
+          f"{st.grouping_checks}, worst weights {st.worst_weights_rel:.2e}; worst: {st.worst_name}")
 
 
 def test_dense_layer_b1_full(cuda):
@@ -74,6 +75,40 @@ def test_full_b8_prefill_and_greedy_sampled_rows(cuda):
     st = run_parity(ctx, wl, n_step, orc, rows=wl.rows, row_map=sample)
     _report(wl.name, st)
     assert st.id_checks >= 2 * n_step
+    ctx.close()
+
+
+def test_full_b8_uocr_prefill_then_greedy_sampled_rows(cuda):
+    """The 288-token prefix of every row built by uocr_prefill (256 embeddings in
+    four chunks, then 32 prompt ids), against the oracle's prefill-by-decode:
+    every layer's prefix keys and values, the last token's layer taps, logits and
+    id of the sampled rows; then greedy steps from that cache."""
+    wl = synth.workload("full_b8")
+    sample = [0, 7]
+    ctx = make_ctx(wl)
+    orc = make_oracle(wl, rows=sample, cache=_cache())
+    n_step = 8
+    st = run_parity(ctx, wl, n_step, orc, rows=wl.rows, row_map=sample, lib_prefill=True)
+    _report(wl.name + " (uocr_prefill)", st)
+    assert st.kv_checks >= 2 * wl.cfg.n_layers
+    assert st.id_checks >= 2 * (n_step + 1)
+    ctx.close()
+
+
+def test_router_same_inputs_stress_scale_64_rows(cuda):
+    """The router where both sides see the same inputs: one MoE layer of the
+    stress workload's shape (router logits ~N(0,1), 64 rows in four token groups,
+    all experts Q4_0) fed the same hidden vectors.  Router logits and routing
+    weights are held to the stated tolerance (rel-L2 2e-3), router sets to the
+    tight 1e-3 gap, and the grouping to the oracle's."""
+    cfg = synth.config_moe_layer().replace(max_rows=64, prefix_len=64,
+                                          router_std=float(1.0 / np.sqrt(1280.0)))
+    wl = synth.make_workload("router_b64", cfg, 64, 4, 5)
+    ctx = make_ctx(wl)
+    st = run_parity(ctx, wl, 4, make_oracle(wl, cache=_cache()), same_router_input=True)
+    _report(wl.name, st)
+    assert st.router_checks == 64 * 4 and st.grouping_checks >= 64 * 4 - st.router_near_ties
+    print(f"worst routing-weight rel-L2 {st.worst_weights_rel:.2e}")
     ctx.close()
 
 
@@ -143,6 +178,7 @@ def test_stress_b64_sampled_rows(cuda):
     st = run_parity(ctx, wl, wl.steps, make_oracle(wl, rows=sample, cache=_cache()), rows=wl.rows,
                     row_map=sample)
     _report(wl.name, st)
+    print(f"worst routing-weight rel-L2 {st.worst_weights_rel:.2e}, grouping rows {st.grouping_checks}")
     # a row's id is not compared at a step where its router set differed at a near tie
     assert st.id_checks >= 0.85 * len(sample) * wl.steps
     assert st.router_near_ties <= 0.02 * st.router_checks

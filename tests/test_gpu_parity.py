@@ -119,3 +119,26 @@ def test_multi_chunk_slabs_q4_routed_q8_shared(cuda):
 def test_multi_chunk_slabs_q8_routed_q4_shared(cuda):
     wl = synth.make_workload("wide_q8r_q4s", _wide(fmt_routed=Q8, fmt_shared=Q4, vocab=0), 3, 10, 109)
     _run(wl, 10)
+
+
+def test_moe_uocr_prefill_three_chunks_then_greedy(cuda):
+    """uocr_prefill against the oracle's prefill-by-decode: 100 embeddings (two
+    chunks, 64 + 36 tokens) then 50 prompt ids (one ragged chunk) per row; every
+    prefix key and value, the last prompt token's layer taps, logits and id, then
+    greedy steps from that cache."""
+    cfg = _moe(prefix_len=150, max_rows=3)
+    wl = synth.make_workload("moe_prefill", cfg, 3, 6, 110, prefix="prefill", n_prefill_embeds=100,
+                             step_input="ids")
+    st = _run(wl, 6, lib_prefill=True)
+    assert st.kv_checks >= 3 * cfg.n_layers + 3 * 6 * cfg.n_layers
+    assert st.id_checks >= 3 * 7
+
+
+def test_dense_uocr_prefill_with_sinks_int8_asym(cuda):
+    """uocr_prefill of a dense decoder with attention sinks, int8-asymmetric
+    weights and head_dim 64 (30 embeddings, then 10 prompt ids), then greedy
+    steps through the ring."""
+    cfg = _dense(fmt_attn=I8, fmt_dense=I8, use_sink=1, prefix_len=40, ring_len=16, max_rows=2, vocab=500)
+    wl = synth.make_workload("dense_prefill_ring", cfg, 2, 5, 111, prefix="prefill", n_prefill_embeds=30,
+                             step_input="ids")
+    _run(wl, 5, lib_prefill=True)
