@@ -251,42 +251,84 @@ def resync_rows(ctx, cfg, res, div, row_map):
             ctx.uocr_kv_write(r, m, s, k, v)
 
 
-def library_prefill(ctx, wl, rows):
-    """Build every row's prefix with uocr_prefill: one call for the image
-    embeddings, one for the prompt ids (the workload's prefix).  Returns the
-    next id and the logits after each row's last prefix token."""
+CHUNK = 64  # tokens of one prefill pass of the library
+
+
+def library_prefill(ctx, wl, rows, row_map=(), moe_layers=()):
+    """Build every row's prefix with uocr_prefill: the image embeddings, then
+    the prompt ids (the workload's prefix).  Rows the oracle follows (row_map)
+    are prefilled one 64-token call at a time (the library's own chunking) so
+    that the router's choice for every prefix token can be read back from the
+    debug taps after each call.  Returns the next id and the logits after each
+    row's last prefix token, lib_sets[row][position][layer] = sorted experts
+    the library chose (followed rows only), and the token count of the last
+    call (its tokens are the ones the layer taps hold)."""
     import torch
 
     cfg = wl.cfg
     dev = torch.device("cuda")
-    ne = wl.prefill_embeds.shape[1]
+    ne, P = wl.prefill_embeds.shape[1], cfg.prefix_len
     nxt = torch.zeros(rows, dtype=torch.int32, device=dev)
     lg = torch.zeros((rows, cfg.vocab), dtype=torch.float32, device=dev)
+    lib_sets = {}
     for r in range(rows):
         x = torch.from_numpy(np.ascontiguousarray(wl.prefill_embeds[r]).view(np.int16)).to(dev)
-        ctx.uocr_prefill(r, ne, 0, x_ptr=x.data_ptr())
         ids = torch.from_numpy(np.ascontiguousarray(wl.prefill_ids[r], np.int32)).to(dev)
-        ctx.uocr_prefill(r, cfg.prefix_len - ne, ne, ids_ptr=ids.data_ptr(), next_ptr=nxt[r:].data_ptr(),
-                         logits_ptr=lg[r].data_ptr())
+        follow = r in row_map
+        step = CHUNK if follow else P
+        sets = {}
+        for a in range(0, P, step):
+            b = min(P, a + step)
+            for lo, hi, kind in ((a, min(b, ne), "x"), (max(a, ne), b, "ids")):
+                if lo >= hi:
+                    continue
+                last = hi == P
+                n_last = hi - lo
+                kw = dict(next_ptr=nxt[r:].data_ptr(), logits_ptr=lg[r].data_ptr()) if last else {}
+                if kind == "x":
+                    ctx.uocr_prefill(r, hi - lo, lo, x_ptr=x[lo:].data_ptr(), **kw)
+                else:
+                    ctx.uocr_prefill(r, hi - lo, lo, ids_ptr=ids[lo - ne:].data_ptr(), **kw)
+                if follow:
+                    for l in moe_layers:
+                        idx = ctx.uocr_debug_router(l, hi - lo)["idx"]
+                        for t in range(hi - lo):
+                            sets.setdefault(lo + t, {})[l] = sorted(int(e) for e in idx[t])
         ctx.uocr_sync()
-    return nxt.cpu().numpy().copy(), lg.cpu().numpy().copy()
+        lib_sets[r] = sets
+    return nxt.cpu().numpy().copy(), lg.cpu().numpy().copy(), lib_sets, n_last
 
 
-def compare_prefill(ctx, cfg, oracle_model, res, lib_rows, lib_next, lib_logits, stats, row_map, n_last_call):
-    """After the prefix: every layer's cached keys and values of the prefix,
-    the layer taps of the last prefix token of the last prefilled row, and the
-    logits / next id after each compared row's last prefix token."""
-    P = cfg.prefix_len
+def compare_prefill(ctx, cfg, res, lib_rows, lib_next, lib_logits, stats, row_map, n_last_call, pk, pv, tie):
+    """After the prefix: each layer's cached keys and values of the prefix, the
+    layer taps of the last prefix token of the last prefilled row, and the
+    logits / next id after each compared row's last prefix token.
+
+    pk, pv: the oracle's prefix caches per layer [rows][nh][P][D]; tie[i][p]:
+    the first MoE layer at which the library took another (equally correct,
+    near-tie) expert set for row i at position p (n_layers if none).  From the
+    layer after it that token's keys and values are not compared (the decode
+    comparison's rule) and are replaced by the oracle's before decoding goes
+    on."""
+    P, L = cfg.prefix_len, cfg.n_layers
     for i, r in enumerate(row_map):
-        for l in range(cfg.n_layers):
+        for l in range(L):
+            keep = [p for p in range(P) if tie[i][p] >= l]
             k, v = ctx.uocr_kv_read(r, l, 0, P)
-            stats.note(*check_close(f"prefill row {r} layer {l} keys", k.astype(np.float64),
-                                    oracle_model.pk[l][i]))
-            stats.note(*check_close(f"prefill row {r} layer {l} values", v.astype(np.float64),
-                                    oracle_model.pv[l][i]))
+            stats.note(*check_close(f"prefill row {r} layer {l} keys", k[:, keep].astype(np.float64),
+                                    pk[l][i][:, keep]))
+            stats.note(*check_close(f"prefill row {r} layer {l} values", v[:, keep].astype(np.float64),
+                                    pv[l][i][:, keep]))
             stats.kv_checks += 1
-        stats.note(*check_close(f"prefill row {r} last-token logits", lib_logits[r], res.logits[i]))
+            for p in range(P):
+                if tie[i][p] < l:  # the library's cache takes the oracle's entries
+                    ctx.uocr_kv_write(r, l, p, pk[l][i][:, p:p + 1].astype(np.float16),
+                                      pv[l][i][:, p:p + 1].astype(np.float16))
         stats.id_checks += 1
+        if tie[i][P - 1] < L:
+            stats.id_near_ties += 1
+            continue
+        stats.note(*check_close(f"prefill row {r} last-token logits", lib_logits[r], res.logits[i]))
         if res.margin[i] > ID_MARGIN:
             assert int(lib_next[r]) == int(res.next_ids[i]), f"prefill row {r}: id {lib_next[r]} != {res.next_ids[i]}"
         else:
@@ -297,11 +339,13 @@ def compare_prefill(ctx, cfg, oracle_model, res, lib_rows, lib_next, lib_logits,
     if last in row_map:
         i = row_map.index(last)
         n_tok = n_last_call
-        for l in range(cfg.n_layers):
+        t = tie[i][P - 1]
+        for l in range(min(t + 1, L)):
             g = ctx.uocr_debug_hidden(2 * l, n_tok)[n_tok - 1:n_tok]
             stats.note(*check_close(f"prefill row {last} layer {l} after attention", g, res.h_attn[l][i:i + 1]))
-            g = ctx.uocr_debug_hidden(2 * l + 1, n_tok)[n_tok - 1:n_tok]
-            stats.note(*check_close(f"prefill row {last} layer {l} output", g, res.hidden[l + 1][i:i + 1]))
+            if l < t:
+                g = ctx.uocr_debug_hidden(2 * l + 1, n_tok)[n_tok - 1:n_tok]
+                stats.note(*check_close(f"prefill row {last} layer {l} output", g, res.hidden[l + 1][i:i + 1]))
 
 
 def run_parity(ctx, wl, steps, oracle_model, rows=None, row_map=None, check_kv=True, log=None,
@@ -320,9 +364,13 @@ def run_parity(ctx, wl, steps, oracle_model, rows=None, row_map=None, check_kv=T
     last_ids = None if wl.first_ids is None else wl.first_ids.copy()
     if lib_prefill:
         assert wl.prefill_embeds is not None
-        lib_next, lib_logits = library_prefill(ctx, wl, runner.rows)
+        moe_layers = [l for l in range(cfg.n_layers) if not cfg.is_dense(l)]
+        lib_next, lib_logits, lib_sets, n_last = library_prefill(ctx, wl, runner.rows, row_map, moe_layers)
         ne = wl.prefill_embeds.shape[1]
         res = None
+        # tie[i][p]: first MoE layer at which the library's set for row i at position p
+        # differs from the oracle's (only allowed where the oracle's gap is a near tie)
+        tie = [[cfg.n_layers] * cfg.prefix_len for _ in range(n_or)]
         for p in range(cfg.prefix_len):
             opos = np.full(n_or, p, np.int32)
             last = p == cfg.prefix_len - 1
@@ -330,8 +378,21 @@ def run_parity(ctx, wl, steps, oracle_model, rows=None, row_map=None, check_kv=T
                 res = oracle_model.step(opos, x=wl.prefill_embeds[row_map, p], want_logits=last)
             else:
                 res = oracle_model.step(opos, ids=wl.prefill_ids[row_map, p - ne], want_logits=last)
-        compare_prefill(ctx, cfg, oracle_model, res, runner.rows, lib_next, lib_logits, stats, row_map,
-                        cfg.prefix_len - ne)
+            for i, r in enumerate(row_map):
+                for l in moe_layers:
+                    if tie[i][p] < cfg.n_layers:
+                        break
+                    want = sorted(int(e) for e in res.router[l]["idx"][i])
+                    got = lib_sets[r][p][l]
+                    stats.router_checks += 1
+                    if got != want:
+                        assert res.router[l]["gap"][i] <= ROUTER_GAP, \
+                            f"prefill row {r} position {p} layer {l}: router set {got} != {want} with " \
+                            f"oracle gap {res.router[l]['gap'][i]:.3e}"
+                        stats.router_near_ties += 1
+                        tie[i][p] = l
+        compare_prefill(ctx, cfg, res, runner.rows, lib_next, lib_logits, stats, row_map, n_last,
+                        oracle_model.pk, oracle_model.pv, tie)
         nxt = lib_next.copy()
         for i, r in enumerate(row_map):
             nxt[r] = res.next_ids[i]  # teacher forcing by the oracle
