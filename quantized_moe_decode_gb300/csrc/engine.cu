@@ -558,11 +558,13 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       xa.n_units = n_units;
       const double units = by_slot ? exp_act : E;
       // CTAs per routed unit and for the shared experts, in proportion to the
-      // bytes each streams, about GE per token group in all
+      // bytes each streams (the shared experts once per 16-row pass), about GE
+      // in all: one grid row covers every token group
       auto split = [&](const DMat& r, const DMat* sh, int rslabs, int sslabs) {
-        const double br = (double)(r.qbytes + r.sbytes), bs = sh ? (double)(sh->qbytes + sh->sbytes) : 0.0;
+        const double br = (double)(r.qbytes + r.sbytes);
+        const double bs = sh ? (double)(sh->qbytes + sh->sbytes) * tg : 0.0;
         const double tot = units * br + bs;
-        const int gt = GE / tg > 1 ? GE / tg : 1;
+        const int gt = GE;
         // parts of whole rounds (G_w slabs); the fewest parts that give the
         // rounds per CTA the byte-proportional target gives
         auto parts = [&](double target, int slabs, int U) {

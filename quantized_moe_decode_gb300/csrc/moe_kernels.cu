@@ -10,12 +10,13 @@
 //            that chose it (its segment of the token grouping, a 16-bit mask)
 //            and each row's slot in its top-k (3 bits per row).
 //   gate/up  shared-expert CTAs first (they need nothing from the router),
-//            then routed CTAs, one per (unit, token group, part of the
-//            expert's slabs).  A routed CTA reads its record, stages its rows,
-//            streams the expert's gate/up slabs once for them and writes SwiGLU
+//            then routed CTAs, one per (unit, part of the expert's slabs).  A
+//            routed CTA reads its unit's record of every token group, gathers
+//            the unit's rows over the whole step, stages them (16 per pass),
+//            streams the expert's gate/up slabs once per pass and writes SwiGLU
 //            activations in the B-fragment order the down projection reads
-//            directly.  CTA (0, 0) also writes the grouping arrays (count,
-//            offset, perm, inv) from the router's choices.
+//            directly.  CTA 0 also writes the grouping arrays (count, offset,
+//            perm, inv) from the router's choices.
 //   down     the same CTA layout; it streams the expert's down slabs and
 //            writes fp32 partials; the last contribution to an output slab (a
 //            counter per slab, no waiting) combines them in a fixed order:
@@ -136,9 +137,42 @@ struct RouteSmem {
   unsigned long long rowmask[256];  // [E] rows that chose expert e (bit r)
   int off[256];
   int4 scan[kWarps];
-  int4 rec;                         // this CTA's routing record
-  int e, nlast, contrib;
+  int4 rec;                         // this CTA's routing record (active-slot units)
+  int4 grec[4];                     // this CTA's unit's record of each token group
+  int rows[64];                     // the unit's rows over all token groups, ascending
+  int ent[64];                      // their entries row * k + slot
+  int e, n, nlast, contrib;
 };
+
+// The rows of a routed unit over all token groups (ascending) and their entries
+// row * k + slot, from the unit's record of each group (rs.grec[0..tg)): warp 0
+// builds the list, one lane per group.  Returns the row count (all threads).
+__device__ __forceinline__ int gather_unit_rows(RouteSmem& rs, int tg, int k) {
+  if (threadIdx.x < 32) {
+    const int g = threadIdx.x;
+    const int4 r = g < tg ? rs.grec[g] : make_int4(-1, 0, 0, 0);
+    const unsigned m = r.x >= 0 ? (unsigned)r.y : 0u;
+    const int c = __popc(m);
+    int base = c;  // inclusive scan over the (at most 4) groups
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, base, o);
+      if (g >= o) base += y;
+    }
+    if (g == 3) rs.n = base;  // groups >= tg count zero rows
+    base -= c;
+    const unsigned long long jb = (unsigned long long)(uint32_t)r.z | ((unsigned long long)(uint32_t)r.w << 32);
+    for (unsigned mm = m; mm; mm &= mm - 1u) {
+      const int bit = __ffs(mm) - 1;
+      const int row = 16 * g + bit;
+      rs.rows[base] = row;
+      rs.ent[base] = row * k + (int)((jb >> (3 * bit)) & 7ull);
+      ++base;
+    }
+  }
+  __syncthreads();
+  return rs.n;
+}
 
 __device__ __forceinline__ void clear_rowmask(RouteSmem& rs, int E) {
   for (int e = threadIdx.x; e < E; e += kThreads) rs.rowmask[e] = 0ull;
@@ -304,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
 // the n_rctas routed CTAs are dealt out over the n active slots once the
 // router has counted them (slot_assign): every routed CTA has work and the
 // grid is one wave whatever the number of experts that received a token.
-// blockIdx.y: token group of 16 rows.
+// The grid has one row (blockIdx.y = 0): a CTA covers every token group.
 struct ExpertCta {
   bool shared;
   int i, part, parts;
@@ -383,6 +417,11 @@ __device__ __forceinline__ void part_range(int n, int gran, int part, int parts,
 __device__ __forceinline__ int groups_of(int U) { return kWarps / warps_per_slab(U); }
 
 // ------------------------------------------------------------------ gate/up
+// One grid for every token group: a routed CTA takes its unit's rows over the
+// whole step (the records of all token groups), so each expert's weights are
+// streamed once per 16 of its rows, not once per token group; shared-expert
+// CTAs take every row.  Rows go through in passes of 16 (NT n-tiles); a pass
+// after the first streams the CTA's slabs again (from L2).
 template <int FR, int FS, int NT>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const ExpertArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -390,14 +429,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
   const StreamPlan& p = a.sp;
   __half* xs = reinterpret_cast<__half*>(smem + p.xs_off);
   float* red = reinterpret_cast<float*>(smem + p.red_off);
-  int* rows = reinterpret_cast<int*>(smem + p.rows_off);  // global row of each token of the expert
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = smem + p.ring_off + (size_t)warp * kRingDepth * p.slot;
 
   if (!(kPdlLate & PDL_EXPERT)) pdl_launch_dependents();
   ExpertCta ec = expert_cta(a);
-  const int g = blockIdx.y, tok0 = g * 16;
-  const int ng = min(16, a.ntok - tok0);  // rows of this token group
   int s0 = 0, s1 = 0;
   SlabWork w;
   UnitStream<FS> uss;
@@ -420,29 +456,24 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
   load_norm_w(nw, a.norm_w, a.H);
   pdl_wait();
 
-  if (blockIdx.x == 0 && blockIdx.y == 0) write_grouping(rs, a);
+  if (blockIdx.x == 0) write_grouping(rs, a);
   // this CTA's rows
-  int e = -1, ntk = ng;
-  if (ec.shared) {
-    for (int t = threadIdx.x; t < ng; t += kThreads) rows[t] = tok0 + t;
-  } else {
-    int4 r;  // {expert, row mask, slot bits}
-    if (a.by_slot) {
+  int e = -1, ntk = a.ntok;
+  if (!ec.shared) {
+    if (a.by_slot) {  // one token group
       const int t = threadIdx.x;
-      r = record_by_slot(a, t < a.n_units ? __ldcg(a.rec + (size_t)g * a.n_units + t) : make_int4(-1, 0, 0, 0), ec,
-                         rs);
-    } else {
-      r = __ldcg(a.rec + (size_t)g * a.n_units + ec.i);
+      rs.grec[0] = record_by_slot(a, t < a.n_units ? __ldcg(a.rec + t) : make_int4(-1, 0, 0, 0), ec, rs);
+    } else if ((int)threadIdx.x < a.tg) {
+      rs.grec[threadIdx.x] = __ldcg(a.rec + (size_t)threadIdx.x * a.n_units + ec.i);
     }
-    e = r.x;
-    const unsigned mask = (unsigned)r.y;
-    ntk = e >= 0 ? __popc(mask) : 0;
+    __syncthreads();
+    e = rs.grec[0].x;
+    for (int g = 1; g < a.tg; ++g) e = e >= 0 ? e : rs.grec[g].x;
+    ntk = e >= 0 ? gather_unit_rows(rs, a.by_slot ? 1 : a.tg, a.k) : 0;
     if (ntk == 0) {
       if (streaming) cp_wait<0>();  // copies in flight land before the CTA leaves
       return;
     }
-    if (threadIdx.x < 16 && ((mask >> threadIdx.x) & 1))
-      rows[__popc(mask & ((1u << threadIdx.x) - 1u))] = tok0 + threadIdx.x;
     if (a.by_slot) {
       part_range(a.wr.n_slabs, groups_of(a.wr.U), ec.part, ec.parts, s0, s1);
       if (s0 == s1) return;  // a part without a round (nothing in flight yet)
@@ -450,39 +481,53 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_gateup(const Ex
       usr.start(a.wr.q + (size_t)e * a.wr.q_stride, a.wr.s + (size_t)e * a.wr.s_stride, w);
       usr.prefetch(ring, p.slot, w, lane);
     }
-  }
-  __syncthreads();
-  // the expert's rows, normalised, packed into consecutive tokens
-  stage_norm_gather(xs, p.ldx, a.h, a.H, rows, ntk, NT * 8, a.norm_w, nw, a.H, a.eps);
-  __syncthreads();
-  const int nt_used = (ntk + 7) >> 3;
-  const BSmem bp(xs, p.ldx);
-  if (ec.shared) {
-    auto epi = [&](int sl, const float* rb, int tid, int nthr) {
-      for (int i = tid; i < NT * 64; i += nthr) {
-        const int tok = i >> 3, pg = i & 7;
-        if (tok >= ntk) continue;
-        float lo, hi;
-        group_sum<NT>(rb, w.ks, tok, pg, lo, hi);
-        const int r = tok0 + tok;
-        *reinterpret_cast<__half*>(a.act_s + bfrag_offset(r >> 3, r & 7, 8 * sl + pg, a.Ish >> 5)) =
-            __float2half_rn(silu(lo) * hi);
-      }
-    };
-    run_stream<FS, NT>(uss, w, ring, p.slot, red, bp, nt_used, epi);
   } else {
-    const int tile0 = (e * a.tg + g) * 2;  // two 8-token tiles per (expert, token group)
-    auto epi = [&](int sl, const float* rb, int tid, int nthr) {
-      for (int i = tid; i < NT * 64; i += nthr) {
-        const int tok = i >> 3, pg = i & 7;
-        if (tok >= ntk) continue;
-        float lo, hi;
-        group_sum<NT>(rb, w.ks, tok, pg, lo, hi);
-        *reinterpret_cast<__half*>(a.act_r + bfrag_offset(tile0 + (tok >> 3), tok & 7, 8 * sl + pg, a.Ie >> 5)) =
-            __float2half_rn(silu(lo) * hi);
+    for (int t = threadIdx.x; t < ntk; t += kThreads) rs.rows[t] = t;
+  }
+  for (int pass = 0; pass * 16 < ntk; ++pass) {
+    const int r0 = pass * 16, n = min(16, ntk - r0);
+    if (pass > 0) {  // the same slabs again for the next 16 rows (L2-resident by now)
+      if (ec.shared) {
+        uss.start(a.ws.q, a.ws.s, w);
+        uss.prefetch(ring, p.slot, w, lane);
+      } else {
+        usr.start(a.wr.q + (size_t)e * a.wr.q_stride, a.wr.s + (size_t)e * a.wr.s_stride, w);
+        usr.prefetch(ring, p.slot, w, lane);
       }
-    };
-    run_stream<FR, NT>(usr, w, ring, p.slot, red, bp, nt_used, epi);
+    }
+    __syncthreads();  // the previous pass's readers of xs are done
+    // the pass's rows, normalised, packed into consecutive tokens
+    stage_norm_gather(xs, p.ldx, a.h, a.H, rs.rows + r0, n, NT * 8, a.norm_w, nw, a.H, a.eps);
+    __syncthreads();
+    const int nt_used = (n + 7) >> 3;
+    const BSmem bp(xs, p.ldx);
+    if (ec.shared) {
+      auto epi = [&](int sl, const float* rb, int tid, int nthr) {
+        for (int i = tid; i < NT * 64; i += nthr) {
+          const int tok = i >> 3, pg = i & 7;
+          if (tok >= n) continue;
+          float lo, hi;
+          group_sum<NT>(rb, w.ks, tok, pg, lo, hi);
+          const int r = r0 + tok;
+          *reinterpret_cast<__half*>(a.act_s + bfrag_offset(r >> 3, r & 7, 8 * sl + pg, a.Ish >> 5)) =
+              __float2half_rn(silu(lo) * hi);
+        }
+      };
+      run_stream<FS, NT>(uss, w, ring, p.slot, red, bp, nt_used, epi);
+    } else {
+      const int tile0 = (e * a.tg + pass) * 2;  // two 8-token tiles per (expert, pass)
+      auto epi = [&](int sl, const float* rb, int tid, int nthr) {
+        for (int i = tid; i < NT * 64; i += nthr) {
+          const int tok = i >> 3, pg = i & 7;
+          if (tok >= n) continue;
+          float lo, hi;
+          group_sum<NT>(rb, w.ks, tok, pg, lo, hi);
+          *reinterpret_cast<__half*>(a.act_r + bfrag_offset(tile0 + (tok >> 3), tok & 7, 8 * sl + pg, a.Ie >> 5)) =
+              __float2half_rn(silu(lo) * hi);
+        }
+      };
+      run_stream<FR, NT>(usr, w, ring, p.slot, red, bp, nt_used, epi);
+    }
   }
   if (kPdlLate & PDL_EXPERT) pdl_launch_dependents();
 }
@@ -492,7 +537,6 @@ template <int FR, int FS, int NT>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const ExpertArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ RouteSmem rs;
-  __shared__ int s_entry[16];  // entry row*k + slot of each token of the expert
   const StreamPlan& p = a.sp;
   float* red = reinterpret_cast<float*>(smem + p.red_off);
   uint8_t* btile = smem + p.extra_off;
@@ -501,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
 
   if (!(kPdlLate & PDL_EXPERT)) pdl_launch_dependents();
   ExpertCta ec = expert_cta(a);
-  const int g = blockIdx.y, tok0 = g * 16, H = a.H, k = a.k, rows = a.ntok;
+  const int H = a.H, k = a.k, rows = a.ntok;
   int s0 = 0, s1 = 0;
   SlabWork w;
   UnitStream<FS> uss;
@@ -523,41 +567,39 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
   if (threadIdx.x == 0) rs.contrib = 0;
   __syncthreads();
   pdl_wait();
-  // contributions every output slab receives: one per routed record with rows, one per shared group
+  // contributions every output slab receives: one per routed unit with rows in any
+  // token group (each unit's CTAs cover every slab once), one for the shared experts
   int4 mine = make_int4(-1, 0, 0, 0);  // active-slot units: record threadIdx.x of the (single) group
   {
     int c = 0;
-    for (int i = threadIdx.x; i < a.n_units * a.tg; i += kThreads) {
-      const int4 v = __ldcg(a.rec + i);
-      c += v.y != 0;
-      if (i == (int)threadIdx.x) mine = v;
+    for (int u = threadIdx.x; u < a.n_units; u += kThreads) {
+      bool any = false;
+      for (int g = 0; g < a.tg; ++g) {
+        const int4 v = __ldcg(a.rec + (size_t)g * a.n_units + u);
+        any |= v.y != 0;
+        if (g == 0 && u == (int)threadIdx.x) mine = v;
+      }
+      c += any;
     }
     if (c) atomicAdd(&rs.contrib, c);
   }
   for (int i = threadIdx.x; i < rows * k; i += kThreads) rs.w[i] = __ldcg(a.wts + i);  // combine weights
-  int e = -1, ntk, k32;
-  const uint8_t* bsrc;
-  if (ec.shared) {
-    ntk = min(16, rows - tok0);
-    k32 = a.Ish >> 5;
-    bsrc = a.act_s + (size_t)(tok0 >> 3) * k32 * 512;
-  } else {
-    const int4 r = a.by_slot ? record_by_slot(a, mine, ec, rs)
-                             : __ldcg(a.rec + (size_t)g * a.n_units + ec.i);  // {expert, row mask, slot bits}
-    e = r.x;
-    const unsigned mask = (unsigned)r.y;
-    ntk = e >= 0 ? __popc(mask) : 0;
+  int e = -1, ntk = rows;
+  const int k32 = (ec.shared ? a.Ish : a.Ie) >> 5;
+  if (!ec.shared) {
+    if (a.by_slot) {
+      rs.grec[0] = record_by_slot(a, mine, ec, rs);
+    } else if ((int)threadIdx.x < a.tg) {
+      rs.grec[threadIdx.x] = __ldcg(a.rec + (size_t)threadIdx.x * a.n_units + ec.i);
+    }
+    __syncthreads();
+    e = rs.grec[0].x;
+    for (int g = 1; g < a.tg; ++g) e = e >= 0 ? e : rs.grec[g].x;
+    ntk = e >= 0 ? gather_unit_rows(rs, a.by_slot ? 1 : a.tg, k) : 0;
     if (ntk == 0) {
       if (streaming) cp_wait<0>();
       return;
     }
-    if (threadIdx.x < 16 && ((mask >> threadIdx.x) & 1)) {
-      const unsigned long long jb = (unsigned long long)(uint32_t)r.z | ((unsigned long long)(uint32_t)r.w << 32);
-      const int j = (int)((jb >> (3 * threadIdx.x)) & 7ull);
-      s_entry[__popc(mask & ((1u << threadIdx.x) - 1u))] = (tok0 + threadIdx.x) * k + j;
-    }
-    k32 = a.Ie >> 5;
-    bsrc = a.act_r + (size_t)((e * a.tg + g) * 2) * k32 * 512;
     if (a.by_slot) {
       part_range(H / 16, groups_of(a.wr.U), ec.part, ec.parts, s0, s1);
       if (s0 == s1) return;  // a part without a round (nothing in flight yet)
@@ -566,31 +608,46 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
       usr.prefetch(ring, p.slot, w, lane);
     }
   }
-  const int tiles = (ntk + 7) >> 3;
-  stage_bytes(btile, bsrc, tiles * k32 * 512);
-  __syncthreads();
-  const int s_contrib = rs.contrib + (a.ws.n_slabs > 0 ? a.tg : 0);
-  const BSmemFrag bp{btile, k32};
-  auto epi = [&](int sl, const float* rb, int tid, int nthr) {
-    for (int i = tid; i < NT * 64; i += nthr) {
-      const int tok = i >> 3, pg = i & 7;
-      if (tok >= ntk) continue;
-      float lo, hi;
-      group_sum<NT>(rb, w.ks, tok, pg, lo, hi);
-      float* dst = ec.shared ? a.part_s + (size_t)(tok0 + tok) * H : a.part_r + (size_t)s_entry[tok] * H;
-      dst[16 * sl + pg] = lo;
-      dst[16 * sl + pg + 8] = hi;
+  for (int pass = 0; pass * 16 < ntk; ++pass) {
+    const int r0 = pass * 16, n = min(16, ntk - r0);
+    if (pass > 0) {
+      if (ec.shared) {
+        uss.start(a.ws.q, a.ws.s, w);
+        uss.prefetch(ring, p.slot, w, lane);
+      } else {
+        usr.start(a.wr.q + (size_t)e * a.wr.q_stride, a.wr.s + (size_t)e * a.wr.s_stride, w);
+        usr.prefetch(ring, p.slot, w, lane);
+      }
     }
-  };
-  if (ec.shared)
-    run_stream<FS, NT>(uss, w, ring, p.slot, red, bp, tiles, epi);
-  else
-    run_stream<FR, NT>(usr, w, ring, p.slot, red, bp, tiles, epi);
+    const int tiles = (n + 7) >> 3;
+    const uint8_t* bsrc = ec.shared ? a.act_s + (size_t)(r0 >> 3) * k32 * 512
+                                    : a.act_r + (size_t)((e * a.tg + pass) * 2) * k32 * 512;
+    __syncthreads();  // the previous pass's readers of btile are done
+    stage_bytes(btile, bsrc, tiles * k32 * 512);
+    __syncthreads();
+    const BSmemFrag bp{btile, k32};
+    auto epi = [&](int sl, const float* rb, int tid, int nthr) {
+      for (int i = tid; i < NT * 64; i += nthr) {
+        const int tok = i >> 3, pg = i & 7;
+        if (tok >= n) continue;
+        float lo, hi;
+        group_sum<NT>(rb, w.ks, tok, pg, lo, hi);
+        float* dst = ec.shared ? a.part_s + (size_t)(r0 + tok) * H : a.part_r + (size_t)rs.ent[r0 + tok] * H;
+        dst[16 * sl + pg] = lo;
+        dst[16 * sl + pg + 8] = hi;
+      }
+    };
+    if (ec.shared)
+      run_stream<FS, NT>(uss, w, ring, p.slot, red, bp, tiles, epi);
+    else
+      run_stream<FR, NT>(usr, w, ring, p.slot, red, bp, tiles, epi);
+  }
   if (kPdlLate & PDL_EXPERT) pdl_launch_dependents();
 
   // one counter per output slab; the last contribution to a slab combines it.
   // All of this CTA's slabs are counted at once (one thread per slab), and all
   // slabs it finishes are combined in one batched pass.
+  const int s_contrib = rs.contrib + (a.ws.n_slabs > 0 ? 1 : 0);
   int* s_last = reinterpret_cast<int*>(red);  // the partial buffers are free now
   __syncthreads();
   if (threadIdx.x == 0) rs.nlast = 0;
@@ -651,7 +708,7 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t st, bool pdl) {
   X(Q8_0, Q8_0, NT_) X(Q4_0, Q8_0, NT_) X(Q4_0, Q4_0, NT_) X(Q8_0, Q4_0, NT_) X(I8ASYM, I8ASYM, NT_)
 
 static dim3 expert_grid(const ExpertArgs& a) {
-  return dim3((a.ws.n_slabs > 0 ? a.cpes : 0) + (a.by_slot ? a.n_rctas : a.n_units * a.cpe), a.tg);
+  return dim3((a.ws.n_slabs > 0 ? a.cpes : 0) + (a.by_slot ? a.n_rctas : a.n_units * a.cpe), 1);
 }
 
 cudaError_t launch_expert_gateup(int fr, int fs, const ExpertArgs& a, cudaStream_t st, bool pdl) {
