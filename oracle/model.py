@@ -99,6 +99,31 @@ def rope(v, pos, theta):
     return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
 
 
+def kv_quant(x):
+    """INT8 KV cache entry of key or value vectors (last axis = one head's D values).
+
+    Symmetric, one scale per vector: s = max|x| / 127, code = round(x / s)
+    (half to even) clamped to [-127, 127]; a zero vector has s = 0 and zero
+    codes.  The scale and the codes are integer decisions taken in floating
+    point, so they are taken in fp32, the precision the kernels store and
+    divide in ("Falcon-OCR INT8 OpenVINO IR", "How it is meant to be run": the
+    service keeps an INT8 KV cache; the per-head scale is this reading).
+    Returns (codes int8 [..., D], s float32 [...]).
+    """
+    x = np.asarray(x, dtype=np.float64).astype(np.float32)
+    amax = np.max(np.abs(x), axis=-1)
+    s = (amax / np.float32(127.0)).astype(np.float32)
+    safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+    q = np.rint((x / safe[..., None]).astype(np.float32))
+    q = np.where(s[..., None] > 0, np.clip(q, -127, 127), 0)
+    return q.astype(np.int8), s
+
+
+def kv_dequant(codes, s):
+    """Value of an INT8 KV entry: s * code (float64)."""
+    return np.asarray(codes, dtype=np.float64) * np.asarray(s, dtype=np.float64)[..., None]
+
+
 def ring_slot(p, P, R):
     """Cache slot of absolute position p: prefix slots 0..P-1, then a ring of R."""
     return p if p < P else P + (p - P) % R
@@ -146,11 +171,11 @@ def route(logits, k):
     return idx.astype(np.int64), w
 
 
-# Logit gap under which the top-k set is not decided by the definition alone:
-# a decode step that meets the float tolerance (hidden states to rel-L2 2e-3
-# after several layers of fp16 activations) moves router logits by up to about
-# this much, so where the k-th and (k+1)-th logits are closer, another set is
-# an equally correct top-k.  It is the margin that also gates greedy token ids.
+# Logit gap under which a selection on logits is not decided by the definition
+# alone.  The decode-step statement fixes 1e-2 as the top-2 margin below which
+# greedy ids may differ; the router's top-k is the step's other selection on
+# logits, so its k-th vs (k+1)-th gap takes the same margin: below it another
+# set is an equally correct top-k for a computation within the float tolerance.
 TIE_TOL = 1e-2
 
 
@@ -210,11 +235,15 @@ class OracleModel:
     kv_prefix: optional list over layers of (k, v) fp16 [rows, nh, P, D]
     (a cached prefix); without it the prefix is filled by decode steps.
     sinks: optional fp32 [layers, heads].
+    kv_int8: the KV cache holds INT8 entries (kv_quant) instead of fp16 values:
+    every key and value vector is quantised when it is written (the cached
+    prefix included) and attention reads s * code.
     """
 
-    def __init__(self, cfg, tensors, rows, kv_prefix=None, sinks=None, cache="float64"):
+    def __init__(self, cfg, tensors, rows, kv_prefix=None, sinks=None, cache="float64", kv_int8=False):
         self.cfg = cfg
         self.rows = rows
+        self.kv_int8 = kv_int8
         self._t = {(t.kind, t.layer, t.expert): t for t in tensors}
         # cache: None (dequantise at every use), "float64", or "float32" (only
         # for matrices whose values are exact in float32, see quant.float32_is_exact)
@@ -228,6 +257,8 @@ class OracleModel:
         for l in range(L):
             if kv_prefix is not None:
                 k, v = kv_prefix[l]
+                if kv_int8:
+                    k, v = kv_dequant(*kv_quant(k)), kv_dequant(*kv_quant(v))
                 self.pk.append(k)
                 self.pv.append(v)
             else:
@@ -308,8 +339,12 @@ class OracleModel:
             for r in range(rows):
                 p = int(positions[r])
                 qh = rope(Q[r].reshape(nh, D), p, cfg.rope_theta)
-                kh = f16(rope(Kx[r].reshape(nh, D), p, cfg.rope_theta))  # the cache holds fp16
-                vh = f16(Vx[r].reshape(nh, D))
+                if self.kv_int8:  # the cache holds INT8 entries, one scale per head
+                    kh = kv_dequant(*kv_quant(rope(Kx[r].reshape(nh, D), p, cfg.rope_theta)))
+                    vh = kv_dequant(*kv_quant(Vx[r].reshape(nh, D)))
+                else:  # the cache holds fp16
+                    kh = f16(rope(Kx[r].reshape(nh, D), p, cfg.rope_theta))
+                    vh = f16(Vx[r].reshape(nh, D))
                 res.k_new[l, r], res.v_new[l, r] = kh, vh
                 s = int(res.slots[r])
                 if s < self.P:

@@ -575,8 +575,16 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
           const int per = (nr + t - 1) / t;
           return (nr + per - 1) / per;
         };
-        xa.cpe = parts(gt * br / tot, rslabs, r.U);
-        xa.cpes = sh ? parts(gt * bs / tot, sslabs, sh->U) : 0;
+        if (by_slot) {
+          xa.cpe = parts(gt * br / tot, rslabs, r.U);
+          xa.cpes = sh ? parts(gt * bs / tot, sslabs, sh->U) : 0;
+        } else {
+          // expert ids: the routed parts rounded down so that the grid stays one
+          // wave; the shared experts take the rest of it
+          xa.cpe = parts(floor(gt * br / tot), rslabs, r.U);
+          const int left = gt - E * xa.cpe;
+          xa.cpes = sh ? parts(left > 1 ? left : 1, sslabs, sh->U) : 0;
+        }
         // active-slot units: the routed CTAs fill the rest of the wave and are
         // dealt out over the experts that did receive a token (at least one each)
         const int rest = gt - xa.cpes;

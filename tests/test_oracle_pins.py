@@ -328,3 +328,58 @@ def test_float32_cache_gives_identical_results():
     ra = a.step(wl.positions(0), ids=wl.first_ids)
     rb = b.step(wl.positions(0), ids=wl.first_ids)
     assert np.array_equal(ra.logits, rb.logits)
+
+
+# ---------------------------------------------------------------- INT8 KV cache
+def test_kv_quant_hand_built_codes_and_scale():
+    """amax 127 gives s = 1 exactly; codes round half to even; the amax maps to 127."""
+    x = np.array([127.0, -63.5, 0.5, 1.5, 2.5, -2.5, 0.0, 126.5, -0.49])
+    codes, s = oracle.kv_quant(x)
+    assert s.dtype == np.float32 and float(s) == 1.0
+    assert codes.tolist() == [127, -64, 0, 2, 2, -2, 0, 126, 0]
+    # a power-of-two rescale changes the scale exactly and no code
+    c2, s2 = oracle.kv_quant(x * 2.0 ** -9)
+    assert float(s2) == 2.0 ** -9 and np.array_equal(c2, codes)
+    assert np.array_equal(oracle.kv_dequant(codes, s), codes.astype(np.float64))
+
+
+def test_kv_quant_negative_amax_zero_vector_and_shapes():
+    codes, s = oracle.kv_quant(np.array([-3.0, 1.0, 0.25]))
+    assert codes[0] == -127 and float(s) == np.float32(3.0) / np.float32(127.0)
+    codes, s = oracle.kv_quant(np.zeros((2, 4)))
+    assert not codes.any() and not s.any()
+    codes, s = oracle.kv_quant(np.ones((3, 5, 8)))
+    assert codes.shape == (3, 5, 8) and s.shape == (3, 5) and (codes == 127).all()
+
+
+def test_kv_quant_round_trip_error_bound_and_code_range():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((64, 128)) * rng.uniform(0.01, 10.0, size=(64, 1))
+    codes, s = oracle.kv_quant(x)
+    err = np.abs(oracle.kv_dequant(codes, s) - x)
+    # half a step, plus the fp32 rounding of x / s
+    assert (err <= s[:, None].astype(np.float64) * (0.5 + 1e-5) + 1e-7 * np.abs(x)).all()
+    assert (np.abs(codes).max(axis=1) == 127).all() and np.abs(codes.astype(int)).max() <= 127
+
+
+def test_int8_kv_model_caches_the_quantised_prefix_and_stays_close_to_fp16():
+    cfg = synth.ModelConfig(hidden=128, n_heads=2, head_dim=64, n_layers=2, n_dense_layers=2, dense_inter=256,
+                            prefix_len=10, ring_len=4, max_rows=2)
+    wl = synth.make_workload("kvq", cfg, 2, 6, 11)
+    kv = wl.kv_prefix.subset([0, 1])
+    m8 = oracle.OracleModel(cfg, wl.tensors, 2, kv_prefix=kv, kv_int8=True)
+    m16 = oracle.OracleModel(cfg, wl.tensors, 2, kv_prefix=kv)
+    for l in range(cfg.n_layers):
+        k, v = kv[l]
+        assert np.array_equal(m8.pk[l], oracle.kv_dequant(*oracle.kv_quant(k)))
+        assert np.array_equal(m8.pv[l], oracle.kv_dequant(*oracle.kv_quant(v)))
+    for s in range(wl.steps):  # past the ring's wrap
+        pos = np.full(2, cfg.prefix_len + s)
+        r8 = m8.step(pos, x=wl.step_x[s])
+        r16 = m16.step(pos, x=wl.step_x[s])
+        # the appended entries are the quantised keys / values of this step
+        for l in range(cfg.n_layers):
+            c, sc = oracle.kv_quant(r8.k_new[l])
+            assert np.array_equal(oracle.kv_dequant(c, sc), r8.k_new[l])
+        d = np.linalg.norm(r8.hidden[-1] - r16.hidden[-1]) / np.linalg.norm(r16.hidden[-1])
+        assert 0 < d < 2e-2, d  # int8 noise, not a different model
