@@ -78,11 +78,18 @@ def class_bytes(cfg, rows, positions, distinct):
     act = rows * H * 4
     out = {}
     out["embed"] = [rows * H * 2 + act]
-    out["qkv"] = [3 * S * H * BPW[cfg.fmt_attn] + act + rows * S * (4 + 2 * 2)] * L
+    # bytes of one cache slot of one row and layer (keys and values): fp16, or
+    # INT8 codes plus one fp32 scale per head
+    slot = 2 * (S + 4 * cfg.n_heads) if getattr(cfg, "kv_int8", 0) else 2 * S * 2
+    if getattr(cfg, "kv_int8", 0):
+        out["qkv"] = [3 * S * H * BPW[cfg.fmt_attn] + act + rows * S * (4 + 2 * 4)] * L
+        out["kv_quant"] = [rows * (2 * S * 4 + slot)] * L
+    else:
+        out["qkv"] = [3 * S * H * BPW[cfg.fmt_attn] + act + rows * S * (4 + 2 * 2)] * L
     kv = 0
     for p in positions:
         n_valid = p + 1 if p < P else P + min(p - P + 1, R)
-        kv += n_valid * 2 * S * 2
+        kv += n_valid * slot
     out["attention"] = [kv + rows * S * (4 + 2)] * L
     out["o_proj"] = [H * S * BPW[cfg.fmt_attn] + rows * S * 2 + 2 * act] * L
     Ie, Ish = cfg.expert_inter, cfg.n_shared * cfg.expert_inter
@@ -267,7 +274,7 @@ def replica_throughput(world, rows, steps, seconds):
 
 
 # ------------------------------------------------------------------ our arm
-def open_workload(name, dev, stream, **kw):
+def open_workload(name, dev, stream, cfg_overrides=None, **kw):
     """Context with the workload loaded and its prefix in the cache (cached
     prefixes written, image + prompt prefixes built by uocr_prefill).  Returns
     (ctx, wl, first ids on the device, prefill seconds or None)."""
@@ -276,6 +283,8 @@ def open_workload(name, dev, stream, **kw):
     from quantized_moe_decode_gb300 import binding
 
     wl = synth.workload(name, steps=0, **kw)
+    if cfg_overrides:
+        wl.cfg = wl.cfg.replace(**cfg_overrides)
     cfg, rows = wl.cfg, wl.rows
     ctx = binding.Context(cfg, max_rows=rows, stream=stream.cuda_stream, device=dev.index or 0)
     binding.load_workload(ctx, wl)
@@ -357,16 +366,17 @@ def step_bytes_over(cfg, rows, positions, distinct):
     return tot / len(positions)
 
 
-def side_config(name, dev, stream, K, W, hbm_peak, **kw):
+def side_config(name, dev, stream, K, W, hbm_peak, cfg_overrides=None, **kw):
     """One extra configuration of the same line: time K greedy steps, report
     tokens/s, bytes and the HBM fraction, and the uocr_prefill time."""
-    ctx, wl, ids, t_pre = open_workload(name, dev, stream, **kw)
+    ctx, wl, ids, t_pre = open_workload(name, dev, stream, cfg_overrides, **kw)
     cfg, rows = wl.cfg, wl.rows
     ms, p0, last = time_greedy(ctx, wl, ids, dev, stream, K, W)
     kernels, distinct = kernel_table(ctx, wl, last, dev, p0 + K)
     sb = step_bytes_over(cfg, rows, range(p0, p0 + K), distinct)
     ms_step = ms / K
-    d = {"workload": wl.name, "rows": rows, "prefix": cfg.prefix_len, "steps": K, "warmup": W,
+    d = {"workload": wl.name + (" INT8 KV" if cfg.kv_int8 else ""), "rows": rows, "prefix": cfg.prefix_len,
+         "steps": K, "warmup": W,
          "positions": [p0, p0 + K - 1], "ms_per_step": ms_step, "tokens_per_s": rows / (ms_step * 1e-3),
          "bytes_per_step": sb, "hbm_gbs": sb / (ms_step * 1e-3) / 1e9,
          "hbm_frac": sb / (ms_step * 1e-3) / 1e9 / hbm_peak,
@@ -461,6 +471,7 @@ def run_ours(args, rank, world):
         K2 = min(K, 200)
         others["full_b8"] = side_config("full_b8", dev, stream, K2, W, hbm_peak)
         others["full_b1"] = side_config("full_b8", dev, stream, K2, W, hbm_peak, rows=1)
+        others["stress_b64_int8_kv"] = side_config(WORKLOAD, dev, stream, K2, W, hbm_peak, {"kv_int8": 1})
     cpu = cpu6 = None
     if not args.no_cpu_baseline:
         n_c, dt_c = time_oracle(wl, ORACLE_ROWS, min_s=15.0, max_steps=20)

@@ -144,6 +144,12 @@ typedef struct {
   void* stream;            /* cudaStream_t the calls are ordered with (0 = legacy) */
   int32_t device;          /* CUDA device ordinal                                */
   int32_t use_graphs;      /* 1: capture each step shape in a CUDA graph         */
+  /* cache format (after the runtime fields so that older callers' layout holds)  */
+  int32_t kv_int8;         /* 1: INT8 KV cache, one fp32 scale per (row, K|V,
+                              head, slot): value = scale * code, the key / value
+                              vector of a head quantised when written
+                              (s = max|x| / 127, code = round(x / s)) -- [Falcon]
+                              "How it is meant to be run" (an INT8 KV cache)   */
 } uocr_config;
 
 typedef struct {
@@ -215,6 +221,21 @@ UOCR_API uocr_status uocr_kv_read(uocr_ctx* ctx, int32_t row, int32_t layer, int
  * card, intro).  Requires slot0+n <= prefix_len+ring_len.  Synchronous.       */
 UOCR_API uocr_status uocr_kv_write(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0,
                           int32_t n, const uint16_t* k, const uint16_t* v);
+
+/* Source: [Falcon] "How it is meant to be run" (an INT8 KV cache).
+ * The INT8 cache's entries of slots [slot0, slot0+n) of one row and layer,
+ * exactly: codes host int8 [n_heads][n][head_dim] and scales host fp32
+ * [n_heads][n] for keys and for values (value = scale * code).  Read copies
+ * them out; write copies them in as they are (no quantisation).  Synchronous.
+ * UOCR_E_STATE when the context's cache is fp16 (kv_int8 = 0).  With an INT8
+ * cache, uocr_kv_write_prefix / uocr_kv_write quantise the given fp16 vectors
+ * (one scale per head vector) and uocr_kv_read returns scale * code rounded to
+ * fp16.                                                                      */
+UOCR_API uocr_status uocr_kv_read_i8(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0, int32_t n,
+                                     int8_t* k_codes, float* k_scales, int8_t* v_codes, float* v_scales);
+UOCR_API uocr_status uocr_kv_write_i8(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0, int32_t n,
+                                      const int8_t* k_codes, const float* k_scales, const int8_t* v_codes,
+                                      const float* v_scales);
 
 /* Source: [Falcon] intro (the sink is one more key whose logit is the sink and
  * whose value is zero; equivalent to rescaling by sigmoid(lse - sink)).

@@ -222,6 +222,7 @@ class StepResult:
     logits: np.ndarray | None = None   # [rows, V]
     next_ids: np.ndarray | None = None  # [rows]
     margin: np.ndarray | None = None    # [rows] top-1 minus top-2 logit
+    kv_entries: dict | None = None      # INT8 cache: layer -> (k codes, k scales, v codes, v scales) [rows][nh]..
 
 
 class OracleModel:
@@ -340,8 +341,12 @@ class OracleModel:
                 p = int(positions[r])
                 qh = rope(Q[r].reshape(nh, D), p, cfg.rope_theta)
                 if self.kv_int8:  # the cache holds INT8 entries, one scale per head
-                    kh = kv_dequant(*kv_quant(rope(Kx[r].reshape(nh, D), p, cfg.rope_theta)))
-                    vh = kv_dequant(*kv_quant(Vx[r].reshape(nh, D)))
+                    kq = kv_quant(rope(Kx[r].reshape(nh, D), p, cfg.rope_theta))
+                    vq = kv_quant(Vx[r].reshape(nh, D))
+                    kh, vh = kv_dequant(*kq), kv_dequant(*vq)
+                    if res.kv_entries is None:
+                        res.kv_entries = {}
+                    res.kv_entries.setdefault(l, []).append((kq[0], kq[1], vq[0], vq[1]))
                 else:  # the cache holds fp16
                     kh = f16(rope(Kx[r].reshape(nh, D), p, cfg.rope_theta))
                     vh = f16(Vx[r].reshape(nh, D))

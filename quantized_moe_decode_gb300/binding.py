@@ -26,7 +26,7 @@ EXPORTED = ["uocr_create", "uocr_destroy", "uocr_load_weights", "uocr_kv_write_p
             "uocr_set_sinks", "uocr_decode_step", "uocr_decode_step_embeds", "uocr_decode_step_host",
             "uocr_prefill", "uocr_generate", "uocr_kv_reset", "uocr_sync", "uocr_last_error", "uocr_memory_report",
             "uocr_debug_hidden", "uocr_debug_router", "uocr_debug_router_logits", "uocr_profile",
-            "uocr_lm_head_argmax_noalloc", "uocr_debug_wait_probe"]
+            "uocr_lm_head_argmax_noalloc", "uocr_debug_wait_probe", "uocr_kv_read_i8", "uocr_kv_write_i8"]
 
 
 class uocr_config(C.Structure):
@@ -35,7 +35,7 @@ class uocr_config(C.Structure):
         "n_shared", "expert_inter", "vocab", "fmt_attn", "fmt_dense", "fmt_shared", "fmt_routed",
         "prefix_len", "ring_len", "max_rows", "use_sink")] + [
         ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("mem_budget", C.c_uint64),
-        ("stream", C.c_void_p), ("device", C.c_int32), ("use_graphs", C.c_int32)]
+        ("stream", C.c_void_p), ("device", C.c_int32), ("use_graphs", C.c_int32), ("kv_int8", C.c_int32)]
 
 
 class uocr_tensor(C.Structure):
@@ -82,6 +82,8 @@ def load(path: str = LIB_PATH):
         "uocr_profile": ([P, I, I, P, P, P, C.POINTER(C.c_char_p), C.POINTER(C.c_float), C.POINTER(I)], I),
         "uocr_lm_head_argmax_noalloc": ([P, I, P, P, P, P], I),
         "uocr_debug_wait_probe": ([P, I], I),
+        "uocr_kv_read_i8": ([P, I, I, I, I, P, P, P, P], I),
+        "uocr_kv_write_i8": ([P, I, I, I, I, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -112,6 +114,7 @@ def make_config(cfg, *, max_rows=None, mem_budget=0, stream=0, device=0, use_gra
     c.stream = int(stream) or None
     c.device = int(device)
     c.use_graphs = int(use_graphs)
+    c.kv_int8 = int(getattr(cfg, "kv_int8", 0))
     return c
 
 
@@ -171,6 +174,26 @@ class Context:
         v = np.empty((nh, n, D), np.float16)
         self._ck(self.lib.uocr_kv_read(self.h, row, layer, slot0, n, k.ctypes.data, v.ctypes.data))
         return k, v
+
+    def uocr_kv_read_i8(self, row, layer, slot0, n):
+        """INT8 cache entries: (k codes int8 [nh][n][D], k scales fp32 [nh][n], v codes, v scales)."""
+        nh, D = self.cfg.n_heads, self.cfg.head_dim
+        kc = np.empty((nh, n, D), np.int8)
+        vc = np.empty((nh, n, D), np.int8)
+        ks = np.empty((nh, n), np.float32)
+        vs = np.empty((nh, n), np.float32)
+        self._ck(self.lib.uocr_kv_read_i8(self.h, row, layer, slot0, n, kc.ctypes.data, ks.ctypes.data,
+                                          vc.ctypes.data, vs.ctypes.data))
+        return kc, ks, vc, vs
+
+    def uocr_kv_write_i8(self, row, layer, slot0, kc, ks, vc, vs):
+        """Write INT8 cache entries as given: codes [nh][n][D], scales [nh][n]."""
+        kc = np.ascontiguousarray(kc, np.int8)
+        vc = np.ascontiguousarray(vc, np.int8)
+        ks = np.ascontiguousarray(ks, np.float32)
+        vs = np.ascontiguousarray(vs, np.float32)
+        self._ck(self.lib.uocr_kv_write_i8(self.h, row, layer, slot0, kc.shape[1], kc.ctypes.data, ks.ctypes.data,
+                                           vc.ctypes.data, vs.ctypes.data))
 
     def uocr_set_sinks(self, sinks):
         s = np.ascontiguousarray(sinks, dtype=np.float32)

@@ -237,8 +237,324 @@ __global__ void __launch_bounds__(UOCR_ATTN_WARPS * 32) k_attn(const AttnArgs a)
   cluster.sync();  // every CTA keeps its partial until all slices are merged
 }
 
+// ------------------------------------------------------------------ INT8 KV cache
+// Entries: per (row, K|V, head, slot) D int8 codes and one fp32 scale,
+// value = scale * code.  Quantisation (one head vector): s = max|x| / 127 and
+// code = round-to-nearest-even(x / s) clamped to [-127, 127], in IEEE fp32; a
+// zero vector has s = 0 and zero codes ("Falcon-OCR INT8 OpenVINO IR", "How
+// it is meant to be run": an INT8 KV cache; the per-head scale is our reading).
+
+// int8 code byte b of w (as a signed value) in fp32, exactly: the byte + 128 is
+// placed in the mantissa of 2^23 (byte permute) and 2^23 + 128 is subtracted.
+template <int B>
+__device__ __forceinline__ float s8_to_f32(uint32_t u_biased) {
+  static_assert(B >= 0 && B < 4, "byte");
+  return __uint_as_float(__byte_perm(u_biased, 0x4B000000u, 0x7540 + B)) - 8388736.0f;
+}
+
+__global__ void k_kv_quant(const KvQuantArgs a) {
+  __shared__ float s_max[8];
+  pdl_launch_dependents();
+  pdl_wait();  // the new keys and values come from the QKV kernel
+  const int t = blockIdx.x, kv = blockIdx.y, head = blockIdx.z, d = threadIdx.x;
+  float x = 0.f;  // threads beyond D (head_dim 16: the block is one whole warp) hold zero
+  if (d < a.D) {
+    if (a.src32) {
+      x = a.src32[(((size_t)t * 2 + kv) * a.nh + head) * a.D + d];
+    } else {
+      const __half* src = kv ? a.src16v : a.src16k;
+      x = __half2float(src[((size_t)head * gridDim.x + t) * a.D + d]);
+    }
+  }
+  float m = fabsf(x);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((d & 31) == 0) s_max[d >> 5] = m;
+  __syncthreads();
+  float amax = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, s_max[w]);
+  const float sc = amax / 127.0f;
+  int q = 0;
+  if (sc > 0.f) q = max(-127, min(127, __float2int_rn(x / sc)));
+  int slot;
+  if (a.pos) {
+    const int p = max(a.pos[t], 0);  // negative positions are reported by the embedding kernel
+    slot = p < a.P ? p : a.P + (p - a.P) % a.R;
+  } else {
+    slot = a.slot0 + t;
+  }
+  const int kvr = a.kv_row0 + t * a.kv_rstep;
+  const size_t vec = ((size_t)kvr * 2 + kv) * a.nh + head;
+  if (d < a.D) a.kv8[(vec * a.SL + slot) * a.D + d] = (int8_t)q;
+  if (d == 0) a.kvs[vec * a.SLp + slot] = sc;
+}
+
+cudaError_t launch_kv_quant(const KvQuantArgs& a, int tokens, cudaStream_t st, bool pdl) {
+  return launch_kernel(k_kv_quant, dim3(tokens, 2, a.nh), dim3(a.D < 32 ? 32 : a.D), 0, st, pdl, a);
+}
+
+// Cache slots [slot0, slot0 + n) of one (layer, row) as fp16 values s * code:
+// k_out / v_out [nh][n][D].
+__global__ void k_kv_dequant(const int8_t* kv8, const float* kvs, int nh, int D, int SL, int SLp, int slot0,
+                             int n, __half* k_out, __half* v_out) {
+  const int t = blockIdx.x, kv = blockIdx.y, head = blockIdx.z, d = threadIdx.x;
+  const size_t vec = (size_t)kv * nh + head;
+  const float v = kvs[vec * SLp + slot0 + t] * (float)kv8[(vec * SL + slot0 + t) * D + d];
+  (kv ? v_out : k_out)[((size_t)head * n + t) * D + d] = __float2half_rn(v);
+}
+
+cudaError_t launch_kv_dequant(const int8_t* kv8, const float* kvs, int nh, int D, int SL, int SLp, int slot0, int n,
+                              __half* k_out, __half* v_out, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  k_kv_dequant<<<dim3(n, 2, nh), D, 0, st>>>(kv8, kvs, nh, D, SL, SLp, slot0, n, k_out, v_out);
+  return cudaGetLastError();
+}
+
+// Split-K attention over the INT8 cache: the same structure as k_attn (TMA bulk
+// stages, online softmax per warp, cluster merge with the sink), with stages of
+// SUB slots holding the key codes, the value codes and both scale runs.  A lane
+// reads 16 codes of a slot per load (D/16 lanes per slot); scores are
+// s_k * (q . code) and values accumulate (p * s_v) * code, all in fp32.
+template <int D>
+struct Attn8Cfg {
+  static constexpr int SUB = 16384 / D;                // slots per stage (16 KB of key codes)
+  static constexpr int CODES = SUB * D;                // bytes of one code block
+  static constexpr int STAGE = 2 * CODES + 2 * SUB * 4;  // K codes, V codes, K scales, V scales
+};
+
+int attn8_smem_bytes(int D) { return 2 * (2 * 16384 + 2 * (16384 / D) * 4) + 64; }
+
+template <int D>
+__global__ void __launch_bounds__(UOCR_ATTN_WARPS * 32) k_attn8(const AttnArgs a) {
+  constexpr int LPS = D / 16;   // lanes per slot
+  constexpr int G = 32 / LPS;   // slots per load instruction
+  constexpr int SPI = 4 * G;    // slots per warp iteration
+  constexpr int NW = UOCR_ATTN_WARPS;
+  constexpr int SUB = Attn8Cfg<D>::SUB, CODES = Attn8Cfg<D>::CODES, STAGE = Attn8Cfg<D>::STAGE;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * STAGE);
+  __shared__ float sm_m[NW], sm_l[NW];
+  __shared__ float sm_acc[NW][D];
+  __shared__ float s_part[D + 2];
+
+  const int split = blockIdx.x, head = blockIdx.y, row = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane / LPS, li = lane % LPS;
+  int p = a.pos[row];
+  if (p < 0) p = 0;
+  const int n_valid = (p < a.P) ? p + 1 : a.P + min(p - a.P + 1, a.R);
+  const int s_begin = split * a.chunk;  // a multiple of 16
+  const int s_end = min(n_valid, s_begin + a.chunk);
+  const int n_sub = s_end > s_begin ? (s_end - s_begin + SUB - 1) / SUB : 0;
+  const int kvr = a.kv_row0 + row * a.kv_rstep;
+  const size_t kvec = ((size_t)kvr * 2 + 0) * a.nh + head, vvec = ((size_t)kvr * 2 + 1) * a.nh + head;
+  const int8_t* Kg = a.kv8 + kvec * a.SL * D;
+  const int8_t* Vg = a.kv8 + vvec * a.SL * D;
+  const float* KSg = a.kvs + kvec * a.SLp;
+  const float* VSg = a.kvs + vvec * a.SLp;
+  auto issue = [&](int sb) {
+    const int s0 = s_begin + sb * SUB, n = min(SUB, s_end - s0);
+    const int n4 = (n + 3) & ~3;  // scale runs in whole 16-byte pieces (SLp covers the round-up)
+    uint8_t* st = smem + (sb & 1) * STAGE;
+    uint64_t* b = bar + (sb & 1);
+    mbar_expect_tx(b, 2u * n * D + 2u * n4 * 4);
+    bulk_g2s(st, Kg + (size_t)s0 * D, n * D, b);
+    bulk_g2s(st + CODES, Vg + (size_t)s0 * D, n * D, b);
+    bulk_g2s(st + 2 * CODES, KSg + s0, n4 * 4, b);
+    bulk_g2s(st + 2 * CODES + SUB * 4, VSg + s0, n4 * 4, b);
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    mbar_init(bar + 1, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (a.early && threadIdx.x == 0)
+    for (int sb = 0; sb < n_sub && sb < 2; ++sb) issue(sb);
+  if (!(kPdlLate & PDL_ATTN)) pdl_launch_dependents();
+  pdl_wait();  // q and the current slot come from the QKV and quantiser kernels
+  if (!a.early && threadIdx.x == 0)
+    for (int sb = 0; sb < n_sub && sb < 2; ++sb) issue(sb);
+
+  float qv[16];
+  {
+    const float* qp = a.q + ((size_t)row * a.nh + head) * D + 16 * li;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) qv[i] = qp[i] * a.scale;
+  }
+  const int cur = p < a.P ? p : a.P + (p - a.P) % a.R;
+
+  float m = -INFINITY, l = 0.f;
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+
+  for (int sb = 0; sb < n_sub; ++sb) {
+    const int s0 = s_begin + sb * SUB, n = min(SUB, s_end - s0);
+    int bad = 0;
+    if (threadIdx.x == 0) {
+      bad = !mbar_wait(bar + (sb & 1), (uint32_t)((sb >> 1) & 1));
+      if (bad) atomicOr(a.status, kStatusTimeout);
+    }
+    if (__syncthreads_or(bad)) {
+      if (threadIdx.x == 0 && sb + 1 < n_sub) mbar_wait(bar + ((sb + 1) & 1), (uint32_t)(((sb + 1) >> 1) & 1));
+      break;
+    }
+    uint8_t* stg = smem + (sb & 1) * STAGE;
+    const int8_t* Ks = reinterpret_cast<const int8_t*>(stg);
+    const int8_t* Vs = Ks + CODES;
+    float* KSs = reinterpret_cast<float*>(stg + 2 * CODES);
+    float* VSs = KSs + SUB;
+    if (a.early && cur >= s0 && cur < s0 + n) {  // the slot this step just wrote
+      for (int i = threadIdx.x; i < D / 16; i += blockDim.x) {
+        reinterpret_cast<uint4*>(stg + (size_t)(cur - s0) * D)[i] = reinterpret_cast<const uint4*>(Kg + (size_t)cur * D)[i];
+        reinterpret_cast<uint4*>(stg + CODES + (size_t)(cur - s0) * D)[i] =
+            reinterpret_cast<const uint4*>(Vg + (size_t)cur * D)[i];
+      }
+      if (threadIdx.x == 0) {
+        KSs[cur - s0] = KSg[cur];
+        VSs[cur - s0] = VSg[cur];
+      }
+      __syncthreads();
+    }
+    for (int base = warp * SPI; base < n; base += NW * SPI) {
+      uint4 kr[4], vr[4];
+      float ks[4], vs[4];
+      bool ok[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int slot = base + j * G + grp;
+        ok[j] = slot < n;
+        if (ok[j]) {
+          kr[j] = lds128(Ks + slot * D + 16 * li);
+          vr[j] = lds128(Vs + slot * D + 16 * li);
+          ks[j] = KSs[slot];
+          vs[j] = VSs[slot];
+        } else {
+          kr[j] = make_uint4(0u, 0u, 0u, 0u);
+          vr[j] = kr[j];
+          ks[j] = 0.f;
+          vs[j] = 0.f;
+        }
+      }
+      float sc[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t w[4] = {kr[j].x ^ 0x80808080u, kr[j].y ^ 0x80808080u, kr[j].z ^ 0x80808080u,
+                               kr[j].w ^ 0x80808080u};
+        float d = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          d = fmaf(qv[4 * i + 0], s8_to_f32<0>(w[i]), d);
+          d = fmaf(qv[4 * i + 1], s8_to_f32<1>(w[i]), d);
+          d = fmaf(qv[4 * i + 2], s8_to_f32<2>(w[i]), d);
+          d = fmaf(qv[4 * i + 3], s8_to_f32<3>(w[i]), d);
+        }
+#pragma unroll
+        for (int o = LPS / 2; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        sc[j] = ok[j] ? d * ks[j] : -INFINITY;
+      }
+      float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+#pragma unroll
+      for (int o = LPS; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float m_new = fmaxf(m, mx);  // finite: slot `base` is valid
+      const float corr = __expf(m - m_new);
+      float ps = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i] *= corr;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float pj = ok[j] ? __expf(sc[j] - m_new) : 0.f;
+        ps += pj;
+        const float pv = pj * vs[j];
+        const uint32_t w[4] = {vr[j].x ^ 0x80808080u, vr[j].y ^ 0x80808080u, vr[j].z ^ 0x80808080u,
+                               vr[j].w ^ 0x80808080u};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[4 * i + 0] = fmaf(pv, s8_to_f32<0>(w[i]), acc[4 * i + 0]);
+          acc[4 * i + 1] = fmaf(pv, s8_to_f32<1>(w[i]), acc[4 * i + 1]);
+          acc[4 * i + 2] = fmaf(pv, s8_to_f32<2>(w[i]), acc[4 * i + 2]);
+          acc[4 * i + 3] = fmaf(pv, s8_to_f32<3>(w[i]), acc[4 * i + 3]);
+        }
+      }
+#pragma unroll
+      for (int o = LPS; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+      l = l * corr + ps;
+      m = m_new;
+    }
+    __syncthreads();  // stage consumed
+    if (threadIdx.x == 0 && sb + 2 < n_sub) issue(sb + 2);
+  }
+  if (kPdlLate & PDL_ATTN) pdl_launch_dependents();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+#pragma unroll
+    for (int o = LPS; o < 32; o <<= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+  }
+  if (lane == 0) {
+    sm_m[warp] = m;
+    sm_l[warp] = l;
+  }
+  if (grp == 0) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sm_acc[warp][16 * li + i] = acc[i];
+  }
+  __syncthreads();
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w]);
+  float wsc[NW];
+#pragma unroll
+  for (int w = 0; w < NW; ++w) wsc[w] = (M == -INFINITY) ? 0.f : __expf(sm_m[w] - M);
+  if (threadIdx.x == 0) {
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) L += sm_l[w] * wsc[w];
+    s_part[0] = M;
+    s_part[1] = L;
+  }
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) v += sm_acc[w][d] * wsc[w];
+    s_part[2 + d] = v;
+  }
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  const int ns = a.nsplit;
+  float Mt = a.sink ? a.sink[head] : -INFINITY;
+  for (int sp = 0; sp < ns; ++sp) Mt = fmaxf(Mt, cluster.map_shared_rank(s_part, sp)[0]);
+  float Lt = a.sink ? __expf(a.sink[head] - Mt) : 0.f;
+  for (int sp = 0; sp < ns; ++sp) {
+    const float* pp = cluster.map_shared_rank(s_part, sp);
+    if (pp[0] != -INFINITY) Lt += pp[1] * __expf(pp[0] - Mt);
+  }
+  const int d0 = split * D / ns, d1 = (split + 1) * D / ns;
+  for (int d = d0 + threadIdx.x; d < d1; d += blockDim.x) {
+    float v = 0.f;
+    for (int sp = 0; sp < ns; ++sp) {
+      const float* pp = cluster.map_shared_rank(s_part, sp);
+      if (pp[0] != -INFINITY) v += pp[2 + d] * __expf(pp[0] - Mt);
+    }
+    a.out[(size_t)row * a.nh * D + head * D + d] = __float2half_rn(v / Lt);
+  }
+  cluster.sync();
+}
+
 cudaError_t launch_attn(const AttnArgs& a, int rows, cudaStream_t st, bool pdl) {
   const dim3 grid(a.nsplit, a.nh, rows);
+  if (a.kv8) {
+    const size_t sm8 = attn8_smem_bytes(a.D);
+    switch (a.D) {
+      case 16: return launch_kernel_cluster(k_attn8<16>, grid, dim3(UOCR_ATTN_WARPS * 32), sm8, st, pdl, a.nsplit, a);
+      case 32: return launch_kernel_cluster(k_attn8<32>, grid, dim3(UOCR_ATTN_WARPS * 32), sm8, st, pdl, a.nsplit, a);
+      case 64: return launch_kernel_cluster(k_attn8<64>, grid, dim3(UOCR_ATTN_WARPS * 32), sm8, st, pdl, a.nsplit, a);
+      case 128: return launch_kernel_cluster(k_attn8<128>, grid, dim3(UOCR_ATTN_WARPS * 32), sm8, st, pdl, a.nsplit, a);
+      case 256: return launch_kernel_cluster(k_attn8<256>, grid, dim3(UOCR_ATTN_WARPS * 32), sm8, st, pdl, a.nsplit, a);
+    }
+    return cudaErrorInvalidValue;
+  }
   const size_t sm = attn_smem_bytes(a.D);
   switch (a.D) {
     case 16: return launch_kernel_cluster(k_attn<16>, grid, dim3(UOCR_ATTN_WARPS * 32), sm, st, pdl, a.nsplit, a);
@@ -256,6 +572,10 @@ static cudaError_t init_attn_attributes() {
   if (e == cudaSuccess) e = allow_max_dyn_smem(k_attn<D_>);
   UOCR_A(16) UOCR_A(32) UOCR_A(64) UOCR_A(128) UOCR_A(256)
 #undef UOCR_A
+#define UOCR_A8(D_) \
+  if (e == cudaSuccess) e = allow_max_dyn_smem(k_attn8<D_>);
+  UOCR_A8(16) UOCR_A8(32) UOCR_A8(64) UOCR_A8(128) UOCR_A8(256)
+#undef UOCR_A8
   return e;
 }
 

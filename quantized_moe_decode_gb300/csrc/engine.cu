@@ -113,8 +113,13 @@ struct uocr_ctx {
   DMat lm;
   double* inv_freq = nullptr;
   float2* rope = nullptr;  // [max_rows][head_dim/2] (cos, sin) of the step's positions
-  __half* kv = nullptr;
-  size_t kv_layer = 0;  // elements per layer
+  __half* kv = nullptr;        // fp16 cache [L][MR][2][nh][SL][D]
+  int8_t* kv8 = nullptr;       // INT8 cache codes, same shape
+  float* kvs = nullptr;        // INT8 cache scales [L][MR][2][nh][SLp]
+  float* kv_new = nullptr;     // INT8 cache: the pass's new keys / values in fp32 [kTokCap][2][nh][D]
+  size_t kv_layer = 0;         // entries (codes or fp16 values) per layer
+  size_t kvs_layer = 0;        // scales per layer
+  int SLp = 0;                 // scale slots per (row, K|V, head): SL rounded up to 16
   int S = 0, SL = 0;
   float* hid = nullptr;  // [2L+1][kTokCap][H]
   __half* x_in = nullptr;
@@ -231,6 +236,7 @@ static uocr_status check_config(uocr_ctx* ctx, const uocr_config& c) {
   if (c.max_rows < 1 || c.max_rows > 64) return bad("max_rows must be in [1, 64]");
   if (c.use_sink != 0 && c.use_sink != 1) return bad("use_sink must be 0 or 1");
   if (!(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f)) return bad("rms_eps >= 0 and rope_theta > 0 required");
+  if (c.kv_int8 != 0 && c.kv_int8 != 1) return bad("kv_int8 must be 0 or 1");
   return UOCR_OK;
 }
 
@@ -285,7 +291,15 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
   ctx->S = S;
   ctx->SL = c.prefix_len + c.ring_len;
   ctx->kv_layer = (size_t)MR * 2 * c.n_heads * ctx->SL * c.head_dim;
-  ctx->kv = cv.take<__half>(ctx->kv_layer * Lc, r.kv_cache);
+  ctx->SLp = (ctx->SL + 15) / 16 * 16;
+  if (c.kv_int8) {
+    ctx->kvs_layer = (size_t)MR * 2 * c.n_heads * ctx->SLp;
+    ctx->kv8 = cv.take<int8_t>(ctx->kv_layer * Lc, r.kv_cache);
+    ctx->kvs = cv.take<float>(ctx->kvs_layer * Lc, r.kv_cache);
+    ctx->kv_new = cv.take<float>((size_t)TC * 2 * S, r.activations);
+  } else {
+    ctx->kv = cv.take<__half>(ctx->kv_layer * Lc, r.kv_cache);
+  }
   // activations
   ctx->hid = cv.take<float>((size_t)(2 * Lc + 1) * TC * H, r.activations);
   ctx->x_in = cv.take<__half>((size_t)TC * H, r.activations);
@@ -334,8 +348,9 @@ struct Prof {
 };
 
 // kernel classes of a step, in launch order
-const char* const kClasses[] = {"embed",  "qkv",    "attention",      "o_proj",              "mlp_gate_up",
-                                "mlp_down", "router", "expert_gate_up", "expert_down_combine", "lm_head_argmax"};
+const char* const kClasses[] = {"embed",       "qkv",      "kv_quant", "attention",      "o_proj",
+                                "mlp_gate_up", "mlp_down", "router",   "expert_gate_up", "expert_down_combine",
+                                "lm_head_argmax"};
 
 struct StepShape {
   int rows;
@@ -396,7 +411,9 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
 
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& w = ctx->L[l];
-    __half* kvl = ctx->kv + ctx->kv_layer * l;
+    __half* kvl = ctx->kv ? ctx->kv + ctx->kv_layer * l : nullptr;
+    int8_t* kv8l = ctx->kv8 ? ctx->kv8 + ctx->kv_layer * l : nullptr;
+    float* kvsl = ctx->kvs ? ctx->kvs + ctx->kvs_layer * l : nullptr;
     // QKV + RoPE + in-place KV append
     GemvArgs qa{};
     qa.w = w.qkv.view();
@@ -418,14 +435,36 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     qa.SL = ctx->SL;
     qa.kv_row0 = kv_row0;
     qa.kv_rstep = kv_rstep;
+    qa.kv_new = kv8l ? ctx->kv_new : nullptr;
     qa.status = ctx->status;
     if (want("qkv")) {
       CK(launch_gemv(c.fmt_attn, SRC_NORM, EPI_QKV, qa, gx_for(w.qkv.n_slabs), tg, st, pdl), "qkv launch");
+    }
+    if (kv8l) {  // INT8 cache: quantise the new keys / values into their slots
+      KvQuantArgs ka{};
+      ka.src32 = ctx->kv_new;
+      ka.kv8 = kv8l;
+      ka.kvs = kvsl;
+      ka.pos = ctx->pos_buf;
+      ka.nh = c.n_heads;
+      ka.D = c.head_dim;
+      ka.P = c.prefix_len;
+      ka.R = c.ring_len;
+      ka.SL = ctx->SL;
+      ka.SLp = ctx->SLp;
+      ka.kv_row0 = kv_row0;
+      ka.kv_rstep = kv_rstep;
+      if (want("kv_quant")) {
+        CK(launch_kv_quant(ka, rows, st, pdl), "kv quant launch");
+      }
     }
     // attention
     AttnArgs aa{};
     aa.q = ctx->q;
     aa.kv = kvl;
+    aa.kv8 = kv8l;
+    aa.kvs = kvsl;
+    aa.SLp = ctx->SLp;
     aa.pos = ctx->pos_buf;
     aa.out = ctx->attn_out;
     aa.sink = c.use_sink ? ctx->sinks + (size_t)l * c.n_heads : nullptr;
@@ -446,6 +485,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       if (ns < 1) ns = 1;
       aa.nsplit = ns;
       aa.chunk = (ctx->SL + ns - 1) / ns;
+      if (kv8l) aa.chunk = (aa.chunk + 15) / 16 * 16;  // scale runs start on 16-byte boundaries
     }
     aa.scale = 1.0f / sqrtf((float)c.head_dim);
     if (want("attention")) {
@@ -1034,6 +1074,113 @@ uocr_status uocr_load_weights(uocr_ctx* ctx, const uocr_tensor* t, size_t n) {
   return UOCR_OK;
 }
 
+}  // extern "C"
+
+// Slots [slot0, slot0 + n) of one (row, layer) from host fp16 [nh][n][D]
+// keys and values; the INT8 cache quantises them on the device.
+static uocr_status kv_put(uocr_ctx* ctx, int row, int layer, int slot0, int n, const uint16_t* k, const uint16_t* v) {
+  const uocr_config& c = ctx->cfg;
+  const size_t D = c.head_dim, nh = c.n_heads;
+  if (n == 0) return UOCR_OK;
+  if (!ctx->kv8) {
+    for (int kv = 0; kv < 2; ++kv) {
+      const uint16_t* src = kv ? v : k;
+      for (size_t h = 0; h < nh; ++h) {
+        __half* dst = ctx->kv + ctx->kv_layer * layer + ((((size_t)row * 2 + kv) * nh + h) * ctx->SL + slot0) * D;
+        CK(cudaMemcpyAsync(dst, src + h * n * D, (size_t)n * D * 2, cudaMemcpyHostToDevice, ctx->st), "kv copy");
+      }
+    }
+    CK(cudaStreamSynchronize(ctx->st), "kv copy");
+    return UOCR_OK;
+  }
+  const size_t bytes = nh * n * D * 2;
+  void* stage = nullptr;
+  CK(cudaMalloc(&stage, 2 * bytes), "kv staging allocation");
+  uint8_t* st8 = reinterpret_cast<uint8_t*>(stage);
+  cudaError_t e = cudaMemcpyAsync(st8, k, bytes, cudaMemcpyHostToDevice, ctx->st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st8 + bytes, v, bytes, cudaMemcpyHostToDevice, ctx->st);
+  if (e == cudaSuccess) {
+    KvQuantArgs ka{};
+    ka.src16k = reinterpret_cast<const __half*>(st8);
+    ka.src16v = reinterpret_cast<const __half*>(st8 + bytes);
+    ka.kv8 = ctx->kv8 + ctx->kv_layer * layer;
+    ka.kvs = ctx->kvs + ctx->kvs_layer * layer;
+    ka.slot0 = slot0;
+    ka.nh = c.n_heads;
+    ka.D = c.head_dim;
+    ka.P = c.prefix_len;
+    ka.R = c.ring_len;
+    ka.SL = ctx->SL;
+    ka.SLp = ctx->SLp;
+    ka.kv_row0 = row;
+    ka.kv_rstep = 0;
+    e = launch_kv_quant(ka, n, ctx->st, false);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->st);
+  cudaFree(stage);
+  return ctx->cuda(e, "kv quantise");
+}
+
+// Slots [slot0, slot0 + n) of one (row, layer) into host fp16 [nh][n][D]
+// (the INT8 cache gives scale * code rounded to fp16).
+static uocr_status kv_get(uocr_ctx* ctx, int row, int layer, int slot0, int n, uint16_t* k, uint16_t* v) {
+  const uocr_config& c = ctx->cfg;
+  const size_t D = c.head_dim, nh = c.n_heads;
+  CK(cudaStreamSynchronize(ctx->st), "kv read");
+  if (n == 0) return UOCR_OK;
+  if (!ctx->kv8) {
+    for (int kv = 0; kv < 2; ++kv) {
+      uint16_t* dst = kv ? v : k;
+      for (size_t h = 0; h < nh; ++h) {
+        const __half* src = ctx->kv + ctx->kv_layer * layer + ((((size_t)row * 2 + kv) * nh + h) * ctx->SL + slot0) * D;
+        CK(cudaMemcpy(dst + h * n * D, src, (size_t)n * D * 2, cudaMemcpyDeviceToHost), "kv read");
+      }
+    }
+    return UOCR_OK;
+  }
+  const size_t bytes = nh * n * D * 2;
+  void* stage = nullptr;
+  CK(cudaMalloc(&stage, 2 * bytes), "kv staging allocation");
+  __half* sk = reinterpret_cast<__half*>(stage);
+  __half* sv = sk + nh * n * D;
+  cudaError_t e = launch_kv_dequant(ctx->kv8 + ctx->kv_layer * layer + (size_t)row * 2 * nh * ctx->SL * D,
+                                    ctx->kvs + ctx->kvs_layer * layer + (size_t)row * 2 * nh * ctx->SLp, c.n_heads,
+                                    c.head_dim, ctx->SL, ctx->SLp, slot0, n, sk, sv, ctx->st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->st);
+  if (e == cudaSuccess) e = cudaMemcpy(k, sk, bytes, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(v, sv, bytes, cudaMemcpyDeviceToHost);
+  cudaFree(stage);
+  return ctx->cuda(e, "kv read");
+}
+
+// INT8 cache entries of slots [slot0, slot0 + n) of one (row, layer), exactly:
+// codes [nh][n][D] and scales [nh][n] per K and V; `put` writes them, else reads.
+static uocr_status kv_i8_io(uocr_ctx* ctx, int row, int layer, int slot0, int n, int8_t* kc, float* ks, int8_t* vc,
+                            float* vs, bool put) {
+  const uocr_config& c = ctx->cfg;
+  const size_t D = c.head_dim, nh = c.n_heads;
+  CK(cudaStreamSynchronize(ctx->st), "kv sync");
+  for (int kv = 0; kv < 2; ++kv) {
+    int8_t* codes = kv ? vc : kc;
+    float* scales = kv ? vs : ks;
+    for (size_t h = 0; h < nh; ++h) {
+      const size_t vec = ((size_t)row * 2 + kv) * nh + h;
+      int8_t* dc = ctx->kv8 + ctx->kv_layer * layer + (vec * ctx->SL + slot0) * D;
+      float* ds = ctx->kvs + ctx->kvs_layer * layer + vec * ctx->SLp + slot0;
+      if (put) {
+        CK(cudaMemcpy(dc, codes + h * n * D, (size_t)n * D, cudaMemcpyHostToDevice), "kv write");
+        CK(cudaMemcpy(ds, scales + h * n, (size_t)n * 4, cudaMemcpyHostToDevice), "kv write");
+      } else {
+        CK(cudaMemcpy(codes + h * n * D, dc, (size_t)n * D, cudaMemcpyDeviceToHost), "kv read");
+        CK(cudaMemcpy(scales + h * n, ds, (size_t)n * 4, cudaMemcpyDeviceToHost), "kv read");
+      }
+    }
+  }
+  return UOCR_OK;
+}
+
+extern "C" {
+
 uocr_status uocr_kv_write_prefix(uocr_ctx* ctx, int32_t row, int32_t layer, const uint16_t* k, const uint16_t* v,
                                  int32_t start, int32_t n) {
   if (!ctx) return UOCR_E_INVALID_ARG;
@@ -1042,17 +1189,7 @@ uocr_status uocr_kv_write_prefix(uocr_ctx* ctx, int32_t row, int32_t layer, cons
   if (!k || !v || row < 0 || row >= c.max_rows || layer < 0 || layer >= c.n_layers || start < 0 || n < 0 ||
       start + n > c.prefix_len)
     return ctx->fail(UOCR_E_INVALID_ARG, "kv_write_prefix: bad row/layer/range");
-  const size_t D = c.head_dim;
-  for (int kv = 0; kv < 2; ++kv) {
-    const uint16_t* src = kv ? v : k;
-    for (int h = 0; h < c.n_heads; ++h) {
-      __half* dst = ctx->kv + ctx->kv_layer * layer + ((((size_t)row * 2 + kv) * c.n_heads + h) * ctx->SL + start) * D;
-      CK(cudaMemcpyAsync(dst, src + (size_t)h * n * D, (size_t)n * D * 2, cudaMemcpyHostToDevice, ctx->st),
-         "kv prefix copy");
-    }
-  }
-  CK(cudaStreamSynchronize(ctx->st), "kv prefix copy");
-  return UOCR_OK;
+  return kv_put(ctx, row, layer, start, n, k, v);
 }
 
 uocr_status uocr_kv_write(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0, int32_t n, const uint16_t* k,
@@ -1063,17 +1200,7 @@ uocr_status uocr_kv_write(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slo
   if (!k || !v || row < 0 || row >= c.max_rows || layer < 0 || layer >= c.n_layers || slot0 < 0 || n < 0 ||
       slot0 + n > ctx->SL)
     return ctx->fail(UOCR_E_INVALID_ARG, "kv_write: bad row/layer/slot range");
-  const size_t D = c.head_dim;
-  for (int kv = 0; kv < 2; ++kv) {
-    const uint16_t* src = kv ? v : k;
-    for (int h = 0; h < c.n_heads; ++h) {
-      __half* dst = ctx->kv + ctx->kv_layer * layer + ((((size_t)row * 2 + kv) * c.n_heads + h) * ctx->SL + slot0) * D;
-      CK(cudaMemcpyAsync(dst, src + (size_t)h * n * D, (size_t)n * D * 2, cudaMemcpyHostToDevice, ctx->st),
-         "kv copy");
-    }
-  }
-  CK(cudaStreamSynchronize(ctx->st), "kv copy");
-  return UOCR_OK;
+  return kv_put(ctx, row, layer, slot0, n, k, v);
 }
 
 uocr_status uocr_kv_read(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0, int32_t n, uint16_t* k,
@@ -1084,17 +1211,33 @@ uocr_status uocr_kv_read(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot
   if (!k || !v || row < 0 || row >= c.max_rows || layer < 0 || layer >= c.n_layers || slot0 < 0 || n < 0 ||
       slot0 + n > ctx->SL)
     return ctx->fail(UOCR_E_INVALID_ARG, "kv_read: bad row/layer/range");
-  CK(cudaStreamSynchronize(ctx->st), "kv read");
-  const size_t D = c.head_dim;
-  for (int kv = 0; kv < 2; ++kv) {
-    uint16_t* dst = kv ? v : k;
-    for (int h = 0; h < c.n_heads; ++h) {
-      const __half* src =
-          ctx->kv + ctx->kv_layer * layer + ((((size_t)row * 2 + kv) * c.n_heads + h) * ctx->SL + slot0) * D;
-      CK(cudaMemcpy(dst + (size_t)h * n * D, src, (size_t)n * D * 2, cudaMemcpyDeviceToHost), "kv read");
-    }
-  }
-  return UOCR_OK;
+  return kv_get(ctx, row, layer, slot0, n, k, v);
+}
+
+uocr_status uocr_kv_read_i8(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0, int32_t n, int8_t* k_codes,
+                            float* k_scales, int8_t* v_codes, float* v_scales) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  const uocr_config& c = ctx->cfg;
+  if (!ctx->kv8) return ctx->fail(UOCR_E_STATE, "kv_read_i8: the cache is fp16 (kv_int8 = 0)");
+  if (!k_codes || !k_scales || !v_codes || !v_scales || row < 0 || row >= c.max_rows || layer < 0 ||
+      layer >= c.n_layers || slot0 < 0 || n < 0 || slot0 + n > ctx->SL)
+    return ctx->fail(UOCR_E_INVALID_ARG, "kv_read_i8: bad row/layer/range");
+  return kv_i8_io(ctx, row, layer, slot0, n, k_codes, k_scales, v_codes, v_scales, false);
+}
+
+uocr_status uocr_kv_write_i8(uocr_ctx* ctx, int32_t row, int32_t layer, int32_t slot0, int32_t n,
+                             const int8_t* k_codes, const float* k_scales, const int8_t* v_codes,
+                             const float* v_scales) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  const uocr_config& c = ctx->cfg;
+  if (!ctx->kv8) return ctx->fail(UOCR_E_STATE, "kv_write_i8: the cache is fp16 (kv_int8 = 0)");
+  if (!k_codes || !k_scales || !v_codes || !v_scales || row < 0 || row >= c.max_rows || layer < 0 ||
+      layer >= c.n_layers || slot0 < 0 || n < 0 || slot0 + n > ctx->SL)
+    return ctx->fail(UOCR_E_INVALID_ARG, "kv_write_i8: bad row/layer/range");
+  return kv_i8_io(ctx, row, layer, slot0, n, const_cast<int8_t*>(k_codes), const_cast<float*>(k_scales),
+                  const_cast<int8_t*>(v_codes), const_cast<float*>(v_scales), true);
 }
 
 uocr_status uocr_set_sinks(uocr_ctx* ctx, const float* sinks) {
@@ -1266,11 +1409,23 @@ uocr_status uocr_kv_reset(uocr_ctx* ctx, int32_t row, int32_t keep_prefix) {
   const uocr_config& c = ctx->cfg;
   if (row < -1 || row >= c.max_rows) return ctx->fail(UOCR_E_INVALID_ARG, "row out of range");
   const int r0 = row < 0 ? 0 : row, r1 = row < 0 ? c.max_rows : row + 1;
+  const int from = keep_prefix ? c.prefix_len : 0;
   for (int l = 0; l < c.n_layers; ++l)
     for (int r = r0; r < r1; ++r) {
-      __half* base = ctx->kv + ctx->kv_layer * l + (size_t)r * 2 * c.n_heads * ctx->SL * c.head_dim;
-      CK(launch_fill_zero_ring(base, c.n_heads, ctx->SL, c.head_dim, keep_prefix ? c.prefix_len : 0, ctx->st),
-         "kv reset");
+      if (!ctx->kv8) {
+        __half* base = ctx->kv + ctx->kv_layer * l + (size_t)r * 2 * c.n_heads * ctx->SL * c.head_dim;
+        CK(launch_fill_zero_ring(base, c.n_heads, ctx->SL, c.head_dim, from, ctx->st), "kv reset");
+        continue;
+      }
+      for (int vec = 0; vec < 2 * c.n_heads; ++vec) {  // codes and scales of slots [from, SL)
+        const size_t v = (size_t)r * 2 * c.n_heads + vec;
+        CK(cudaMemsetAsync(ctx->kv8 + ctx->kv_layer * l + (v * ctx->SL + from) * c.head_dim, 0,
+                           (size_t)(ctx->SL - from) * c.head_dim, ctx->st),
+           "kv reset");
+        CK(cudaMemsetAsync(ctx->kvs + ctx->kvs_layer * l + v * ctx->SLp + from, 0, (size_t)(ctx->SL - from) * 4,
+                           ctx->st),
+           "kv reset");
+      }
     }
   return UOCR_OK;
 }

@@ -135,6 +135,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
           float* qo = a.q_out + ((size_t)gt * a.nh + head) * a.D;
           qo[dlo] = vlo;
           qo[dhi] = vhi;
+        } else if (a.kv_new) {  // INT8 cache: the quantiser writes the slot
+          float* kn = a.kv_new + (((size_t)gt * 2 + (sec - 1)) * a.nh + head) * a.D;
+          kn[dlo] = vlo;
+          kn[dhi] = vhi;
         } else {
           const int slot = pos < a.P ? pos : a.P + (pos - a.P) % a.R;
           const int kvr = a.kv_row0 + gt * a.kv_rstep;

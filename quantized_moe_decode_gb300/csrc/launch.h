@@ -50,6 +50,8 @@ struct GemvArgs {
   const float2* rope;       // [rows][D/2] (cos, sin) of the step's positions
   int nh, D, S, P, R, SL;
   int kv_row0, kv_rstep;    // token t writes cache row kv_row0 + t * kv_rstep (decode: 0, 1; prefill: row, 0)
+  float* kv_new;            // INT8 cache: rotated k and v go here in fp32 [tokens][2][nh][D] (k_kv_quant
+                            // quantises them into the cache); nullptr: written to the fp16 cache directly
   // EPI_LOGITS
   int n_valid;              // vocab
   unsigned long long* keys; // [rows]
@@ -113,7 +115,10 @@ struct ExpertArgs {
 
 struct AttnArgs {
   const float* q;           // [rows][nh][D]
-  const __half* kv;         // layer base [rows][2][nh][SL][D]
+  const __half* kv;         // layer base [rows][2][nh][SL][D] (fp16 cache)
+  const int8_t* kv8;        // INT8 cache: codes [rows][2][nh][SL][D] (nullptr: fp16 cache)
+  const float* kvs;         //             scales [rows][2][nh][SLp]
+  int SLp;                  //             scale slots per (row, K|V, head): SL rounded up to 16
   const int* pos;
   __half* out;              // [rows][nh*D]
   const float* sink;        // [nh] or nullptr
@@ -123,6 +128,20 @@ struct AttnArgs {
                             //    (decode: only the current slot changes, and it is re-read)
   float scale;
   int* status;
+};
+
+// Quantise key / value vectors into the INT8 cache: one CTA per (token, K|V,
+// head), one thread per dimension.  src: fp32 [tokens][2][nh][D] (the step's
+// new keys and values) or fp16 [nh][n][D] per K and V (a written prefix).
+struct KvQuantArgs {
+  const float* src32;       // [tokens][2][nh][D], or nullptr
+  const __half* src16k;     // [nh][n][D] keys when src32 == nullptr
+  const __half* src16v;     // [nh][n][D] values
+  int8_t* kv8;              // layer base of the codes [rows][2][nh][SL][D]
+  float* kvs;               // layer base of the scales [rows][2][nh][SLp]
+  const int* pos;           // [tokens] positions (src32), or nullptr: slots slot0 + t
+  int slot0;
+  int nh, D, P, R, SL, SLp, kv_row0, kv_rstep;
 };
 
 struct EmbedArgs {
@@ -223,6 +242,10 @@ cudaError_t launch_embed(const EmbedArgs& a, int rows, cudaStream_t st);
 cudaError_t launch_pack(const PackArgs& a, cudaStream_t st);
 cudaError_t launch_fill_zero_ring(__half* kv_layer_row, int nh, int SL, int D, int from_slot, cudaStream_t st);
 cudaError_t launch_f32_to_f16(const float* src, __half* dst, long long n, cudaStream_t st);
+cudaError_t launch_kv_quant(const KvQuantArgs& a, int tokens, cudaStream_t st, bool pdl);
+cudaError_t launch_kv_dequant(const int8_t* kv8, const float* kvs, int nh, int D, int SL, int SLp, int slot0, int n,
+                              __half* k_out, __half* v_out, cudaStream_t st);
+int attn8_smem_bytes(int D);
 // A bounded mbarrier wait on a copy of 16 bytes from src that is issued only
 // when `issue` is set; a wait that runs out sets kStatusTimeout in *status.
 cudaError_t launch_wait_probe(const void* src, int issue, int* status, cudaStream_t st);

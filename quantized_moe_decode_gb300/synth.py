@@ -69,6 +69,7 @@ class ModelConfig:
     rms_eps: float = 1e-6
     rope_theta: float = 10000.0
     router_std: float = 0.02
+    kv_int8: int = 0  # INT8 KV cache (one scale per head vector) instead of fp16
 
     @property
     def moe(self) -> bool:

@@ -42,6 +42,7 @@ import numpy as np
 import oracle
 
 REL_L2 = 2e-3
+oracle_kv_quant = oracle.kv_quant  # entries of values the oracle's INT8 cache holds (scale * code: idempotent)
 MAX_ABS = 2e-2
 ROUTER_GAP = oracle.TIE_TOL  # router sets are compared where the oracle's gap exceeds it
 ROUTER_GAP_SAME_INPUT = 1e-3  # ... and where the router's inputs coincide on both sides
@@ -76,6 +77,8 @@ class Stats:
     id_checks: int = 0
     id_near_ties: int = 0
     kv_checks: int = 0
+    kv_codes: int = 0          # INT8 cache codes compared
+    kv_code_steps: int = 0     # ... that differ from the oracle's by one step
     grouping_checks: int = 0
     worst_weights_rel: float = 0.0
     tainted_rows: set = field(default_factory=set)
@@ -166,6 +169,10 @@ def compare_step(ctx, cfg, res, lib_rows, stats, row_map=None, check_kv=True, sa
             for i in keep:
                 r = row_map[i]
                 s = int(res.slots[i])
+                if cfg.kv_int8:
+                    check_int8_entries(ctx.uocr_kv_read_i8(r, l, s, 1), res.kv_entries[l][i], stats,
+                                       f"layer {l} row {r} slot {s}")
+                    continue
                 k, v = ctx.uocr_kv_read(r, l, s, 1)
                 stats.note(*check_close(f"layer {l} row {r} k at slot {s}", k[:, 0].astype(np.float64),
                                         res.k_new[l, i]))
@@ -240,12 +247,39 @@ def compare_step(ctx, cfg, res, lib_rows, stats, row_map=None, check_kv=True, sa
     return div
 
 
+def check_int8_entries(got, want, stats, name, exact=False):
+    """INT8 cache entries of the library (codes [nh][n][D], scales [nh][n] per
+    K and V, as uocr_kv_read_i8 gives them) against the oracle's (codes
+    [nh][(n,)D], scales [nh][(n)]).  The scales are floating-point outputs (the
+    stated tolerance).  A code is an integer decided in floating point: where
+    both sides' inputs coincide (exact) it must be equal; elsewhere the two
+    sides' values differ within the float tolerance, far less than half a code
+    step, so a code may differ by at most one step, and such steps are counted."""
+    gkc, gks, gvc, gvs = got
+    okc, oks, ovc, ovs = want
+    for nm, gc, gs, oc, os_ in (("k", gkc, gks, okc, oks), ("v", gvc, gvs, ovc, ovs)):
+        gc = gc.reshape(np.asarray(oc).shape)
+        gs = gs.reshape(np.asarray(os_).shape)
+        stats.note(*check_close(f"{name} {nm} scales", gs, os_))
+        d = np.abs(gc.astype(np.int32) - np.asarray(oc).astype(np.int32))
+        if exact:
+            assert not d.any() and np.array_equal(gs, os_), f"{name} {nm}: INT8 entries differ from the oracle's"
+        assert d.max(initial=0) <= 1, f"{name} {nm}: a code differs by {d.max()} steps"
+        stats.kv_codes += d.size
+        stats.kv_code_steps += int(np.count_nonzero(d))
+    stats.kv_checks += 1
+
+
 def resync_rows(ctx, cfg, res, div, row_map):
     """Give the library the oracle's cache entries of this step for the layers
     above a near-tie divergence (the oracle's K/V are fp16 values already)."""
     for i, l in enumerate(div):
         r, s = row_map[i], int(res.slots[i])
         for m in range(l + 1, cfg.n_layers):
+            if cfg.kv_int8:
+                kc, ks, vc, vs = res.kv_entries[m][i]
+                ctx.uocr_kv_write_i8(r, m, s, kc[:, None, :], ks[:, None], vc[:, None, :], vs[:, None])
+                continue
             k = res.k_new[m, i].astype(np.float16)[:, None, :]
             v = res.v_new[m, i].astype(np.float16)[:, None, :]
             ctx.uocr_kv_write(r, m, s, k, v)
@@ -314,16 +348,27 @@ def compare_prefill(ctx, cfg, res, lib_rows, lib_next, lib_logits, stats, row_ma
     for i, r in enumerate(row_map):
         for l in range(L):
             keep = [p for p in range(P) if tie[i][p] >= l]
-            k, v = ctx.uocr_kv_read(r, l, 0, P)
-            stats.note(*check_close(f"prefill row {r} layer {l} keys", k[:, keep].astype(np.float64),
-                                    pk[l][i][:, keep]))
-            stats.note(*check_close(f"prefill row {r} layer {l} values", v[:, keep].astype(np.float64),
-                                    pv[l][i][:, keep]))
-            stats.kv_checks += 1
+            if cfg.kv_int8:  # the oracle's entries: its cached values are scale * code
+                okc, oks = oracle_kv_quant(pk[l][i][:, keep])
+                ovc, ovs = oracle_kv_quant(pv[l][i][:, keep])
+                kc, ks, vc, vs = ctx.uocr_kv_read_i8(r, l, 0, P)
+                check_int8_entries((kc[:, keep], ks[:, keep], vc[:, keep], vs[:, keep]), (okc, oks, ovc, ovs), stats,
+                                   f"prefill row {r} layer {l}")
+            else:
+                k, v = ctx.uocr_kv_read(r, l, 0, P)
+                stats.note(*check_close(f"prefill row {r} layer {l} keys", k[:, keep].astype(np.float64),
+                                        pk[l][i][:, keep]))
+                stats.note(*check_close(f"prefill row {r} layer {l} values", v[:, keep].astype(np.float64),
+                                        pv[l][i][:, keep]))
+                stats.kv_checks += 1
             for p in range(P):
                 if tie[i][p] < l:  # the library's cache takes the oracle's entries
-                    ctx.uocr_kv_write(r, l, p, pk[l][i][:, p:p + 1].astype(np.float16),
-                                      pv[l][i][:, p:p + 1].astype(np.float16))
+                    if cfg.kv_int8:
+                        kq, vq = oracle_kv_quant(pk[l][i][:, p:p + 1]), oracle_kv_quant(pv[l][i][:, p:p + 1])
+                        ctx.uocr_kv_write_i8(r, l, p, kq[0], kq[1], vq[0], vq[1])
+                    else:
+                        ctx.uocr_kv_write(r, l, p, pk[l][i][:, p:p + 1].astype(np.float16),
+                                          pv[l][i][:, p:p + 1].astype(np.float16))
         stats.id_checks += 1
         if tie[i][P - 1] < L:
             stats.id_near_ties += 1

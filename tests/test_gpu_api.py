@@ -202,3 +202,40 @@ def test_prefill_refusals(cuda):
     ctx.uocr_prefill(0, 3, SL - 3, ids_ptr=ids.data_ptr())  # the last ring slots, no wrap
     ctx.uocr_sync()
     ctx.close()
+
+
+def test_int8_cache_prefix_quantised_exactly_and_entry_io(cuda):
+    """A written prefix is fp16 on both sides, so the INT8 entries (codes and
+    scales, decided in fp32) equal the oracle's bit for bit; exact entries
+    written with uocr_kv_write_i8 read back unchanged; uocr_kv_read gives
+    scale * code in fp16; the fp16 cache refuses the INT8 calls."""
+    import oracle
+
+    cfg = _cfg(kv_int8=1, prefix_len=40, head_dim=64, n_heads=4)
+    wl = _wl(seed=208, kv_int8=1, prefix_len=40, head_dim=64, n_heads=4)
+    ctx = make_ctx(wl)
+    nh, D = cfg.n_heads, cfg.head_dim
+    for r in range(wl.rows):
+        for l in range(cfg.n_layers):
+            k, v = wl.kv_prefix.get(l, r)
+            kc, ks, vc, vs = ctx.uocr_kv_read_i8(r, l, 0, cfg.prefix_len)
+            okc, oks = oracle.kv_quant(k)
+            ovc, ovs = oracle.kv_quant(v)
+            assert np.array_equal(kc, okc) and np.array_equal(ks, oks), (r, l)
+            assert np.array_equal(vc, ovc) and np.array_equal(vs, ovs), (r, l)
+    kd, vd = ctx.uocr_kv_read(1, 1, 3, 5)
+    kc, ks, vc, vs = ctx.uocr_kv_read_i8(1, 1, 3, 5)
+    assert np.array_equal(kd, (ks[..., None] * kc.astype(np.float32)).astype(np.float16))
+    rng = np.random.default_rng(3)
+    ck = rng.integers(-127, 128, size=(nh, 4, D)).astype(np.int8)
+    sk = rng.uniform(0.01, 0.1, size=(nh, 4)).astype(np.float32)
+    ctx.uocr_kv_write_i8(2, 0, cfg.prefix_len + 1, ck, sk, -ck, 2 * sk)
+    got = ctx.uocr_kv_read_i8(2, 0, cfg.prefix_len + 1, 4)
+    assert np.array_equal(got[0], ck) and np.array_equal(got[1], sk)
+    assert np.array_equal(got[2], -ck) and np.array_equal(got[3], 2 * sk)
+    ctx.close()
+    f16 = make_ctx(_wl(seed=209))
+    with pytest.raises(binding.UocrError) as e:
+        f16.uocr_kv_read_i8(0, 0, 0, 1)
+    assert e.value.status == binding.UOCR_E_STATE
+    f16.close()

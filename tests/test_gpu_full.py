@@ -171,6 +171,44 @@ def test_sink_sweep_rows_1_6_12_24_64(cuda, T):
     ctx.close()
 
 
+def _check_int8_prefix(ctx, wl, rows, layers):
+    """The cached prefix quantised by the library equals the oracle's entries exactly."""
+    import oracle
+
+    for r in rows:
+        for l in layers:
+            k, v = wl.kv_prefix.get(l, r)
+            kc, ks, vc, vs = ctx.uocr_kv_read_i8(r, l, 0, wl.cfg.prefix_len)
+            for got, want in ((kc, ks), oracle.kv_quant(k)), ((vc, vs), oracle.kv_quant(v)):
+                assert np.array_equal(got[0], want[0]) and np.array_equal(got[1], want[1]), (r, l)
+
+
+def test_int8_kv_moe_layer_b1_ring_wraps(cuda):
+    wl = synth.workload("moe_layer_b1", steps=160)
+    wl.cfg = wl.cfg.replace(kv_int8=1)
+    ctx = make_ctx(wl)
+    _check_int8_prefix(ctx, wl, [0], [0])
+    st = run_parity(ctx, wl, 160, make_oracle(wl, cache=_cache()))
+    _report(wl.name + " (INT8 KV)", st)
+    print(f"INT8 entries: {st.kv_codes} codes, {st.kv_code_steps} one step off")
+    assert st.kv_checks == 160 and st.kv_code_steps <= 0.01 * st.kv_codes
+    ctx.close()
+
+
+def test_int8_kv_stress_b64_sampled_rows(cuda):
+    wl = synth.workload("stress_b64", steps=24)
+    wl.cfg = wl.cfg.replace(kv_int8=1)
+    sample = [0, 63]
+    ctx = make_ctx(wl)
+    _check_int8_prefix(ctx, wl, sample, [0, 11])
+    st = run_parity(ctx, wl, 24, make_oracle(wl, rows=sample, cache=_cache()), rows=wl.rows, row_map=sample)
+    _report(wl.name + " (INT8 KV)", st)
+    print(f"INT8 entries: {st.kv_codes} codes, {st.kv_code_steps} one step off")
+    assert st.id_checks >= 0.85 * len(sample) * 24
+    assert st.kv_code_steps <= 0.05 * st.kv_codes
+    ctx.close()
+
+
 def test_stress_b64_sampled_rows(cuda):
     wl = synth.workload("stress_b64")
     sample = [0, 63]

@@ -142,3 +142,36 @@ def test_dense_uocr_prefill_with_sinks_int8_asym(cuda):
     wl = synth.make_workload("dense_prefill_ring", cfg, 2, 5, 111, prefix="prefill", n_prefill_embeds=30,
                              step_input="ids")
     _run(wl, 5, lib_prefill=True)
+
+
+# ---------------------------------------------------------------- INT8 KV cache
+def _code_steps_small(st, frac=0.02):
+    print(f"INT8 entries: {st.kv_codes} codes, {st.kv_code_steps} one step off")
+    assert st.kv_codes > 0 and st.kv_code_steps <= frac * st.kv_codes
+
+
+def test_int8_kv_dense_ring_wrap_sinks_head_dim_64(cuda):
+    cfg = _dense(kv_int8=1, use_sink=1, fmt_attn=I8, fmt_dense=Q8)
+    wl = synth.make_workload("i8kv_dense", cfg, 3, 20, 120)
+    _code_steps_small(_run(wl, 20))
+
+
+def test_int8_kv_moe_prefill_by_decode_then_greedy(cuda):
+    wl = synth.make_workload("i8kv_moe_lm", _moe(kv_int8=1), 5, 10, 121, prefix="prefill", n_prefill_embeds=8,
+                             step_input="ids")
+    st = _run(wl, 10)
+    assert st.id_checks >= 5 * 10
+    _code_steps_small(st)
+
+
+def test_int8_kv_moe_forty_rows_three_token_groups(cuda):
+    cfg = _moe(kv_int8=1, max_rows=40, fmt_shared=Q4, vocab=0, prefix_len=10)
+    wl = synth.make_workload("i8kv_moe_40rows", cfg, 40, 8, 122)
+    _code_steps_small(_run(wl, 8))
+
+
+def test_int8_kv_uocr_prefill_two_chunks(cuda):
+    cfg = _moe(kv_int8=1, prefix_len=90, max_rows=2)
+    wl = synth.make_workload("i8kv_prefill", cfg, 2, 5, 123, prefix="prefill", n_prefill_embeds=70,
+                             step_input="ids")
+    _code_steps_small(_run(wl, 5, lib_prefill=True))
