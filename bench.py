@@ -104,9 +104,12 @@ def class_bytes(cfg, rows, positions, distinct):
             out.setdefault("expert_gate_up", []).append(
                 U * 2 * Ie * H * BPW[cfg.fmt_routed] + 2 * Ish * H * BPW[cfg.fmt_shared]
                 + rows * H * 2 + rows * (cfg.top_k * Ie + Ish) * 2)
-            out.setdefault("expert_down_combine", []).append(
+            out.setdefault("expert_down", []).append(
                 U * H * Ie * BPW[cfg.fmt_routed] + H * Ish * BPW[cfg.fmt_shared]
-                + rows * (cfg.top_k * Ie + Ish) * 2 + 2 * act)
+                + rows * (cfg.top_k * Ie + Ish) * 2 + rows * (cfg.top_k + 1) * H * 4)
+            # residual + k weighted partials + the shared partial in, the layer output out
+            out.setdefault("expert_combine", []).append(rows * (cfg.top_k + 2) * H * 4 + rows * cfg.top_k * 4
+                                                        + act)
     if V:
         out["lm_head_argmax"] = [V * H * 2 + act + rows * 8]
     return out
@@ -411,7 +414,8 @@ def run_ours(args, rank, world):
     t_setup = time.perf_counter()
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
-    ctx, wl, ids, _ = open_workload(WORKLOAD, dev, stream)
+    kw = {"rows": args.rows} if args.rows else {}
+    ctx, wl, ids, _ = open_workload(args.workload, dev, stream, {"kv_int8": 1} if args.kv_int8 else None, **kw)
     cfg, rows = wl.cfg, wl.rows
     K, W = args.steps, args.warmup
     log(f"[bench] setup {time.perf_counter() - t_setup:.1f}s")
@@ -482,7 +486,10 @@ def run_ours(args, rank, world):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 activations x Q8_0/Q4_0 weights, f32 accumulate", "data": "synthetic",
-        "config": dict(HEADLINE_CONFIG, global_batch=rows * world, positions=[p0, p0 + K - 1],
+        "config": dict(HEADLINE_CONFIG if (args.workload == WORKLOAD and not args.rows and not args.kv_int8)
+                       else {"workload": wl.name + (" INT8 KV" if args.kv_int8 else ""), "rows": rows,
+                             "prefix": cfg.prefix_len, "ring": cfg.ring_len},
+                       global_batch=rows * world, positions=[p0, p0 + K - 1],
                        parallelism="replicas" if world > 1 else "single",
                        l2="inputs larger than L2: %.2f GB touched per step" % (step_bytes / 1e9)),
         "hbm_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
@@ -598,6 +605,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-side-configs", action="store_true", help="only the headline configuration")
+    ap.add_argument("--workload", default=WORKLOAD, help="measure another named workload instead (profiling runs)")
+    ap.add_argument("--rows", type=int, default=0, help="rows of that workload (0: its own)")
+    ap.add_argument("--kv-int8", action="store_true", help="with an INT8 KV cache")
     ap.add_argument("--cpu-sample", nargs=2, type=float, help=argparse.SUPPRESS)
     ap.add_argument("--sweep", action="store_true", help="time the other workloads (extra JSON lines) instead")
     args = ap.parse_args()

@@ -131,7 +131,6 @@ struct uocr_ctx {
   uint8_t* act_s = nullptr;  // B-fragment order, rows x n_shared*Ie
   float* part_r = nullptr;
   float* part_s = nullptr;
-  int* slab_counter = nullptr;
   float* r_logits = nullptr;
   int *r_idx = nullptr, *r_count = nullptr, *r_offset = nullptr, *r_perm = nullptr, *r_inv = nullptr;
   int4* r_rec = nullptr;  // [L][token groups][E] routing records
@@ -313,7 +312,6 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
     ctx->act_s = cv.take<uint8_t>((size_t)(TC + 7) / 8 * 8 * (Ish > 0 ? Ish : 32) * 2, r.activations);
     ctx->part_r = cv.take<float>((size_t)TC * k * H, r.activations);
     ctx->part_s = cv.take<float>((size_t)TC * H, r.activations);
-    ctx->slab_counter = cv.take<int>(H / 16, r.activations);
     ctx->r_logits = cv.take<float>((size_t)Lc * TC * E, r.routing);
     ctx->r_idx = cv.take<int>((size_t)Lc * TC * k, r.routing);
     ctx->r_w = cv.take<float>((size_t)Lc * TC * k, r.routing);
@@ -349,7 +347,7 @@ struct Prof {
 
 // kernel classes of a step, in launch order
 const char* const kClasses[] = {"embed",       "qkv",      "kv_quant", "attention",      "o_proj",
-                                "mlp_gate_up", "mlp_down", "router",   "expert_gate_up", "expert_down_combine",
+                                "mlp_gate_up", "mlp_down", "router",   "expert_gate_up", "expert_down", "expert_combine",
                                 "lm_head_argmax"};
 
 struct StepShape {
@@ -592,7 +590,6 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       xa.part_r = ctx->part_r;
       xa.part_s = ctx->part_s;
       xa.out = hid(2 * l + 2);
-      xa.slab_counter = ctx->slab_counter;
       xa.status = ctx->status;
       xa.by_slot = by_slot;
       xa.n_units = n_units;
@@ -648,8 +645,11 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
         xa.sp = plan_stream(nt, c.fmt_routed, 0, 0, nt * (kmax / 32) * 512);
       }
       split(w.ex_down, shd, H / 16, H / 16);
-      if (want("expert_down_combine")) {
+      if (want("expert_down")) {
         CK(launch_expert_down(c.fmt_routed, fs, xa, st, pdl), "expert down launch");
+      }
+      if (want("expert_combine")) {
+        CK(launch_expert_combine(xa, st, pdl), "expert combine launch");
       }
     }
   }

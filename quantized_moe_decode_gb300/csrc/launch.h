@@ -109,7 +109,6 @@ struct ExpertArgs {
   float* part_r;            // [rows*k][H] per entry row*k + slot
   float* part_s;            // [rows][H]
   float* out;               // layer output residual [rows][H]
-  int* slab_counter;        // [H/16]
   int* status;
 };
 
@@ -237,6 +236,7 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t st, bool pdl);
 int router_cluster(int n_slabs);
 cudaError_t launch_expert_gateup(int fmt_r, int fmt_s, const ExpertArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_expert_down(int fmt_r, int fmt_s, const ExpertArgs& a, cudaStream_t st, bool pdl);
+cudaError_t launch_expert_combine(const ExpertArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_attn(const AttnArgs& a, int rows, cudaStream_t st, bool pdl);
 cudaError_t launch_embed(const EmbedArgs& a, int rows, cudaStream_t st);
 cudaError_t launch_pack(const PackArgs& a, cudaStream_t st);

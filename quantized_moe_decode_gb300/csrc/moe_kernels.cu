@@ -18,9 +18,10 @@
 //            directly.  CTA 0 also writes the grouping arrays (count, offset,
 //            perm, inv) from the router's choices.
 //   down     the same CTA layout; it streams the expert's down slabs and
-//            writes fp32 partials; the last contribution to an output slab (a
-//            counter per slab, no waiting) combines them in a fixed order:
-//            residual + sum_j w_j * expert_j + shared.
+//            writes fp32 partials per (row, slot) and per row for the shared
+//            experts.
+//   combine  one thread per output: residual + sum_j w_j * expert_j (slot
+//            order) + shared, in the same fixed order for every row.
 //
 // Routed units are expert ids when most experts are expected to receive a
 // token (the CTA streams the head of its expert's weights before the routing
@@ -133,7 +134,6 @@ __device__ __forceinline__ void topk_rank(const RowLogits& rl, int E, int k, int
 // Routing state of a CTA in shared memory.
 struct RouteSmem {
   int idx[64 * 8];                  // [row][k] chosen experts
-  float w[64 * 8];                  // [row][k] weights
   unsigned long long rowmask[256];  // [E] rows that chose expert e (bit r)
   int off[256];
   int4 scan[kWarps];
@@ -141,7 +141,7 @@ struct RouteSmem {
   int4 grec[4];                     // this CTA's unit's record of each token group
   int rows[64];                     // the unit's rows over all token groups, ascending
   int ent[64];                      // their entries row * k + slot
-  int e, n, nlast, contrib;
+  int e, n;
 };
 
 // The rows of a routed unit over all token groups (ascending) and their entries
@@ -564,26 +564,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
     usr.prefetch(ring, p.slot, w, lane);
     streaming = true;
   }
-  if (threadIdx.x == 0) rs.contrib = 0;
-  __syncthreads();
   pdl_wait();
-  // contributions every output slab receives: one per routed unit with rows in any
-  // token group (each unit's CTAs cover every slab once), one for the shared experts
   int4 mine = make_int4(-1, 0, 0, 0);  // active-slot units: record threadIdx.x of the (single) group
-  {
-    int c = 0;
-    for (int u = threadIdx.x; u < a.n_units; u += kThreads) {
-      bool any = false;
-      for (int g = 0; g < a.tg; ++g) {
-        const int4 v = __ldcg(a.rec + (size_t)g * a.n_units + u);
-        any |= v.y != 0;
-        if (g == 0 && u == (int)threadIdx.x) mine = v;
-      }
-      c += any;
-    }
-    if (c) atomicAdd(&rs.contrib, c);
-  }
-  for (int i = threadIdx.x; i < rows * k; i += kThreads) rs.w[i] = __ldcg(a.wts + i);  // combine weights
+  if (a.by_slot && (int)threadIdx.x < a.n_units) mine = __ldcg(a.rec + threadIdx.x);
   int e = -1, ntk = rows;
   const int k32 = (ec.shared ? a.Ish : a.Ie) >> 5;
   if (!ec.shared) {
@@ -644,54 +627,32 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_expert_down(const Expe
   }
   if (kPdlLate & PDL_EXPERT) pdl_launch_dependents();
 
-  // one counter per output slab; the last contribution to a slab combines it.
-  // All of this CTA's slabs are counted at once (one thread per slab), and all
-  // slabs it finishes are combined in one batched pass.
-  const int s_contrib = rs.contrib + (a.ws.n_slabs > 0 ? 1 : 0);
-  int* s_last = reinterpret_cast<int*>(red);  // the partial buffers are free now
-  __syncthreads();
-  if (threadIdx.x == 0) rs.nlast = 0;
-  __syncthreads();
-  for (int t = threadIdx.x; t < s1 - s0; t += kThreads) {
-    __threadfence();
-    const int done = atomicAdd(a.slab_counter + s0 + t, 1);
-    if (done == s_contrib - 1) s_last[atomicAdd(&rs.nlast, 1)] = s0 + t;
-  }
-  __syncthreads();
-  const int nlast = rs.nlast;
-  if (nlast == 0) return;
-  __threadfence();
-  constexpr int B = UOCR_COMBINE_B;  // items per thread per batch: loads first, then sums
-  const int items = nlast * rows * 16;
-  for (int i0 = threadIdx.x; i0 < items; i0 += B * kThreads) {
-    float pr[B][8], ps[B], hv[B];
+}
+
+// ------------------------------------------------------------------ combine
+// out[r][c] = h[r][c] + sum_j w[r][j] * part_r[r*k + j][c] (slot order) + part_s[r][c]:
+// one thread per output, after every expert CTA of the down launch has written
+// its partials (griddepcontrol.wait), in the same fixed order for every row.
+__global__ void __launch_bounds__(256) k_expert_combine(const ExpertArgs a) {
+  pdl_launch_dependents();
+  const int H = a.H, k = a.k;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int r = i / H, c = i - r * H;
+  float w[8];
+  const bool ok = r < a.ntok;
+  pdl_wait();
+  if (!ok) return;
 #pragma unroll
-    for (int b = 0; b < B; ++b) {
-      const int i = i0 + b * kThreads;
-      const int it = i < items ? i : 0;
-      const int sl = s_last[it / (rows * 16)], rc = it % (rows * 16);
-      const int r = rc >> 4, col = 16 * sl + (rc & 15);
+  for (int j = 0; j < 8; ++j) w[j] = j < k ? __ldcg(a.wts + r * k + j) : 0.f;
+  float pr[8];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj)
-        pr[b][jj] = jj < k ? __ldcg(a.part_r + (size_t)(r * k + jj) * H + col) : 0.f;
-      ps[b] = a.ws.n_slabs > 0 ? __ldcg(a.part_s + (size_t)r * H + col) : 0.f;
-      hv[b] = a.h[(size_t)r * H + col];
-    }
+  for (int j = 0; j < 8; ++j) pr[j] = j < k ? __ldcg(a.part_r + (size_t)(r * k + j) * H + c) : 0.f;
+  const float ps = a.ws.n_slabs > 0 ? __ldcg(a.part_s + (size_t)r * H + c) : 0.f;
+  float v = a.h[(size_t)r * H + c];
 #pragma unroll
-    for (int b = 0; b < B; ++b) {
-      const int i = i0 + b * kThreads;
-      if (i >= items) continue;
-      const int sl = s_last[i / (rows * 16)], rc = i % (rows * 16);
-      const int r = rc >> 4, col = 16 * sl + (rc & 15);
-      float v = hv[b];  // residual + sum_j w_j * expert_j (slot order) + shared
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj)
-        if (jj < k) v += rs.w[r * k + jj] * pr[b][jj];
-      v += ps[b];
-      a.out[(size_t)r * H + col] = v;
-    }
-  }
-  for (int t = threadIdx.x; t < nlast; t += kThreads) atomicExch(a.slab_counter + s_last[t], 0);
+  for (int j = 0; j < 8; ++j)
+    if (j < k) v += w[j] * pr[j];
+  a.out[(size_t)r * H + c] = v + ps;
 }
 
 // ------------------------------------------------------------------ launchers
@@ -720,6 +681,11 @@ cudaError_t launch_expert_gateup(int fr, int fs, const ExpertArgs& a, cudaStream
   UOCR_PAIRS(X, 2)
 #undef X
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_expert_combine(const ExpertArgs& a, cudaStream_t st, bool pdl) {
+  const int n = a.ntok * a.H;
+  return launch_kernel(k_expert_combine, dim3((n + 255) / 256), dim3(256), 0, st, pdl, a);
 }
 
 cudaError_t launch_expert_down(int fr, int fs, const ExpertArgs& a, cudaStream_t st, bool pdl) {

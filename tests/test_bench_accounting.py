@@ -27,13 +27,13 @@ def test_expert_weights_scale_with_the_experts_picked():
     cfg = synth.config_stress(max_rows=64)  # every expert Q4_0, shared ones too
     one = _weights_only(cfg, {l: 1 for l in range(1, 12)})
     none = _weights_only(cfg, {l: 0 for l in range(1, 12)})
-    per_expert = (one["expert_gate_up"][0] + one["expert_down_combine"][0]
-                  - none["expert_gate_up"][0] - none["expert_down_combine"][0])
+    per_expert = (one["expert_gate_up"][0] + one["expert_down"][0]
+                  - none["expert_gate_up"][0] - none["expert_down"][0])
     assert per_expert == 1_935_360  # 3 * 896 * 1280 * 18 / 32
-    assert none["expert_gate_up"][0] + none["expert_down_combine"][0] == 3_870_720  # two shared, Q4_0
+    assert none["expert_gate_up"][0] + none["expert_down"][0] == 3_870_720  # two shared, Q4_0
     full = synth.config_full(max_rows=8)  # shared experts Q8_0
     z = _weights_only(full, {l: 0 for l in range(1, 12)})
-    assert z["expert_gate_up"][0] + z["expert_down_combine"][0] == 7_311_360  # 2 * 3 * 896 * 1280 * 34 / 32
+    assert z["expert_gate_up"][0] + z["expert_down"][0] == 7_311_360  # 2 * 3 * 896 * 1280 * 34 / 32
 
 
 def test_kv_bytes_per_row_and_layer_follow_the_valid_slots():
