@@ -86,7 +86,16 @@ typedef enum {
  *   UOCR_Q4_0    {fp16 d; uint8 qs[16]}         18 B   value = d*(q-8), q of
  *                element j<16 = low nibble of qs[j], j>=16 = high nibble of qs[j-16]
  *   UOCR_I8ASYM  {fp16 s; fp16 z; uint8 q[32]}  36 B   value = s*(q-z)      */
-typedef enum { UOCR_F16 = 0, UOCR_Q8_0 = 1, UOCR_Q4_0 = 2, UOCR_I8ASYM = 3 } uocr_format;
+typedef enum {
+  UOCR_F16 = 0,
+  UOCR_Q8_0 = 1,
+  UOCR_Q4_0 = 2,
+  UOCR_I8ASYM = 3,
+  UOCR_Q8_0_G64 = 4, /* {fp16 d; int8 q[64]}   66 B   value = d*q                      */
+  UOCR_Q4_0_G64 = 5  /* {fp16 d; uint8 qs[32]} 34 B   value = d*(q-8), q of element
+                        j<32 = low nibble of qs[j], j>=32 = high nibble of qs[j-32]
+                        ([Metal] "Quantizzazione": groups of 64 values)          */
+} uocr_format;
 
 /* Weight tensor kinds.  Source: [Metal] "Il decoder e il Mixture of Experts"
  * (attention, one dense MLP layer, MoE layers with a router, 64 routed and 2
@@ -112,7 +121,9 @@ typedef enum {
   UOCR_T_SHARED_DOWN = 15,  /* [H][Ie]  fmt_shared                           */
   UOCR_T_EXPERT_GATE = 16,  /* [Ie][H]  fmt_routed     expert = routed index */
   UOCR_T_EXPERT_UP = 17,    /* [Ie][H]  fmt_routed                           */
-  UOCR_T_EXPERT_DOWN = 18   /* [H][Ie]  fmt_routed                           */
+  UOCR_T_EXPERT_DOWN = 18,  /* [H][Ie]  fmt_routed                           */
+  UOCR_T_PROJ = 19,         /* [H][proj_in]  fmt_proj   projector (proj_in > 0) layer 0 */
+  UOCR_T_PROJ_BIAS = 20     /* [1][H]   F16             projector bias          layer 0 */
 } uocr_tensor_kind;
 
 /* Source: [Metal] "Il decoder e il Mixture of Experts" (model constants, the
@@ -150,6 +161,10 @@ typedef struct {
                               vector of a head quantised when written
                               (s = max|x| / 127, code = round(x / s)) -- [Falcon]
                               "How it is meant to be run" (an INT8 KV cache)   */
+  /* projector of visual features into the hidden space ([Metal] "Il modello":
+     2048 -> 1280; "Quantizzazione": the Q8 profile covers the projector)       */
+  int32_t proj_in;         /* input width, multiple of 64 (0 = no projector)     */
+  int32_t fmt_proj;        /* uocr_format of UOCR_T_PROJ                         */
 } uocr_config;
 
 typedef struct {
@@ -273,6 +288,19 @@ UOCR_API uocr_status uocr_decode_step(uocr_ctx* ctx, int32_t rows, const int32_t
 UOCR_API uocr_status uocr_decode_step_embeds(uocr_ctx* ctx, int32_t rows, const uint16_t* x,
                                     const int32_t* positions, float* y, uint16_t* y_f16,
                                     int32_t* next_ids, float* logits);
+
+/* Source: [Metal] "Il modello: una pipeline vision-language completa" (the
+ * encoders' features pass through a projector from 2048 to 1280 dimensions,
+ * then take the image placeholder's span of the prompt) and "Quantizzazione"
+ * (the projector is quantised in the Q8 profile, biases stay fp16).
+ * out = fp16(W_proj feats + b_proj) for n feature vectors: one launch of the
+ * fused dequant GEMM (every weight read serves 16 features per token group,
+ * on the tensor cores).  Needs proj_in > 0 and UOCR_T_PROJ / UOCR_T_PROJ_BIAS
+ * loaded (the decoder's weights are not needed).
+ *   feats  device fp16 [n][proj_in]
+ *   out    device fp16 [n][hidden] (e.g. the x of uocr_prefill)
+ * Asynchronous (see conventions); not captured in a graph.                  */
+UOCR_API uocr_status uocr_project(uocr_ctx* ctx, int32_t n, const uint16_t* feats, uint16_t* out);
 
 /* Source: [Metal] intro and "Il modello" (prefill of the prompt, with the
  * visual tokens in the placeholder span, before token-by-token decoding);

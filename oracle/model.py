@@ -54,6 +54,7 @@ T_GATE, T_UP, T_DOWN = 9, 10, 11
 T_ROUTER = 12
 T_SHARED_GATE, T_SHARED_UP, T_SHARED_DOWN = 13, 14, 15
 T_EXPERT_GATE, T_EXPERT_UP, T_EXPERT_DOWN = 16, 17, 18
+T_PROJ, T_PROJ_BIAS = 19, 20
 
 
 # ------------------------------------------------------------------ primitives
@@ -122,6 +123,22 @@ def kv_quant(x):
 def kv_dequant(codes, s):
     """Value of an INT8 KV entry: s * code (float64)."""
     return np.asarray(codes, dtype=np.float64) * np.asarray(s, dtype=np.float64)[..., None]
+
+
+def project(feats, W, b=None):
+    """The projector that takes visual features into the decoder's hidden space:
+    y = W x (+ b), stored in fp16 as the decoder's input embeddings.
+
+    "Unlimited-OCR on Apple Silicon with C and Metal", "Il modello: una
+    pipeline vision-language completa" (the two encoders' features pass through
+    a projector from 2048 to 1280 dimensions) and "Quantizzazione" (the Q8
+    profile covers the projector; biases stay fp16).  A single linear map with
+    a bias is the reading taken.
+    """
+    y = np.asarray(feats, dtype=np.float64) @ W.T
+    if b is not None:
+        y = y + b
+    return f16(y)
 
 
 def ring_slot(p, P, R):
@@ -287,6 +304,12 @@ class OracleModel:
             else:
                 self._cache[key] = m
         return m
+
+    # ---------------------------------------------------------------- projector
+    def project(self, feats):
+        """Visual features [n, proj_in] -> fp16 embeddings [n, hidden]."""
+        b = self.w(T_PROJ_BIAS) if (T_PROJ_BIAS, 0, 0) in self._t else None
+        return project(feats, self.w(T_PROJ), b)
 
     # ---------------------------------------------------------------- attention
     def _valid(self, row, p):

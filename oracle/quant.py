@@ -14,6 +14,14 @@ blocks run along the row, rows are stored one after another):
 * I8ASYM {fp16 s; fp16 z; uint8 q[32]}   value = s * (q - z)
 * F16    plain little-endian fp16 matrix
 
+and the same Q8_0 / Q4_0 definitions over groups of 64 values (the Metal
+page's "La quantizzazione opera su gruppi di 64 valori"):
+
+* Q8_0_G64 {fp16 d; int8 q[64]}          value = d * q
+* Q4_0_G64 {fp16 d; uint8 qs[32]}        value = d * (q - 8), q of element
+           j < 32 the low nibble of qs[j], of j >= 32 the high nibble of
+           qs[j - 32] (the 32-value rule with the half moved to 32: a reading)
+
 Cites: "Unlimited-OCR on Apple Silicon with C and Metal", section
 "Quantizzazione: Q8 prima, Q4 dove conviene" (Q8_0 / Q4_0 profiles with the
 dequantisation fused into the kernels); "Falcon-OCR INT8 OpenVINO IR" model
@@ -25,16 +33,18 @@ from __future__ import annotations
 
 import numpy as np
 
-F16, Q8_0, Q4_0, I8ASYM = 0, 1, 2, 3
+F16, Q8_0, Q4_0, I8ASYM, Q8_0_G64, Q4_0_G64 = 0, 1, 2, 3, 4, 5
 BLOCK = 32
-_BYTES = {Q8_0: 34, Q4_0: 18, I8ASYM: 36}
+_GROUP = {Q8_0: 32, Q4_0: 32, I8ASYM: 32, Q8_0_G64: 64, Q4_0_G64: 64}
+_BYTES = {Q8_0: 34, Q4_0: 18, I8ASYM: 36, Q8_0_G64: 66, Q4_0_G64: 34}
 
 
 def _blocks(blob, fmt, rows, cols):
-    if cols % BLOCK:
-        raise ValueError("cols must be a multiple of 32")
+    g = _GROUP[fmt]
+    if cols % g:
+        raise ValueError(f"cols must be a multiple of {g}")
     raw = np.frombuffer(np.asarray(blob, dtype=np.uint8).tobytes(), dtype=np.uint8)
-    nb = cols // BLOCK
+    nb = cols // g
     if raw.size != rows * nb * _BYTES[fmt]:
         raise ValueError("blob size does not match the shape")
     return raw.reshape(rows, nb, _BYTES[fmt])
@@ -45,17 +55,17 @@ def _f16_field(raw, lo):
     return raw[:, :, lo:lo + 2].copy().view("<f2")[:, :, 0].astype(np.float64)
 
 
-def dequant_q8_0(blob, rows, cols):
-    raw = _blocks(blob, Q8_0, rows, cols)
+def dequant_q8_0(blob, rows, cols, fmt=Q8_0):
+    raw = _blocks(blob, fmt, rows, cols)
     d = _f16_field(raw, 0)
-    q = raw[:, :, 2:34].copy().view(np.int8).astype(np.float64)
+    q = raw[:, :, 2:].copy().view(np.int8).astype(np.float64)
     return (d[:, :, None] * q).reshape(rows, cols)
 
 
-def dequant_q4_0(blob, rows, cols):
-    raw = _blocks(blob, Q4_0, rows, cols)
+def dequant_q4_0(blob, rows, cols, fmt=Q4_0):
+    raw = _blocks(blob, fmt, rows, cols)
     d = _f16_field(raw, 0)
-    qs = raw[:, :, 2:18]
+    qs = raw[:, :, 2:]
     q = np.concatenate([qs & 0x0F, qs >> 4], axis=-1).astype(np.float64)
     return (d[:, :, None] * (q - 8.0)).reshape(rows, cols)
 
@@ -85,6 +95,10 @@ def dequant(blob, fmt, rows, cols):
         return dequant_q4_0(blob, rows, cols)
     if fmt == I8ASYM:
         return dequant_i8asym(blob, rows, cols)
+    if fmt == Q8_0_G64:
+        return dequant_q8_0(blob, rows, cols, Q8_0_G64)
+    if fmt == Q4_0_G64:
+        return dequant_q4_0(blob, rows, cols, Q4_0_G64)
     raise ValueError(f"unknown format {fmt}")
 
 

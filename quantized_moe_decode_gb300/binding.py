@@ -26,7 +26,7 @@ EXPORTED = ["uocr_create", "uocr_destroy", "uocr_load_weights", "uocr_kv_write_p
             "uocr_set_sinks", "uocr_decode_step", "uocr_decode_step_embeds", "uocr_decode_step_host",
             "uocr_prefill", "uocr_generate", "uocr_kv_reset", "uocr_sync", "uocr_last_error", "uocr_memory_report",
             "uocr_debug_hidden", "uocr_debug_router", "uocr_debug_router_logits", "uocr_profile",
-            "uocr_lm_head_argmax_noalloc", "uocr_debug_wait_probe", "uocr_kv_read_i8", "uocr_kv_write_i8"]
+            "uocr_lm_head_argmax_noalloc", "uocr_debug_wait_probe", "uocr_kv_read_i8", "uocr_kv_write_i8", "uocr_project"]
 
 
 class uocr_config(C.Structure):
@@ -35,7 +35,8 @@ class uocr_config(C.Structure):
         "n_shared", "expert_inter", "vocab", "fmt_attn", "fmt_dense", "fmt_shared", "fmt_routed",
         "prefix_len", "ring_len", "max_rows", "use_sink")] + [
         ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("mem_budget", C.c_uint64),
-        ("stream", C.c_void_p), ("device", C.c_int32), ("use_graphs", C.c_int32), ("kv_int8", C.c_int32)]
+        ("stream", C.c_void_p), ("device", C.c_int32), ("use_graphs", C.c_int32), ("kv_int8", C.c_int32),
+        ("proj_in", C.c_int32), ("fmt_proj", C.c_int32)]
 
 
 class uocr_tensor(C.Structure):
@@ -84,6 +85,7 @@ def load(path: str = LIB_PATH):
         "uocr_debug_wait_probe": ([P, I], I),
         "uocr_kv_read_i8": ([P, I, I, I, I, P, P, P, P], I),
         "uocr_kv_write_i8": ([P, I, I, I, I, P, P, P, P], I),
+        "uocr_project": ([P, I, P, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -115,6 +117,8 @@ def make_config(cfg, *, max_rows=None, mem_budget=0, stream=0, device=0, use_gra
     c.device = int(device)
     c.use_graphs = int(use_graphs)
     c.kv_int8 = int(getattr(cfg, "kv_int8", 0))
+    c.proj_in = int(getattr(cfg, "proj_in", 0))
+    c.fmt_proj = int(getattr(cfg, "fmt_proj", 1))
     return c
 
 
@@ -211,6 +215,10 @@ class Context:
         """Prefill n positions of cache row `row` from device token ids or fp16 hidden vectors."""
         self._ck(self.lib.uocr_prefill(self.h, row, ids_ptr or None, x_ptr or None, n, start_pos, next_ptr or None,
                                        logits_ptr or None))
+
+    def uocr_project(self, n, feats_ptr, out_ptr):
+        """Projector: device fp16 features [n][proj_in] -> device fp16 [n][hidden]."""
+        self._ck(self.lib.uocr_project(self.h, n, feats_ptr, out_ptr))
 
     def uocr_debug_wait_probe(self, issue_copy):
         self._ck(self.lib.uocr_debug_wait_probe(self.h, int(issue_copy)))

@@ -674,16 +674,18 @@ __device__ __forceinline__ Code locate(const PackArgs& a, PackSrcRef r, int k) {
     src = k / a.I;
     kk = k - src * a.I;
   }
-  const int bb = a.fmt == Q8_0 ? 34 : (a.fmt == Q4_0 ? 18 : 36);
-  const uint8_t* blk = a.src[src] + ((size_t)r.row * (a.src_cols / 32) + kk / 32) * bb;
-  return Code{blk, kk & 31};
+  const uint8_t* blk = a.src[src] + ((size_t)r.row * (a.src_cols / a.group) + kk / a.group) * a.bb;
+  return Code{blk, kk % a.group};
 }
 
 __device__ __forceinline__ uint32_t get_code(const PackArgs& a, PackSrcRef r, int k) {
   if (r.src < 0) return a.fmt == Q4_0 ? 8u : 0u;
   const Code c = locate(a, r, k);
   if (a.fmt == Q8_0) return c.blk[2 + c.j];
-  if (a.fmt == Q4_0) return c.j < 16 ? (c.blk[2 + c.j] & 0xF) : (c.blk[2 + c.j - 16] >> 4);
+  if (a.fmt == Q4_0) {  // element j < group/2: low nibble of byte j, else high nibble of byte j - group/2
+    const int half = a.group / 2;
+    return c.j < half ? (c.blk[2 + c.j] & 0xF) : (c.blk[2 + c.j - half] >> 4);
+  }
   return c.blk[4 + c.j];  // I8ASYM
 }
 

@@ -29,7 +29,7 @@ namespace {
 struct DMat {
   uint8_t* q = nullptr;
   uint8_t* s = nullptr;
-  int fmt = 0, n_slabs = 0, U = 0, K = 0;
+  int fmt = 0, cfmt = 0, n_slabs = 0, U = 0, K = 0;  // packed and canonical format
   size_t qbytes = 0, sbytes = 0;  // of one matrix (one expert for expert arrays)
   PMat view(int n_experts_stride = 0) const {
     PMat p;
@@ -52,10 +52,25 @@ size_t packed_s_bytes(int n_rows_packed, int K, int fmt) {
   const size_t slabs = (size_t)(n_rows_packed + 15) / 16;
   return slabs * (K / unit_k(fmt)) * unit_scale_bytes(fmt);
 }
+// Canonical block formats: values per block and bytes per block.  The group-64
+// variants pack into the layout of their 32-value format (a Q8_0 unit of 32
+// inputs is half a block and takes the block's scale; a Q4_0 unit of 64
+// inputs is one block), so every kernel runs on the packed format kf(fmt).
+int fmt_group(int fmt) { return fmt == UOCR_Q8_0_G64 || fmt == UOCR_Q4_0_G64 ? 64 : 32; }
+int fmt_block_bytes(int fmt) {
+  switch (fmt) {
+    case UOCR_Q8_0: return 34;
+    case UOCR_Q4_0: return 18;
+    case UOCR_I8ASYM: return 36;
+    case UOCR_Q8_0_G64: return 66;
+    case UOCR_Q4_0_G64: return 34;
+  }
+  return 0;
+}
+int kf(int fmt) { return fmt == UOCR_Q8_0_G64 ? Q8_0 : fmt == UOCR_Q4_0_G64 ? Q4_0 : fmt; }
 size_t blob_bytes(int fmt, int rows, int cols) {
   if (fmt == F16) return (size_t)rows * cols * 2;
-  const int bb = fmt == Q8_0 ? 34 : (fmt == Q4_0 ? 18 : 36);
-  return (size_t)rows * (cols / 32) * bb;
+  return (size_t)rows * (cols / fmt_group(fmt)) * fmt_block_bytes(fmt);
 }
 
 struct LayerW {
@@ -111,6 +126,8 @@ struct uocr_ctx {
   __half* emb = nullptr;
   __half* final_norm = nullptr;
   DMat lm;
+  DMat proj;                 // projector [H][proj_in]
+  __half* proj_b = nullptr;  // its bias [H]
   double* inv_freq = nullptr;
   float2* rope = nullptr;  // [max_rows][head_dim/2] (cos, sin) of the step's positions
   __half* kv = nullptr;        // fp16 cache [L][MR][2][nh][SL][D]
@@ -161,7 +178,7 @@ struct uocr_ctx {
       if (!layer_dense(l)) return true;
     return false;
   }
-  int shared_fmt() const { return cfg.n_shared > 0 ? cfg.fmt_shared : cfg.fmt_routed; }
+  int shared_fmt() const { return kf(cfg.n_shared > 0 ? cfg.fmt_shared : cfg.fmt_routed); }
 
   uocr_status fail(uocr_status s, const char* fmt, ...) {
     char buf[1024];
@@ -185,9 +202,11 @@ struct uocr_ctx {
   } while (0)
 
 // ------------------------------------------------------------------ config
-static bool fmt_ok(int f) { return f >= UOCR_F16 && f <= UOCR_I8ASYM; }
-static bool quant_fmt(int f) { return f == UOCR_Q8_0 || f == UOCR_Q4_0 || f == UOCR_I8ASYM; }
+static bool fmt_ok(int f) { return f >= UOCR_F16 && f <= UOCR_Q4_0_G64; }
+static bool quant_fmt(int f) { return f != UOCR_F16 && fmt_ok(f); }
 static bool expert_pair_ok(int fr, int fs) {
+  fr = kf(fr);
+  fs = kf(fs);
   return (fr == Q8_0 && fs == Q8_0) || (fr == Q4_0 && fs == Q8_0) || (fr == Q4_0 && fs == Q4_0) ||
          (fr == Q8_0 && fs == Q4_0) || (fr == I8ASYM && fs == I8ASYM);
 }
@@ -217,10 +236,10 @@ static uocr_status check_config(uocr_ctx* ctx, const uocr_config& c) {
     const int fs = c.n_shared > 0 ? c.fmt_shared : c.fmt_routed;
     if (!quant_fmt(c.fmt_routed) || !expert_pair_ok(c.fmt_routed, fs))
       return bad("unsupported (routed, shared) expert format pair");
-    if (plan_stream(2, c.fmt_routed, c.hidden, 16).bytes > kSmemLimit)
+    if (plan_stream(2, kf(c.fmt_routed), c.hidden, 16).bytes > kSmemLimit)
       return bad("hidden too large for the expert kernels");
     const int kmax = c.n_shared * c.expert_inter > c.expert_inter ? c.n_shared * c.expert_inter : c.expert_inter;
-    if (plan_stream(2, c.fmt_routed, 0, 0, 2 * (kmax / 32) * 512).bytes > kSmemLimit)
+    if (plan_stream(2, kf(c.fmt_routed), 0, 0, 2 * (kmax / 32) * 512).bytes > kSmemLimit)
       return bad("expert_inter * n_shared too large for the expert kernels");
   }
   if (c.vocab < 0) return bad("vocab must be >= 0");
@@ -236,6 +255,11 @@ static uocr_status check_config(uocr_ctx* ctx, const uocr_config& c) {
   if (c.use_sink != 0 && c.use_sink != 1) return bad("use_sink must be 0 or 1");
   if (!(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f)) return bad("rms_eps >= 0 and rope_theta > 0 required");
   if (c.kv_int8 != 0 && c.kv_int8 != 1) return bad("kv_int8 must be 0 or 1");
+  if (c.proj_in < 0 || c.proj_in % 64) return bad("proj_in must be 0 or a positive multiple of 64");
+  if (c.proj_in > 0) {
+    if (!quant_fmt(c.fmt_proj)) return bad("fmt_proj must be a quantised format");
+    if (plan_stream(2, kf(c.fmt_proj), c.proj_in).bytes > kSmemLimit) return bad("proj_in too large");
+  }
   return UOCR_OK;
 }
 
@@ -247,7 +271,9 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
   const int H = c.hidden, S = c.n_heads * c.head_dim, MR = c.max_rows, Lc = c.n_layers, V = c.vocab;
   const int E = c.n_experts, k = c.top_k, Ie = c.expert_inter, Ish = c.n_shared * c.expert_inter;
   const int TC = kTokCap;  // tokens of one pass (decode rows or a prefill chunk)
-  auto mat = [&](DMat& m, int rows_packed, int K, int fmt, int count = 1) {
+  auto mat = [&](DMat& m, int rows_packed, int K, int cfmt, int count = 1) {
+    const int fmt = kf(cfmt);
+    m.cfmt = cfmt;
     m.fmt = fmt;
     m.K = K;
     m.U = K / unit_k(fmt);
@@ -282,6 +308,10 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
     ctx->emb = cv.take<__half>((size_t)V * H, r.weights);
     ctx->final_norm = cv.take<__half>(H, r.weights);
     mat(ctx->lm, V, H, F16);
+  }
+  if (c.proj_in > 0) {
+    mat(ctx->proj, H, c.proj_in, c.fmt_proj);
+    ctx->proj_b = cv.take<__half>(H, r.weights);
   }
   ctx->inv_freq = cv.take<double>(c.head_dim / 2, r.weights);
   ctx->rope = cv.take<float2>((size_t)TC * (c.head_dim / 2), r.activations);
@@ -415,7 +445,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     // QKV + RoPE + in-place KV append
     GemvArgs qa{};
     qa.w = w.qkv.view();
-    qa.sp = plan_stream(nt, c.fmt_attn, H, nt * 8, nt * 8 * (c.head_dim / 2) * 8);
+    qa.sp = plan_stream(nt, kf(c.fmt_attn), H, nt * 8, nt * 8 * (c.head_dim / 2) * 8);
     qa.ntok = rows;
     qa.xf = hid(2 * l);
     qa.ld_src = H;
@@ -436,7 +466,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     qa.kv_new = kv8l ? ctx->kv_new : nullptr;
     qa.status = ctx->status;
     if (want("qkv")) {
-      CK(launch_gemv(c.fmt_attn, SRC_NORM, EPI_QKV, qa, gx_for(w.qkv.n_slabs), tg, st, pdl), "qkv launch");
+      CK(launch_gemv(kf(c.fmt_attn), SRC_NORM, EPI_QKV, qa, gx_for(w.qkv.n_slabs), tg, st, pdl), "qkv launch");
     }
     if (kv8l) {  // INT8 cache: quantise the new keys / values into their slots
       KvQuantArgs ka{};
@@ -492,7 +522,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     // O projection + residual
     GemvArgs oa{};
     oa.w = w.o.view();
-    oa.sp = plan_stream(nt, c.fmt_attn, S);
+    oa.sp = plan_stream(nt, kf(c.fmt_attn), S);
     oa.ntok = rows;
     oa.xh = ctx->attn_out;
     oa.ld_src = S;
@@ -501,12 +531,12 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     oa.ld_out = H;
     oa.status = ctx->status;
     if (want("o_proj")) {
-      CK(launch_gemv(c.fmt_attn, SRC_F16, EPI_RESID, oa, gx_for(w.o.n_slabs), tg, st, pdl), "o_proj launch");
+      CK(launch_gemv(kf(c.fmt_attn), SRC_F16, EPI_RESID, oa, gx_for(w.o.n_slabs), tg, st, pdl), "o_proj launch");
     }
     if (w.dense) {
       GemvArgs ga{};
       ga.w = w.gateup.view();
-      ga.sp = plan_stream(nt, c.fmt_dense, H);
+      ga.sp = plan_stream(nt, kf(c.fmt_dense), H);
       ga.ntok = rows;
       ga.xf = hid(2 * l + 1);
       ga.ld_src = H;
@@ -516,12 +546,12 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       ga.ld_out = c.dense_inter;
       ga.status = ctx->status;
       if (want("mlp_gate_up")) {
-        CK(launch_gemv(c.fmt_dense, SRC_NORM, EPI_SWIGLU, ga, gx_for(w.gateup.n_slabs), tg, st, pdl),
+        CK(launch_gemv(kf(c.fmt_dense), SRC_NORM, EPI_SWIGLU, ga, gx_for(w.gateup.n_slabs), tg, st, pdl),
            "gate/up launch");
       }
       GemvArgs da{};
       da.w = w.down.view();
-      da.sp = plan_stream(nt, c.fmt_dense, c.dense_inter);
+      da.sp = plan_stream(nt, kf(c.fmt_dense), c.dense_inter);
       da.ntok = rows;
       da.xh = ctx->act_dense;
       da.ld_src = c.dense_inter;
@@ -530,7 +560,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       da.ld_out = H;
       da.status = ctx->status;
       if (want("mlp_down")) {
-        CK(launch_gemv(c.fmt_dense, SRC_F16, EPI_RESID, da, gx_for(w.down.n_slabs), tg, st, pdl), "down launch");
+        CK(launch_gemv(kf(c.fmt_dense), SRC_F16, EPI_RESID, da, gx_for(w.down.n_slabs), tg, st, pdl), "down launch");
       }
     } else {
       const int E = c.n_experts, k = c.top_k;
@@ -632,21 +662,21 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       // gate/up + SwiGLU (and the routing of every row)
       xa.wr = w.ex_gateup.view(1);
       xa.ws = shg ? shg->view() : PMat{};
-      xa.sp = plan_stream(nt, c.fmt_routed, H, 16);
+      xa.sp = plan_stream(nt, kf(c.fmt_routed), H, 16);
       split(w.ex_gateup, shg, w.ex_gateup.n_slabs, shg ? shg->n_slabs : 0);
       if (want("expert_gate_up")) {
-        CK(launch_expert_gateup(c.fmt_routed, fs, xa, st, pdl), "expert gate/up launch");
+        CK(launch_expert_gateup(kf(c.fmt_routed), fs, xa, st, pdl), "expert gate/up launch");
       }
       // down + combine
       xa.wr = w.ex_down.view(1);
       xa.ws = shd ? shd->view() : PMat{};
       {
         const int kmax = xa.Ish > xa.Ie ? xa.Ish : xa.Ie;
-        xa.sp = plan_stream(nt, c.fmt_routed, 0, 0, nt * (kmax / 32) * 512);
+        xa.sp = plan_stream(nt, kf(c.fmt_routed), 0, 0, nt * (kmax / 32) * 512);
       }
       split(w.ex_down, shd, H / 16, H / 16);
       if (want("expert_down")) {
-        CK(launch_expert_down(c.fmt_routed, fs, xa, st, pdl), "expert down launch");
+        CK(launch_expert_down(kf(c.fmt_routed), fs, xa, st, pdl), "expert down launch");
       }
       if (want("expert_combine")) {
         CK(launch_expert_combine(xa, st, pdl), "expert combine launch");
@@ -728,9 +758,11 @@ struct Expect {
 static bool expect_for(uocr_ctx* ctx, const uocr_tensor& t, Expect& ex, std::string& why) {
   const uocr_config& c = ctx->cfg;
   const int H = c.hidden, S = ctx->S, V = c.vocab, E = c.n_experts;
-  const bool glob = t.kind == UOCR_T_EMBED || t.kind == UOCR_T_FINAL_NORM || t.kind == UOCR_T_LM_HEAD;
+  const bool proj = t.kind == UOCR_T_PROJ || t.kind == UOCR_T_PROJ_BIAS;
+  const bool glob = t.kind == UOCR_T_EMBED || t.kind == UOCR_T_FINAL_NORM || t.kind == UOCR_T_LM_HEAD || proj;
   if (glob) {
-    if (V <= 0) return why = "the config has no vocabulary", false;
+    if (proj && c.proj_in <= 0) return why = "the config has no projector (proj_in = 0)", false;
+    if (!proj && V <= 0) return why = "the config has no vocabulary", false;
     if (t.layer != 0 || t.expert != 0) return why = "global tensors use layer 0, expert 0", false;
   } else if (t.layer < 0 || t.layer >= c.n_layers) {
     return why = "layer out of range", false;
@@ -744,6 +776,8 @@ static bool expect_for(uocr_ctx* ctx, const uocr_tensor& t, Expect& ex, std::str
     case UOCR_T_EMBED: ex = {UOCR_F16, V, H, G_SINGLE, 1, 0}; return true;
     case UOCR_T_FINAL_NORM: ex = {UOCR_F16, 1, H, G_SINGLE, 1, 0}; return true;
     case UOCR_T_LM_HEAD: ex = {UOCR_F16, V, H, G_SINGLE, 1, 0}; return true;
+    case UOCR_T_PROJ: ex = {c.fmt_proj, H, c.proj_in, G_SINGLE, 1, 0}; return true;
+    case UOCR_T_PROJ_BIAS: ex = {UOCR_F16, 1, H, G_SINGLE, 1, 0}; return true;
     case UOCR_T_ATTN_NORM:
     case UOCR_T_MLP_NORM: ex = {UOCR_F16, 1, H, G_SINGLE, 1, 0}; return need_expert0();
     case UOCR_T_WQ:
@@ -797,6 +831,8 @@ static uocr_status pack_into(uocr_ctx* ctx, const DMat& dst, size_t expert_off_q
   pa.q = dst.q + expert_off_q;
   pa.s = dst.s ? dst.s + expert_off_s : nullptr;
   pa.fmt = dst.fmt;
+  pa.group = fmt_group(dst.cfmt);
+  pa.bb = fmt_block_bytes(dst.cfmt);
   pa.n_slabs = dst.n_slabs;
   pa.U = dst.U * (unit_bytes(dst.fmt) / 512);  // the packer counts 512-byte (sub-)units
   pa.K = dst.K;
@@ -816,7 +852,9 @@ static uocr_status pack_into(uocr_ctx* ctx, const DMat& dst, size_t expert_off_q
 static uocr_status finish_group(uocr_ctx* ctx, int kind, int layer, int expert, Group grp, std::vector<void*>& srcs) {
   const uocr_config& c = ctx->cfg;
   const int H = c.hidden;
-  LayerW* w = (kind == UOCR_T_EMBED || kind == UOCR_T_FINAL_NORM || kind == UOCR_T_LM_HEAD) ? nullptr : &ctx->L[layer];
+  LayerW* w = (kind == UOCR_T_EMBED || kind == UOCR_T_FINAL_NORM || kind == UOCR_T_LM_HEAD || kind == UOCR_T_PROJ)
+                  ? nullptr
+                  : &ctx->L[layer];
   switch (grp) {
     case G_QKV: return pack_into(ctx, w->qkv, 0, 0, MAP_QKV, srcs, ctx->S, H, 0);
     case G_DENSE_GU: return pack_into(ctx, w->gateup, 0, 0, MAP_SWIGLU, srcs, c.dense_inter, H, c.dense_inter);
@@ -835,6 +873,7 @@ static uocr_status finish_group(uocr_ctx* ctx, int kind, int layer, int expert, 
       return pack_into(ctx, w->ex_down, w->ex_down.qbytes * expert, w->ex_down.sbytes * expert, MAP_IDENT, srcs, H,
                        c.expert_inter, 0);
     case UOCR_T_LM_HEAD: return pack_into(ctx, ctx->lm, 0, 0, MAP_IDENT, srcs, c.vocab, H, 0);
+    case UOCR_T_PROJ: return pack_into(ctx, ctx->proj, 0, 0, MAP_IDENT, srcs, H, c.proj_in, 0);
   }
   return ctx->fail(UOCR_E_FORMAT, "internal: no packer for kind %d", kind);
 }
@@ -857,9 +896,10 @@ static uocr_status load_one(uocr_ctx* ctx, const uocr_tensor& t) {
   // plain copies
   const uocr_config& c = ctx->cfg;
   if (t.kind == UOCR_T_EMBED || t.kind == UOCR_T_FINAL_NORM || t.kind == UOCR_T_ATTN_NORM ||
-      t.kind == UOCR_T_MLP_NORM) {
+      t.kind == UOCR_T_MLP_NORM || t.kind == UOCR_T_PROJ_BIAS) {
     void* dst = t.kind == UOCR_T_EMBED        ? (void*)ctx->emb
                 : t.kind == UOCR_T_FINAL_NORM ? (void*)ctx->final_norm
+                : t.kind == UOCR_T_PROJ_BIAS  ? (void*)ctx->proj_b
                 : t.kind == UOCR_T_ATTN_NORM  ? (void*)ctx->L[t.layer].attn_norm
                                               : (void*)ctx->L[t.layer].mlp_norm;
     CK(cudaMemcpy(dst, t.data, t.bytes, cudaMemcpyHostToDevice), "weight copy");
@@ -1366,6 +1406,33 @@ uocr_status uocr_prefill(uocr_ctx* ctx, int32_t row, const int32_t* token_ids, c
   if (next_id) CK(cudaMemcpyAsync(next_id, ctx->next_ids, 4, cudaMemcpyDeviceToDevice, ctx->st), "id copy");
   if (logits)
     CK(cudaMemcpyAsync(logits, ctx->logits, (size_t)c.vocab * 4, cudaMemcpyDeviceToDevice, ctx->st), "logits copy");
+  return step_epilogue(ctx);
+}
+
+uocr_status uocr_project(uocr_ctx* ctx, int32_t n, const uint16_t* feats, uint16_t* out) {
+  if (!ctx) return UOCR_E_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  const uocr_config& c = ctx->cfg;
+  if (c.proj_in <= 0) return ctx->fail(UOCR_E_STATE, "project: the config has no projector (proj_in = 0)");
+  if (!ctx->loaded.count({UOCR_T_PROJ, 0, 0}) || !ctx->loaded.count({UOCR_T_PROJ_BIAS, 0, 0}))
+    return ctx->fail(UOCR_E_STATE, "project: the projector weight and bias have not been loaded");
+  if (!feats || !out || n < 1) return ctx->fail(UOCR_E_INVALID_ARG, "project: NULL pointer or n < 1");
+  CK(cudaEventRecord(ctx->ev_in, ctx->ust), "event record");
+  CK(cudaStreamWaitEvent(ctx->st, ctx->ev_in, 0), "stream wait");
+  const int tg = (n + 15) / 16;  // token groups of 16 features (two n-tiles each)
+  int gx = ctx->gemv_ctas_per_sm * ctx->n_sm / tg;
+  gx = gx < 1 ? 1 : gx > ctx->proj.n_slabs ? ctx->proj.n_slabs : gx;
+  GemvArgs pa{};
+  pa.w = ctx->proj.view();
+  pa.sp = plan_stream(2, ctx->proj.fmt, c.proj_in);
+  pa.ntok = n;
+  pa.xh = reinterpret_cast<const __half*>(feats);
+  pa.ld_src = c.proj_in;
+  pa.out_h = reinterpret_cast<__half*>(out);
+  pa.ld_out = c.hidden;
+  pa.bias = ctx->proj_b;
+  pa.status = ctx->status;
+  CK(launch_gemv(ctx->proj.fmt, SRC_F16, EPI_BIAS_F16, pa, gx, tg, ctx->st, false), "projector launch");
   return step_epilogue(ctx);
 }
 

@@ -104,6 +104,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
         a.out_f[(size_t)gt * a.ld_out + col + 8] = a.res_in[(size_t)gt * a.ld_out + col + 8] + hi;
       } else if constexpr (EPI == EPI_SWIGLU) {
         a.out_h[(size_t)gt * a.ld_out + 8 * s + pg] = __float2half_rn(silu(lo) * hi);
+      } else if constexpr (EPI == EPI_BIAS_F16) {
+        const int col = 16 * s + pg;
+        const float b0 = a.bias ? __half2float(a.bias[col]) : 0.f, b1 = a.bias ? __half2float(a.bias[col + 8]) : 0.f;
+        a.out_h[(size_t)gt * a.ld_out + col] = __float2half_rn(lo + b0);
+        a.out_h[(size_t)gt * a.ld_out + col + 8] = __float2half_rn(hi + b1);
       } else if constexpr (EPI == EPI_LOGITS) {
         const int r0 = 16 * s + pg, r1 = r0 + 8;
         unsigned long long best = 0ull;
@@ -194,6 +199,9 @@ static cudaError_t dispatch_epi(int src, int epi, const GemvArgs& a, int gx, int
   if (src == SRC_NORM && epi == EPI_QKV) return launch_one<FMT, NT, SRC_NORM, EPI_QKV>(a, gx, gy, st, pdl);
   if (src == SRC_F16 && epi == EPI_RESID) return launch_one<FMT, NT, SRC_F16, EPI_RESID>(a, gx, gy, st, pdl);
   if (src == SRC_NORM && epi == EPI_SWIGLU) return launch_one<FMT, NT, SRC_NORM, EPI_SWIGLU>(a, gx, gy, st, pdl);
+  if constexpr (NT == 2 && FMT != F16) {
+    if (src == SRC_F16 && epi == EPI_BIAS_F16) return launch_one<FMT, NT, SRC_F16, EPI_BIAS_F16>(a, gx, gy, st, pdl);
+  }
   if constexpr (FMT == F16) {
     if (src == SRC_NORM && epi == EPI_LOGITS) return launch_one<FMT, NT, SRC_NORM, EPI_LOGITS>(a, gx, gy, st, pdl);
   }
@@ -226,6 +234,9 @@ static cudaError_t set_attr_fmt() {
   UOCR_SET(SRC_NORM, EPI_QKV)
   UOCR_SET(SRC_F16, EPI_RESID)
   UOCR_SET(SRC_NORM, EPI_SWIGLU)
+  if constexpr (NT == 2 && FMT != F16) {
+    UOCR_SET(SRC_F16, EPI_BIAS_F16)
+  }
   if constexpr (FMT == F16) {
     UOCR_SET(SRC_NORM, EPI_LOGITS)
   }

@@ -26,7 +26,7 @@ struct StreamPlan {
 StreamPlan plan_stream(int nt, int fmt, int k_stage, int n_rows_list = 0, int extra_bytes = 0);
 
 enum Src : int { SRC_NORM = 0, SRC_F16 = 1 };
-enum Epi : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
+enum Epi : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3, EPI_BIAS_F16 = 4 };
 
 struct GemvArgs {
   PMat w;
@@ -41,7 +41,8 @@ struct GemvArgs {
   // outputs
   const float* res_in;      // EPI_RESID: out = res_in + W x
   float* out_f;             // EPI_RESID output / EPI_LOGITS logits (nullable)
-  __half* out_h;            // EPI_SWIGLU output
+  __half* out_h;            // EPI_SWIGLU output; EPI_BIAS_F16: out = fp16(W x + bias)
+  const __half* bias;       // EPI_BIAS_F16 [rows of W] or nullptr
   int ld_out;
   // EPI_QKV
   const int* pos;
@@ -161,7 +162,8 @@ struct EmbedArgs {
 struct PackArgs {
   uint8_t* q;
   uint8_t* s;
-  int fmt, n_slabs, U, K;
+  int fmt, n_slabs, U, K;   // packed format
+  int group, bb;            // canonical blocks: values and bytes per block
   int map;                  // PackMap
   const uint8_t* src[8];    // canonical blobs on the device
   int src_rows, src_cols;   // shape of each source

@@ -32,9 +32,13 @@ import numpy as np
 
 # Weight formats (values match uocr_format in include/uocr.h).
 F16, Q8_0, Q4_0, I8ASYM = 0, 1, 2, 3
-FMT_NAMES = {F16: "f16", Q8_0: "q8_0", Q4_0: "q4_0", I8ASYM: "i8asym"}
+# group-64 variants of Q8_0 / Q4_0 (the Metal page's group size)
+Q8_0_G64, Q4_0_G64 = 4, 5
+FMT_NAMES = {F16: "f16", Q8_0: "q8_0", Q4_0: "q4_0", I8ASYM: "i8asym", Q8_0_G64: "q8_0_g64",
+             Q4_0_G64: "q4_0_g64"}
 BLOCK = 32
-BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, I8ASYM: 36}
+GROUP = {Q8_0: 32, Q4_0: 32, I8ASYM: 32, Q8_0_G64: 64, Q4_0_G64: 64}
+BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, I8ASYM: 36, Q8_0_G64: 66, Q4_0_G64: 34}
 
 # Tensor kinds (values match uocr_tensor_kind in include/uocr.h).
 T_EMBED, T_FINAL_NORM, T_LM_HEAD = 0, 1, 2
@@ -43,6 +47,7 @@ T_GATE, T_UP, T_DOWN = 9, 10, 11
 T_ROUTER = 12
 T_SHARED_GATE, T_SHARED_UP, T_SHARED_DOWN = 13, 14, 15
 T_EXPERT_GATE, T_EXPERT_UP, T_EXPERT_DOWN = 16, 17, 18
+T_PROJ, T_PROJ_BIAS = 19, 20
 
 
 @dataclass
@@ -70,6 +75,8 @@ class ModelConfig:
     rope_theta: float = 10000.0
     router_std: float = 0.02
     kv_int8: int = 0  # INT8 KV cache (one scale per head vector) instead of fp16
+    proj_in: int = 0  # projector input width (visual features; 0 = no projector)
+    fmt_proj: int = Q8_0
 
     @property
     def moe(self) -> bool:
@@ -128,33 +135,34 @@ def _fp16_bytes(a: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(a.astype(np.float16)).view(np.uint8)
 
 
-def encode_q8_0(x: np.ndarray) -> np.ndarray:
+def encode_q8_0(x: np.ndarray, group: int = BLOCK) -> np.ndarray:
     n, k = x.shape
-    xb = x.reshape(n, k // BLOCK, BLOCK).astype(np.float32)
+    xb = x.reshape(n, k // group, group).astype(np.float32)
     amax = np.abs(xb).max(axis=-1)
     d = (amax / 127.0).astype(np.float16)
     df = d.astype(np.float32)
     inv = np.divide(1.0, df, out=np.zeros_like(df), where=df != 0)
     q = np.clip(np.rint(xb * inv[..., None]), -127, 127).astype(np.int8)
-    out = np.empty((n, k // BLOCK, 34), np.uint8)
-    out[..., 0:2] = d.view(np.uint8).reshape(n, k // BLOCK, 2)
+    out = np.empty((n, k // group, 2 + group), np.uint8)
+    out[..., 0:2] = d.view(np.uint8).reshape(n, k // group, 2)
     out[..., 2:] = q.view(np.uint8)
     return out.reshape(-1)
 
 
-def encode_q4_0(x: np.ndarray) -> np.ndarray:
+def encode_q4_0(x: np.ndarray, group: int = BLOCK) -> np.ndarray:
     n, k = x.shape
-    xb = x.reshape(n, k // BLOCK, BLOCK).astype(np.float32)
+    xb = x.reshape(n, k // group, group).astype(np.float32)
     am = np.abs(xb).argmax(axis=-1)
     m = np.take_along_axis(xb, am[..., None], axis=-1)[..., 0]
     d = (m / -8.0).astype(np.float16)
     df = d.astype(np.float32)
     inv = np.divide(1.0, df, out=np.zeros_like(df), where=df != 0)
     q = np.clip(np.rint(xb * inv[..., None]) + 8, 0, 15).astype(np.uint8)
-    out = np.empty((n, k // BLOCK, 18), np.uint8)
-    out[..., 0:2] = d.view(np.uint8).reshape(n, k // BLOCK, 2)
-    # element j < 16 -> low nibble of byte j; element j >= 16 -> high nibble of byte j-16
-    out[..., 2:] = q[..., :16] | (q[..., 16:] << 4)
+    half = group // 2
+    out = np.empty((n, k // group, 2 + half), np.uint8)
+    out[..., 0:2] = d.view(np.uint8).reshape(n, k // group, 2)
+    # element j < half -> low nibble of byte j; element j >= half -> high nibble of byte j-half
+    out[..., 2:] = q[..., :half] | (q[..., half:] << 4)
     return out.reshape(-1)
 
 
@@ -184,13 +192,17 @@ def encode(x: np.ndarray, fmt: int) -> np.ndarray:
         return encode_q4_0(x)
     if fmt == I8ASYM:
         return encode_i8asym(x)
+    if fmt == Q8_0_G64:
+        return encode_q8_0(x, 64)
+    if fmt == Q4_0_G64:
+        return encode_q4_0(x, 64)
     raise ValueError(f"unknown format {fmt}")
 
 
 def blob_bytes(fmt: int, rows: int, cols: int) -> int:
     if fmt == F16:
         return rows * cols * 2
-    return rows * (cols // BLOCK) * BLOCK_BYTES[fmt]
+    return rows * (cols // GROUP[fmt]) * BLOCK_BYTES[fmt]
 
 
 # ---------------------------------------------------------------- weights
@@ -234,6 +246,9 @@ def make_weights(cfg: ModelConfig, rng: np.random.Generator) -> list:
     if cfg.vocab:
         ts.append(_norm(rng, T_FINAL_NORM, 0, H))
         ts.append(_linear(rng, T_LM_HEAD, 0, 0, F16, cfg.vocab, H))
+    if cfg.proj_in:  # drawn last: configs without a projector keep their streams
+        ts.append(_linear(rng, T_PROJ, 0, 0, cfg.fmt_proj, H, cfg.proj_in))
+        ts.append(_linear(rng, T_PROJ_BIAS, 0, 0, F16, 1, H))
     return ts
 
 

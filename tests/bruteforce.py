@@ -26,22 +26,24 @@ def decode_rows(t):
     if fmt == 0:
         vals = struct.unpack("<%de" % (rows * cols), b)
         return [list(vals[r * cols:(r + 1) * cols]) for r in range(rows)]
-    size = {1: 34, 2: 18, 3: 36}[fmt]
+    size = {1: 34, 2: 18, 3: 36, 4: 66, 5: 34}[fmt]
+    group = {1: 32, 2: 32, 3: 32, 4: 64, 5: 64}[fmt]
     pos = 0
     for _ in range(rows):
         row = []
-        for _ in range(cols // 32):
+        for _ in range(cols // group):
             blk = b[pos:pos + size]
             pos += size
-            if fmt == 1:
+            if fmt in (1, 4):
                 d = _half(blk[0], blk[1])
-                for j in range(32):
+                for j in range(group):
                     q = blk[2 + j]
                     q = q - 256 if q >= 128 else q
                     row.append(d * q)
-            elif fmt == 2:
+            elif fmt in (2, 5):
                 d = _half(blk[0], blk[1])
-                codes = [blk[2 + j] % 16 for j in range(16)] + [blk[2 + j] // 16 for j in range(16)]
+                half = group // 2
+                codes = [blk[2 + j] % 16 for j in range(half)] + [blk[2 + j] // 16 for j in range(half)]
                 for q in codes:
                     row.append(d * (q - 8))
             else:

@@ -19,7 +19,7 @@ from quantized_moe_decode_gb300 import synth
 from bruteforce import BruteModel, decode_rows, rot
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-FMT = {"q8_0": 1, "q4_0": 2, "i8asym": 3}
+FMT = {"q8_0": 1, "q4_0": 2, "i8asym": 3, "q8_0_g64": 4, "q4_0_g64": 5}
 
 
 # ------------------------------------------------------------------ dequantisation
@@ -35,30 +35,30 @@ def _golden_blocks():
     return out
 
 
-@pytest.mark.parametrize("case", range(8))
+@pytest.mark.parametrize("case", range(11))
 def test_hand_built_blocks_dequantise_exactly(case):
     name, raw, expected = _golden_blocks()[case]
-    got = dequant(np.frombuffer(raw, np.uint8), FMT[name], 1, 32)[0]
+    got = dequant(np.frombuffer(raw, np.uint8), FMT[name], 1, len(expected))[0]
     assert got.tolist() == expected
 
 
-@pytest.mark.parametrize("fmt", [synth.F16, synth.Q8_0, synth.Q4_0, synth.I8ASYM])
+@pytest.mark.parametrize("fmt", [synth.F16, synth.Q8_0, synth.Q4_0, synth.I8ASYM, synth.Q8_0_G64, synth.Q4_0_G64])
 def test_dequant_matches_scalar_parser(fmt):
     rng = np.random.default_rng(7)
-    x = rng.standard_normal((5, 96), dtype=np.float32) * 0.02
-    t = synth.Tensor(0, 0, 0, fmt, 5, 96, synth.encode(x, fmt))
-    got = dequant(t.blob, fmt, 5, 96)
+    x = rng.standard_normal((5, 128), dtype=np.float32) * 0.02
+    t = synth.Tensor(0, 0, 0, fmt, 5, 128, synth.encode(x, fmt))
+    got = dequant(t.blob, fmt, 5, 128)
     ref = np.array(decode_rows(t))
     assert np.array_equal(got, ref)
     # and the encoding is a faithful quantisation of the draw (catches a wrong scale / sign)
-    assert np.max(np.abs(got - x)) < (0.02 * 4 / 7 if fmt == synth.Q4_0 else 0.02 * 4 / 100)
+    assert np.max(np.abs(got - x)) < (0.02 * 4 / 7 if fmt in (synth.Q4_0, synth.Q4_0_G64) else 0.02 * 4 / 100)
 
 
 def test_q8_q4_values_are_exact_in_float32():
     rng = np.random.default_rng(8)
-    for fmt in (synth.Q8_0, synth.Q4_0, synth.I8ASYM):
-        x = rng.standard_normal((7, 64), dtype=np.float32)
-        w = dequant(synth.encode(x, fmt), fmt, 7, 64)
+    for fmt in (synth.Q8_0, synth.Q4_0, synth.I8ASYM, synth.Q8_0_G64, synth.Q4_0_G64):
+        x = rng.standard_normal((7, 128), dtype=np.float32)
+        w = dequant(synth.encode(x, fmt), fmt, 7, 128)
         assert float32_is_exact(w)
 
 
@@ -383,3 +383,44 @@ def test_int8_kv_model_caches_the_quantised_prefix_and_stays_close_to_fp16():
             assert np.array_equal(oracle.kv_dequant(c, sc), r8.k_new[l])
         d = np.linalg.norm(r8.hidden[-1] - r16.hidden[-1]) / np.linalg.norm(r16.hidden[-1])
         assert 0 < d < 2e-2, d  # int8 noise, not a different model
+
+
+# ---------------------------------------------------------------- projector
+def _q8_block_row(d_bits, codes):
+    """One Q8_0 row from hand-built blocks: fp16 scale bits + 32 int8 codes per block."""
+    out = bytearray()
+    for i in range(0, len(codes), 32):
+        out += int(d_bits).to_bytes(2, "little") + bytes((c + 256) % 256 for c in codes[i:i + 32])
+    return out
+
+
+def test_projector_one_hot_feature_selects_a_column_plus_bias():
+    # W [4][64] from Q8_0 blocks with d = 2^-7 (fp16 0x2000) and codes W[r][k] = (r * 7 + k) % 21 - 10;
+    # every value is k/128 exactly, so a one-hot feature gives column j plus the bias exactly in fp16
+    rows, cols = 4, 64
+    codes = [[(r * 7 + k) % 21 - 10 for k in range(cols)] for r in range(rows)]
+    blob = np.frombuffer(b"".join(bytes(_q8_block_row(0x2000, codes[r])) for r in range(rows)), np.uint8)
+    W = dequant(blob, synth.Q8_0, rows, cols)
+    assert W[1, 3] == ((1 * 7 + 3) % 21 - 10) / 128.0
+    b = np.array([0.5, -0.25, 0.0, 1.0])
+    for j in (0, 13, 63):
+        x = np.zeros((1, cols))
+        x[0, j] = 2.0
+        y = oracle.project(x, W, b)
+        assert y[0].tolist() == [2.0 * codes[r][j] / 128.0 + b[r] for r in range(rows)]
+    # without a bias the map is linear: opposite features give opposite outputs exactly
+    x = np.zeros((2, cols))
+    x[0, 5], x[1, 5] = 1.0, -1.0
+    y = oracle.project(x, W)
+    assert np.array_equal(y[0], -y[1])
+
+
+def test_projector_output_is_fp16_of_the_exact_product():
+    rng = np.random.default_rng(12)
+    W = dequant(synth.encode(rng.standard_normal((8, 128), dtype=np.float32) * 0.02, synth.Q4_0_G64),
+                synth.Q4_0_G64, 8, 128)
+    x = rng.standard_normal((3, 128)).astype(np.float16).astype(np.float64)
+    b = rng.standard_normal(8).astype(np.float16).astype(np.float64)
+    y = oracle.project(x, W, b)
+    exact = np.array([[sum(x[t, k] * W[r, k] for k in range(128)) + b[r] for r in range(8)] for t in range(3)])
+    assert np.array_equal(y, exact.astype(np.float16).astype(np.float64))
