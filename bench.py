@@ -50,7 +50,8 @@ HEADLINE_CONFIG = {
                 "layers 1-11 64 routed top-6 + 2 shared experts of 896, vocab 102400 fp16 LM head), 64 rows, "
                 "2048 cached prefix tokens + 128-slot ring, all experts Q4_0, Q8_0 attention/dense, greedy",
     "rows": 64, "prefix": 2048, "ring": 128, "seed": 4}
-BPW = {synth.F16: 2.0, synth.Q8_0: 34 / 32, synth.Q4_0: 18 / 32, synth.I8ASYM: 36 / 32}
+BPW = {synth.F16: 2.0, synth.Q8_0: 34 / 32, synth.Q4_0: 18 / 32, synth.I8ASYM: 36 / 32, synth.Q8_0_G64: 66 / 64,
+       synth.Q4_0_G64: 34 / 64}
 
 
 def log(*a):
@@ -292,6 +293,8 @@ def open_workload(name, dev, stream, cfg_overrides=None, **kw):
     ctx = binding.Context(cfg, max_rows=rows, stream=stream.cuda_stream, device=dev.index or 0)
     binding.load_workload(ctx, wl)
     ids = torch.zeros(rows, dtype=torch.int32, device=dev)
+    if not cfg.vocab:  # hidden-vector inputs: nothing to prefill, no ids
+        return ctx, wl, ids, None
     t_pre = None
     if wl.prefill_embeds is not None:
         ne = wl.prefill_embeds.shape[1]
@@ -312,10 +315,29 @@ def open_workload(name, dev, stream, cfg_overrides=None, **kw):
 def time_greedy(ctx, wl, ids, dev, stream, K, W, dist=None):
     """W untimed then K timed greedy steps chained on the device (one graph
     replay per step), CUDA events on the caller's stream.  Returns (ms, first
-    timed position, last ids)."""
+    timed position, last ids).  Workloads without a vocabulary take a resident
+    hidden vector per step instead (uocr_decode_step_embeds)."""
     import torch
 
     rows, start = wl.rows, wl.start_pos
+    if not wl.cfg.vocab:
+        n = W + K
+        xs = np.resize(np.ascontiguousarray(wl.step_x), (n, rows, wl.cfg.hidden)).astype(np.float16)
+        x_all = torch.from_numpy(xs.view(np.int16)).to(dev)
+        pos_all = torch.tensor([[start + s] * rows for s in range(n)], dtype=torch.int32, device=dev)
+        for s_ in range(W):
+            ctx.uocr_decode_step_embeds(rows, x_all[s_].data_ptr(), pos_all[s_].data_ptr())
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        e0.record(stream)
+        for s_ in range(W, n):
+            ctx.uocr_decode_step_embeds(rows, x_all[s_].data_ptr(), pos_all[s_].data_ptr())
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ctx.uocr_sync()
+        return e0.elapsed_time(e1), start + W, x_all[n - 1].clone()
     out = torch.zeros((max(K, W, 1), rows), dtype=torch.int32, device=dev)
     pos = torch.full((rows,), start, dtype=torch.int32, device=dev)
     if W:
@@ -346,7 +368,10 @@ def kernel_table(ctx, wl, ids, dev, position):
     prof = {}
     n_prof = 3
     for _ in range(n_prof):
-        t = ctx.uocr_profile(rows, 0, ids.data_ptr(), 0, pos.data_ptr())
+        if cfg.vocab:
+            t = ctx.uocr_profile(rows, 0, ids.data_ptr(), 0, pos.data_ptr())
+        else:  # `ids` holds the last hidden vectors
+            t = ctx.uocr_profile(rows, 1, 0, ids.data_ptr(), pos.data_ptr())
         for k_, v_ in t.items():
             prof[k_] = prof.get(k_, 0.0) + v_ / n_prof
     distinct = {l: int(np.count_nonzero(ctx.uocr_debug_router(l, rows)["count"]))
@@ -392,6 +417,41 @@ def side_config(name, dev, stream, K, W, hbm_peak, cfg_overrides=None, **kw):
                                "host wall clock around the calls and one uocr_sync"}
     ctx.close()
     return d
+
+
+def time_projector(dev, stream, hbm_peak, n=256, reps=20):
+    """uocr_project of n visual feature vectors of 2048 into the 1280-wide hidden
+    space (Q8_0 weights): CUDA events over `reps` back-to-back calls."""
+    import torch
+
+    from quantized_moe_decode_gb300 import binding
+
+    cfg = synth.ModelConfig(hidden=1280, n_heads=10, head_dim=128, n_layers=1, n_dense_layers=1, dense_inter=256,
+                            prefix_len=4, ring_len=8, max_rows=1, proj_in=2048, fmt_proj=synth.Q8_0)
+    wl = synth.make_workload("projector", cfg, 1, 1, 7)
+    ctx = binding.Context(cfg, max_rows=1, stream=stream.cuda_stream, device=dev.index or 0)
+    binding.load_workload(ctx, wl)
+    x = torch.randn((n, 2048), device=dev).half()
+    out = torch.empty((n, 1280), dtype=torch.float16, device=dev)
+    for _ in range(3):
+        ctx.uocr_project(n, x.data_ptr(), out.data_ptr())
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        ctx.uocr_project(n, x.data_ptr(), out.data_ptr())
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    ctx.close()
+    wbytes = 1280 * 2048 * BPW[synth.Q8_0] + 1280 * 2
+    b = wbytes + n * 2048 * 2 + n * 1280 * 2
+    flops = 2.0 * n * 2048 * 1280
+    return {"features": n, "shape": "2048 -> 1280, Q8_0 + fp16 bias", "ms_per_call": ms,
+            "tokens_per_s": n / (ms * 1e-3), "bytes_per_call": b, "gbs": b / (ms * 1e-3) / 1e9,
+            "tflops": flops / (ms * 1e-3) / 1e12,
+            "how": "uocr_project, %d back-to-back calls, CUDA events on the caller's stream (weights L2-resident "
+                   "after the first call: a latency figure, not an HBM one)" % reps}
 
 
 def run_ours(args, rank, world):
@@ -443,11 +503,12 @@ def run_ours(args, rank, world):
     value = replica_throughput(world, rows, K, ms * 1e-3)
 
     # ---- end to end through the host-buffer entry point (pinned host buffers)
-    K_e2e = min(K, 100)
+    K_e2e = min(K, 100) if cfg.vocab else 0
     h_ids = torch.empty(rows, dtype=torch.int32, pin_memory=True)
     h_pos = torch.empty(rows, dtype=torch.int32, pin_memory=True)
     h_out = torch.empty(rows, dtype=torch.int32, pin_memory=True)
-    h_ids.copy_(last.cpu())
+    if cfg.vocab:
+        h_ids.copy_(last.cpu())
     lib = ctx.lib
     if dist:
         dist.barrier()
@@ -460,7 +521,7 @@ def run_ours(args, rank, world):
             raise RuntimeError(lib.uocr_last_error(ctx.h).decode())
         h_ids.copy_(h_out)
     e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
-    e2e = {"value": replica_throughput(world, rows, K_e2e, e2e_s), "unit": "tokens/s",
+    e2e = {"value": replica_throughput(world, rows, K_e2e, e2e_s) if K_e2e else None, "unit": "tokens/s",
            "h2d_bytes_per_step": rows * 4 * 2, "d2h_bytes_per_step": rows * 4, "steps": K_e2e,
            "how": "uocr_decode_step_host (host ids/positions in, host ids out, synchronous) per step"}
     ctx.close()
@@ -476,6 +537,8 @@ def run_ours(args, rank, world):
         others["full_b8"] = side_config("full_b8", dev, stream, K2, W, hbm_peak)
         others["full_b1"] = side_config("full_b8", dev, stream, K2, W, hbm_peak, rows=1)
         others["stress_b64_int8_kv"] = side_config(WORKLOAD, dev, stream, K2, W, hbm_peak, {"kv_int8": 1})
+        others["full_b8_g64"] = side_config("full_b8_g64", dev, stream, K2, W, hbm_peak)
+        others["projector"] = time_projector(dev, stream, hbm_peak)
     cpu = cpu6 = None
     if not args.no_cpu_baseline:
         n_c, dt_c = time_oracle(wl, ORACLE_ROWS, min_s=15.0, max_steps=20)

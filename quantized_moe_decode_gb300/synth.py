@@ -402,6 +402,12 @@ def workload(name: str, steps: int | None = None, rows: int | None = None, T: in
         r = rows or 8
         return make_workload(name, config_full(max_rows=r), r, steps or 200, 2,
                              prefix="prefill", n_prefill_embeds=256, step_input="ids")
+    if name == "full_b8_g64":  # the full decoder with the Metal page's group-64 blocks
+        r = rows or 8
+        cfg = config_full(max_rows=r).replace(fmt_attn=Q8_0_G64, fmt_dense=Q8_0_G64, fmt_shared=Q8_0_G64,
+                                              fmt_routed=Q4_0_G64)
+        return make_workload(name, cfg, r, steps or 200, 2, prefix="prefill", n_prefill_embeds=256,
+                             step_input="ids")
     if name == "sink":
         r = rows or 1
         return make_workload(f"sink_r{r}_T{T}", config_sink(T, max_rows=r), r, steps or 32, 3)

@@ -112,6 +112,39 @@ def test_router_same_inputs_stress_scale_64_rows(cuda):
     ctx.close()
 
 
+def test_projector_2048_to_1280_image_tokens(cuda):
+    """The projector at its full size: 256 visual feature vectors of 2048 into the
+    1280-wide hidden space (Q8_0 weights, fp16 bias), against the oracle."""
+    import torch
+
+    from parity import check_close
+
+    cfg = synth.ModelConfig(hidden=1280, n_heads=10, head_dim=128, n_layers=1, n_dense_layers=1, dense_inter=256,
+                            prefix_len=4, ring_len=8, max_rows=1, proj_in=2048, fmt_proj=synth.Q8_0)
+    wl = synth.make_workload("projector", cfg, 1, 1, 7)
+    ctx = make_ctx(wl)
+    rng = np.random.default_rng(8)
+    feats = rng.standard_normal((256, 2048)).astype(np.float16)
+    x = torch.from_numpy(feats.view(np.int16)).cuda()
+    out = torch.zeros((256, 1280), dtype=torch.int16, device="cuda")
+    ctx.uocr_project(256, x.data_ptr(), out.data_ptr())
+    ctx.uocr_sync()
+    got = out.cpu().numpy().view(np.float16).astype(np.float64)
+    e, m, _ = check_close("projector", got, make_oracle(wl).project(feats.astype(np.float64)))
+    print(f"\nprojector 256 x 2048 -> 1280: rel-L2 {e:.2e} max-abs {m:.2e}")
+    ctx.close()
+
+
+def test_group64_moe_layer_b1_ring_wraps(cuda):
+    wl = synth.make_workload("moe_layer_b1_g64", synth.config_moe_layer().replace(
+        fmt_attn=synth.Q8_0_G64, fmt_shared=synth.Q4_0_G64, fmt_routed=synth.Q4_0_G64), 1, 140, 1)
+    ctx = make_ctx(wl)
+    st = run_parity(ctx, wl, 140, make_oracle(wl, cache=_cache()))
+    _report(wl.name, st)
+    assert st.kv_checks == 140
+    ctx.close()
+
+
 def _gpu_prefill(ctx, wl):
     """The workload's prefill-by-decode on the library alone; returns the first greedy ids."""
     run = GpuRunner(ctx, wl)

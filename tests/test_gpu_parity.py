@@ -175,3 +175,50 @@ def test_int8_kv_uocr_prefill_two_chunks(cuda):
     wl = synth.make_workload("i8kv_prefill", cfg, 2, 5, 123, prefix="prefill", n_prefill_embeds=70,
                              step_input="ids")
     _code_steps_small(_run(wl, 5, lib_prefill=True))
+
+
+# ---------------------------------------------------------------- group-64 blocks
+G8, G4 = synth.Q8_0_G64, synth.Q4_0_G64
+
+
+def test_group64_dense_q8_attention_q4_mlp_ring_wrap(cuda):
+    cfg = _dense(fmt_attn=G8, fmt_dense=G4)
+    wl = synth.make_workload("g64_dense", cfg, 3, 12, 130)
+    st = _run(wl, 12)
+    assert st.kv_checks == 12 * 2 * 3
+
+
+def test_group64_moe_q4_routed_q8_shared_with_lm_head(cuda):
+    cfg = _moe(fmt_attn=G8, fmt_dense=G8, fmt_shared=G8, fmt_routed=G4, max_rows=12)
+    wl = synth.make_workload("g64_moe", cfg, 12, 8, 131, prefix="prefill", n_prefill_embeds=5, step_input="ids")
+    st = _run(wl, 8)
+    assert st.id_checks >= 12 * 8 and st.router_checks > 0
+
+
+def test_group64_moe_both_q4_forty_rows(cuda):
+    cfg = _moe(fmt_shared=G4, fmt_routed=G4, max_rows=40, vocab=0, prefix_len=9)
+    wl = synth.make_workload("g64_moe40", cfg, 40, 6, 132)
+    _run(wl, 6)
+
+
+# ---------------------------------------------------------------- projector
+@pytest.mark.parametrize("fmt,n", [(Q8, 40), (G4, 7), (I8, 33)])
+def test_projector_against_the_oracle(cuda, fmt, n):
+    torch = cuda
+    import oracle
+
+    cfg = _dense(proj_in=512, fmt_proj=fmt, max_rows=1)
+    wl = synth.make_workload("proj", cfg, 1, 1, 133)
+    ctx = make_ctx(wl)
+    rng = np.random.default_rng(134)
+    feats = rng.standard_normal((n, 512)).astype(np.float16)
+    x = torch.from_numpy(feats.view(np.int16)).cuda()
+    out = torch.zeros((n, cfg.hidden), dtype=torch.int16, device="cuda")
+    ctx.uocr_project(n, x.data_ptr(), out.data_ptr())
+    ctx.uocr_sync()
+    got = out.cpu().numpy().view(np.float16).astype(np.float64)
+    want = make_oracle(wl).project(feats.astype(np.float64))
+    from parity import check_close
+    e, m, _ = check_close("projector", got, want)
+    print(f"\nprojector fmt {fmt} n {n}: rel-L2 {e:.2e} max-abs {m:.2e}")
+    ctx.close()
