@@ -403,15 +403,17 @@ UOCR_API uocr_status uocr_profile(uocr_ctx* ctx, int32_t rows, int32_t input_kin
  * synchronises the device and stalls every other stream), or a host framework
  * that hands the library only the buffers it already owns.  The regular steps
  * keep their scratch in the context arena; this call instead keeps the
- * kernel's scratch (one argmax key per row and a CTA counter, 520 bytes) in a
- * static device array of the library, which every GPU that loads the library
- * holds until the process exits.
+ * kernel's scratch (one argmax key per row, a CTA counter and, for more than
+ * 16 rows, the rows staged for the tensor-core kernel: 1 KB + 256 KB in all)
+ * in a static device array of the library, which every GPU that loads the
+ * library holds until the process exits.  It runs the same kernel as the
+ * decode step at the same row count, so its logits and ids equal the step's.
  *   hidden    device fp32 [rows][hidden]: residual stream after the last layer
  *   next_ids  device int32 [rows]: argmax id per row (lowest index on ties)
  *   logits    device fp32 [rows][vocab] or NULL
  *   stream    cudaStream_t the work is enqueued on (0 = legacy default stream)
- * rows must be in [1, 64] (the scratch capacity), else UOCR_E_INVALID_ARG and
- * nothing is launched.  Uses the context's loaded LM head and final norm.
+ * rows must be in [1, 64] and, above 16 rows, hidden <= 2048 (the scratch
+ * capacity), else UOCR_E_INVALID_ARG and nothing is launched.  Uses the context's loaded LM head and final norm.
  * The first call on a device looks up the scratch address on that device
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * All calls share the one scratch array and each call clears it first, so

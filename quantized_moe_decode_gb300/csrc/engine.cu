@@ -126,6 +126,9 @@ struct uocr_ctx {
   __half* emb = nullptr;
   __half* final_norm = nullptr;
   DMat lm;
+  uint8_t* lm_tc = nullptr;  // LM head in the tensor-core operand layout (max_rows > 16)
+  uint8_t* lm_xc = nullptr;  // the rows staged for it [H/64][64 x 64] fp16
+  int lm_mtiles = 0;
   DMat proj;                 // projector [H][proj_in]
   __half* proj_b = nullptr;  // its bias [H]
   double* inv_freq = nullptr;
@@ -308,6 +311,11 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
     ctx->emb = cv.take<__half>((size_t)V * H, r.weights);
     ctx->final_norm = cv.take<__half>(H, r.weights);
     mat(ctx->lm, V, H, F16);
+    if (MR > 16) {  // steps of more than 16 rows run the LM head on the tensor cores (tcgen05)
+      ctx->lm_mtiles = (V + 127) / 128;
+      ctx->lm_tc = cv.take<uint8_t>((size_t)ctx->lm_mtiles * (H / 64) * 16384, r.weights);
+      ctx->lm_xc = cv.take<uint8_t>((size_t)(H / 64) * 64 * 64 * 2, r.activations);
+    }
   }
   if (c.proj_in > 0) {
     mat(ctx->proj, H, c.proj_in, c.fmt_proj);
@@ -684,7 +692,35 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     }
   }
 
-  if (sh.lm) {
+  if (sh.lm && ctx->lm_tc && !sh.prefill && rows > 16) {
+    // many rows: one read of every weight tile for all of them, on the tensor cores
+    TcLmArgs ta{};
+    ta.w = ctx->lm_tc;
+    ta.xc = ctx->lm_xc;
+    ta.x = hid(2 * c.n_layers);
+    ta.ld_x = H;
+    ta.norm_w = ctx->final_norm;
+    ta.eps = c.rms_eps;
+    ta.K = H;
+    ta.V = c.vocab;
+    ta.n_mtiles = ctx->lm_mtiles;
+    ta.ntok = rows;
+    ta.npad = tc_lm_npad(rows);
+    ta.logits = sh.logits ? ctx->logits : nullptr;
+    ta.keys = ctx->keys;
+    ta.counter = ctx->lm_counter;
+    ta.next_ids = ctx->next_ids;
+    ta.status = ctx->status;
+    if (sh.chain) {
+      ta.feed_ids = ctx->ids_buf;
+      ta.feed_pos = ctx->pos_buf;
+      ta.hist = ctx->hist;
+      ta.hist_ctr = ctx->hist_ctr;
+    }
+    if (want("lm_head_argmax")) {
+      CK(launch_tc_lm(ta, ctx->n_sm, st, pdl), "tensor-core lm head launch");
+    }
+  } else if (sh.lm) {
     // a prefill chunk needs the next id after its last token only
     const int lm_rows = sh.prefill ? 1 : rows;
     const int lm_nt = lm_rows <= 8 ? 1 : 2, lm_tg = (lm_rows + 15) / 16;
@@ -872,7 +908,14 @@ static uocr_status finish_group(uocr_ctx* ctx, int kind, int layer, int expert, 
     case UOCR_T_EXPERT_DOWN:
       return pack_into(ctx, w->ex_down, w->ex_down.qbytes * expert, w->ex_down.sbytes * expert, MAP_IDENT, srcs, H,
                        c.expert_inter, 0);
-    case UOCR_T_LM_HEAD: return pack_into(ctx, ctx->lm, 0, 0, MAP_IDENT, srcs, c.vocab, H, 0);
+    case UOCR_T_LM_HEAD: {
+      uocr_status s = pack_into(ctx, ctx->lm, 0, 0, MAP_IDENT, srcs, c.vocab, H, 0);
+      if (s == UOCR_OK && ctx->lm_tc) {
+        CK(launch_pack_canon(srcs[0], ctx->lm_tc, c.vocab, H, ctx->st), "lm head tensor-core pack");
+        CK(cudaStreamSynchronize(ctx->st), "lm head tensor-core pack");
+      }
+      return s;
+    }
     case UOCR_T_PROJ: return pack_into(ctx, ctx->proj, 0, 0, MAP_IDENT, srcs, H, c.proj_in, 0);
   }
   return ctx->fail(UOCR_E_FORMAT, "internal: no packer for kind %d", kind);
@@ -969,13 +1012,20 @@ static uocr_status check_complete(uocr_ctx* ctx) {
 
 // ------------------------------------------------------------------ scratch-free LM head
 // Scratch of uocr_lm_head_argmax_noalloc: one 64-bit argmax key per row (up to
-// kNoAllocMaxRows) followed by the kernel's finished-CTA counter.  It lives in
-// this file-scope device array, so every GPU that loads the library holds these
-// 520 bytes until the process exits and no call ever allocates.  Host code
-// must not pass the symbol itself to a kernel: its device address is fetched
-// per device with cudaGetSymbolAddress.
+// kNoAllocMaxRows) and the kernel's finished-CTA counter, then room for the
+// rows staged in the tensor cores' operand layout (steps of more than 16 rows).
+// It lives in this file-scope device array (1 KB + 256 KB), so every GPU that
+// loads the library holds it until the process exits and no call ever
+// allocates.  Host code must not pass the symbol itself to a kernel: its
+// device address is fetched per device with cudaGetSymbolAddress.
 constexpr int kNoAllocMaxRows = 64;
-static __device__ __align__(256) unsigned long long g_lm_noalloc_scratch[kNoAllocMaxRows + 1];
+// Beyond 16 rows the LM head runs on the tensor cores, which need the rows
+// staged in their operand layout: 128 bytes per input for 64 rows, here for
+// hidden sizes up to kNoAllocMaxHidden.
+constexpr int kNoAllocMaxHidden = 2048;
+constexpr size_t kNoAllocKeysBytes = 1024;  // keys [64] + counter, rounded up
+constexpr size_t kNoAllocBytes = kNoAllocKeysBytes + (size_t)kNoAllocMaxHidden * 128;
+static __device__ __align__(256) unsigned long long g_lm_noalloc_scratch[kNoAllocBytes / 8];
 static std::mutex g_noalloc_mu;
 static std::map<int, unsigned long long*> g_noalloc_addr;  // device ordinal -> device address
 
@@ -1650,6 +1700,8 @@ uocr_status uocr_lm_head_argmax_noalloc(uocr_ctx* ctx, int32_t rows, const float
   if (rows < 1 || rows > kNoAllocMaxRows)
     return ctx->fail(UOCR_E_INVALID_ARG, "rows %d outside [1, %d], the capacity of the static scratch", rows,
                      kNoAllocMaxRows);
+  if (rows > 16 && ctx->lm_tc && c.hidden > kNoAllocMaxHidden)
+    return ctx->fail(UOCR_E_INVALID_ARG, "rows > 16 need hidden <= %d (the static scratch)", kNoAllocMaxHidden);
   uocr_status s = check_complete(ctx);
   if (s != UOCR_OK) return s;
   unsigned long long* scratch = nullptr;
@@ -1672,6 +1724,27 @@ static uocr_status noalloc_launch(uocr_ctx* ctx, int rows, const float* hidden, 
   // the keys and the counter must start at zero; a previous call leaves them zero
   // when it completes, but clear them anyway in case it did not
   CK(cudaMemsetAsync(scratch, 0, sizeof(unsigned long long) * (kNoAllocMaxRows + 1), st), "scratch clear");
+  if (rows > 16 && ctx->lm_tc) {  // the kernel the decode step runs at this row count
+    TcLmArgs ta{};
+    ta.w = ctx->lm_tc;
+    ta.xc = reinterpret_cast<uint8_t*>(scratch) + kNoAllocKeysBytes;
+    ta.x = hidden;
+    ta.ld_x = c.hidden;
+    ta.norm_w = ctx->final_norm;
+    ta.eps = c.rms_eps;
+    ta.K = c.hidden;
+    ta.V = c.vocab;
+    ta.n_mtiles = ctx->lm_mtiles;
+    ta.ntok = rows;
+    ta.npad = tc_lm_npad(rows);
+    ta.logits = logits;
+    ta.keys = scratch;
+    ta.counter = reinterpret_cast<int*>(scratch + kNoAllocMaxRows);
+    ta.next_ids = next_ids;
+    ta.status = ctx->status;
+    CK(launch_tc_lm(ta, ctx->n_sm, st, false), "tensor-core lm head launch");
+    return UOCR_OK;
+  }
   const int nt = rows <= 8 ? 1 : 2;
   const int tg = (rows + 15) / 16;
   int gx = ctx->gemv_ctas_per_sm * ctx->n_sm / tg;  // the grid of the step's LM-head launch

@@ -173,6 +173,30 @@ struct PackArgs {
 };
 enum PackMap : int { MAP_IDENT = 0, MAP_QKV = 1, MAP_SWIGLU = 2, MAP_KCAT = 3 };
 
+// The tensor-core LM head (tc_kernels.cu) for steps of 17..64 rows.
+struct TcLmArgs {
+  const uint8_t* w;          // canonical fp16 tiles [n_mtiles][K/64][128 x 64]
+  uint8_t* xc;               // staged rows, canonical [K/64][npad x 64] fp16
+  const float* x;            // residual rows [ntok][ld_x] (final RMSNorm input)
+  int ld_x;
+  const __half* norm_w;      // final norm weight [K]
+  float eps;
+  int K, V, n_mtiles, ntok, npad;
+  float* logits;             // [ntok][V] or nullptr
+  unsigned long long* keys;  // [ntok], zero on entry
+  int* counter;
+  int* next_ids;
+  int* feed_ids;             // nullable: chain into the next step (as GemvArgs)
+  int* feed_pos;
+  int* hist;
+  int* hist_ctr;
+  int* status;
+};
+int tc_lm_npad(int rows);
+int tc_lm_smem_bytes(int npad);
+cudaError_t launch_tc_lm(const TcLmArgs& a, int n_sm, cudaStream_t st, bool pdl);
+cudaError_t launch_pack_canon(const void* src_f16, uint8_t* dst, int V, int K, cudaStream_t st);
+
 // Launch with or without programmatic dependent launch (the kernel may start
 // while the previous kernel on the stream finishes; it calls
 // griddepcontrol.wait before touching anything that kernel produces).

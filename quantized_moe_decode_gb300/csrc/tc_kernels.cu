@@ -1,0 +1,384 @@
+// Tensor-core (tcgen05) LM head for steps with more than 16 rows.
+//
+// At 17..64 rows the LM head is a dense contraction (logits = W x for V = 102400
+// fp16 rows, H inputs, N rows of the step), and the fragment-ordered GEMV
+// streams W once per 16-row token group.  Here every weight tile is read once
+// for all the step's rows:
+//
+//   * W is packed a second time, in the canonical K-major layout of the tensor
+//     core's shared-memory operands without swizzle: tiles of 128 rows x 64
+//     inputs (16 KB), element (r, k) of a tile at
+//     (r/8)*1024 + (k/8)*128 + (r%8)*16 + (k%8)*2 bytes (8-row x 16-byte core
+//     matrices; 128 bytes between core matrices along K, 1024 along M); tile
+//     (m, kb) at ((m * KB) + kb) * 16 KB, so one 1-D TMA bulk copy moves a tile.
+//   * k_lm_stage writes the final-normalised rows (fp16) in the same layout,
+//     NPAD rows per 64-input block (rows beyond the step's are zero).
+//   * k_tc_lm: one CTA per SM walks M tiles.  Warp 4 (one lane) streams
+//     (weight tile, activation block) pairs into an S-stage ring with bulk
+//     copies on full/empty mbarriers; warp 5 (one lane) issues tcgen05.mma
+//     (M = 128, N = NPAD, K = 16, fp16 x fp16 -> fp32) into one of two TMEM
+//     accumulators; warps 0..3 read the finished accumulator (tcgen05.ld, each
+//     warp its 32-lane quadrant = 32 vocabulary rows), store logits on request
+//     and keep each token's best (logit, lowest index) key; the last CTA to
+//     finish writes the ids, as the GEMV path does.
+//
+// Every mbarrier wait is bounded; a wait that gives up sets kStatusTimeout and
+// its role stops, so every role reaches the final barrier and the TMEM is freed.
+//
+// Source: "Unlimited-OCR on Apple Silicon with C and Metal", "Il decoder e il
+// Mixture of Experts" (the decode loop ends in an argmax over the language
+// head); "Falcon-OCR INT8 OpenVINO IR", "How it is meant to be run" (the rows of
+// a step share one read of the weights).
+#include "launch.h"
+
+namespace uocr {
+
+// ------------------------------------------------------------------ tcgen05 / TMEM wrappers
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16; accumulate = 0 overwrites D.
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the mbarrier once every tcgen05.mma this thread issued has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+// Thread t of the warp gets 32 consecutive 32-bit columns of TMEM lane (lane field of taddr) + t.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, no swizzle: start address, byte offset
+// between core matrices along K (leading) and along M/N (stride), version 1.
+__device__ __forceinline__ uint64_t smem_desc(const void* p, uint32_t lbo, uint32_t sbo) {
+  const uint32_t a = smem_u32(p);
+  uint64_t d = (uint64_t)((a & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+// Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+constexpr int kTcTileRows = 128;
+constexpr int kTcTileK = 64;
+constexpr int kTcTileBytes = kTcTileRows * kTcTileK * 2;  // 16 KB
+constexpr int kTcThreads = 192;                           // 4 epilogue warps, producer, MMA
+constexpr int kTcSmemBudget = 200 * 1024;                 // stage ring (the rest: barriers, per-warp bests)
+
+__host__ __device__ constexpr int tc_block_b_bytes(int npad) { return npad * kTcTileK * 2; }
+__host__ __device__ constexpr int tc_stages(int npad) {
+  return kTcSmemBudget / (kTcTileBytes + tc_block_b_bytes(npad)) < 12 ? kTcSmemBudget / (kTcTileBytes + tc_block_b_bytes(npad))
+                                                                    : 12;
+}
+
+__device__ __forceinline__ int canon_offset(int r, int k) {
+  return (r >> 3) * 1024 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+
+// ------------------------------------------------------------------ packer
+// Row-major fp16 W [V][K] -> canonical tiles; rows >= V are zero.  One thread
+// per 16-byte chunk (8 inputs of one row).
+__global__ void k_pack_canon(const __half* src, uint8_t* dst, int V, int K, int n_mtiles) {
+  const int KB = K / kTcTileK;
+  const long long total = (long long)n_mtiles * KB * kTcTileRows * 8;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+    const int k8 = (int)(i & 7);
+    const int r = (int)((i >> 3) % kTcTileRows);
+    const long long tile = (i >> 3) / kTcTileRows;  // m * KB + kb
+    const int kb = (int)(tile % KB);
+    const int m = (int)(tile / KB);
+    const int row = m * kTcTileRows + r;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (row < V) v = *reinterpret_cast<const uint4*>(src + (size_t)row * K + kb * kTcTileK + k8 * 8);
+    *reinterpret_cast<uint4*>(dst + tile * kTcTileBytes + canon_offset(r, k8 * 8)) = v;
+  }
+}
+
+cudaError_t launch_pack_canon(const void* src_f16, uint8_t* dst, int V, int K, cudaStream_t st) {
+  const int n_mtiles = (V + kTcTileRows - 1) / kTcTileRows;
+  const long long total = (long long)n_mtiles * (K / kTcTileK) * kTcTileRows * 8;
+  const long long blocks = (total + 255) / 256;
+  k_pack_canon<<<(int)(blocks < 65535 ? blocks : 65535), 256, 0, st>>>(reinterpret_cast<const __half*>(src_f16), dst,
+                                                                        V, K, n_mtiles);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ activation staging
+// Block t: row t of the step (t < ntok) final-normalised to fp16, or zeros,
+// written in the canonical layout: block kb holds inputs [64 kb, 64 kb + 64)
+// of all NPAD rows (NPAD * 128 bytes).
+__global__ void __launch_bounds__(256) k_lm_stage(const TcLmArgs a) {
+  pdl_launch_dependents();
+  const int t = blockIdx.x, K = a.K;
+  const int warp = threadIdx.x >> 5;
+  __shared__ float s_part[8];
+  pdl_wait();  // the residual rows come from the previous kernel
+  float ss = 0.f;
+  if (t < a.ntok)
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+      const float v = a.x[(size_t)t * a.ld_x + k];
+      ss += v * v;
+    }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) s_part[warp] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_part[w];
+  const float r = rsqrtf(tot / (float)K + a.eps);
+  const int bb = tc_block_b_bytes(a.npad);
+  for (int k2 = threadIdx.x; k2 < K / 2; k2 += blockDim.x) {
+    const int k = 2 * k2;
+    __half2 h = __floats2half2_rn(0.f, 0.f);
+    if (t < a.ntok) {
+      const float x0 = a.x[(size_t)t * a.ld_x + k], x1 = a.x[(size_t)t * a.ld_x + k + 1];
+      h = __floats2half2_rn(x0 * r * __half2float(a.norm_w[k]), x1 * r * __half2float(a.norm_w[k + 1]));
+    }
+    *reinterpret_cast<__half2*>(a.xc + (size_t)(k / kTcTileK) * bb + canon_offset(t, k % kTcTileK)) = h;
+  }
+}
+
+// ------------------------------------------------------------------ the tensor-core LM head
+template <int NPAD>
+__global__ void __launch_bounds__(kTcThreads, 1) k_tc_lm(const TcLmArgs a) {
+  constexpr int S = tc_stages(NPAD);
+  constexpr int BB = tc_block_b_bytes(NPAD);
+  constexpr int STAGE = kTcTileBytes + BB;
+  constexpr int NCOLS = 2 * NPAD < 32 ? 32 : 2 * NPAD;  // two accumulators, a power of two
+  constexpr uint32_t IDESC = idesc_f16(kTcTileRows, NPAD);
+  static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 128, "N of the MMA");
+  extern __shared__ __align__(1024) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* done = acc_empty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
+  __shared__ unsigned long long s_best[4][NPAD];
+  __shared__ int s_last;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KB = a.K / kTcTileK;
+  const int n_mt = a.n_mtiles;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full + b, 1);
+      mbar_init(acc_empty + b, 4);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < 4 * NPAD; i += blockDim.x) (&s_best[0][0])[i] = 0ull;
+  if (warp == 5) {
+    tmem_alloc(s_tmem, NCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  pdl_launch_dependents();
+
+  if (warp == 4) {  // ---------------- producer
+    if (lane == 0) {
+      const int my_tiles = blockIdx.x < n_mt ? (n_mt - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+      const int total = my_tiles * KB;
+      const int pre = total < S ? total : S;
+      auto tile_of = [&](int i) { return (size_t)(blockIdx.x + (i / KB) * gridDim.x) * KB + (i % KB); };
+      // the weight tiles do not depend on the previous kernel: the first S go out now
+      for (int i = 0; i < pre; ++i) {
+        mbar_expect_tx(full + i, (uint32_t)STAGE);
+        bulk_g2s(smem + i * STAGE, a.w + tile_of(i) * kTcTileBytes, kTcTileBytes, full + i);
+      }
+      pdl_wait();  // the staged activations come from k_lm_stage
+      for (int i = 0; i < pre; ++i)
+        bulk_g2s(smem + i * STAGE + kTcTileBytes, a.xc + (size_t)(i % KB) * BB, BB, full + i);
+      bool ok = true;
+      for (int it = pre; it < total; ++it) {
+        const int s = it % S;
+        if (!mbar_wait(empty + s, (uint32_t)(((it / S) - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + s * STAGE;
+        mbar_expect_tx(full + s, (uint32_t)STAGE);
+        bulk_g2s(st, a.w + tile_of(it) * kTcTileBytes, kTcTileBytes, full + s);
+        bulk_g2s(st + kTcTileBytes, a.xc + (size_t)(it % KB) * BB, BB, full + s);
+      }
+      // every copy issued has landed before the CTA can leave (bounded)
+      const int issued = ok ? total : 0;
+      for (int i = issued > S ? issued - S : 0; i < issued; ++i)
+        if (!mbar_wait(full + (i % S), (uint32_t)((i / S) & 1))) ok = false;
+      if (!ok) atomicOr(a.status, kStatusTimeout);
+    }
+  } else if (warp == 5) {  // ---------------- MMA issue
+    if (lane == 0) {
+      int it = 0, tl = 0;
+      bool ok = true;
+      for (int mt = blockIdx.x; mt < n_mt && ok; mt += gridDim.x, ++tl) {
+        const int buf = tl & 1;
+        if (tl >= 2 && !mbar_wait(acc_empty + buf, (uint32_t)(((tl >> 1) - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * NPAD);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % S;
+          if (!mbar_wait(full + s, (uint32_t)((it / S) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t* st = smem + s * STAGE;
+#pragma unroll
+          for (int ks = 0; ks < kTcTileK / 16; ++ks)
+            tc_mma_f16(d, smem_desc(st + ks * 256, 128, 1024), smem_desc(st + kTcTileBytes + ks * 256, 128, 1024),
+                       IDESC, (kb | ks) != 0);
+          tc_commit(empty + s);  // the stage is free once these MMAs have read it
+        }
+        if (!ok) break;
+        tc_commit(acc_full + buf);
+      }
+      // no MMA may still be running when the TMEM is freed: wait (bounded) for the last ones
+      tc_commit(done);
+      if (!mbar_wait(done, 0)) ok = false;
+      if (!ok) atomicOr(a.status, kStatusTimeout);
+    }
+  } else {  // ---------------- epilogue: warps 0..3, TMEM lanes 32 w .. 32 w + 31
+    pdl_wait();
+    int tl = 0;
+    for (int mt = blockIdx.x; mt < n_mt; mt += gridDim.x, ++tl) {
+      const int buf = tl & 1;
+      const int ok = lane == 0 ? (int)mbar_wait(acc_full + buf, (uint32_t)((tl >> 1) & 1)) : 1;
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) atomicOr(a.status, kStatusTimeout);
+        break;
+      }
+      tc_fence_after();
+      const int row = mt * kTcTileRows + warp * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < NPAD / 32; ++c) {
+        uint32_t r[32];
+        tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * NPAD + c * 32), r);
+        tc_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int tok = c * 32 + j;
+          const float v = __uint_as_float(r[j]);
+          unsigned long long key = 0ull;
+          if (tok < a.ntok && row < a.V) {
+            if (a.logits) a.logits[(size_t)tok * a.V + row] = v;
+            key = argmax_key(v, row);
+          }
+#pragma unroll
+          for (int o = 16; o; o >>= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+            key = other > key ? other : key;
+          }
+          if (lane == 0 && key > s_best[warp][tok]) s_best[warp][tok] = key;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty + buf);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, NCOLS);
+  }
+  // this CTA's best per row of the step -> the global keys; the last CTA writes the ids
+  for (int t = threadIdx.x; t < a.ntok; t += blockDim.x) {
+    unsigned long long k = s_best[0][t];
+    for (int w = 1; w < 4; ++w) k = s_best[w][t] > k ? s_best[w][t] : k;
+    if (k) atomicMax(a.keys + t, k);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int done = atomicAdd(a.counter, 1);
+    s_last = done == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    const int step = a.hist ? *a.hist_ctr : 0;
+    for (int t = threadIdx.x; t < a.ntok; t += blockDim.x) {
+      const unsigned long long key = atomicExch(a.keys + t, 0ull);
+      const int id = argmax_key_index(key);
+      a.next_ids[t] = id;
+      if (a.feed_ids) {
+        a.feed_ids[t] = id;
+        a.feed_pos[t] += 1;
+      }
+      if (a.hist) a.hist[(size_t)step * a.ntok + t] = id;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      if (a.hist) *a.hist_ctr = step + 1;
+      atomicExch(a.counter, 0);
+    }
+  }
+}
+
+int tc_lm_npad(int rows) { return rows <= 32 ? 32 : 64; }
+
+int tc_lm_smem_bytes(int npad) {
+  const int S = tc_stages(npad);
+  return S * (kTcTileBytes + tc_block_b_bytes(npad)) + (2 * S + 5) * 8 + 16;
+}
+
+cudaError_t launch_tc_lm(const TcLmArgs& a, int n_sm, cudaStream_t st, bool pdl) {
+  const int gx = a.n_mtiles < n_sm ? a.n_mtiles : n_sm;
+  cudaError_t e = launch_kernel(k_lm_stage, dim3(a.npad), dim3(256), 0, st, pdl, a);
+  if (e != cudaSuccess) return e;
+  if (a.npad == 32) return launch_kernel(k_tc_lm<32>, dim3(gx), dim3(kTcThreads), tc_lm_smem_bytes(32), st, pdl, a);
+  if (a.npad == 64) return launch_kernel(k_tc_lm<64>, dim3(gx), dim3(kTcThreads), tc_lm_smem_bytes(64), st, pdl, a);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t init_tc_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(k_tc_lm<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_lm_smem_bytes(32));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_tc_lm<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_lm_smem_bytes(64));
+  return e;
+}
+
+}  // namespace uocr

@@ -222,3 +222,15 @@ def test_projector_against_the_oracle(cuda, fmt, n):
     e, m, _ = check_close("projector", got, want)
     print(f"\nprojector fmt {fmt} n {n}: rel-L2 {e:.2e} max-abs {m:.2e}")
     ctx.close()
+
+
+# ---------------------------------------------------------------- tensor-core LM head
+@pytest.mark.parametrize("rows", [20, 64])
+def test_lm_head_on_tensor_cores_rows_above_16(cuda, rows):
+    """Steps of more than 16 rows run the LM head as a tcgen05 GEMM (N = 32 or 64
+    padded rows, vocabulary 1000: the last 128-row tile is ragged): logits and
+    greedy ids against the oracle over several steps."""
+    cfg = _dense(vocab=1000, max_rows=rows, n_layers=1, n_dense_layers=1)
+    wl = synth.make_workload("tc_lm", cfg, rows, 4, 140, step_input="ids")
+    st = _run(wl, 4)
+    assert st.id_checks == rows * 4
