@@ -120,6 +120,21 @@ def kv_quant(x):
     return q.astype(np.int8), s
 
 
+def act_quant(x, group=32):
+    """Dynamic int8 quantisation of projection inputs, per group of `group`
+    consecutive inputs (last axis): the same symmetric rule as kv_quant per
+    group (s = max|x| / 127, code = round-half-even(x / s), fp32 decisions).
+    Returns the quantised values s * code (float64), the ones the projection
+    multiplies ("Falcon-OCR INT8 OpenVINO IR": the runtime quantises the linear
+    layers' inputs dynamically in groups of 32, src_dyn_quant_group_size:32).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    shape = x.shape
+    g = x.reshape(shape[:-1] + (shape[-1] // group, group))
+    codes, s = kv_quant(g)
+    return kv_dequant(codes, s).reshape(shape)
+
+
 def kv_dequant(codes, s):
     """Value of an INT8 KV entry: s * code (float64)."""
     return np.asarray(codes, dtype=np.float64) * np.asarray(s, dtype=np.float64)[..., None]
@@ -258,10 +273,14 @@ class OracleModel:
     prefix included) and attention reads s * code.
     """
 
-    def __init__(self, cfg, tensors, rows, kv_prefix=None, sinks=None, cache="float64", kv_int8=False):
+    def __init__(self, cfg, tensors, rows, kv_prefix=None, sinks=None, cache="float64", kv_int8=False,
+                 act_int8=False):
         self.cfg = cfg
         self.rows = rows
         self.kv_int8 = kv_int8
+        # dynamic int8 activations: the inputs of the dense projections (Q/K/V, O,
+        # dense gate/up and down) are quantised per group of 32 before the matmul
+        self.act_int8 = act_int8
         self._t = {(t.kind, t.layer, t.expert): t for t in tensors}
         # cache: None (dequantise at every use), "float64", or "float32" (only
         # for matrices whose values are exact in float32, see quant.float32_is_exact)
@@ -354,8 +373,9 @@ class OracleModel:
         res.hidden[0] = X
         for r in range(rows):
             self.slot_pos[r, res.slots[r]] = positions[r]
+        aq = act_quant if self.act_int8 else (lambda v: v)
         for l in range(L):
-            Xn = f16(rmsnorm(X, self.w(T_ATTN_NORM, l), cfg.rms_eps))
+            Xn = aq(f16(rmsnorm(X, self.w(T_ATTN_NORM, l), cfg.rms_eps)))
             Q = Xn @ self.w(T_WQ, l).T
             Kx = Xn @ self.w(T_WK, l).T
             Vx = Xn @ self.w(T_WV, l).T
@@ -382,11 +402,15 @@ class OracleModel:
                     self.rk[l][r, :, s - self.P] = kh
                     self.rv[l][r, :, s - self.P] = vh
                 attn[r] = f16(self._attention(l, r, qh, p).reshape(-1))
-            Hh = X + attn @ self.w(T_WO, l).T
+            Hh = X + aq(attn) @ self.w(T_WO, l).T
             res.h_attn[l] = Hh
             Hn = f16(rmsnorm(Hh, self.w(T_MLP_NORM, l), cfg.rms_eps))
             if l < cfg.n_dense_layers or cfg.n_experts == 0:
-                Y = Hh + swiglu_rows(Hn, self.w(T_GATE, l), self.w(T_UP, l), self.w(T_DOWN, l), act_fp16=True)
+                if self.act_int8:
+                    a = f16(silu(aq(Hn) @ self.w(T_GATE, l).T) * (aq(Hn) @ self.w(T_UP, l).T))
+                    Y = Hh + aq(a) @ self.w(T_DOWN, l).T
+                else:
+                    Y = Hh + swiglu_rows(Hn, self.w(T_GATE, l), self.w(T_UP, l), self.w(T_DOWN, l), act_fp16=True)
             else:
                 Y, info = self._moe(l, Hh, Hn)
                 res.router[l] = info

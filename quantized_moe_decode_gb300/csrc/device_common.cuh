@@ -497,38 +497,78 @@ __device__ __forceinline__ SlabWork slab_work(int first, int stride, int n, int 
 
 // The units a warp fetches, in the order it consumes them: for each of its
 // group's slabs (first + m*stride, m = grp, grp + G, ...) the run of uw units
-// starting at rank*uw.  The unit index is recomputed from warp-uniform counters
-// (measured faster than per-lane running pointers).
+// starting at rank*uw.  UOCR_STREAM_PTR selects how a unit's address is formed:
+// 1 = this lane's code and scale pointers advance by one unit per fetch and are
+// recomputed only when the run moves to the next slab; 0 = the unit index is
+// recomputed from the warp-uniform counters at every fetch.
+#ifndef UOCR_STREAM_PTR
+#define UOCR_STREAM_PTR 1
+#endif
 template <int FMT>
 struct UnitStream {
+  static constexpr int UB = unit_bytes(FMT);
+  static constexpr int SB = unit_scale_bytes(FMT);
+  static constexpr int SE = FMT == Q8_0 ? 4 : 8;  // bytes of a lane's scale entry
   const uint8_t* q;
   const uint8_t* sc;
+  const uint8_t* qp;  // this lane's next code bytes / scale entry (UOCR_STREAM_PTR)
+  const uint8_t* sp;
   int m, i;
-  const SlabWork* wp;
+  int first, stride, n, U, uw, G, rank;
+  __device__ __forceinline__ void set_run(int lane) {
+    const size_t unit0 = (size_t)(first + m * stride) * U + rank * uw;
+    qp = q + unit0 * UB + lane * 16;
+    sp = sc + unit0 * SB + (lane >> 2) * SE;
+  }
   __device__ __forceinline__ void start(const uint8_t* q_, const uint8_t* sc_, const SlabWork& w) {
     q = q_;
     sc = sc_;
+    first = w.first;
+    stride = w.stride;
+    n = w.n;
+    U = w.U;
+    uw = w.uw;
+    G = w.G;
+    rank = w.rank;
     m = w.grp;
     i = 0;
-    wp = &w;
+    if (UOCR_STREAM_PTR && m < n) set_run(threadIdx.x & 31);
   }
   __device__ __forceinline__ void fetch_next(uint8_t* slot, int lane) {
-    const SlabWork& w = *wp;
-    if (m < w.n) {
-      const size_t unit = (size_t)(w.first + m * w.stride) * w.U + w.rank * w.uw + i;
-      const uint8_t* qu = q + unit * unit_bytes(FMT);
+    if (m < n) {
+#if UOCR_STREAM_PTR
+      cp_async16(slot + lane * 16, qp);
+      if constexpr (FMT == F16) {
+        cp_async16(slot + 512 + lane * 16, qp + 512);
+      } else if constexpr (FMT == Q8_0) {
+        cp_async4(slot + 512 + lane * 8, sp);
+      } else {
+        cp_async8(slot + 512 + lane * 8, sp);
+      }
+      qp += UB;
+      sp += SB;
+      if (++i == uw) {
+        i = 0;
+        m += G;
+        if (m < n) set_run(lane);
+      }
+#else
+      const size_t unit = (size_t)(first + m * stride) * U + rank * uw + i;
+      const uint8_t* qu = q + unit * UB;
       cp_async16(slot + lane * 16, qu + lane * 16);
       if constexpr (FMT == F16) {
         cp_async16(slot + 512 + lane * 16, qu + 512 + lane * 16);
-      } else if constexpr (FMT == Q8_0) {
-        cp_async4(slot + 512 + lane * 8, sc + unit * unit_scale_bytes(FMT) + (lane >> 2) * 4);
       } else {
-        cp_async8(slot + 512 + lane * 8, sc + unit * unit_scale_bytes(FMT) + (lane >> 2) * 8);
+        if constexpr (FMT == Q8_0)
+          cp_async4(slot + 512 + lane * 8, sc + unit * SB + (lane >> 2) * SE);
+        else
+          cp_async8(slot + 512 + lane * 8, sc + unit * SB + (lane >> 2) * SE);
       }
-      if (++i == w.uw) {
+      if (++i == uw) {
         i = 0;
-        m += w.G;
+        m += G;
       }
+#endif
     }
     cp_commit();  // one group per call, empty or not, keeps the wait counts uniform
   }

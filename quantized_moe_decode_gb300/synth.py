@@ -75,6 +75,7 @@ class ModelConfig:
     rope_theta: float = 10000.0
     router_std: float = 0.02
     kv_int8: int = 0  # INT8 KV cache (one scale per head vector) instead of fp16
+    act_int8: int = 0  # dynamic int8 activations (groups of 32) on the dense projections
     proj_in: int = 0  # projector input width (visual features; 0 = no projector)
     fmt_proj: int = Q8_0
 

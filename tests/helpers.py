@@ -17,4 +17,4 @@ def make_oracle(wl, rows=None, cache="float64"):
     rows = list(range(wl.rows)) if rows is None else list(rows)
     kv = None if wl.kv_prefix is None else wl.kv_prefix.subset(rows)
     return oracle.OracleModel(wl.cfg, wl.tensors, len(rows), kv_prefix=kv, sinks=wl.sinks, cache=cache,
-                              kv_int8=bool(wl.cfg.kv_int8))
+                              kv_int8=bool(wl.cfg.kv_int8), act_int8=bool(getattr(wl.cfg, "act_int8", 0)))

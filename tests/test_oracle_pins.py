@@ -424,3 +424,42 @@ def test_projector_output_is_fp16_of_the_exact_product():
     y = oracle.project(x, W, b)
     exact = np.array([[sum(x[t, k] * W[r, k] for k in range(128)) + b[r] for r in range(8)] for t in range(3)])
     assert np.array_equal(y, exact.astype(np.float16).astype(np.float64))
+
+
+# ---------------------------------------------------------------- dynamic int8 activations
+def test_act_quant_groups_of_32_hand_built():
+    # group 0: amax 127 -> s = 1, codes round half to even; group 1: all zero; group 2: s = 2^-3
+    x = np.zeros(96)
+    x[:32] = np.linspace(-127, 127, 32)
+    x[5] = 2.5
+    x[64:96] = np.arange(32) * 0.125 - 2.0
+    y = oracle.act_quant(x)
+    assert np.array_equal(y[:32][[0, 31]], [-127.0, 127.0]) and y[5] == 2.0
+    assert not y[32:64].any()
+    # group 2: amax 2.0 -> s = 2/127 (fp32); every value within half a step
+    s2 = np.float32(2.0) / np.float32(127.0)
+    assert np.all(np.abs(y[64:96] - x[64:96]) <= float(s2) / 2 + 1e-12)
+    # per-group scale: multiplying one group by 2^k scales only that group's result
+    x2 = x.copy()
+    x2[64:96] *= 8.0
+    y2 = oracle.act_quant(x2)
+    assert np.array_equal(y2[64:96], 8.0 * y[64:96]) and np.array_equal(y2[:64], y[:64])
+
+
+def test_int8_activation_model_is_close_to_fp16_and_exact_on_its_grid():
+    cfg = synth.ModelConfig(hidden=128, n_heads=2, head_dim=64, n_layers=2, n_dense_layers=2, dense_inter=256,
+                            prefix_len=6, ring_len=4, max_rows=2)
+    wl = synth.make_workload("actq", cfg, 2, 3, 13)
+    kv = wl.kv_prefix.subset([0, 1])
+    m8 = oracle.OracleModel(cfg, wl.tensors, 2, kv_prefix=kv, act_int8=True)
+    m16 = oracle.OracleModel(cfg, wl.tensors, 2, kv_prefix=kv)
+    for s in range(wl.steps):
+        pos = np.full(2, cfg.prefix_len + s)
+        r8 = m8.step(pos, x=wl.step_x[s])
+        r16 = m16.step(pos, x=wl.step_x[s])
+        d = np.linalg.norm(r8.hidden[-1] - r16.hidden[-1]) / np.linalg.norm(r16.hidden[-1])
+        assert 0 < d < 3e-2, d
+    # a vector already on the grid (codes times a power-of-two scale) is its own quantisation
+    g = np.arange(-16, 16) * 2.0 ** -4
+    g[0] = -127 * 2.0 ** -4
+    assert np.array_equal(oracle.act_quant(g), g)
