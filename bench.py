@@ -394,6 +394,11 @@ def step_bytes_over(cfg, rows, positions, distinct):
     return tot / len(positions)
 
 
+def wl_label(wl):
+    """Workload name plus the cache / activation options that change the kernels."""
+    return wl.name + (" INT8 KV" if wl.cfg.kv_int8 else "") + (" int8 act" if getattr(wl.cfg, "act_int8", 0) else "")
+
+
 def side_config(name, dev, stream, K, W, hbm_peak, cfg_overrides=None, **kw):
     """One extra configuration of the same line: time K greedy steps, report
     tokens/s, bytes and the HBM fraction, and the uocr_prefill time."""
@@ -403,7 +408,7 @@ def side_config(name, dev, stream, K, W, hbm_peak, cfg_overrides=None, **kw):
     kernels, distinct = kernel_table(ctx, wl, last, dev, p0 + K)
     sb = step_bytes_over(cfg, rows, range(p0, p0 + K), distinct)
     ms_step = ms / K
-    d = {"workload": wl.name + (" INT8 KV" if cfg.kv_int8 else ""), "rows": rows, "prefix": cfg.prefix_len,
+    d = {"workload": wl_label(wl), "rows": rows, "prefix": cfg.prefix_len,
          "steps": K, "warmup": W,
          "positions": [p0, p0 + K - 1], "ms_per_step": ms_step, "tokens_per_s": rows / (ms_step * 1e-3),
          "bytes_per_step": sb, "hbm_gbs": sb / (ms_step * 1e-3) / 1e9,
@@ -475,7 +480,8 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     kw = {"rows": args.rows} if args.rows else {}
-    ctx, wl, ids, _ = open_workload(args.workload, dev, stream, {"kv_int8": 1} if args.kv_int8 else None, **kw)
+    over = dict(({"kv_int8": 1} if args.kv_int8 else {}), **({"act_int8": 1} if args.act_int8 else {}))
+    ctx, wl, ids, _ = open_workload(args.workload, dev, stream, over or None, **kw)
     cfg, rows = wl.cfg, wl.rows
     K, W = args.steps, args.warmup
     log(f"[bench] setup {time.perf_counter() - t_setup:.1f}s")
@@ -538,6 +544,9 @@ def run_ours(args, rank, world):
         others["full_b1"] = side_config("full_b8", dev, stream, K2, W, hbm_peak, rows=1)
         others["stress_b64_int8_kv"] = side_config(WORKLOAD, dev, stream, K2, W, hbm_peak, {"kv_int8": 1})
         others["full_b8_g64"] = side_config("full_b8_g64", dev, stream, K2, W, hbm_peak)
+        # the Falcon-OCR card's serving setting: INT8-asym weights, INT8 KV cache, int8 activations
+        others["sink_b24_T350_int8"] = side_config("sink", dev, stream, K2, W, hbm_peak,
+                                                   {"kv_int8": 1, "act_int8": 1}, rows=24, T=350)
         others["projector"] = time_projector(dev, stream, hbm_peak)
     cpu = cpu6 = None
     if not args.no_cpu_baseline:
@@ -549,8 +558,8 @@ def run_ours(args, rank, world):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 activations x Q8_0/Q4_0 weights, f32 accumulate", "data": "synthetic",
-        "config": dict(HEADLINE_CONFIG if (args.workload == WORKLOAD and not args.rows and not args.kv_int8)
-                       else {"workload": wl.name + (" INT8 KV" if args.kv_int8 else ""), "rows": rows,
+        "config": dict(HEADLINE_CONFIG if (args.workload == WORKLOAD and not args.rows and not over)
+                       else {"workload": wl_label(wl), "rows": rows,
                              "prefix": cfg.prefix_len, "ring": cfg.ring_len},
                        global_batch=rows * world, positions=[p0, p0 + K - 1],
                        parallelism="replicas" if world > 1 else "single",
@@ -581,9 +590,11 @@ def run_ours(args, rank, world):
 # ------------------------------------------------------------------ other workloads
 def run_sweep(args):
     """One extra JSON line per workload (not the benchmark line): the sink decoder at
-    1 and 64 rows with 350 and 3000 cached tokens.  Each times `--steps` decode steps
-    (capped at 24) after 4 warm-up steps with CUDA events on the caller's stream;
-    inputs are resident on the device."""
+    1 and 64 rows with 350 and 3000 cached tokens, and at the Falcon-OCR card's
+    1 / 6 / 12 / 24 rows with 350 cached tokens in its own serving setting (INT8 KV
+    cache, dynamic int8 activations).  Each times `--steps` decode steps (capped at
+    24) after 4 warm-up steps with CUDA events on the caller's stream; inputs are
+    resident on the device."""
     import torch
 
     from quantized_moe_decode_gb300 import binding, build
@@ -594,11 +605,15 @@ def run_sweep(args):
     stream = torch.cuda.current_stream()
     hbm_peak, _ = peaks()
     K, W = min(args.steps, 24), 4
-    cases = [("sink", dict(rows=1, T=350)), ("sink", dict(rows=64, T=350)), ("sink", dict(rows=1, T=3000)),
-             ("sink", dict(rows=64, T=3000))]
-    for name, kw in cases:
+    falcon = {"kv_int8": 1, "act_int8": 1}
+    cases = [("sink", dict(rows=1, T=350), None), ("sink", dict(rows=64, T=350), None),
+             ("sink", dict(rows=1, T=3000), None), ("sink", dict(rows=64, T=3000), None)]
+    cases += [("sink", dict(rows=r, T=350), falcon) for r in (1, 6, 12, 24, 64)]
+    for name, kw, over in cases:
         t0 = time.perf_counter()
         wl = synth.workload(name, steps=K + W, **kw)
+        if over:
+            wl.cfg = wl.cfg.replace(**over)
         cfg, rows = wl.cfg, wl.rows
         ctx = binding.Context(cfg, max_rows=rows, stream=stream.cuda_stream, device=0)
         binding.load_workload(ctx, wl)
@@ -651,7 +666,7 @@ def run_sweep(args):
                     for l in range(cfg.n_layers) if not cfg.is_dense(l)}
         step_bytes = sum(sum(v) for v in class_bytes(cfg, rows, [last] * rows, distinct).values())
         gbs = step_bytes / (ms * 1e-3) / 1e9
-        print(json.dumps({"sweep": wl.name, "rows": rows, "cached_prefix": cfg.prefix_len, "steps": K,
+        print(json.dumps({"sweep": wl_label(wl), "rows": rows, "cached_prefix": cfg.prefix_len, "steps": K,
                           "positions": [start + W, last], "ms_per_step": ms, "tokens_per_s": rows / (ms * 1e-3),
                           "bytes_per_step": step_bytes, "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak,
                           "setup_s": round(time.perf_counter() - t0, 1)}), flush=True)
@@ -671,6 +686,7 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, help="measure another named workload instead (profiling runs)")
     ap.add_argument("--rows", type=int, default=0, help="rows of that workload (0: its own)")
     ap.add_argument("--kv-int8", action="store_true", help="with an INT8 KV cache")
+    ap.add_argument("--act-int8", action="store_true", help="with dynamic int8 activations")
     ap.add_argument("--cpu-sample", nargs=2, type=float, help=argparse.SUPPRESS)
     ap.add_argument("--sweep", action="store_true", help="time the other workloads (extra JSON lines) instead")
     args = ap.parse_args()

@@ -165,6 +165,13 @@ typedef struct {
      2048 -> 1280; "Quantizzazione": the Q8 profile covers the projector)       */
   int32_t proj_in;         /* input width, multiple of 64 (0 = no projector)     */
   int32_t fmt_proj;        /* uocr_format of UOCR_T_PROJ                         */
+  /* dynamic int8 activations ([Falcon] "How it is meant to be run": the linear
+     layers' inputs quantised dynamically in groups of 32).  1: the inputs of
+     the dense projections (Q/K/V, O, dense gate/up and down) are quantised
+     per group of 32 (s = max|x| / 127, code = round(x / s), fp32 decisions)
+     and multiplied on the int8 tensor cores; fmt_attn and fmt_dense must then
+     be quantised formats.  Router, experts, LM head and projector unchanged. */
+  int32_t act_int8;
 } uocr_config;
 
 typedef struct {

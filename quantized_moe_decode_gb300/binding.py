@@ -36,7 +36,7 @@ class uocr_config(C.Structure):
         "prefix_len", "ring_len", "max_rows", "use_sink")] + [
         ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("mem_budget", C.c_uint64),
         ("stream", C.c_void_p), ("device", C.c_int32), ("use_graphs", C.c_int32), ("kv_int8", C.c_int32),
-        ("proj_in", C.c_int32), ("fmt_proj", C.c_int32)]
+        ("proj_in", C.c_int32), ("fmt_proj", C.c_int32), ("act_int8", C.c_int32)]
 
 
 class uocr_tensor(C.Structure):
@@ -119,6 +119,7 @@ def make_config(cfg, *, max_rows=None, mem_budget=0, stream=0, device=0, use_gra
     c.kv_int8 = int(getattr(cfg, "kv_int8", 0))
     c.proj_in = int(getattr(cfg, "proj_in", 0))
     c.fmt_proj = int(getattr(cfg, "fmt_proj", 1))
+    c.act_int8 = int(getattr(cfg, "act_int8", 0))
     return c
 
 

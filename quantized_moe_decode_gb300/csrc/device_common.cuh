@@ -29,6 +29,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace uocr {
 
 enum Fmt : int { F16 = 0, Q8_0 = 1, Q4_0 = 2, I8ASYM = 3 };
@@ -135,6 +137,27 @@ __device__ __forceinline__ void mma_16816_z(float (&d)[4], const uint32_t (&a)[4
       "{%10,%10,%10,%10};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+}
+
+// int8 tensor-core MMA, m16n8k32, int32 accumulate from zero: A signed or
+// unsigned bytes (ASIGNED), B signed bytes.
+template <bool ASIGNED>
+__device__ __forceinline__ void mma_i8_z(int (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  const int z = 0;
+  if constexpr (ASIGNED)
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(z));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(z));
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t& r0, uint32_t& r1, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(smem_u32(p)));
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
@@ -455,6 +478,320 @@ __device__ __forceinline__ void unit_mma(float (&acc)[NT][4], const uint8_t* a, 
   }
 }
 
+// ------------------------------------------------------------------ int8 activations
+// Dynamic int8 activations ("Falcon-OCR INT8 OpenVINO IR": the linear layers'
+// inputs are quantised dynamically in groups of 32): each group of 32 inputs
+// of a row has a scale s = max|x| / 127 and codes round(x / s), and the
+// product runs on the int8 tensor cores (m16n8k32, exact int32 per group).
+//
+// The k order inside a group: lane (g, t) of a packed 8-bit unit holds, per
+// row, the codes of k = 2t, 2t+1, 2t+8, 2t+9 (and 16 + the same); a Q4_0 word's
+// low / high nibbles give k = 2t, 2t+8, 2t+1, 2t+9.  The int8 A fragment wants
+// "virtual" k = 4t .. 4t+3 (and 16 + the same), so virtual position v stands
+// for the real k those bytes hold, and the activation codes of a group are
+// staged at the same virtual positions: the sum over k is unchanged.
+template <int FMT>
+__host__ __device__ __forceinline__ int act_vpos(int k) {  // real k (0..31) -> virtual position
+  const int h = k & 16, kk = k & 15;
+  const int hi8 = kk >> 3, t = (kk & 7) >> 1, odd = kk & 1;
+  const int j = FMT == Q4_0 ? (odd ? 2 : 0) + hi8 : hi8 * 2 + odd;
+  return h + 4 * t + j;
+}
+
+// Activation codes staged in shared memory: xq[row][ldq] int8 (ldq = K + 16;
+// groups of 32 in virtual order), scales sc[group][ldr] fp32 and code sums
+// sm[group][ldr] int32 (ldr = the padded row count; rows 2t, 2t+1 adjacent).
+struct BSmemI8 {
+  const uint8_t* lane_base;  // this lane's ldmatrix row address at k = 0, n-tile 0
+  int nt_stride;             // bytes between n-tiles (8 rows)
+  const float* sc;
+  const int* sm;
+  int ldr;
+  __device__ __forceinline__ BSmemI8(const int8_t* xq, int ldq, const float* sc_, const int* sm_, int ldr_)
+      : lane_base(reinterpret_cast<const uint8_t*>(xq) + (threadIdx.x & 7) * ldq + 16 * ((threadIdx.x & 31) >> 3)),
+        nt_stride(8 * ldq),
+        sc(sc_),
+        sm(sm_),
+        ldr(ldr_) {}
+};
+
+__device__ __forceinline__ BSmemI8 make_bsmem_i8(const uint8_t* base, int ntok_pad, int K) {
+  const float* sc = reinterpret_cast<const float*>(base + ntok_pad * (K + 16));
+  return BSmemI8(reinterpret_cast<const int8_t*>(base), K + 16, sc, reinterpret_cast<const int*>(sc + (K / 32) * ntok_pad),
+                 ntok_pad);
+}
+
+// Bytes of the int8 staging of ntok_pad rows of K inputs (codes, scales, sums).
+__host__ __device__ __forceinline__ int act_i8_codes_bytes(int ntok_pad, int K) { return ntok_pad * (K + 16); }
+__host__ __device__ __forceinline__ int act_i8_bytes(int ntok_pad, int K) {
+  return act_i8_codes_bytes(ntok_pad, K) + 2 * (K / 32) * ntok_pad * 4;
+}
+
+// One unit against int8 activations: Q8_0 / I8ASYM units hold one group of 32,
+// Q4_0 units two.  acc[nt][i] follows the C fragment as in unit_mma.
+template <int FMT, int NT>
+__device__ __forceinline__ void unit_mma_i8(float (&acc)[NT][4], const uint8_t* a, const uint8_t* scp,
+                                            const BSmemI8& bp, int kk, int lane, int nt_used) {
+  static_assert(FMT == Q8_0 || FMT == Q4_0 || FMT == I8ASYM, "int8 activations need 8- or 4-bit weight codes");
+  const uint4 q = lds128(a + lane * 16);
+  const int t = lane & 3;
+  if constexpr (FMT == Q8_0 || FMT == I8ASYM) {
+    const uint32_t A[4] = {__byte_perm(q.x, q.y, 0x5410), __byte_perm(q.x, q.y, 0x7632),
+                           __byte_perm(q.z, q.w, 0x5410), __byte_perm(q.z, q.w, 0x7632)};
+    float d_lo, d_hi, z_lo = 0.f, z_hi = 0.f;
+    if constexpr (FMT == Q8_0) {
+      const uint32_t sv = *reinterpret_cast<const uint32_t*>(scp);
+      d_lo = half_lo(sv);
+      d_hi = half_hi(sv);
+    } else {
+      const uint2 sv = *reinterpret_cast<const uint2*>(scp);
+      d_lo = half_lo(sv.x);
+      d_hi = half_hi(sv.x);
+      z_lo = half_lo(sv.y);
+      z_hi = half_hi(sv.y);
+    }
+    const int grp = kk >> 5;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      if (NT == 1 || nt < nt_used) {
+        uint32_t b0, b1;
+        ldsm_x2(b0, b1, bp.lane_base + nt * bp.nt_stride + kk);
+        int c[4];
+        mma_i8_z<FMT == Q8_0>(c, A, b0, b1);
+        const int ix = grp * bp.ldr + nt * 8 + 2 * t;  // rows 2t, 2t+1 of the n-tile
+        const float2 sx = *reinterpret_cast<const float2*>(bp.sc + ix);
+        float c0 = (float)c[0], c1 = (float)c[1], c2 = (float)c[2], c3 = (float)c[3];
+        if constexpr (FMT == I8ASYM) {  // sum (q - z) x = sum q x - z sum x
+          const int2 m = *reinterpret_cast<const int2*>(bp.sm + ix);
+          c0 = fmaf(-z_lo, (float)m.x, c0);
+          c1 = fmaf(-z_lo, (float)m.y, c1);
+          c2 = fmaf(-z_hi, (float)m.x, c2);
+          c3 = fmaf(-z_hi, (float)m.y, c3);
+        }
+        acc[nt][0] = fmaf(d_lo * sx.x, c0, acc[nt][0]);
+        acc[nt][1] = fmaf(d_lo * sx.y, c1, acc[nt][1]);
+        acc[nt][2] = fmaf(d_hi * sx.x, c2, acc[nt][2]);
+        acc[nt][3] = fmaf(d_hi * sx.y, c3, acc[nt][3]);
+      }
+    }
+  } else {  // Q4_0: groups kk/32 and kk/32 + 1, unsigned nibbles, sum (q - 8) x = sum q x - 8 sum x
+    const uint32_t m4 = 0x0F0F0F0Fu;
+    const uint32_t A0[4] = {q.x & m4, (q.x >> 4) & m4, q.y & m4, (q.y >> 4) & m4};
+    const uint32_t A1[4] = {q.z & m4, (q.z >> 4) & m4, q.w & m4, (q.w >> 4) & m4};
+    const uint2 sv = *reinterpret_cast<const uint2*>(scp);
+    const float d0_lo = half_lo(sv.x), d0_hi = half_hi(sv.x), d1_lo = half_lo(sv.y), d1_hi = half_hi(sv.y);
+    const int grp = kk >> 5;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      if (NT == 1 || nt < nt_used) {
+        uint32_t B[4];
+        ldsm_x4(B, bp.lane_base + nt * bp.nt_stride + kk);
+        int c[4], e[4];
+        mma_i8_z<false>(c, A0, B[0], B[1]);
+        mma_i8_z<false>(e, A1, B[2], B[3]);
+        const int ix = grp * bp.ldr + nt * 8 + 2 * t;  // group grp, rows 2t, 2t+1; group grp+1 at + ldr
+        const float2 sx = *reinterpret_cast<const float2*>(bp.sc + ix);
+        const float2 sy = *reinterpret_cast<const float2*>(bp.sc + ix + bp.ldr);
+        const int2 mx = *reinterpret_cast<const int2*>(bp.sm + ix);
+        const int2 my = *reinterpret_cast<const int2*>(bp.sm + ix + bp.ldr);
+        // int32 exact: |sum q x| <= 15 * 127 * 32
+        const float c0 = (float)(c[0] - 8 * mx.x), c1 = (float)(c[1] - 8 * mx.y);
+        const float c2 = (float)(c[2] - 8 * mx.x), c3 = (float)(c[3] - 8 * mx.y);
+        const float e0 = (float)(e[0] - 8 * my.x), e1 = (float)(e[1] - 8 * my.y);
+        const float e2 = (float)(e[2] - 8 * my.x), e3 = (float)(e[3] - 8 * my.y);
+        acc[nt][0] = fmaf(d0_lo * sx.x, c0, fmaf(d1_lo * sy.x, e0, acc[nt][0]));
+        acc[nt][1] = fmaf(d0_lo * sx.y, c1, fmaf(d1_lo * sy.y, e1, acc[nt][1]));
+        acc[nt][2] = fmaf(d0_hi * sx.x, c2, fmaf(d1_hi * sy.x, e2, acc[nt][2]));
+        acc[nt][3] = fmaf(d0_hi * sx.y, c3, fmaf(d1_hi * sy.y, e3, acc[nt][3]));
+      }
+    }
+  }
+}
+
+// A unit against whichever activations the B provider stages.
+template <int FMT, int NT, class BP>
+__device__ __forceinline__ void unit_any(float (&acc)[NT][4], const uint8_t* a, const uint8_t* sc, const BP& bp, int kk,
+                                         int lane, int nt_used) {
+  if constexpr (std::is_same<BP, BSmemI8>::value)
+    unit_mma_i8<FMT, NT>(acc, a, sc, bp, kk, lane, nt_used);
+  else
+    unit_mma<FMT, NT>(acc, a, sc, bp, kk, lane, nt_used);
+}
+
+// Codes of one group of 32 inputs held by 4 lanes (lane q = lane & 3 holds the
+// inputs 8q .. 8q+7 as P0 = codes 0..3, P1 = codes 4..7) -> the 8 bytes this
+// lane stores at virtual offset 16 (q >> 1) + 8 (q & 1): the even lane of a
+// pair builds virtual words 0-1 of its half, the odd lane words 2-3, each from
+// its own and its partner's codes (word t = real 2t, 2t+1, 2t+8, 2t+9 for
+// 8-bit codes; 2t, 2t+8, 2t+1, 2t+9 for Q4_0; see act_vpos).
+template <int FMT>
+__device__ __forceinline__ uint2 act_i8_words(uint32_t P0, uint32_t P1, int q) {
+  const bool odd = q & 1;
+  const uint32_t mine = odd ? P1 : P0;
+  const uint32_t other = __shfl_xor_sync(0xffffffffu, odd ? P0 : P1, 1);
+  const uint32_t lo = odd ? other : mine, hi = odd ? mine : other;  // even lane's codes, odd lane's codes
+  constexpr uint32_t s0 = FMT == Q4_0 ? 0x5140u : 0x5410u, s1 = FMT == Q4_0 ? 0x7362u : 0x7632u;
+  return make_uint2(__byte_perm(lo, hi, s0), __byte_perm(lo, hi, s1));
+}
+
+// round-half-even(x / s) of the IEEE quotient: the rare inputs within 2^-12 of
+// a half-integer (kept out of line so that the staging code stays small)
+static __device__ __noinline__ float act_i8_exact_code(float x, float s) { return rintf(x / s); }
+
+// Quantise 8 consecutive inputs (lane q of a 4-lane group of 32) and store the
+// group's codes, scale and code sum.  on: the lane's group lies inside the row
+// (whole groups only, so the 4 lanes agree).
+template <int FMT>
+__device__ __forceinline__ void act_i8_group(const float (&h)[8], bool on, uint8_t* gq, float* gsc, int* gsm) {
+  const int q = threadIdx.x & 3;
+  float m = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(h[e]));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  // fp32 decisions: code = round-half-even(x / s) of the IEEE quotient.  x * (1/s)
+  // lies within 3 ulp(127) < 2^-12 of that quotient, so wherever it is farther
+  // than 2^-12 from a half-integer both round to the same code; the rest take
+  // the exact divide.
+  const float sc = m / 127.0f;
+  const float inv = sc > 0.f ? 1.0f / sc : 0.f;
+  uint32_t P[2] = {0u, 0u};
+  int cs = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float y = h[e] * inv;
+    float cf = rintf(y);
+    if (fabsf(y - cf) > 0.5f - 0x1p-12f) cf = act_i8_exact_code(h[e], sc);
+    const int c = max(-127, min(127, (int)cf));
+    cs += c;
+    P[e >> 2] |= (uint32_t)(c & 0xFF) << (8 * (e & 3));
+  }
+  cs += __shfl_xor_sync(0xffffffffu, cs, 1);
+  cs += __shfl_xor_sync(0xffffffffu, cs, 2);
+  const uint2 wds = act_i8_words<FMT>(P[0], P[1], q);
+  if (on) {
+    *reinterpret_cast<uint2*>(gq + 16 * (q >> 1) + 8 * (q & 1)) = wds;
+    if (q == 0) {
+      *gsc = sc;
+      *gsm = cs;
+    }
+  }
+}
+
+// Rows tk < ntok of the CTA's token group quantised per group of 32 into the
+// layout of BSmemI8 at `base` (codes, then scales, then sums; ldr = ntok_pad);
+// rows ntok..ntok_pad hold zero codes and scales.  NORM: RMSNorm of fp32 rows
+// (weight w) rounded to fp16 as the fp16 staging rounds them; else fp16 rows.
+// All warps share the (row, 256-input chunk) items, two in flight per warp, so
+// a single row costs one load latency per pass, not one per 128 inputs.
+constexpr int kActChunk = 256;
+constexpr int kActMaxChunks = 32;  // K <= 8192
+template <int FMT, bool NORM>
+__device__ __forceinline__ void stage_act_i8(uint8_t* base, const float* xf, const __half* xh, int lds, int ntok,
+                                             int ntok_pad, const __half* w, int K, float eps) {
+  __shared__ float s_part[16 * kActMaxChunks];  // per (row, chunk) sums of squares (NORM)
+  __shared__ float s_r[16];                     // per row 1 / rms (NORM)
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5, lane = threadIdx.x & 31;
+  const int ng = K / 32, ldq = K + 16, nch = (K + kActChunk - 1) / kActChunk;
+  uint8_t* xq = base;
+  float* xsc = reinterpret_cast<float*>(base + act_i8_codes_bytes(ntok_pad, K));
+  int* xsm = reinterpret_cast<int*>(xsc + ng * ntok_pad);
+  for (int tk = ntok + warp; tk < ntok_pad; tk += nw) {  // padding rows
+    for (int i = lane; i < K / 16; i += 32) *reinterpret_cast<uint4*>(xq + tk * ldq + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = lane; i < ng; i += 32) {
+      xsc[i * ntok_pad + tk] = 0.f;
+      xsm[i * ntok_pad + tk] = 0;
+    }
+  }
+  const int items = ntok * nch;
+  constexpr int NI = NORM ? 4 : 8;  // items in flight per warp
+  if constexpr (NORM) {
+    for (int i0 = warp; i0 < items; i0 += NI * nw) {
+      float4 v[NI][2];
+#pragma unroll
+      for (int u = 0; u < NI; ++u) {
+        const int it = i0 + u * nw, tk = it / nch, k0 = (it - tk * nch) * kActChunk + 8 * lane;
+        const bool on = it < items && k0 < K;
+        const float4* src = reinterpret_cast<const float4*>(xf + (size_t)tk * lds + k0);
+        v[u][0] = on ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u][1] = on ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < NI; ++u) {
+        const int it = i0 + u * nw;
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) ss += v[u][j].x * v[u][j].x + v[u][j].y * v[u][j].y + v[u][j].z * v[u][j].z + v[u][j].w * v[u][j].w;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0 && it < items) s_part[(it / nch) * kActMaxChunks + it % nch] = ss;
+      }
+    }
+    __syncthreads();
+    if ((int)threadIdx.x < ntok) {
+      float ss = 0.f;
+      for (int c = 0; c < nch; ++c) ss += s_part[threadIdx.x * kActMaxChunks + c];
+      s_r[threadIdx.x] = rsqrtf(ss / (float)K + eps);
+    }
+    __syncthreads();
+  }
+  for (int i0 = warp; i0 < items; i0 += NI * nw) {
+    // raw loads of all NI items first (one latency per pass), then quantise
+    uint4 raw[NI][NORM ? 3 : 1];
+#pragma unroll
+    for (int u = 0; u < NI; ++u) {
+      const int it = i0 + u * nw, tk = it / nch, k0 = (it - tk * nch) * kActChunk + 8 * lane;
+      const bool on = it < items && k0 < K;
+      if constexpr (NORM) {
+        const uint4* src = reinterpret_cast<const uint4*>(xf + (size_t)tk * lds + k0);
+        raw[u][0] = on ? src[0] : make_uint4(0u, 0u, 0u, 0u);
+        raw[u][1] = on ? src[1] : make_uint4(0u, 0u, 0u, 0u);
+        raw[u][2] = on ? *reinterpret_cast<const uint4*>(w + k0) : make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        raw[u][0] = on ? *reinterpret_cast<const uint4*>(xh + (size_t)tk * lds + k0) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    // one item at a time through a rotating window (raw[0] is the current item), in a
+    // rolled loop: the quantiser's code is run once per CTA from a cold instruction cache
+#pragma unroll 1
+    for (int u = 0; u < NI; ++u) {
+      const int it = i0 + u * nw, tk = it / nch, k0 = (it - tk * nch) * kActChunk + 8 * lane;
+      if (it >= items) break;  // warp-uniform: no later item of this pass is valid either
+      const bool on = k0 < K;
+      float h[8];
+      if constexpr (NORM) {
+        const uint32_t xr[8] = {raw[0][0].x, raw[0][0].y, raw[0][0].z, raw[0][0].w,
+                                raw[0][1].x, raw[0][1].y, raw[0][1].z, raw[0][1].w};
+        const uint32_t wr[4] = {raw[0][2].x, raw[0][2].y, raw[0][2].z, raw[0][2].w};
+        const float r = on ? s_r[tk] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // fp16(x * r * w), the value the fp16 staging stores
+          const __half2 wj = u32_h2(wr[j]);
+          const float2 f = __half22float2(__floats2half2_rn(__uint_as_float(xr[2 * j]) * r * __low2float(wj),
+                                                            __uint_as_float(xr[2 * j + 1]) * r * __high2float(wj)));
+          h[2 * j] = f.x;
+          h[2 * j + 1] = f.y;
+        }
+      } else {
+        const uint32_t hr[4] = {raw[0][0].x, raw[0][0].y, raw[0][0].z, raw[0][0].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __half22float2(u32_h2(hr[j]));
+          h[2 * j] = f.x;
+          h[2 * j + 1] = f.y;
+        }
+      }
+      const int g = k0 >> 5;  // group of 32 (the 4 lanes of this group agree on `on`)
+      act_i8_group<FMT>(h, on, xq + tk * ldq + 32 * g, xsc + g * ntok_pad + tk, xsm + g * ntok_pad + tk);
+#pragma unroll
+      for (int j = 0; j + 1 < NI; ++j) {
+#pragma unroll
+        for (int c = 0; c < (NORM ? 3 : 1); ++c) raw[j][c] = raw[j + 1][c];
+      }
+    }
+  }
+}
+
 template <int NT>
 __device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
 #pragma unroll
@@ -626,8 +963,8 @@ __device__ __forceinline__ void run_stream(UnitStream<FMT>& us, const SlabWork& 
         cp_wait<kRingDepth - 2>();  // units i and i+1 have landed (this lane's bytes)
         uint8_t* s0 = next_slot();
         uint8_t* s1 = next_slot();
-        unit_mma<FMT, NT>(acc, s0, s0 + 512 + lane * 8, bp, (k0 + i) * KU, lane, nt_used);
-        unit_mma<FMT, NT>(acc, s1, s1 + 512 + lane * 8, bp, (k0 + i + 1) * KU, lane, nt_used);
+        unit_any<FMT, NT>(acc, s0, s0 + 512 + lane * 8, bp, (k0 + i) * KU, lane, nt_used);
+        unit_any<FMT, NT>(acc, s1, s1 + 512 + lane * 8, bp, (k0 + i + 1) * KU, lane, nt_used);
         us.fetch_next(s0, lane);  // refill both with the units kRingDepth ahead
         us.fetch_next(s1, lane);
       }
@@ -635,7 +972,7 @@ __device__ __forceinline__ void run_stream(UnitStream<FMT>& us, const SlabWork& 
     for (; i < w.uw; ++i) {
       cp_wait<kRingDepth - 1>();  // unit i has landed (this lane's bytes)
       uint8_t* s0 = next_slot();
-      unit_mma<FMT, NT>(acc, s0, s0 + 512 + lane * 8, bp, (k0 + i) * KU, lane, nt_used);
+      unit_any<FMT, NT>(acc, s0, s0 + 512 + lane * 8, bp, (k0 + i) * KU, lane, nt_used);
       us.fetch_next(s0, lane);  // refill it with the unit kRingDepth ahead
     }
     float* rb = gred + par * w.ks * (NT * 128);

@@ -258,6 +258,12 @@ static uocr_status check_config(uocr_ctx* ctx, const uocr_config& c) {
   if (c.use_sink != 0 && c.use_sink != 1) return bad("use_sink must be 0 or 1");
   if (!(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f)) return bad("rms_eps >= 0 and rope_theta > 0 required");
   if (c.kv_int8 != 0 && c.kv_int8 != 1) return bad("kv_int8 must be 0 or 1");
+  if (c.act_int8 != 0 && c.act_int8 != 1) return bad("act_int8 must be 0 or 1");
+  if (c.act_int8 && (!quant_fmt(c.fmt_attn) || (has_dense && !quant_fmt(c.fmt_dense))))
+    return bad("act_int8 needs quantised fmt_attn and fmt_dense (int8 codes against int8 activations)");
+  if (c.act_int8 && (c.hidden > kActMaxChunks * kActChunk || c.n_heads * c.head_dim > kActMaxChunks * kActChunk ||
+                     (has_dense && c.dense_inter > kActMaxChunks * kActChunk)))
+    return bad("act_int8: projection inputs are limited to 8192");
   if (c.proj_in < 0 || c.proj_in % 64) return bad("proj_in must be 0 or a positive multiple of 64");
   if (c.proj_in > 0) {
     if (!quant_fmt(c.fmt_proj)) return bad("fmt_proj must be a quantised format");
@@ -474,7 +480,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     qa.kv_new = kv8l ? ctx->kv_new : nullptr;
     qa.status = ctx->status;
     if (want("qkv")) {
-      CK(launch_gemv(kf(c.fmt_attn), SRC_NORM, EPI_QKV, qa, gx_for(w.qkv.n_slabs), tg, st, pdl), "qkv launch");
+      CK(launch_gemv(kf(c.fmt_attn), c.act_int8 ? SRC_NORM_I8 : SRC_NORM, EPI_QKV, qa, gx_for(w.qkv.n_slabs), tg, st, pdl), "qkv launch");
     }
     if (kv8l) {  // INT8 cache: quantise the new keys / values into their slots
       KvQuantArgs ka{};
@@ -539,7 +545,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     oa.ld_out = H;
     oa.status = ctx->status;
     if (want("o_proj")) {
-      CK(launch_gemv(kf(c.fmt_attn), SRC_F16, EPI_RESID, oa, gx_for(w.o.n_slabs), tg, st, pdl), "o_proj launch");
+      CK(launch_gemv(kf(c.fmt_attn), c.act_int8 ? SRC_F16_I8 : SRC_F16, EPI_RESID, oa, gx_for(w.o.n_slabs), tg, st, pdl), "o_proj launch");
     }
     if (w.dense) {
       GemvArgs ga{};
@@ -554,7 +560,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       ga.ld_out = c.dense_inter;
       ga.status = ctx->status;
       if (want("mlp_gate_up")) {
-        CK(launch_gemv(kf(c.fmt_dense), SRC_NORM, EPI_SWIGLU, ga, gx_for(w.gateup.n_slabs), tg, st, pdl),
+        CK(launch_gemv(kf(c.fmt_dense), c.act_int8 ? SRC_NORM_I8 : SRC_NORM, EPI_SWIGLU, ga, gx_for(w.gateup.n_slabs), tg, st, pdl),
            "gate/up launch");
       }
       GemvArgs da{};
@@ -568,7 +574,7 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       da.ld_out = H;
       da.status = ctx->status;
       if (want("mlp_down")) {
-        CK(launch_gemv(kf(c.fmt_dense), SRC_F16, EPI_RESID, da, gx_for(w.down.n_slabs), tg, st, pdl), "down launch");
+        CK(launch_gemv(kf(c.fmt_dense), c.act_int8 ? SRC_F16_I8 : SRC_F16, EPI_RESID, da, gx_for(w.down.n_slabs), tg, st, pdl), "down launch");
       }
     } else {
       const int E = c.n_experts, k = c.top_k;

@@ -15,6 +15,10 @@
 // place; only the new token's K/V are produced); "How it is meant to be run"
 // (the rows of a step share one read of the weights).
 //
+// With dynamic int8 activations ("Falcon-OCR INT8 OpenVINO IR": the linear
+// layers' inputs quantised per group of 32) the staged rows are int8 codes with
+// fp32 scales and the units run on the int8 tensor cores (the _I8 sources).
+//
 // Each persistent CTA owns slabs blockIdx.x, +gridDim.x, ...; each warp streams
 // its units through its own shared-memory ring filled by 16-byte cp.async
 // copies, the first ones issued before the CTA waits for the kernel that
@@ -51,6 +55,8 @@ StreamPlan plan_stream(int nt, int fmt, int k_stage, int n_rows_list, int extra_
 
 template <int FMT, int NT, int SRC, int EPI>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a) {
+  constexpr bool A8 = SRC == SRC_NORM_I8 || SRC == SRC_F16_I8;
+  constexpr bool NORM = SRC == SRC_NORM || SRC == SRC_NORM_I8;
   extern __shared__ __align__(128) unsigned char smem[];
   const StreamPlan& p = a.sp;
   __shared__ int s_last;
@@ -72,6 +78,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
   us.prefetch(ring, p.slot, w, lane);
   NormW nw;
   if constexpr (SRC == SRC_NORM) load_norm_w(nw, a.norm_w, K);
+  (void)nw;
 
   pdl_wait();  // activations come from the previous kernel
   int* s_pos = reinterpret_cast<int*>(smem + p.rows_off);
@@ -83,14 +90,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
   if constexpr (EPI == EPI_LOGITS) {
     if (threadIdx.x < NT * 8) s_best[threadIdx.x] = 0ull;
   }
-  if constexpr (SRC == SRC_NORM) {
+  if constexpr (A8) {  // the int8 staging fits in the fp16 staging area
+    stage_act_i8<FMT, NORM>(smem + p.xs_off, NORM ? a.xf + (size_t)tok0 * a.ld_src : nullptr,
+                            NORM ? nullptr : a.xh + (size_t)tok0 * a.ld_src, a.ld_src, ntok, NT * 8, a.norm_w, K, a.eps);
+  } else if constexpr (SRC == SRC_NORM) {
     stage_norm_rows(xs, p.ldx, a.xf + (size_t)tok0 * a.ld_src, a.ld_src, ntok, NT * 8, a.norm_w, nw, K, a.eps);
   } else {
     stage_f16(xs, p.ldx, a.xh + (size_t)tok0 * a.ld_src, a.ld_src, ntok, NT * 8, K);
   }
   __syncthreads();
 
-  const BSmem bp(xs, p.ldx);
   auto epi = [&](int s, const float* rb, int tid, int nthr) {
     for (int i = tid; i < NT * 64; i += nthr) {
       const int tok = i >> 3, pg = i & 7;
@@ -154,7 +163,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
       }
     }
   };
-  run_stream<FMT, NT>(us, w, ring, p.slot, red, bp, NT, epi);
+  if constexpr (A8) {
+    const BSmemI8 bp = make_bsmem_i8(smem + p.xs_off, NT * 8, K);
+    run_stream<FMT, NT>(us, w, ring, p.slot, red, bp, NT, epi);
+  } else {
+    const BSmem bp(xs, p.ldx);
+    run_stream<FMT, NT>(us, w, ring, p.slot, red, bp, NT, epi);
+  }
   if (kPdlLate & PDL_GEMV) pdl_launch_dependents();
 
   if constexpr (EPI == EPI_LOGITS) {
@@ -199,6 +214,11 @@ static cudaError_t dispatch_epi(int src, int epi, const GemvArgs& a, int gx, int
   if (src == SRC_NORM && epi == EPI_QKV) return launch_one<FMT, NT, SRC_NORM, EPI_QKV>(a, gx, gy, st, pdl);
   if (src == SRC_F16 && epi == EPI_RESID) return launch_one<FMT, NT, SRC_F16, EPI_RESID>(a, gx, gy, st, pdl);
   if (src == SRC_NORM && epi == EPI_SWIGLU) return launch_one<FMT, NT, SRC_NORM, EPI_SWIGLU>(a, gx, gy, st, pdl);
+  if constexpr (FMT != F16) {
+    if (src == SRC_NORM_I8 && epi == EPI_QKV) return launch_one<FMT, NT, SRC_NORM_I8, EPI_QKV>(a, gx, gy, st, pdl);
+    if (src == SRC_F16_I8 && epi == EPI_RESID) return launch_one<FMT, NT, SRC_F16_I8, EPI_RESID>(a, gx, gy, st, pdl);
+    if (src == SRC_NORM_I8 && epi == EPI_SWIGLU) return launch_one<FMT, NT, SRC_NORM_I8, EPI_SWIGLU>(a, gx, gy, st, pdl);
+  }
   if constexpr (NT == 2 && FMT != F16) {
     if (src == SRC_F16 && epi == EPI_BIAS_F16) return launch_one<FMT, NT, SRC_F16, EPI_BIAS_F16>(a, gx, gy, st, pdl);
   }
@@ -234,6 +254,11 @@ static cudaError_t set_attr_fmt() {
   UOCR_SET(SRC_NORM, EPI_QKV)
   UOCR_SET(SRC_F16, EPI_RESID)
   UOCR_SET(SRC_NORM, EPI_SWIGLU)
+  if constexpr (FMT != F16) {
+    UOCR_SET(SRC_NORM_I8, EPI_QKV)
+    UOCR_SET(SRC_F16_I8, EPI_RESID)
+    UOCR_SET(SRC_NORM_I8, EPI_SWIGLU)
+  }
   if constexpr (NT == 2 && FMT != F16) {
     UOCR_SET(SRC_F16, EPI_BIAS_F16)
   }

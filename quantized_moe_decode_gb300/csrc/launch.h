@@ -25,7 +25,9 @@ struct StreamPlan {
 
 StreamPlan plan_stream(int nt, int fmt, int k_stage, int n_rows_list = 0, int extra_bytes = 0);
 
-enum Src : int { SRC_NORM = 0, SRC_F16 = 1 };
+// Projection inputs: RMSNorm of fp32 rows, or fp16 rows; the _I8 forms
+// quantise them to int8 per group of 32 and run the int8 tensor-core product.
+enum Src : int { SRC_NORM = 0, SRC_F16 = 1, SRC_NORM_I8 = 2, SRC_F16_I8 = 3 };
 enum Epi : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3, EPI_BIAS_F16 = 4 };
 
 struct GemvArgs {

@@ -27,6 +27,18 @@ Comparison rules (the decode-step statement's tolerances):
   2 d (to first order: dw_i = w_i (dl_i - sum_j w_j dl_j)), so there the
   weights are held to max(2e-3, 2 d) with the logits themselves at the
   stated tolerance;
+* dynamic int8 activations (the Falcon-OCR card's groups of 32): both sides
+  take the code decisions in fp32, but on inputs that agree only to rounding
+  (fp16 activations of an fp32 and a float64 residual stream), so an input
+  near a rounding boundary of the code grid can land one code step apart.  One
+  step moves the projection by s * w (s = group max / 127): a full grid step,
+  sqrt(12) times the rms error the grid itself adds per input.  A fraction f
+  of codes one step apart moves the output by about sqrt(12 f) * eps_q, with
+  eps_q = (group max / rms) / (127 sqrt 12) ~ 0.5-0.7% the grid's own relative
+  error on these activations; f up to 25% stays within 1e-2.  So int8-
+  activation runs hold every vector to rel-L2 <= 1e-2 (max-abs unchanged) and
+  the median over all compared vectors to the plain 2e-3; a wrong scale, zero
+  point or k order errs by tens of percent;
 * a router set that differs at a near tie is counted, not failed; it changes
   that row's layer output, so the rest of the row's layers at that step are
   not compared, and before the next step the library's cache entries of the
@@ -42,6 +54,8 @@ import numpy as np
 import oracle
 
 REL_L2 = 2e-3
+REL_L2_INT8_ACT = 1e-2  # per vector with int8 activations (median still <= REL_L2)
+_active_rel = [REL_L2]  # the per-vector bound of the run in progress
 oracle_kv_quant = oracle.kv_quant  # entries of values the oracle's INT8 cache holds (scale * code: idempotent)
 MAX_ABS = 2e-2
 ROUTER_GAP = oracle.TIE_TOL  # router sets are compared where the oracle's gap exceeds it
@@ -56,7 +70,8 @@ def rel_l2(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
-def check_close(name, got, want, rel=REL_L2, mx=MAX_ABS):
+def check_close(name, got, want, rel=None, mx=MAX_ABS):
+    rel = _active_rel[0] if rel is None else rel
     got = np.asarray(got, np.float64)
     want = np.asarray(want, np.float64)
     assert got.shape == want.shape, (name, got.shape, want.shape)
@@ -84,9 +99,11 @@ class Stats:
     tainted_rows: set = field(default_factory=set)
 
     worst_name: str = ""
+    rels: list = field(default_factory=list)  # rel-L2 of every compared vector
 
     def note(self, e, m, name=""):
         self.float_checks += 1
+        self.rels.append(e)
         if e > self.worst_rel:
             self.worst_name = name
         self.worst_rel = max(self.worst_rel, e)
@@ -393,13 +410,29 @@ def compare_prefill(ctx, cfg, res, lib_rows, lib_next, lib_logits, stats, row_ma
                 stats.note(*check_close(f"prefill row {last} layer {l} output", g, res.hidden[l + 1][i:i + 1]))
 
 
-def run_parity(ctx, wl, steps, oracle_model, rows=None, row_map=None, check_kv=True, log=None,
-               same_router_input=False, lib_prefill=False):
+def run_parity(ctx, wl, steps, oracle_model, **kw):
     """Run `steps` decode steps (plus the prefill-by-decode prefix when the
     workload has one) on both sides and compare.  With lib_prefill the library
     builds the prefix with uocr_prefill (one call per row and input kind)
     while the oracle takes its decode steps, and the two are compared once
-    the prefix is complete.  Returns Stats."""
+    the prefix is complete.  Workloads with int8 activations take their own
+    per-vector bound and must keep the median within the plain one.  Returns
+    Stats."""
+    a8 = bool(getattr(wl.cfg, "act_int8", 0))
+    _active_rel[0] = REL_L2_INT8_ACT if a8 else REL_L2
+    try:
+        st = _run_parity(ctx, wl, steps, oracle_model, **kw)
+    finally:
+        _active_rel[0] = REL_L2
+    if a8:
+        med = float(np.median(st.rels))
+        print(f"int8 activations: median rel-L2 {med:.2e}, 99th percentile {np.percentile(st.rels, 99):.2e}")
+        assert med <= REL_L2, f"median rel-L2 {med:.3e} above {REL_L2} with int8 activations"
+    return st
+
+
+def _run_parity(ctx, wl, steps, oracle_model, rows=None, row_map=None, check_kv=True, log=None,
+                same_router_input=False, lib_prefill=False):
     cfg = wl.cfg
     runner = GpuRunner(ctx, wl, rows)
     n_or = oracle_model.rows

@@ -39,6 +39,11 @@ def test_invalid_config_is_rejected_on_the_host(libuocr):
     with pytest.raises(binding.UocrError) as e:
         binding.Context(moe.replace(fmt_routed=synth.F16))
     assert e.value.status == binding.UOCR_E_INVALID_ARG
+    # int8 activations multiply int8 weight codes: fp16 projections are refused
+    for bad in (dict(act_int8=1, fmt_attn=synth.F16), dict(act_int8=1, fmt_dense=synth.F16), dict(act_int8=2)):
+        with pytest.raises(binding.UocrError) as e:
+            binding.Context(cfg.replace(**bad))
+        assert e.value.status == binding.UOCR_E_INVALID_ARG
 
 
 def test_budget_refusal_names_every_category(libuocr):

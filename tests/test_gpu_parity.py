@@ -41,7 +41,7 @@ def _run(wl, steps, **kw):
     st = run_parity(ctx, wl, steps, orc, **kw)
     print(f"\n{wl.name}: {st.steps} steps, {st.float_checks} float checks (worst rel-L2 {st.worst_rel:.2e}, "
           f"max-abs {st.worst_abs:.2e}), router {st.router_checks} ({st.router_near_ties} near ties), "
-          f"ids {st.id_checks} ({st.id_near_ties} near ties), kv {st.kv_checks}")
+          f"ids {st.id_checks} ({st.id_near_ties} near ties), kv {st.kv_checks}; worst: {st.worst_name}")
     ctx.close()
     return st
 
@@ -199,6 +199,41 @@ def test_group64_moe_both_q4_forty_rows(cuda):
     cfg = _moe(fmt_shared=G4, fmt_routed=G4, max_rows=40, vocab=0, prefix_len=9)
     wl = synth.make_workload("g64_moe40", cfg, 40, 6, 132)
     _run(wl, 6)
+
+
+# ---------------------------------------------------------------- int8 activations
+def test_int8_activations_dense_q8_attention_q4_mlp_ring_wrap(cuda):
+    cfg = _dense(act_int8=1, fmt_attn=Q8, fmt_dense=Q4)
+    wl = synth.make_workload("a8_dense", cfg, 3, 20, 140)
+    st = _run(wl, 20)
+    assert st.kv_checks == 20 * 2 * 3
+
+
+def test_int8_activations_i8asym_sink_decoder_forty_rows(cuda):
+    # three token groups (16, 16, 8) of the two-n-tile kernels; zero points corrected from code sums
+    cfg = _dense(act_int8=1, fmt_attn=I8, fmt_dense=I8, use_sink=1, max_rows=40, prefix_len=9)
+    wl = synth.make_workload("a8_sink40", cfg, 40, 8, 141)
+    _run(wl, 8)
+
+
+def test_int8_activations_with_int8_kv_sink_decoder_single_row(cuda):
+    cfg = _dense(act_int8=1, kv_int8=1, fmt_attn=I8, fmt_dense=I8, use_sink=1, max_rows=1, hidden=1024,
+                 n_heads=8, head_dim=64, dense_inter=1024, n_layers=2, n_dense_layers=2, prefix_len=33)
+    wl = synth.make_workload("a8_i8kv_sink", cfg, 1, 10, 142)
+    _code_steps_small(_run(wl, 10))
+
+
+def test_int8_activations_moe_prefill_by_decode_then_greedy(cuda):
+    wl = synth.make_workload("a8_moe_lm", _moe(act_int8=1, max_rows=12), 12, 8, 143, prefix="prefill",
+                             n_prefill_embeds=6, step_input="ids")
+    st = _run(wl, 8)
+    assert st.id_checks >= 12 * 8 and st.router_checks > 0
+
+
+def test_int8_activations_group64_blocks(cuda):
+    cfg = _dense(act_int8=1, fmt_attn=G8, fmt_dense=G4, max_rows=9)
+    wl = synth.make_workload("a8_g64", cfg, 9, 10, 144)
+    _run(wl, 10)
 
 
 # ---------------------------------------------------------------- projector
