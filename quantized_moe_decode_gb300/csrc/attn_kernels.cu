@@ -835,12 +835,14 @@ cudaError_t launch_fill_zero_ring(__half* kv_layer_row, int nh, int SL, int D, i
 cudaError_t init_gemv_attributes();
 cudaError_t init_moe_attributes();
 cudaError_t init_tc_attributes();
+cudaError_t init_tc_expert_attributes();
 
 cudaError_t init_kernel_attributes() {
   cudaError_t e = init_gemv_attributes();
   if (e == cudaSuccess) e = init_moe_attributes();
   if (e == cudaSuccess) e = init_attn_attributes();
   if (e == cudaSuccess) e = init_tc_attributes();
+  if (e == cudaSuccess) e = init_tc_expert_attributes();
   return e;
 }
 

@@ -226,12 +226,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same with a suspend-time hint: the thread sleeps until the phase
+// completes or about `ns` nanoseconds pass (waits that can last microseconds
+// leave the issue slots to the warps doing the work).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait: false after kSpinLimit polls (each poll may suspend briefly).
 constexpr uint32_t kSpinLimit = 1u << 22;
 template <uint32_t Limit = kSpinLimit>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t i = 0; i < Limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// Bounded sleeping wait: false after Limit polls of up to `ns` each.
+template <uint32_t Limit = (1u << 16)>
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  for (uint32_t i = 0; i < Limit; ++i)
+    if (mbar_try_wait_sleep(bar, parity, ns)) return true;
   return false;
 }
 

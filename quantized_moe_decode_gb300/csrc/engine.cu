@@ -171,6 +171,9 @@ struct uocr_ctx {
   bool pdl = true;  // programmatic dependent launch between the step's kernels
   int gemv_ctas_per_sm = 2;    // streaming CTAs per SM of a GEMV launch
   int expert_ctas_per_sm = 2;  // CTAs per SM an expert launch is sized for (active experts only)
+  // tensor-core expert kernels for steps of more than 16 rows (one CTA per SM)
+  bool tc_experts = false;
+  TcxPlan tcx_gu{}, tcx_dn{};
 
   int H() const { return cfg.hidden; }
   int MR() const { return cfg.max_rows; }
@@ -585,6 +588,8 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       const int max_act = E < rows * k ? E : rows * k;
       const double exp_act = E * (1.0 - pow(1.0 - (double)k / E, rows));
       const int by_slot = exp_act < 0.75 * E && tg == 1;
+      // more than 16 rows: the expert contraction on the tensor cores (expert-id units)
+      const bool tcx = ctx->tc_experts && rows > 16 && !by_slot;
       const int n_units = by_slot ? max_act : E;
       int4* rec = ctx->r_rec + (size_t)l * ((TC + 15) / 16) * E;
 
@@ -643,13 +648,16 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       // in all: one grid row covers every token group
       auto split = [&](const DMat& r, const DMat* sh, int rslabs, int sslabs) {
         const double br = (double)(r.qbytes + r.sbytes);
-        const double bs = sh ? (double)(sh->qbytes + sh->sbytes) * tg : 0.0;
+        // the shared experts are streamed once per pass: 16 rows (GEMV), 32 (tensor cores)
+        const int sh_passes = tcx ? (rows + kTcxRowsShared - 1) / kTcxRowsShared : tg;
+        const double bs = sh ? (double)(sh->qbytes + sh->sbytes) * sh_passes : 0.0;
         const double tot = units * br + bs;
-        const int gt = GE;
-        // parts of whole rounds (G_w slabs); the fewest parts that give the
-        // rounds per CTA the byte-proportional target gives
+        const int gt = tcx ? ctx->n_sm : GE;  // the tensor-core kernels run one CTA per SM
+        // parts of whole rounds (G_w slabs; a 128-row tile of 8 slabs on the tensor
+        // cores); the fewest parts that give the rounds per CTA the byte-proportional
+        // target gives
         auto parts = [&](double target, int slabs, int U) {
-          const int gw = kWarps / warps_per_slab(U);
+          const int gw = tcx ? 8 : kWarps / warps_per_slab(U);
           const int nr = (slabs + gw - 1) / gw;
           int t = (int)ceil(target);
           t = t < 1 ? 1 : t > nr ? nr : t;
@@ -679,7 +687,10 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       xa.sp = plan_stream(nt, kf(c.fmt_routed), H, 16);
       split(w.ex_gateup, shg, w.ex_gateup.n_slabs, shg ? shg->n_slabs : 0);
       if (want("expert_gate_up")) {
-        CK(launch_expert_gateup(kf(c.fmt_routed), fs, xa, st, pdl), "expert gate/up launch");
+        if (tcx)
+          CK(launch_tc_expert(0, kf(c.fmt_routed), fs, xa, ctx->tcx_gu, st, pdl), "tensor-core expert gate/up launch");
+        else
+          CK(launch_expert_gateup(kf(c.fmt_routed), fs, xa, st, pdl), "expert gate/up launch");
       }
       // down + combine
       xa.wr = w.ex_down.view(1);
@@ -690,7 +701,10 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       }
       split(w.ex_down, shd, H / 16, H / 16);
       if (want("expert_down")) {
-        CK(launch_expert_down(kf(c.fmt_routed), fs, xa, st, pdl), "expert down launch");
+        if (tcx)
+          CK(launch_tc_expert(1, kf(c.fmt_routed), fs, xa, ctx->tcx_dn, st, pdl), "tensor-core expert down launch");
+        else
+          CK(launch_expert_down(kf(c.fmt_routed), fs, xa, st, pdl), "expert down launch");
       }
       if (want("expert_combine")) {
         CK(launch_expert_combine(xa, st, pdl), "expert combine launch");
@@ -1122,6 +1136,26 @@ uocr_status uocr_create(const uocr_config* cfg, uocr_ctx** out) {
     };
     ctx->gemv_ctas_per_sm = knob("UOCR_GEMV_CTAS_PER_SM", ctx->gemv_ctas_per_sm);
     ctx->expert_ctas_per_sm = knob("UOCR_EXPERT_CTAS_PER_SM", ctx->expert_ctas_per_sm);
+    // the tensor-core expert kernels on request (UOCR_TC_EXPERTS=1) where the formats and
+    // the shared memory allow them.  Off by default: at the few rows per expert of a
+    // decode step they stream the weights at about 0.6 the speed of the fragment-GEMV
+    // kernels (dequantising into shared memory costs the SM what the mma.sync products
+    // cost it there, and one CTA per SM keeps fewer weight bytes in flight).
+    const char* tv = std::getenv("UOCR_TC_EXPERTS");
+    const bool want_tc = tv && tv[0] == '1';
+    if (want_tc && ctx->any_moe() && tcx_format_ok(kf(cfg->fmt_routed), ctx->shared_fmt())) {
+      int optin = 0;
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, cfg->device);
+      const int limit = optin - 8 * 1024;  // the kernel's static routing state and slack
+      const int H = cfg->hidden, Ie = cfg->expert_inter, Ish = cfg->n_shared * cfg->expert_inter;
+      const int bg = kTcxRowsRouted * H * 2 > kTcxRowsShared * H * 2 * (Ish > 0) ? kTcxRowsRouted * H * 2
+                                                                                  : kTcxRowsShared * H * 2;
+      const int bd = kTcxRowsRouted * Ie * 2 > kTcxRowsShared * Ish * 2 ? kTcxRowsRouted * Ie * 2
+                                                                         : kTcxRowsShared * Ish * 2;
+      ctx->tcx_gu = tcx_plan(bg, limit);
+      ctx->tcx_dn = tcx_plan(bd, limit);
+      ctx->tc_experts = ctx->tcx_gu.stages >= 2 && ctx->tcx_dn.stages >= 2;
+    }
   }
   // zero everything (KV cache, counters, argmax keys, status)
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->arena, 0, m.off, ctx->st);

@@ -197,6 +197,22 @@ struct TcLmArgs {
 int tc_lm_npad(int rows);
 int tc_lm_smem_bytes(int npad);
 cudaError_t launch_tc_lm(const TcLmArgs& a, int n_sm, cudaStream_t st, bool pdl);
+
+// Tensor-core expert kernels (steps with more than 16 rows): shared-memory plan
+// of one CTA (A stages, resident B operand of b_bytes, producer rings,
+// barriers) within smem_limit bytes; stages < 2 means it does not fit.
+struct TcxPlan {
+  int stages, a_off, b_off, ring_off, bar_off, bytes;
+};
+TcxPlan tcx_plan(int b_bytes, int smem_limit);
+bool tcx_format_ok(int fr, int fs);  // both Q8_0 / Q4_0 codes
+constexpr int kTcxRowsRouted = 16;   // token rows of a routed pass (B columns)
+constexpr int kTcxRowsShared = 32;   // ... of a shared-expert pass
+// mode 0: gate/up + SwiGLU (activations in the canonical layout, per (expert,
+// group) slot of 16 rows for routed experts, per pass of 32 rows for the
+// shared ones); mode 1: down -> fp32 partials.  Expert-id units only.
+cudaError_t launch_tc_expert(int mode, int fr, int fs, const ExpertArgs& a, const TcxPlan& pl, cudaStream_t st,
+                             bool pdl);
 cudaError_t launch_pack_canon(const void* src_f16, uint8_t* dst, int V, int K, cudaStream_t st);
 
 // Launch with or without programmatic dependent launch (the kernel may start

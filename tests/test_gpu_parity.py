@@ -236,6 +236,56 @@ def test_int8_activations_group64_blocks(cuda):
     _run(wl, 10)
 
 
+# ---------------------------------------------------------------- tensor-core experts
+# The tcgen05 expert kernels (more than 16 rows, off by default) are switched on
+# per context by UOCR_TC_EXPERTS=1, read when the context is created.
+@pytest.fixture
+def tc_experts(monkeypatch):
+    monkeypatch.setenv("UOCR_TC_EXPERTS", "1")
+
+
+def _layer_outputs(cfg, wl, tc, monkeypatch):
+    import torch
+
+    monkeypatch.setenv("UOCR_TC_EXPERTS", tc)
+    ctx = make_ctx(wl)
+    x = torch.from_numpy(np.ascontiguousarray(wl.step_x[0]).view(np.int16)).cuda()
+    pos = torch.full((wl.rows,), cfg.prefix_len, dtype=torch.int32, device="cuda")
+    y = torch.zeros((wl.rows, cfg.hidden), dtype=torch.float32, device="cuda")
+    ctx.uocr_decode_step_embeds(wl.rows, x.data_ptr(), pos.data_ptr(), y.data_ptr())
+    ctx.uocr_sync()
+    out = y.cpu().numpy().astype(np.float64)
+    ctx.close()
+    return out
+
+
+def test_tensor_core_experts_forty_rows_q4_routed_q8_shared(cuda, tc_experts):
+    cfg = _moe(max_rows=40, vocab=0, prefix_len=10)
+    wl = synth.make_workload("tcx_moe40", cfg, 40, 6, 150)
+    st = _run(wl, 6)
+    assert st.router_checks > 0 and st.grouping_checks > 0
+
+
+def test_tensor_core_experts_q8_routed_q4_shared_two_token_groups_with_lm_head(cuda, tc_experts):
+    cfg = _moe(fmt_routed=Q8, fmt_shared=Q4, max_rows=24)
+    wl = synth.make_workload("tcx_moe24_lm", cfg, 24, 6, 151, prefix="prefill", n_prefill_embeds=5,
+                             step_input="ids")
+    st = _run(wl, 6)
+    assert st.id_checks >= 24 * 6
+
+
+def test_tensor_core_experts_run_and_agree_with_the_fragment_kernels(cuda, monkeypatch):
+    cfg = _moe(max_rows=33, vocab=0, prefix_len=10)
+    wl = synth.make_workload("tcx_ab", cfg, 33, 1, 152)
+    on = _layer_outputs(cfg, wl, "1", monkeypatch)
+    off = _layer_outputs(cfg, wl, "0", monkeypatch)
+    # different kernels (the scale folded into the fp16 weight on the tensor cores):
+    # not bit-identical, within the stated tolerance of each other
+    assert np.any(on != off)
+    rel = float(np.linalg.norm(on - off) / np.linalg.norm(off))
+    assert rel <= 2e-3, rel
+
+
 # ---------------------------------------------------------------- projector
 @pytest.mark.parametrize("fmt,n", [(Q8, 40), (G4, 7), (I8, 33)])
 def test_projector_against_the_oracle(cuda, fmt, n):
