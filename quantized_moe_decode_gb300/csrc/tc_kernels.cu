@@ -34,6 +34,19 @@
 namespace uocr {
 
 // ------------------------------------------------------------------ LM-head tiling
+// UOCR_TC_SPLIT: bulk copies per 16 KB weight tile (build-time tuning)
+#ifndef UOCR_TC_SPLIT
+#define UOCR_TC_SPLIT 1
+#endif
+constexpr int kTcSplit = UOCR_TC_SPLIT;
+static_assert(kTcSplit >= 1 && kTcSplit <= 16 && (kTcTileBytes / kTcSplit) % 16 == 0, "tile copy split");
+
+// A weight tile into shared memory in kTcSplit bulk copies on one mbarrier.
+__device__ __forceinline__ void tile_g2s(uint8_t* dst, const uint8_t* src, uint64_t* bar) {
+#pragma unroll
+  for (int c = 0; c < kTcSplit; ++c)
+    bulk_g2s(dst + c * (kTcTileBytes / kTcSplit), src + c * (kTcTileBytes / kTcSplit), kTcTileBytes / kTcSplit, bar);
+}
 constexpr int kTcThreads = 192;                           // 4 epilogue warps, producer, MMA
 constexpr int kTcSmemBudget = 200 * 1024;                 // stage ring (the rest: barriers, per-warp bests)
 
@@ -123,6 +136,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_lm(const TcLmArgs a) {
   uint64_t* done = acc_empty + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
   __shared__ unsigned long long s_best[4][NPAD];
+  __shared__ float s_tr[4][32][33];  // per epilogue warp: a 32 x 32 chunk transposed (padded: no bank conflicts)
   __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -160,7 +174,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_lm(const TcLmArgs a) {
       // the weight tiles do not depend on the previous kernel: the first S go out now
       for (int i = 0; i < pre; ++i) {
         mbar_expect_tx(full + i, (uint32_t)STAGE);
-        bulk_g2s(smem + i * STAGE, a.w + tile_of(i) * kTcTileBytes, kTcTileBytes, full + i);
+        tile_g2s(smem + i * STAGE, a.w + tile_of(i) * kTcTileBytes, full + i);
       }
       pdl_wait();  // the staged activations come from k_lm_stage
       for (int i = 0; i < pre; ++i)
@@ -174,7 +188,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_lm(const TcLmArgs a) {
         }
         uint8_t* st = smem + s * STAGE;
         mbar_expect_tx(full + s, (uint32_t)STAGE);
-        bulk_g2s(st, a.w + tile_of(it) * kTcTileBytes, kTcTileBytes, full + s);
+        tile_g2s(st, a.w + tile_of(it) * kTcTileBytes, full + s);
         bulk_g2s(st + kTcTileBytes, a.xc + (size_t)(it % KB) * BB, BB, full + s);
       }
       // every copy issued has landed before the CTA can leave (bounded)
@@ -228,32 +242,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_lm(const TcLmArgs a) {
         break;
       }
       tc_fence_after();
-      const int row = mt * kTcTileRows + warp * 32 + lane;
+      const int row0 = mt * kTcTileRows + warp * 32, row = row0 + lane;
 #pragma unroll 1
       for (int c = 0; c < NPAD / 32; ++c) {
         uint32_t r[32];
         tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * NPAD + c * 32), r);
         tc_wait_ld();
+        if (c == NPAD / 32 - 1) {  // the whole accumulator is in registers: the MMA may reuse it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty + buf);
+        }
+        // lane = vocabulary row: store the logits on request, then pass the chunk
+        // through shared memory so that lane = token scans its 32 rows
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int tok = c * 32 + j;
-          const float v = __uint_as_float(r[j]);
-          unsigned long long key = 0ull;
-          if (tok < a.ntok && row < a.V) {
-            if (a.logits) a.logits[(size_t)tok * a.V + row] = v;
-            key = argmax_key(v, row);
-          }
-#pragma unroll
-          for (int o = 16; o; o >>= 1) {
-            const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
-            key = other > key ? other : key;
-          }
-          if (lane == 0 && key > s_best[warp][tok]) s_best[warp][tok] = key;
+          if (a.logits && tok < a.ntok && row < a.V) a.logits[(size_t)tok * a.V + row] = __uint_as_float(r[j]);
+          s_tr[warp][j][lane] = __uint_as_float(r[j]);
         }
+        __syncwarp();
+        const int tok = c * 32 + lane;
+        if (tok < a.ntok) {
+          unsigned long long best = s_best[warp][tok];  // this lane's token: no other thread writes it
+#pragma unroll 8
+          for (int rr = 0; rr < 32; ++rr) {
+            if (row0 + rr < a.V) {
+              const unsigned long long key = argmax_key(s_tr[warp][lane][rr], row0 + rr);
+              best = key > best ? key : best;
+            }
+          }
+          s_best[warp][tok] = best;
+        }
+        __syncwarp();  // the chunk buffer is free for the next chunk
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty + buf);
     }
   }
   tc_fence_before();
