@@ -147,6 +147,7 @@ struct uocr_ctx {
   __half* attn_out = nullptr;
   __half* act_dense = nullptr;
   __half* xhat = nullptr;
+  uint8_t* act8 = nullptr;   // int8 activations: staging blocks of the 16-row token groups (written once per projection)
   uint8_t* act_r = nullptr;  // B-fragment order, padded expert entries x Ie
   uint8_t* act_s = nullptr;  // B-fragment order, rows x n_shared*Ie
   float* part_r = nullptr;
@@ -352,6 +353,11 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
   ctx->q = cv.take<float>((size_t)TC * S, r.activations);
   ctx->attn_out = cv.take<__half>((size_t)TC * S, r.activations);
   if (c.n_dense_layers > 0 || E == 0) ctx->act_dense = cv.take<__half>((size_t)TC * c.dense_inter, r.activations);
+  if (c.act_int8) {
+    int kmax = c.hidden > c.n_heads * c.head_dim ? c.hidden : c.n_heads * c.head_dim;
+    if ((c.n_dense_layers > 0 || E == 0) && c.dense_inter > kmax) kmax = c.dense_inter;
+    ctx->act8 = cv.take<uint8_t>((size_t)(TC / 16) * act_i8_bytes(16, kmax), r.activations);
+  }
   if (ctx->any_moe()) {
     ctx->xhat = cv.take<__half>((size_t)TC * H, r.activations);
     const int TG = (TC + 15) / 16;
@@ -454,6 +460,9 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     CK(launch_embed(ea, rows, st), "embed launch");
   }
 
+  // int8 activations above 8 rows: each projection's input quantised once per
+  // token group by its own small kernel instead of in every streaming CTA
+  const bool a8g = c.act_int8 && nt == 2;
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& w = ctx->L[l];
     __half* kvl = ctx->kv ? ctx->kv + ctx->kv_layer * l : nullptr;
@@ -483,7 +492,11 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     qa.kv_new = kv8l ? ctx->kv_new : nullptr;
     qa.status = ctx->status;
     if (want("qkv")) {
-      CK(launch_gemv(kf(c.fmt_attn), c.act_int8 ? SRC_NORM_I8 : SRC_NORM, EPI_QKV, qa, gx_for(w.qkv.n_slabs), tg, st, pdl), "qkv launch");
+      if (a8g) {
+        qa.x8 = ctx->act8;
+        CK(launch_act_quant(kf(c.fmt_attn), true, qa, ctx->act8, st, pdl), "qkv int8 staging launch");
+      }
+      CK(launch_gemv(kf(c.fmt_attn), a8g ? SRC_I8_COPY : c.act_int8 ? SRC_NORM_I8 : SRC_NORM, EPI_QKV, qa, gx_for(w.qkv.n_slabs), tg, st, pdl), "qkv launch");
     }
     if (kv8l) {  // INT8 cache: quantise the new keys / values into their slots
       KvQuantArgs ka{};
@@ -548,7 +561,11 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     oa.ld_out = H;
     oa.status = ctx->status;
     if (want("o_proj")) {
-      CK(launch_gemv(kf(c.fmt_attn), c.act_int8 ? SRC_F16_I8 : SRC_F16, EPI_RESID, oa, gx_for(w.o.n_slabs), tg, st, pdl), "o_proj launch");
+      if (a8g) {
+        oa.x8 = ctx->act8;
+        CK(launch_act_quant(kf(c.fmt_attn), false, oa, ctx->act8, st, pdl), "o_proj int8 staging launch");
+      }
+      CK(launch_gemv(kf(c.fmt_attn), a8g ? SRC_I8_COPY : c.act_int8 ? SRC_F16_I8 : SRC_F16, EPI_RESID, oa, gx_for(w.o.n_slabs), tg, st, pdl), "o_proj launch");
     }
     if (w.dense) {
       GemvArgs ga{};
@@ -563,7 +580,11 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       ga.ld_out = c.dense_inter;
       ga.status = ctx->status;
       if (want("mlp_gate_up")) {
-        CK(launch_gemv(kf(c.fmt_dense), c.act_int8 ? SRC_NORM_I8 : SRC_NORM, EPI_SWIGLU, ga, gx_for(w.gateup.n_slabs), tg, st, pdl),
+        if (a8g) {
+          ga.x8 = ctx->act8;
+          CK(launch_act_quant(kf(c.fmt_dense), true, ga, ctx->act8, st, pdl), "gate/up int8 staging launch");
+        }
+        CK(launch_gemv(kf(c.fmt_dense), a8g ? SRC_I8_COPY : c.act_int8 ? SRC_NORM_I8 : SRC_NORM, EPI_SWIGLU, ga, gx_for(w.gateup.n_slabs), tg, st, pdl),
            "gate/up launch");
       }
       GemvArgs da{};
@@ -577,7 +598,11 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       da.ld_out = H;
       da.status = ctx->status;
       if (want("mlp_down")) {
-        CK(launch_gemv(kf(c.fmt_dense), c.act_int8 ? SRC_F16_I8 : SRC_F16, EPI_RESID, da, gx_for(w.down.n_slabs), tg, st, pdl), "down launch");
+        if (a8g) {
+          da.x8 = ctx->act8;
+          CK(launch_act_quant(kf(c.fmt_dense), false, da, ctx->act8, st, pdl), "down int8 staging launch");
+        }
+        CK(launch_gemv(kf(c.fmt_dense), a8g ? SRC_I8_COPY : c.act_int8 ? SRC_F16_I8 : SRC_F16, EPI_RESID, da, gx_for(w.down.n_slabs), tg, st, pdl), "down launch");
       }
     } else {
       const int E = c.n_experts, k = c.top_k;

@@ -55,7 +55,7 @@ StreamPlan plan_stream(int nt, int fmt, int k_stage, int n_rows_list, int extra_
 
 template <int FMT, int NT, int SRC, int EPI>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a) {
-  constexpr bool A8 = SRC == SRC_NORM_I8 || SRC == SRC_F16_I8;
+  constexpr bool A8 = SRC == SRC_NORM_I8 || SRC == SRC_F16_I8 || SRC == SRC_I8_COPY;
   constexpr bool NORM = SRC == SRC_NORM || SRC == SRC_NORM_I8;
   extern __shared__ __align__(128) unsigned char smem[];
   const StreamPlan& p = a.sp;
@@ -90,7 +90,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
   if constexpr (EPI == EPI_LOGITS) {
     if (threadIdx.x < NT * 8) s_best[threadIdx.x] = 0ull;
   }
-  if constexpr (A8) {  // the int8 staging fits in the fp16 staging area
+  if constexpr (SRC == SRC_I8_COPY) {  // written once by k_act_quant for this token group
+    stage_bytes(smem + p.xs_off, a.x8 + (size_t)blockIdx.y * act_i8_bytes(16, K), act_i8_bytes(NT * 8, K));
+  } else if constexpr (A8) {  // the int8 staging fits in the fp16 staging area
     stage_act_i8<FMT, NORM>(smem + p.xs_off, NORM ? a.xf + (size_t)tok0 * a.ld_src : nullptr,
                             NORM ? nullptr : a.xh + (size_t)tok0 * a.ld_src, a.ld_src, ntok, NT * 8, a.norm_w, K, a.eps);
   } else if constexpr (SRC == SRC_NORM) {
@@ -204,6 +206,92 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
   }
 }
 
+// ------------------------------------------------------------------ int8 staging, once per step
+// Row blockIdx.x of the 16-row token groups: its K inputs (RMSNorm of fp32 rows
+// rounded to fp16 as the fp16 staging rounds them, or fp16 rows) quantised per
+// group of 32 into block blockIdx.x / 16 of `out`, in the layout the GEMV CTAs
+// stage (codes at the units' k order, scales and code sums [K/32][16]).
+template <int FMT, bool NORM>
+__global__ void __launch_bounds__(256) k_act_quant(const GemvArgs a, uint8_t* out) {
+  pdl_launch_dependents();
+  __shared__ float s_part[8];
+  const int row = blockIdx.x, tk = row & 15;
+  const int K = a.w.K, ng = K / 32, ldq = K + 16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* base = out + (size_t)(row >> 4) * act_i8_bytes(16, K);
+  uint8_t* xq = base + (size_t)tk * ldq;
+  float* xsc = reinterpret_cast<float*>(base + act_i8_codes_bytes(16, K));
+  int* xsm = reinterpret_cast<int*>(xsc + ng * 16);
+  pdl_wait();  // the source rows come from the previous kernel
+  if (row >= a.ntok) {  // a padding row of the last token group
+    for (int i = threadIdx.x; i < K / 16; i += blockDim.x) *reinterpret_cast<uint4*>(xq + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < ng; i += blockDim.x) {
+      xsc[i * 16 + tk] = 0.f;
+      xsm[i * 16 + tk] = 0;
+    }
+    return;
+  }
+  float r = 1.f;
+  if constexpr (NORM) {
+    const float4* src = reinterpret_cast<const float4*>(a.xf + (size_t)row * a.ld_src);
+    float ss = 0.f;
+    for (int f = threadIdx.x; f < K / 4; f += blockDim.x) {
+      const float4 v = src[f];
+      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) s_part[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_part[w];
+    r = rsqrtf(tot / (float)K + a.eps);
+  }
+  for (int c = warp; c * kActChunk < K; c += blockDim.x >> 5) {  // 256 inputs per warp pass
+    const int k0 = c * kActChunk + 8 * lane;
+    const bool on = k0 < K;  // whole groups of 32 (K is a multiple of 32)
+    float h[8];
+    if constexpr (NORM) {
+      const float4* src = reinterpret_cast<const float4*>(a.xf + (size_t)row * a.ld_src + k0);
+      const float4 x0 = on ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f), x1 = on ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+      const uint4 wv = on ? *reinterpret_cast<const uint4*>(a.norm_w + k0) : make_uint4(0u, 0u, 0u, 0u);
+      const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const uint32_t wr[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // fp16(x * r * w), the value the fp16 staging stores
+        const __half2 wj = u32_h2(wr[j]);
+        const float2 f = __half22float2(__floats2half2_rn(xs[2 * j] * r * __low2float(wj), xs[2 * j + 1] * r * __high2float(wj)));
+        h[2 * j] = f.x;
+        h[2 * j + 1] = f.y;
+      }
+    } else {
+      const uint4 hv = on ? *reinterpret_cast<const uint4*>(a.xh + (size_t)row * a.ld_src + k0) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t hr[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __half22float2(u32_h2(hr[j]));
+        h[2 * j] = f.x;
+        h[2 * j + 1] = f.y;
+      }
+    }
+    const int g = k0 >> 5;
+    act_i8_group<FMT>(h, on, xq + 32 * g, xsc + g * 16 + tk, xsm + g * 16 + tk);
+  }
+}
+
+cudaError_t launch_act_quant(int fmt, bool norm, const GemvArgs& a, uint8_t* out, cudaStream_t st, bool pdl) {
+  const dim3 grid((a.ntok + 15) / 16 * 16);
+#define UOCR_AQ(F_)                                                                                  \
+  if (fmt == F_)                                                                                     \
+    return norm ? launch_kernel(k_act_quant<F_, true>, grid, dim3(256), 0, st, pdl, a, out)           \
+                : launch_kernel(k_act_quant<F_, false>, grid, dim3(256), 0, st, pdl, a, out);
+  UOCR_AQ(Q8_0)
+  UOCR_AQ(Q4_0)
+  UOCR_AQ(I8ASYM)
+#undef UOCR_AQ
+  return cudaErrorInvalidValue;
+}
+
 template <int FMT, int NT, int SRC, int EPI>
 static cudaError_t launch_one(const GemvArgs& a, int gx, int gy, cudaStream_t st, bool pdl) {
   return launch_kernel(k_gemv<FMT, NT, SRC, EPI>, dim3(gx, gy), dim3(kThreads), a.sp.bytes, st, pdl, a);
@@ -214,6 +302,11 @@ static cudaError_t dispatch_epi(int src, int epi, const GemvArgs& a, int gx, int
   if (src == SRC_NORM && epi == EPI_QKV) return launch_one<FMT, NT, SRC_NORM, EPI_QKV>(a, gx, gy, st, pdl);
   if (src == SRC_F16 && epi == EPI_RESID) return launch_one<FMT, NT, SRC_F16, EPI_RESID>(a, gx, gy, st, pdl);
   if (src == SRC_NORM && epi == EPI_SWIGLU) return launch_one<FMT, NT, SRC_NORM, EPI_SWIGLU>(a, gx, gy, st, pdl);
+  if constexpr (FMT != F16 && NT == 2) {
+    if (src == SRC_I8_COPY && epi == EPI_QKV) return launch_one<FMT, NT, SRC_I8_COPY, EPI_QKV>(a, gx, gy, st, pdl);
+    if (src == SRC_I8_COPY && epi == EPI_RESID) return launch_one<FMT, NT, SRC_I8_COPY, EPI_RESID>(a, gx, gy, st, pdl);
+    if (src == SRC_I8_COPY && epi == EPI_SWIGLU) return launch_one<FMT, NT, SRC_I8_COPY, EPI_SWIGLU>(a, gx, gy, st, pdl);
+  }
   if constexpr (FMT != F16) {
     if (src == SRC_NORM_I8 && epi == EPI_QKV) return launch_one<FMT, NT, SRC_NORM_I8, EPI_QKV>(a, gx, gy, st, pdl);
     if (src == SRC_F16_I8 && epi == EPI_RESID) return launch_one<FMT, NT, SRC_F16_I8, EPI_RESID>(a, gx, gy, st, pdl);
@@ -254,6 +347,11 @@ static cudaError_t set_attr_fmt() {
   UOCR_SET(SRC_NORM, EPI_QKV)
   UOCR_SET(SRC_F16, EPI_RESID)
   UOCR_SET(SRC_NORM, EPI_SWIGLU)
+  if constexpr (FMT != F16 && NT == 2) {
+    UOCR_SET(SRC_I8_COPY, EPI_QKV)
+    UOCR_SET(SRC_I8_COPY, EPI_RESID)
+    UOCR_SET(SRC_I8_COPY, EPI_SWIGLU)
+  }
   if constexpr (FMT != F16) {
     UOCR_SET(SRC_NORM_I8, EPI_QKV)
     UOCR_SET(SRC_F16_I8, EPI_RESID)

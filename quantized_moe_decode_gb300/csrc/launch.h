@@ -27,7 +27,9 @@ StreamPlan plan_stream(int nt, int fmt, int k_stage, int n_rows_list = 0, int ex
 
 // Projection inputs: RMSNorm of fp32 rows, or fp16 rows; the _I8 forms
 // quantise them to int8 per group of 32 and run the int8 tensor-core product.
-enum Src : int { SRC_NORM = 0, SRC_F16 = 1, SRC_NORM_I8 = 2, SRC_F16_I8 = 3 };
+// SRC_I8_COPY: the int8 staging of each 16-row token group was written once by
+// k_act_quant (GemvArgs::x8) and is copied, not recomputed, by every CTA.
+enum Src : int { SRC_NORM = 0, SRC_F16 = 1, SRC_NORM_I8 = 2, SRC_F16_I8 = 3, SRC_I8_COPY = 4 };
 enum Epi : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3, EPI_BIAS_F16 = 4 };
 
 struct GemvArgs {
@@ -40,6 +42,7 @@ struct GemvArgs {
   int ld_src;
   const __half* norm_w;
   float eps;
+  const uint8_t* x8;        // SRC_I8_COPY: int8 staging blocks, one per token group of 16 rows
   // outputs
   const float* res_in;      // EPI_RESID: out = res_in + W x
   float* out_f;             // EPI_RESID output / EPI_LOGITS logits (nullable)
@@ -273,6 +276,11 @@ cudaError_t allow_max_dyn_smem(void (*kern)(KArgs...)) {
 }
 
 // launchers (return the launch error)
+// Int8 staging of a projection's input, once per step: one CTA per row of each
+// 16-row token group (rows beyond ntok zero), RMSNorm first when norm is set;
+// block g of `out` (act_i8_bytes(16, K) bytes) is what a two-n-tile GEMV CTA
+// of token group g stages.  Reads the source fields of `a` (K = a.w.K).
+cudaError_t launch_act_quant(int fmt, bool norm, const GemvArgs& a, uint8_t* out, cudaStream_t st, bool pdl);
 cudaError_t launch_gemv(int fmt, int src, int epi, const GemvArgs& a, int grid_x, int grid_y, cudaStream_t st,
                         bool pdl);
 // grid (cluster, token groups); cluster = min(8, router slabs) CTAs per token group
