@@ -66,7 +66,8 @@ __device__ __forceinline__ void topk_rank(const RowLogits& rl, int E, int k, int
                                           float (&wt)[QN]) {
 #pragma unroll
   for (int q = 0; q < QN; ++q) rank[q] = 0;
-  for (int src = 0; src < 32; ++src) {  // kept rolled: this code runs once per launch, cold
+#pragma unroll 4
+  for (int src = 0; src < 32; ++src) {  // the router warms this code up before it waits
 #pragma unroll
     for (int qs = 0; qs < QN; ++qs) {
       const float o = __shfl_sync(0xffffffffu, rl.v[qs], src);
