@@ -17,7 +17,10 @@
 //
 // With dynamic int8 activations ("Falcon-OCR INT8 OpenVINO IR": the linear
 // layers' inputs quantised per group of 32) the staged rows are int8 codes with
-// fp32 scales and the units run on the int8 tensor cores (the _I8 sources).
+// fp32 scales and the units run on the int8 tensor cores: up to 8 rows every
+// CTA quantises its rows while staging them (the _I8 sources); above 8 rows
+// k_act_quant writes each token group's staging once and the CTAs copy it
+// (SRC_I8_COPY).
 //
 // Each persistent CTA owns slabs blockIdx.x, +gridDim.x, ...; each warp streams
 // its units through its own shared-memory ring filled by 16-byte cp.async
