@@ -356,7 +356,10 @@ static void carve(uocr_ctx* ctx, Carver& cv) {
   if (c.act_int8) {
     int kmax = c.hidden > c.n_heads * c.head_dim ? c.hidden : c.n_heads * c.head_dim;
     if ((c.n_dense_layers > 0 || E == 0) && c.dense_inter > kmax) kmax = c.dense_inter;
-    ctx->act8 = cv.take<uint8_t>((size_t)(TC / 16) * act_i8_bytes(16, kmax), r.activations);
+    ctx->act8 = cv.take<uint8_t>((size_t)(TC / 8) * act_i8_bytes(8, kmax) > (size_t)(TC / 16) * act_i8_bytes(16, kmax)
+                                     ? (size_t)(TC / 8) * act_i8_bytes(8, kmax)
+                                     : (size_t)(TC / 16) * act_i8_bytes(16, kmax),
+                                 r.activations);
   }
   if (ctx->any_moe()) {
     ctx->xhat = cv.take<__half>((size_t)TC * H, r.activations);
@@ -460,9 +463,10 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     CK(launch_embed(ea, rows, st), "embed launch");
   }
 
-  // int8 activations above 8 rows: each projection's input quantised once per
-  // token group by its own small kernel instead of in every streaming CTA
-  const bool a8g = c.act_int8 && nt == 2;
+  // int8 activations from 4 rows: each projection's input quantised once per
+  // token group by its own small kernel instead of in every streaming CTA (below
+  // that, the extra launch costs more than the CTAs' own quantisation)
+  const bool a8g = c.act_int8 && rows >= 4;
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& w = ctx->L[l];
     __half* kvl = ctx->kv ? ctx->kv + ctx->kv_layer * l : nullptr;

@@ -17,8 +17,8 @@
 //
 // With dynamic int8 activations ("Falcon-OCR INT8 OpenVINO IR": the linear
 // layers' inputs quantised per group of 32) the staged rows are int8 codes with
-// fp32 scales and the units run on the int8 tensor cores: up to 8 rows every
-// CTA quantises its rows while staging them (the _I8 sources); above 8 rows
+// fp32 scales and the units run on the int8 tensor cores: below 4 rows every
+// CTA quantises its rows while staging them (the _I8 sources); from 4 rows
 // k_act_quant writes each token group's staging once and the CTAs copy it
 // (SRC_I8_COPY).
 //
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
     if (threadIdx.x < NT * 8) s_best[threadIdx.x] = 0ull;
   }
   if constexpr (SRC == SRC_I8_COPY) {  // written once by k_act_quant for this token group
-    stage_bytes(smem + p.xs_off, a.x8 + (size_t)blockIdx.y * act_i8_bytes(16, K), act_i8_bytes(NT * 8, K));
+    stage_bytes(smem + p.xs_off, a.x8 + (size_t)blockIdx.y * act_i8_bytes(NT * 8, K), act_i8_bytes(NT * 8, K));
   } else if constexpr (A8) {  // the int8 staging fits in the fp16 staging area
     stage_act_i8<FMT, NORM>(smem + p.xs_off, NORM ? a.xf + (size_t)tok0 * a.ld_src : nullptr,
                             NORM ? nullptr : a.xh + (size_t)tok0 * a.ld_src, a.ld_src, ntok, NT * 8, a.norm_w, K, a.eps);
@@ -210,27 +210,28 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_gemv(const GemvArgs a)
 }
 
 // ------------------------------------------------------------------ int8 staging, once per step
-// Row blockIdx.x of the 16-row token groups: its K inputs (RMSNorm of fp32 rows
-// rounded to fp16 as the fp16 staging rounds them, or fp16 rows) quantised per
-// group of 32 into block blockIdx.x / 16 of `out`, in the layout the GEMV CTAs
-// stage (codes at the units' k order, scales and code sums [K/32][16]).
+// Row blockIdx.x of the G-row token groups (G = 8 or 16, the rows of a GEMV
+// CTA): its K inputs (RMSNorm of fp32 rows rounded to fp16 as the fp16 staging
+// rounds them, or fp16 rows) quantised per group of 32 into block blockIdx.x / G
+// of `out`, in the layout the GEMV CTAs stage (codes at the units' k order,
+// scales and code sums [K/32][G]).
 template <int FMT, bool NORM>
-__global__ void __launch_bounds__(256) k_act_quant(const GemvArgs a, uint8_t* out) {
+__global__ void __launch_bounds__(256) k_act_quant(const GemvArgs a, uint8_t* out, int G) {
   pdl_launch_dependents();
   __shared__ float s_part[8];
-  const int row = blockIdx.x, tk = row & 15;
+  const int row = blockIdx.x, tk = row % G;
   const int K = a.w.K, ng = K / 32, ldq = K + 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t* base = out + (size_t)(row >> 4) * act_i8_bytes(16, K);
+  uint8_t* base = out + (size_t)(row / G) * act_i8_bytes(G, K);
   uint8_t* xq = base + (size_t)tk * ldq;
-  float* xsc = reinterpret_cast<float*>(base + act_i8_codes_bytes(16, K));
-  int* xsm = reinterpret_cast<int*>(xsc + ng * 16);
+  float* xsc = reinterpret_cast<float*>(base + act_i8_codes_bytes(G, K));
+  int* xsm = reinterpret_cast<int*>(xsc + ng * G);
   pdl_wait();  // the source rows come from the previous kernel
   if (row >= a.ntok) {  // a padding row of the last token group
     for (int i = threadIdx.x; i < K / 16; i += blockDim.x) *reinterpret_cast<uint4*>(xq + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
     for (int i = threadIdx.x; i < ng; i += blockDim.x) {
-      xsc[i * 16 + tk] = 0.f;
-      xsm[i * 16 + tk] = 0;
+      xsc[i * G + tk] = 0.f;
+      xsm[i * G + tk] = 0;
     }
     return;
   }
@@ -278,16 +279,17 @@ __global__ void __launch_bounds__(256) k_act_quant(const GemvArgs a, uint8_t* ou
       }
     }
     const int g = k0 >> 5;
-    act_i8_group<FMT>(h, on, xq + 32 * g, xsc + g * 16 + tk, xsm + g * 16 + tk);
+    act_i8_group<FMT>(h, on, xq + 32 * g, xsc + g * G + tk, xsm + g * G + tk);
   }
 }
 
 cudaError_t launch_act_quant(int fmt, bool norm, const GemvArgs& a, uint8_t* out, cudaStream_t st, bool pdl) {
-  const dim3 grid((a.ntok + 15) / 16 * 16);
+  const int G = a.sp.nt * 8;  // the rows of one CTA of the GEMV that copies the blocks
+  const dim3 grid((a.ntok + G - 1) / G * G);
 #define UOCR_AQ(F_)                                                                                  \
   if (fmt == F_)                                                                                     \
-    return norm ? launch_kernel(k_act_quant<F_, true>, grid, dim3(256), 0, st, pdl, a, out)           \
-                : launch_kernel(k_act_quant<F_, false>, grid, dim3(256), 0, st, pdl, a, out);
+    return norm ? launch_kernel(k_act_quant<F_, true>, grid, dim3(256), 0, st, pdl, a, out, G)        \
+                : launch_kernel(k_act_quant<F_, false>, grid, dim3(256), 0, st, pdl, a, out, G);
   UOCR_AQ(Q8_0)
   UOCR_AQ(Q4_0)
   UOCR_AQ(I8ASYM)
@@ -305,7 +307,7 @@ static cudaError_t dispatch_epi(int src, int epi, const GemvArgs& a, int gx, int
   if (src == SRC_NORM && epi == EPI_QKV) return launch_one<FMT, NT, SRC_NORM, EPI_QKV>(a, gx, gy, st, pdl);
   if (src == SRC_F16 && epi == EPI_RESID) return launch_one<FMT, NT, SRC_F16, EPI_RESID>(a, gx, gy, st, pdl);
   if (src == SRC_NORM && epi == EPI_SWIGLU) return launch_one<FMT, NT, SRC_NORM, EPI_SWIGLU>(a, gx, gy, st, pdl);
-  if constexpr (FMT != F16 && NT == 2) {
+  if constexpr (FMT != F16) {
     if (src == SRC_I8_COPY && epi == EPI_QKV) return launch_one<FMT, NT, SRC_I8_COPY, EPI_QKV>(a, gx, gy, st, pdl);
     if (src == SRC_I8_COPY && epi == EPI_RESID) return launch_one<FMT, NT, SRC_I8_COPY, EPI_RESID>(a, gx, gy, st, pdl);
     if (src == SRC_I8_COPY && epi == EPI_SWIGLU) return launch_one<FMT, NT, SRC_I8_COPY, EPI_SWIGLU>(a, gx, gy, st, pdl);
@@ -350,7 +352,7 @@ static cudaError_t set_attr_fmt() {
   UOCR_SET(SRC_NORM, EPI_QKV)
   UOCR_SET(SRC_F16, EPI_RESID)
   UOCR_SET(SRC_NORM, EPI_SWIGLU)
-  if constexpr (FMT != F16 && NT == 2) {
+  if constexpr (FMT != F16) {
     UOCR_SET(SRC_I8_COPY, EPI_QKV)
     UOCR_SET(SRC_I8_COPY, EPI_RESID)
     UOCR_SET(SRC_I8_COPY, EPI_SWIGLU)

@@ -277,9 +277,9 @@ cudaError_t allow_max_dyn_smem(void (*kern)(KArgs...)) {
 
 // launchers (return the launch error)
 // Int8 staging of a projection's input, once per step: one CTA per row of each
-// 16-row token group (rows beyond ntok zero), RMSNorm first when norm is set;
-// block g of `out` (act_i8_bytes(16, K) bytes) is what a two-n-tile GEMV CTA
-// of token group g stages.  Reads the source fields of `a` (K = a.w.K).
+// token group of G = a.sp.nt * 8 rows (rows beyond ntok zero), RMSNorm first
+// when norm is set; block g of `out` (act_i8_bytes(G, K) bytes) is what the
+// GEMV CTAs of token group g stage.  Reads the source fields of `a` (K = a.w.K).
 cudaError_t launch_act_quant(int fmt, bool norm, const GemvArgs& a, uint8_t* out, cudaStream_t st, bool pdl);
 cudaError_t launch_gemv(int fmt, int src, int epi, const GemvArgs& a, int grid_x, int grid_y, cudaStream_t st,
                         bool pdl);

@@ -216,6 +216,13 @@ def test_int8_activations_i8asym_sink_decoder_forty_rows(cuda):
     _run(wl, 8)
 
 
+def test_int8_activations_six_rows_staged_once_q4_attention(cuda):
+    # 4..8 rows: one 8-row token group quantised once per projection and copied by every CTA
+    cfg = _dense(act_int8=1, fmt_attn=Q4, fmt_dense=I8, use_sink=1, max_rows=6, prefix_len=7)
+    wl = synth.make_workload("a8_six", cfg, 6, 12, 145)
+    _run(wl, 12)
+
+
 def test_int8_activations_with_int8_kv_sink_decoder_single_row(cuda):
     cfg = _dense(act_int8=1, kv_int8=1, fmt_attn=I8, fmt_dense=I8, use_sink=1, max_rows=1, hidden=1024,
                  n_heads=8, head_dim=64, dense_inter=1024, n_layers=2, n_dense_layers=2, prefix_len=33)
