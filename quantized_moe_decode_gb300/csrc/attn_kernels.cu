@@ -566,6 +566,32 @@ cudaError_t launch_attn(const AttnArgs& a, int rows, cudaStream_t st, bool pdl) 
   return cudaErrorInvalidValue;
 }
 
+// Attention CTAs of one launch that fit on an SM at once (shared memory bound).
+int attn_ctas_per_sm(int D, bool int8_cache) {
+  int n = 0;
+  cudaError_t e = cudaSuccess;
+#define UOCR_OCC(K_, SM_) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K_, UOCR_ATTN_WARPS * 32, SM_);
+  if (int8_cache) {
+    switch (D) {
+      case 16: UOCR_OCC(k_attn8<16>, attn8_smem_bytes(16)) break;
+      case 32: UOCR_OCC(k_attn8<32>, attn8_smem_bytes(32)) break;
+      case 64: UOCR_OCC(k_attn8<64>, attn8_smem_bytes(64)) break;
+      case 128: UOCR_OCC(k_attn8<128>, attn8_smem_bytes(128)) break;
+      default: UOCR_OCC(k_attn8<256>, attn8_smem_bytes(256)) break;
+    }
+  } else {
+    switch (D) {
+      case 16: UOCR_OCC(k_attn<16>, attn_smem_bytes(16)) break;
+      case 32: UOCR_OCC(k_attn<32>, attn_smem_bytes(32)) break;
+      case 64: UOCR_OCC(k_attn<64>, attn_smem_bytes(64)) break;
+      case 128: UOCR_OCC(k_attn<128>, attn_smem_bytes(128)) break;
+      default: UOCR_OCC(k_attn<256>, attn_smem_bytes(256)) break;
+    }
+  }
+#undef UOCR_OCC
+  return e == cudaSuccess && n > 0 ? n : 1;
+}
+
 static cudaError_t init_attn_attributes() {
   cudaError_t e = cudaSuccess;
 #define UOCR_A(D_) \

@@ -172,6 +172,8 @@ struct uocr_ctx {
   bool pdl = true;  // programmatic dependent launch between the step's kernels
   int gemv_ctas_per_sm = 2;    // streaming CTAs per SM of a GEMV launch
   int expert_ctas_per_sm = 2;  // CTAs per SM an expert launch is sized for (active experts only)
+  int attn_min_splits = 1;     // lower bound of the attention splits per (row, head)
+  int attn_slots = 0;          // attention CTAs resident on the whole GPU at once
   // tensor-core expert kernels for steps of more than 16 rows (one CTA per SM)
   bool tc_experts = false;
   TcxPlan tcx_gu{}, tcx_dn{};
@@ -540,7 +542,18 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
     aa.early = sh.prefill ? 0 : 1;
     aa.status = ctx->status;
     {
-      int ns = (2 * ctx->n_sm + rows * c.n_heads - 1) / (rows * c.n_heads);
+      const int pairs = rows * c.n_heads;
+      int ns = (2 * ctx->n_sm + pairs - 1) / pairs;
+      // more than one wave of resident CTAs with the last one less than half full:
+      // one more split (at most doubling) evens the waves out (64 rows x 10 heads:
+      // 640 CTAs on 456 slots -> 1280; measured 124 -> 108 us per launch)
+      if (const int slots = ctx->attn_slots; slots > 0 && pairs * ns > slots) {
+        const int last = pairs * ns - (pairs * ns - 1) / slots * slots;
+        const int ns2 = ns + 1;
+        const int last2 = pairs * ns2 - (pairs * ns2 - 1) / slots * slots;
+        if (2 * last < slots && ns2 <= 2 * ns && last2 > last) ns = ns2;
+      }
+      if (ns < ctx->attn_min_splits) ns = ctx->attn_min_splits;
       const int cap = (ctx->SL + 63) / 64;
       if (ns > cap) ns = cap;
       if (ns > kMaxSplits) ns = kMaxSplits;
@@ -1165,6 +1178,8 @@ uocr_status uocr_create(const uocr_config* cfg, uocr_ctx** out) {
     };
     ctx->gemv_ctas_per_sm = knob("UOCR_GEMV_CTAS_PER_SM", ctx->gemv_ctas_per_sm);
     ctx->expert_ctas_per_sm = knob("UOCR_EXPERT_CTAS_PER_SM", ctx->expert_ctas_per_sm);
+    ctx->attn_min_splits = knob("UOCR_ATTN_MIN_SPLITS", ctx->attn_min_splits);
+    ctx->attn_slots = attn_ctas_per_sm(cfg->head_dim, cfg->kv_int8 != 0) * ctx->n_sm;
     // the tensor-core expert kernels on request (UOCR_TC_EXPERTS=1) where the formats and
     // the shared memory allow them.  Off by default: at the few rows per expert of a
     // decode step they stream the weights at about 0.6 the speed of the fragment-GEMV

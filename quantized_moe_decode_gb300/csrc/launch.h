@@ -281,6 +281,7 @@ cudaError_t allow_max_dyn_smem(void (*kern)(KArgs...)) {
 // when norm is set; block g of `out` (act_i8_bytes(G, K) bytes) is what the
 // GEMV CTAs of token group g stage.  Reads the source fields of `a` (K = a.w.K).
 cudaError_t launch_act_quant(int fmt, bool norm, const GemvArgs& a, uint8_t* out, cudaStream_t st, bool pdl);
+int attn_ctas_per_sm(int D, bool int8_cache);  // resident attention CTAs per SM (occupancy)
 cudaError_t launch_gemv(int fmt, int src, int epi, const GemvArgs& a, int grid_x, int grid_y, cudaStream_t st,
                         bool pdl);
 // grid (cluster, token groups); cluster = min(8, router slabs) CTAs per token group
