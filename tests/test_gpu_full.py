@@ -204,6 +204,25 @@ def test_sink_sweep_rows_1_6_12_24_64(cuda, T):
     ctx.close()
 
 
+def test_sink_decoder_falcon_setting_int8_kv_int8_activations(cuda):
+    # the Falcon card's serving setting: int8-asym weights, an INT8 KV cache and
+    # dynamic int8 activations, at its own row counts (in-kernel quantisation at 1
+    # row, one 8-row group at 6, 16-row groups at 24) with 350 cached tokens
+    wl = synth.workload("sink", rows=24, T=350, steps=3)
+    wl.cfg = wl.cfg.replace(kv_int8=1, act_int8=1)
+    ctx = make_ctx(wl)
+    _check_int8_prefix(ctx, wl, [0, 23], [0, wl.cfg.n_layers - 1])
+    for r in (1, 6, 24):
+        ctx.uocr_kv_reset(-1, 1)
+        sample = sorted({0, r - 1})
+        st = run_parity(ctx, wl, 3, make_oracle(wl, rows=sample, cache=_cache()), rows=r, row_map=sample)
+        _report(f"{wl.name} rows {r} (INT8 KV, int8 activations)", st)
+        # the codes are held per head vector to the steps the float bound allows (parity.py)
+        print(f"INT8 entries: {st.kv_codes} codes, {st.kv_code_steps} off by a step or more")
+        assert st.kv_codes > 0
+    ctx.close()
+
+
 def _check_int8_prefix(ctx, wl, rows, layers):
     """The cached prefix quantised by the library equals the oracle's entries exactly."""
     import oracle
