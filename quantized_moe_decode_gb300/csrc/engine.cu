@@ -545,13 +545,15 @@ static uocr_status enqueue_step(uocr_ctx* ctx, const StepShape& sh, Prof* prof) 
       const int pairs = rows * c.n_heads;
       int ns = (2 * ctx->n_sm + pairs - 1) / pairs;
       // more than one wave of resident CTAs with the last one less than half full:
-      // one more split (at most doubling) evens the waves out (64 rows x 10 heads:
-      // 640 CTAs on 456 slots -> 1280; measured 124 -> 108 us per launch)
+      // one more split (at most doubling) evens the waves out, where each split
+      // keeps at least 512 slots (64 rows x 10 heads over 2176 slots: 640 CTAs on
+      // 456 resident -> 1280, 124 -> 108 us per launch; over 478 slots the merge
+      // costs more than the fuller last wave gains)
       if (const int slots = ctx->attn_slots; slots > 0 && pairs * ns > slots) {
         const int last = pairs * ns - (pairs * ns - 1) / slots * slots;
         const int ns2 = ns + 1;
         const int last2 = pairs * ns2 - (pairs * ns2 - 1) / slots * slots;
-        if (2 * last < slots && ns2 <= 2 * ns && last2 > last) ns = ns2;
+        if (2 * last < slots && ns2 <= 2 * ns && last2 > last && ctx->SL >= 512 * ns2) ns = ns2;
       }
       if (ns < ctx->attn_min_splits) ns = ctx->attn_min_splits;
       const int cap = (ctx->SL + 63) / 64;

@@ -123,9 +123,10 @@ def test_host_side_refusals(cuda):
         ctx.uocr_load_weights([wrong_fmt])
     assert e.value.status == binding.UOCR_E_FORMAT
     binding.load_workload(ctx, wl)
-    with pytest.raises(binding.UocrError) as e:
-        ctx.uocr_decode_step(5, ids.data_ptr(), ids.data_ptr(), ids.data_ptr())
-    assert e.value.status == binding.UOCR_E_INVALID_ARG
+    for bad_rows in (5, 0, -1):  # above max_rows, an empty step, a negative count
+        with pytest.raises(binding.UocrError) as e:
+            ctx.uocr_decode_step(bad_rows, ids.data_ptr(), ids.data_ptr(), ids.data_ptr())
+        assert e.value.status == binding.UOCR_E_INVALID_ARG
     rep = ctx.uocr_memory_report()
     assert rep["total"] >= rep["weights"] + rep["kv_cache"] > 0
     ctx.close()
