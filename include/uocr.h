@@ -170,7 +170,9 @@ typedef struct {
      the dense projections (Q/K/V, O, dense gate/up and down) are quantised
      per group of 32 (s = max|x| / 127, code = round(x / s), fp32 decisions)
      and multiplied on the int8 tensor cores; fmt_attn and fmt_dense must then
-     be quantised formats.  Router, experts, LM head and projector unchanged. */
+     be quantised formats and hidden, n_heads*head_dim and dense_inter at most
+     8192 (else uocr_create returns UOCR_E_INVALID_ARG).  Router, experts, LM
+     head and projector unchanged.  0 or 1. */
   int32_t act_int8;
 } uocr_config;
 
