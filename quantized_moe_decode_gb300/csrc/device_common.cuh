@@ -44,7 +44,7 @@ constexpr int kThreads = kConsumers;
 //   UOCR_MIN_BLOCKS  minimum resident CTAs per SM asked of the compiler
 //   UOCR_UNROLL      units consumed per step of the inner loop (1 or 2)
 #ifndef UOCR_RING_DEPTH
-#define UOCR_RING_DEPTH 6
+#define UOCR_RING_DEPTH 5
 #endif
 #ifndef UOCR_MIN_BLOCKS
 #define UOCR_MIN_BLOCKS 2

@@ -446,6 +446,24 @@ def test_act_quant_groups_of_32_hand_built():
     assert np.array_equal(y2[64:96], 8.0 * y[64:96]) and np.array_equal(y2[:64], y[:64])
 
 
+def test_int8_activation_grid_error_behind_the_parity_bound():
+    # The int8-activation parity bound reads "every code one step apart" as about
+    # sqrt(12) x the grid's own relative error eps_q; on N(0, 1) activations in
+    # groups of 32 eps_q is 0.5-0.7% (group max / rms ~ 2.1-2.6), so the bound
+    # sqrt(12) eps_q stays within 2.5e-2, and one step on every code is exactly
+    # s per input, sqrt(12) times the uniform rounding error's rms.
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((4096, 32 * 32))
+    q = oracle.act_quant(x)
+    eps_q = np.linalg.norm(q - x) / np.linalg.norm(x)
+    assert 0.004 < eps_q < 0.008, eps_q
+    assert np.sqrt(12.0) * eps_q < 2.5e-2
+    g = x.reshape(-1, 32)
+    s = np.max(np.abs(g), axis=1) / 127.0
+    step_err = np.sqrt(np.mean(s ** 2)) * np.sqrt(g.size / g.shape[0]) / np.sqrt(np.mean(np.sum(g ** 2, axis=1)))
+    assert abs(step_err / eps_q - np.sqrt(12.0)) < 0.1 * np.sqrt(12.0)
+
+
 def test_int8_activation_model_is_close_to_fp16_and_exact_on_its_grid():
     cfg = synth.ModelConfig(hidden=128, n_heads=2, head_dim=64, n_layers=2, n_dense_layers=2, dense_inter=256,
                             prefix_len=6, ring_len=4, max_rows=2)
