@@ -3,12 +3,15 @@
 //   router   one thread-block cluster per token group of 16 rows: its CTAs
 //            share the E/16 slabs of the fp16 router GEMV (RMSNorm prologue)
 //            and keep their logits in shared memory; after a cluster barrier
-//            rank 0 reads all E logits of each row through distributed shared
+//            each rank takes a share of the rows (row r by rank r % cluster
+//            size), reads all E logits of the row through distributed shared
 //            memory, takes the top-k (lowest index wins a tie) and the softmax
-//            weights renormalised over them, and writes one record per routed
-//            unit (active slot or expert id): the expert, the rows of the group
-//            that chose it (its segment of the token grouping, a 16-bit mask)
-//            and each row's slot in its top-k (3 bits per row).
+//            weights renormalised over them, and ORs the choices into rank 0's
+//            per-expert masks (remote atomics, then a cluster-scope release
+//            fence); after a second barrier rank 0 writes one record per
+//            routed unit (active slot or expert id): the expert, the rows of
+//            the group that chose it (its segment of the token grouping, a
+//            16-bit mask) and each row's slot in its top-k (3 bits per row).
 //   gate/up  shared-expert CTAs first (they need nothing from the router),
 //            then routed CTAs, one per (unit, part of the expert's slabs).  A
 //            routed CTA reads its unit's record of every token group, gathers
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
   UnitStream<F16> us;
   us.start(a.w.q, a.w.s, w);
   us.prefetch(ring, p.slot, w, lane);
-  if (kWarmTopk && rank == 0 && E <= 64) {
+  if (kWarmTopk && E <= 64) {
     // run the top-k once on placeholder logits while the previous kernel drains:
     // it pulls the (once-per-launch, otherwise cold) code into the instruction cache
     RowLogits rl;
@@ -135,6 +138,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
   }
   NormW nw;
   load_norm_w(nw, a.norm_w, H);
+  if (rank == 0)  // every rank ORs its rows' choices into rank 0's masks (cleared before the first cluster barrier)
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+      s_mask[e] = 0u;
+      s_jbits[e] = 0ull;
+    }
   pdl_wait();
   stage_norm_rows(xs, p.ldx, a.h + (size_t)tok0 * H, H, ntok, NT * 8, a.norm_w, nw, H, a.eps);
   __syncthreads();
@@ -158,17 +166,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
   };
   run_stream<F16, NT>(us, w, ring, p.slot, red, bp, NT, epi);
   if (kPdlLate & PDL_ROUTER) pdl_launch_dependents();
-  cluster.sync();  // every CTA's logits are in its shared memory
+  cluster.sync();  // every CTA's logits are in its shared memory, rank 0's masks are clear
 
-  if (rank == 0) {
-    for (int e = threadIdx.x; e < E; e += kThreads) {
-      s_mask[e] = 0u;
-      s_jbits[e] = 0ull;
-    }
-    __syncthreads();
+  {  // the group's rows are ranked by all CTAs of the cluster: row r by rank r % cs
+    unsigned* mask0 = cluster.map_shared_rank(&s_mask[0], 0);
+    unsigned long long* jbits0 = cluster.map_shared_rank(&s_jbits[0], 0);
     const int k = a.k;
     const int qn = (E + 31) / 32;
-    for (int r = warp; r < ntok; r += kWarps) {
+    for (int r = rank + cs * warp; r < ntok; r += cs * kWarps) {
       RowLogits rl;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -190,8 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
           if (e < E && rk[q] < k) {
             a.idx[(tok0 + r) * k + rk[q]] = e;
             a.wts[(tok0 + r) * k + rk[q]] = wt[q];
-            atomicOr(&s_mask[e], 1u << r);  // a row picks an expert at most once
-            atomicOr(&s_jbits[e], (unsigned long long)rk[q] << (3 * r));
+            atomicOr(&mask0[e], 1u << r);  // a row picks an expert at most once
+            // the row's 3-bit slot, as 32-bit ORs on the two halves of the expert's word
+            const unsigned long long bits = (unsigned long long)rk[q] << (3 * r);
+            unsigned* jw = reinterpret_cast<unsigned*>(jbits0 + e);
+            if ((unsigned)bits) atomicOr(jw, (unsigned)bits);
+            if ((unsigned)(bits >> 32)) atomicOr(jw + 1, (unsigned)(bits >> 32));
           }
         }
       };
@@ -199,7 +208,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
       else if (qn <= 4) emit(std::integral_constant<int, 4>{});
       else emit(std::integral_constant<int, 8>{});
     }
-    __syncthreads();
+  }
+  // the remote ORs are complete and visible at cluster scope before the barrier
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+  cluster.sync();  // every rank's choices are in rank 0's masks; no CTA reads a peer after this
+
+  if (rank == 0) {
     const int e = threadIdx.x;
     const unsigned mk = e < E ? s_mask[e] : 0u;
     const unsigned long long jb = e < E ? s_jbits[e] : 0ull;
@@ -213,7 +227,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_router(const RouterArgs a) {
       rec[e] = make_int4(mk ? e : -1, (int)mk, (int)(uint32_t)jb, (int)(uint32_t)(jb >> 32));
     }
   }
-  cluster.sync();  // peers keep their shared memory until rank 0 has read it
 }
 
 // ------------------------------------------------------------------ gate/up
