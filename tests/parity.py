@@ -117,7 +117,7 @@ class Stats:
         self.worst_abs = max(self.worst_abs, m)
 
 
-class GpuRunner:
+class LibraryRunner:
     """Drives one library context over a workload with torch device buffers."""
 
     def __init__(self, ctx, wl, rows=None):
@@ -458,7 +458,7 @@ def run_parity(ctx, wl, steps, oracle_model, **kw):
 def _run_parity(ctx, wl, steps, oracle_model, rows=None, row_map=None, check_kv=True, log=None,
                 same_router_input=False, lib_prefill=False):
     cfg = wl.cfg
-    runner = GpuRunner(ctx, wl, rows)
+    runner = LibraryRunner(ctx, wl, rows)
     n_or = oracle_model.rows
     row_map = list(range(n_or)) if row_map is None else row_map
     stats = Stats()

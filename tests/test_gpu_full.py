@@ -19,7 +19,7 @@ import pytest
 from quantized_moe_decode_gb300 import synth
 
 from helpers import make_ctx, make_oracle
-from parity import GpuRunner, run_parity
+from parity import LibraryRunner, run_parity
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -147,7 +147,7 @@ def test_group64_moe_layer_b1_ring_wraps(cuda):
 
 def _gpu_prefill(ctx, wl):
     """The workload's prefill-by-decode on the library alone; returns the first greedy ids."""
-    run = GpuRunner(ctx, wl)
+    run = LibraryRunner(ctx, wl)
     ne = wl.prefill_embeds.shape[1]
     for p in range(wl.cfg.prefix_len):
         pos = np.full(wl.rows, p, np.int32)
@@ -177,7 +177,7 @@ def test_full_b8_generate_equals_step_loop_bitwise(cuda):
     a.uocr_generate(wl.rows, ids.data_ptr(), pos.data_ptr(), n, out.data_ptr())
     a.uocr_sync()
     assert (pos.cpu().numpy() == p0).all()  # the caller's inputs are not modified
-    run = GpuRunner(b, wl)
+    run = LibraryRunner(b, wl)
     cur = ids_b
     hist = []
     for s in range(n):
